@@ -1,0 +1,550 @@
+#!/usr/bin/env python
+"""Throughput of token-tree verification on GB300: tree nodes verified per second.
+
+One step = one pass of the whole hot path over one batch of synthetic input:
+tree preparation (ancestor bitsets), one layer of tree attention, and the
+verification of the workload (greedy and/or multi-step speculative sampling).
+`value` = tree nodes verified / s over the whole job with inputs resident in
+HBM; `e2e` = the same metric when every step also copies its inputs from
+pinned host memory and reads its results back.
+
+Timing: W untimed warm-up steps, then exactly K steps between CUDA events on
+the launching stream, bracketed by barrier + synchronize; each step replays a
+CUDA graph of the step on one of R input copies whose total size is at least
+4x the L2 cache, so every step reads its inputs from HBM.  Under torchrun each
+rank runs an independent replica (replicas only: no data exchange) and the
+maximum time over ranks is reported.
+
+`--impl reference` times the CPU oracle (the only reference implementation:
+the pages ship no code) on the host cores over a bounded sample of the same
+workload.
+"""
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "tree nodes verified/sec (attn+verify)"
+UNIT = "nodes/s"
+DEFAULT_WORKLOAD = "llama7b-layer-P1024-n20"
+
+
+def parse_args():
+    p = argparse.ArgumentParser(description=__doc__)
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=50000)
+    p.add_argument("--warmup", type=int, default=200)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU oracle sample budget")
+    return p.parse_args()
+
+
+# --------------------------------------------------------------------------- common
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def workload_inputs(spec):
+    import workloads as W
+    trees = W.make_trees(spec)
+    att = W.make_attention_inputs(spec, trees)
+    gi = W.make_greedy_inputs(spec, trees) if spec.greedy else None
+    si = W.make_stochastic_inputs(spec, trees) if spec.stochastic else None
+    return trees, att, gi, si
+
+
+def config_of(spec, extra=None):
+    cfg = {"workload": spec.name, "B": spec.B, "Hq": spec.Hq, "Hkv": spec.Hkv, "D": spec.D,
+           "prefix": list(spec.prefix) if isinstance(spec.prefix, tuple) else spec.prefix,
+           "nodes_per_request": spec.nodes, "vocab": spec.V,
+           "verify": "+".join(v for v, on in (("greedy", spec.greedy), ("stochastic", spec.stochastic)) if on),
+           "tree": spec.tree}
+    if extra:
+        cfg.update(extra)
+    return cfg
+
+
+def attention_bytes(spec, trees):
+    """Algorithmic bytes of one tree-attention launch: every (request, KV head)
+    reads its K and V rows 0 .. P_b+n_b-1 once, Q is read once, O written once."""
+    esz = 2 if spec.dtype == "bf16" else 4
+    sizes = np.diff(trees.node_offsets)
+    keys = int((trees.prefix_len + sizes).sum())
+    N = int(trees.node_offsets[-1])
+    return 2 * keys * spec.Hkv * spec.D * esz + 2 * N * spec.Hq * spec.D * esz
+
+
+def verify_bytes(spec, trees, n_rejected_rows=0):
+    """Greedy: every logits row once.  Stochastic: every LLM row once plus the
+    full proposal row of each rejected child (count from the oracle)."""
+    N = int(trees.node_offsets[-1])
+    b = 0
+    if spec.greedy:
+        b += N * spec.V * 4
+    if spec.stochastic:
+        b += (N + n_rejected_rows) * spec.V * 4
+    return b
+
+
+class ClockSampler:
+    """nvidia-smi samples (200 ms) while the benchmark runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.samples = []
+        self.proc = None
+        self.gpu = gpu_index
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.QUERY,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) >= 9:
+                self.samples.append((time.time(), f))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        win = [f for (t, f) in self.samples if t0 - 0.25 <= t <= t1 + 0.25]
+        if not win:
+            win = [f for (_, f) in self.samples]
+        if not win:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"],
+                    "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(f[1]) for f in win if num(f[1]) is not None]
+        smax = [num(f[2]) for f in win if num(f[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for f in win for i in range(4) if f[5 + i].lower().startswith("active")})
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": reasons, "samples": len(win),
+                "power_w_max": max((num(f[3]) or 0.0) for f in win)}
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            j = json.load(f)
+        return float(j["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "tree_speculative_verification_attention_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload):
+    """DRAM bytes per attention launch from the committed ncu summary, if it
+    was taken on the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        j = json.load(f)
+    e = j.get(workload)
+    if not e or e.get("source_hash") != kernel_source_hash():
+        return None
+    return float(e["dram_bytes_per_launch"])
+
+
+# --------------------------------------------------------------------------- CPU oracle
+
+
+def oracle_step_time(spec, trees, att, gi, si, budget_s, heads_sample=None):
+    """Times the oracle on a bounded sample of one step and extrapolates to the
+    whole step.  Returns (seconds per full step, cores, sample description)."""
+    import oracle
+    Hkv = spec.Hkv
+    G = spec.Hq // Hkv
+    kv_heads = list(range(Hkv)) if heads_sample is None else list(range(min(Hkv, heads_sample)))
+    qh = [g * G + r for g in kv_heads for r in range(G)]
+    q = att.q[:, qh].float().numpy()
+    k = att.k_cache[:, :, kv_heads].float().numpy()
+    v = att.v_cache[:, :, kv_heads].float().numpy()
+    reps, t_att, t_ver = 0, 0.0, 0.0
+    t_begin = time.perf_counter()
+    while True:
+        t0 = time.perf_counter()
+        oracle.tree_attention(q, k, v, trees.prefix_len, trees.node_offsets, trees.parent)
+        t1 = time.perf_counter()
+        if gi is not None:
+            oracle.verify_greedy(gi.logits, gi.tokens, trees.parent, trees.node_offsets)
+        if si is not None:
+            oracle.verify_stochastic(si.llm_logits, si.ssm_probs, si.tokens, trees.parent,
+                                     trees.node_offsets, si.u_accept, si.u_sample)
+        t2 = time.perf_counter()
+        t_att += t1 - t0
+        t_ver += t2 - t1
+        reps += 1
+        if time.perf_counter() - t_begin >= budget_s:
+            break
+    scale = Hkv / len(kv_heads)
+    per_step = (t_att * scale + t_ver) / reps
+    sample = ("%d repetition(s) of: tree attention over %d of %d KV heads (x%.0f to the full layer) + "
+              "the full verification" % (reps, len(kv_heads), Hkv, scale))
+    return per_step, oracle.num_threads(), sample
+
+
+def choose_heads_sample(spec, trees):
+    """KV heads whose oracle attention takes about 0.5 s at ~1 GFLOP/s per core."""
+    sizes = np.diff(trees.node_offsets)
+    flops_per_head = 4.0 * spec.D * float(((trees.prefix_len + sizes) * sizes).sum()) * (spec.Hq // spec.Hkv)
+    import oracle
+    budget = 0.5 * 1e9 * max(1, oracle.num_threads())
+    return max(1, min(spec.Hkv, int(budget // max(flops_per_head, 1.0))))
+
+
+def run_reference(args, spec):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    trees, att, gi, si = workload_inputs(spec)
+    n_nodes = int(trees.node_offsets[-1])
+    heads = choose_heads_sample(spec, trees)
+    per_step, cores, sample = oracle_step_time(spec, trees, att, gi, si, 0.0, heads)  # warm
+    for _ in range(max(0, args.warmup - 1)):
+        oracle_step_time(spec, trees, att, gi, si, 0.0, heads)
+    total = 0.0
+    for _ in range(args.steps):
+        s, cores, sample = oracle_step_time(spec, trees, att, gi, si, 0.0, heads)
+        total += s
+    ms = 1e3 * total / args.steps
+    value = n_nodes / (total / args.steps)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_of(spec, {"reference": "CPU fp64 oracle (the pages ship no code)"}),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": "per step: " + sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------- GPU
+
+
+def run_ours(args, spec):
+    import torch
+    import torch.distributed as dist
+
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import tree_speculative_verification_attention_gb300 as tsv
+
+    trees, att, gi, si = workload_inputs(spec)
+    B, N = spec.B, int(trees.node_offsets[-1])
+    stream = torch.cuda.Stream(dev)
+    torch.cuda.set_stream(stream)
+
+    def to_dev(x):
+        t = x if isinstance(x, torch.Tensor) else torch.as_tensor(np.ascontiguousarray(x))
+        return t.to(dev)
+
+    base = {"q": to_dev(att.q), "k": to_dev(att.k_cache), "v": to_dev(att.v_cache),
+            "parent": to_dev(trees.parent), "offs": to_dev(trees.node_offsets),
+            "plen": to_dev(trees.prefix_len)}
+    if gi is not None:
+        base.update(logits=to_dev(gi.logits), gtok=to_dev(gi.tokens))
+    if si is not None:
+        base.update(llm=to_dev(si.llm_logits), ssm=to_dev(si.ssm_probs), stok=to_dev(si.tokens),
+                    ua=to_dev(si.u_accept), us=to_dev(si.u_sample))
+    per_copy = sum(t.numel() * t.element_size() for t in base.values())
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    R = int(min(64, max(1, math.ceil(4 * l2 / per_copy))))
+    copies = [base] + [{k: t.clone() for k, t in base.items()} for _ in range(R - 1)]
+
+    h = tsv.handle(local)
+    ws_attn = tsv.tsv_tree_attention_workspace_size(h, tsv.TSV_BF16 if spec.dtype == "bf16" else tsv.TSV_F32,
+                                                    B, trees.prefix_len, trees.node_offsets, spec.Hq,
+                                                    spec.Hkv, spec.D, True)
+    ws_g = tsv.tsv_tree_verify_greedy_workspace_size(h, B, N, spec.V)
+    ws_s = tsv.tsv_tree_verify_stochastic_workspace_size(h, B, N, spec.V)
+    ws_bytes = max(ws_attn, 1) + max(ws_g, 1) + max(ws_s, 1) + 3 * 256
+
+    def make_state(c):
+        st = {"anc": torch.empty((N, tsv.TSV_ANC_WORDS), dtype=torch.int32, device=dev),
+              "depth": torch.empty(N, dtype=torch.int32, device=dev),
+              "status": torch.zeros(B, dtype=torch.int32, device=dev),
+              "out": torch.empty_like(c["q"]),
+              "ws": torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)}
+        st["ws_attn"] = st["ws"][:max(ws_attn, 1)]
+        off = (max(ws_attn, 1) + 255) // 256 * 256
+        st["ws_g"] = st["ws"][off:off + max(ws_g, 1)]
+        off += (max(ws_g, 1) + 255) // 256 * 256
+        st["ws_s"] = st["ws"][off:off + max(ws_s, 1)]
+        mk = lambda: {k: torch.empty(n, dtype=torch.int32, device=dev) for k, n in
+                      (("path", N), ("accept_len", B), ("bonus", B), ("n_tried", B), ("status", B))}
+        st["g"], st["s"] = mk(), mk()
+        return st
+
+    def attention(c, st):
+        tsv.tree_attention(c["q"], c["k"], c["v"], trees.prefix_len, trees.node_offsets, c["plen"],
+                           c["offs"], parent=c["parent"], anc=st["anc"], out=st["out"],
+                           workspace=st["ws_attn"], status=st["status"])
+
+    def step(c, st):
+        tsv.tsv_tree_prepare(h, c["parent"], c["offs"], B, st["anc"], st["depth"], st["status"])
+        attention(c, st)
+        if gi is not None:
+            tsv.tree_verify_greedy(c["logits"], c["gtok"], c["parent"], c["offs"], workspace=st["ws_g"],
+                                   out=st["g"])
+        if si is not None:
+            tsv.tree_verify_stochastic(c["llm"], c["ssm"], c["stok"], c["parent"], c["offs"], c["ua"],
+                                       c["us"], workspace=st["ws_s"], out=st["s"])
+
+    states = [make_state(c) for c in copies]
+    # Eager run once (also checks statuses), then capture one graph per input copy.
+    for c, st in zip(copies, states):
+        step(c, st)
+    torch.cuda.synchronize()
+    assert (states[0]["status"].cpu() == 0).all()
+    graphs, attn_graphs = [], []
+    for c, st in zip(copies, states):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            step(c, st)
+        graphs.append(g)
+        ga = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(ga, stream=stream):
+            attention(c, st)
+        attn_graphs.append(ga)
+    torch.cuda.synchronize()
+    # Kernels per step: prepare, attention (+ the split merge when the plan cuts
+    # requests into chunks, i.e. when the attention needs workspace), two per
+    # verification; checked against the captured graph when torch exposes it.
+    attn_kernels = 1 + (1 if ws_attn > 0 else 0)
+    kernels_per_step = 1 + attn_kernels + (2 if gi is not None else 0) + (2 if si is not None else 0)
+    counted = graph_kernel_count(graphs[0])
+    if counted is not None:
+        assert counted == kernels_per_step, (counted, kernels_per_step)
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    for i in range(args.warmup):
+        graphs[i % R].replay()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    # ---------------------------------------------------------------- timed region
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_wall0 = time.time()
+    e0.record(stream)
+    for i in range(args.steps):
+        graphs[i % R].replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    if world > 1:
+        dist.barrier()
+    ms_total = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([ms_total], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / args.steps
+    value = world * N / (ms_step * 1e-3)
+
+    # ---------------------------------------------------------------- attention kernel, per launch
+    reps = max(R, min(20000, args.steps))
+    torch.cuda._sleep(int(2e6))
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
+    ev[0].record(stream)
+    for i in range(reps):
+        attn_graphs[i % R].replay()
+        ev[i + 1].record(stream)
+    torch.cuda.synchronize()
+    durs = np.array([ev[i].elapsed_time(ev[i + 1]) for i in range(reps)])
+    attn_ms = float(durs.mean())
+    sampler.stop()
+    clocks = sampler.summary(t_wall0, t_wall1)
+
+    # ---------------------------------------------------------------- end to end
+    e2e = measure_e2e(args, spec, trees, att, gi, si, h, tsv, dev, stream, ws_attn, ws_g, ws_s)
+
+    # ---------------------------------------------------------------- roofline
+    peak, peak_kind = measured_peaks()
+    abytes = attention_bytes(spec, trees)
+    achieved = abytes / (attn_ms * 1e-3) / 1e9
+    traffic = recorded_traffic(spec.name)
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "traffic": traffic,
+                "kernel": "tree_attn_tc_kernel" + (" + attn_combine_kernel" if attn_kernels > 1 else ""),
+                "launch_ms": attn_ms, "algorithmic_bytes": abytes, "peak_kind": peak_kind + " hbm_gbs"}
+    step_bytes = abytes + verify_bytes(spec, trees)
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": spec.dtype, "data": "synthetic",
+            "config": config_of(spec, {"l2": "rotating %d input copies (%.0f MB > 4x L2)" % (R, R * per_copy / 1e6),
+                                       "graph": "one CUDA graph per step", "parallelism": "replicas"}),
+            "roofline": roofline,
+            "step_hbm_gbs": step_bytes / (ms_step * 1e-3) / 1e9,
+            "step_roofline_frac": step_bytes / (ms_step * 1e-3) / 1e9 / peak,
+            "e2e": e2e, "gpu_launches": kernels_per_step * args.steps, "clocks": clocks}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        per_step, cores, sample = oracle_step_time(spec, trees, att, gi, si, args.cpu_seconds,
+                                                   choose_heads_sample(spec, trees))
+        line["cpu_baseline"] = {"value": N / per_step, "unit": UNIT, "cores": cores, "kind": "oracle",
+                                "sample": sample}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def graph_kernel_count(g):
+    """Kernel nodes in a captured torch CUDA graph."""
+    try:
+        from cuda.bindings import runtime as cudart
+        raw = g.raw_cuda_graph() if hasattr(g, "raw_cuda_graph") else None
+        if raw is None:
+            return None
+        err, _, n = cudart.cudaGraphGetNodes(raw, 0)
+        err, nodes, n = cudart.cudaGraphGetNodes(raw, n)
+        count = 0
+        for nd in nodes:
+            err, t = cudart.cudaGraphNodeGetType(nd)
+            if t == cudart.cudaGraphNodeType.cudaGraphNodeTypeKernel:
+                count += 1
+        return count
+    except Exception:
+        return None
+
+
+def measure_e2e(args, spec, trees, att, gi, si, h, tsv, dev, stream, ws_attn, ws_g, ws_s):
+    """Inputs copied from pinned host memory and results read back every step."""
+    import torch
+    B, N = spec.B, int(trees.node_offsets[-1])
+    host = {"q": att.q, "k": att.k_cache, "v": att.v_cache, "parent": torch.from_numpy(trees.parent),
+            "offs": torch.from_numpy(trees.node_offsets), "plen": torch.from_numpy(trees.prefix_len)}
+    if gi is not None:
+        host.update(logits=torch.from_numpy(gi.logits), gtok=torch.from_numpy(gi.tokens))
+    if si is not None:
+        host.update(llm=torch.from_numpy(si.llm_logits), ssm=torch.from_numpy(si.ssm_probs),
+                    stok=torch.from_numpy(si.tokens), ua=torch.from_numpy(si.u_accept),
+                    us=torch.from_numpy(si.u_sample))
+    host = {k: t.contiguous().pin_memory() for k, t in host.items()}
+    d = {k: torch.empty_like(t, device=dev) for k, t in host.items()}
+    anc = torch.empty((N, tsv.TSV_ANC_WORDS), dtype=torch.int32, device=dev)
+    status = torch.zeros(B, dtype=torch.int32, device=dev)
+    out = torch.empty_like(d["q"])
+    wsa = torch.zeros(max(ws_attn, 1), dtype=torch.uint8, device=dev)
+    wsg = torch.zeros(max(ws_g, 1), dtype=torch.uint8, device=dev)
+    wss = torch.zeros(max(ws_s, 1), dtype=torch.uint8, device=dev)
+    res = {k: torch.empty(n, dtype=torch.int32, device=dev) for k, n in
+           (("path", N), ("accept_len", B), ("bonus", B), ("n_tried", B), ("status", B))}
+    res2 = {k: torch.empty_like(t) for k, t in res.items()}
+    out_h = torch.empty_like(out, device="cpu").pin_memory()
+    res_h = {k: torch.empty_like(t, device="cpu").pin_memory() for k, t in res.items()}
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_h.numel() * out_h.element_size()
+    if gi is not None:
+        d2h += sum(res_h[k].numel() * 4 for k in ("path", "accept_len", "bonus"))
+    if si is not None:
+        d2h += sum(res_h[k].numel() * 4 for k in ("path", "accept_len", "bonus"))
+
+    def step():
+        for k in host:
+            d[k].copy_(host[k], non_blocking=True)
+        tsv.tsv_tree_prepare(h, d["parent"], d["offs"], B, anc, None, status)
+        tsv.tree_attention(d["q"], d["k"], d["v"], trees.prefix_len, trees.node_offsets, d["plen"], d["offs"],
+                           parent=d["parent"], anc=anc, out=out, workspace=wsa, status=status)
+        out_h.copy_(out, non_blocking=True)
+        if gi is not None:
+            tsv.tree_verify_greedy(d["logits"], d["gtok"], d["parent"], d["offs"], workspace=wsg, out=res)
+            for k in ("path", "accept_len", "bonus"):
+                res_h[k].copy_(res[k], non_blocking=True)
+        if si is not None:
+            tsv.tree_verify_stochastic(d["llm"], d["ssm"], d["stok"], d["parent"], d["offs"], d["ua"], d["us"],
+                                       workspace=wss, out=res2)
+            for k in ("path", "accept_len", "bonus"):
+                res_h[k].copy_(res2[k], non_blocking=True)
+
+    step()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        step()
+    steps = max(20, min(2000, args.steps // 10))
+    for _ in range(5):
+        g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    return {"value": N / (ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": ms, "steps": steps, "api": "C ABI via the ctypes binding, pinned host buffers"}
+
+
+def main():
+    args = parse_args()
+    import workloads as W
+    if args.workload not in W.SPECS:
+        raise SystemExit("unknown workload %s (known: %s)" % (args.workload, ", ".join(W.SPECS)))
+    spec = W.SPECS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, spec)
+    else:
+        run_ours(args, spec)
+
+
+if __name__ == "__main__":
+    main()

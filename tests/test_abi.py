@@ -1,0 +1,81 @@
+"""The C-ABI library builds, loads without a GPU and exports every entry point
+that include/tsv.h declares; host-side argument checks need no device."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "tsv.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*(tsv_[a-z_0-9]+)\s*\(", text, re.M)
+    return sorted(set(names))
+
+
+def _build_module():
+    import importlib.util
+    path = os.path.join(ROOT, "tree_speculative_verification_attention_gb300", "build.py")
+    spec = importlib.util.spec_from_file_location("tsv_build", path)
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return ctypes.CDLL(_build_module().build())
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("tsv_tree_prepare", "tsv_tree_attention", "tsv_tree_verify_greedy",
+              "tsv_tree_verify_stochastic", "tsv_create", "tsv_destroy"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    out = subprocess.run(["nm", "-D", "--defined-only", _build_module().LIB], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\bT (tsv_[a-z_0-9]+)$", out, re.M))
+    assert set(declared_functions()) <= exported
+
+
+def test_binding_mirrors_the_header(lib):
+    import tree_speculative_verification_attention_gb300 as tsv
+    assert set(tsv.EXPORTED) == set(declared_functions())
+    for name in tsv.EXPORTED:
+        if name != "tsv_status_string":
+            assert callable(getattr(tsv, name))
+
+
+def test_status_strings(lib):
+    lib.tsv_status_string.restype = ctypes.c_char_p
+    assert lib.tsv_status_string(0) == b"ok"
+    assert b"tree" in lib.tsv_status_string(2)
+    assert lib.tsv_status_string(99) == b"unknown status"
+    assert lib.tsv_version() == 100
+
+
+def test_null_handle_and_bad_arguments_are_rejected_on_the_host(lib):
+    assert lib.tsv_destroy(None) == 1
+    assert lib.tsv_tree_prepare(None, None, None, 1, None, None, None, None) == 1
+    size = ctypes.c_size_t()
+    assert lib.tsv_tree_verify_greedy_workspace_size(None, 1, 1, ctypes.c_int64(10), ctypes.byref(size)) == 1
+    h = ctypes.c_void_p()
+    assert lib.tsv_create(None, 0) == 1
+
+
+def test_create_without_a_device_reports_cuda_error(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a device is present")
+    h = ctypes.c_void_p()
+    assert lib.tsv_create(ctypes.byref(h), 0) == 4
+    assert not h.value

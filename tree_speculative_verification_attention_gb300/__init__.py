@@ -1,0 +1,292 @@
+"""Python binding of libtsv — token-tree speculative verification on GB300.
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels of ``libtsv.so`` (built in-tree for sm_103a by ``build.py``).  Importing
+this package fails loudly when the library has not been built; there is no
+fallback implementation.  PyTorch supplies device memory and the current
+stream.
+
+Two layers:
+  * ``tsv_*`` functions mirror the C ABI of ``include/tsv.h`` one to one
+    (tensors are passed by their data pointers, ``None`` is NULL, host arrays
+    are int32 numpy arrays);
+  * ``tree_prepare``, ``tree_attention``, ``tree_verify_greedy`` and
+    ``tree_verify_stochastic`` allocate outputs and workspace with torch and
+    call the mirror functions.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libtsv.so")
+
+TSV_OK, TSV_ERR_INVALID_ARG, TSV_ERR_BAD_TREE, TSV_ERR_UNSUPPORTED, TSV_ERR_CUDA, TSV_ERR_TIMEOUT = range(6)
+TSV_F32, TSV_BF16 = 0, 1
+TSV_ATTN_DEFAULT, TSV_ATTN_SIMT = 0, 1
+TSV_MAX_NODES, TSV_MAX_BATCH, TSV_ANC_WORDS = 256, 128, 8
+
+EXPORTED = (
+    "tsv_status_string", "tsv_version", "tsv_create", "tsv_destroy", "tsv_tree_prepare",
+    "tsv_tree_attention_workspace_size", "tsv_tree_attention",
+    "tsv_tree_verify_greedy_workspace_size", "tsv_tree_verify_greedy",
+    "tsv_tree_verify_stochastic_workspace_size", "tsv_tree_verify_stochastic",
+)
+
+
+class TSVError(RuntimeError):
+    def __init__(self, code, where):
+        super().__init__("%s: %s (status %d)" % (where, status_string(code), code))
+        self.code = code
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            "libtsv.so is not built: run `python tree_speculative_verification_attention_gb300/build.py`"
+            " (or __graft_entry__.build()) first")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, i32, i64, u32, f32, sz = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_uint32,
+                                  ctypes.c_float, ctypes.c_size_t)
+    i32p = ctypes.POINTER(ctypes.c_int32)
+    szp = ctypes.POINTER(ctypes.c_size_t)
+    sig = {
+        "tsv_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+        "tsv_version": (ctypes.c_int, []),
+        "tsv_create": (ctypes.c_int, [ctypes.POINTER(vp), ctypes.c_int]),
+        "tsv_destroy": (ctypes.c_int, [vp]),
+        "tsv_tree_prepare": (ctypes.c_int, [vp, vp, vp, i32, vp, vp, vp, vp]),
+        "tsv_tree_attention_workspace_size": (
+            ctypes.c_int, [vp, ctypes.c_int, i32, i32p, i32p, i32, i32, i32, ctypes.c_int, u32, szp]),
+        "tsv_tree_attention": (
+            ctypes.c_int, [vp, ctypes.c_int, vp, vp, vp, i64, i64, i64, vp, i32p, i32p, vp, vp, vp, vp,
+                           i32, i32, i32, i32, f32, vp, sz, vp, u32, vp]),
+        "tsv_tree_verify_greedy_workspace_size": (ctypes.c_int, [vp, i32, i32, i64, szp]),
+        "tsv_tree_verify_greedy": (
+            ctypes.c_int, [vp, vp, i64, vp, vp, vp, i32, i32, vp, vp, vp, vp, sz, vp, vp]),
+        "tsv_tree_verify_stochastic_workspace_size": (ctypes.c_int, [vp, i32, i32, i64, szp]),
+        "tsv_tree_verify_stochastic": (
+            ctypes.c_int, [vp, vp, vp, i64, vp, vp, vp, vp, vp, f32, i32, i32, vp, vp, vp, vp, vp, sz,
+                           vp, vp]),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(lib, name)
+        f.restype, f.argtypes = res, args
+    return lib
+
+
+_lib = _load()
+
+
+def status_string(code: int) -> str:
+    return _lib.tsv_status_string(int(code)).decode()
+
+
+def _check(code, where):
+    if code != TSV_OK:
+        raise TSVError(code, where)
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _host_i32(a):
+    a = np.ascontiguousarray(np.asarray(a, dtype=np.int32))
+    return a, a.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+
+
+def _dtype_code(dt):
+    if dt == torch.bfloat16:
+        return TSV_BF16
+    if dt == torch.float32:
+        return TSV_F32
+    raise TypeError("tree attention takes bfloat16 or float32 tensors, got %s" % dt)
+
+
+# ----------------------------------------------------------------- C ABI mirror
+
+
+def tsv_version() -> int:
+    return _lib.tsv_version()
+
+
+def tsv_create(device: int = 0):
+    h = ctypes.c_void_p()
+    _check(_lib.tsv_create(ctypes.byref(h), int(device)), "tsv_create")
+    return h
+
+
+def tsv_destroy(h):
+    _check(_lib.tsv_destroy(h), "tsv_destroy")
+
+
+def tsv_tree_prepare(h, parent, node_offsets, B, anc, depth, status, stream=None):
+    _check(_lib.tsv_tree_prepare(h, _ptr(parent), _ptr(node_offsets), int(B), _ptr(anc), _ptr(depth),
+                                 _ptr(status), _stream(stream)), "tsv_tree_prepare")
+
+
+def tsv_tree_attention_workspace_size(h, dtype_code, B, prefix_len_host, node_offsets_host, Hq, Hkv, D,
+                                      anc_given, flags=TSV_ATTN_DEFAULT) -> int:
+    pl, plp = _host_i32(prefix_len_host)
+    no, nop = _host_i32(node_offsets_host)
+    out = ctypes.c_size_t()
+    _check(_lib.tsv_tree_attention_workspace_size(h, int(dtype_code), int(B), plp, nop, int(Hq), int(Hkv),
+                                                  int(D), int(bool(anc_given)), int(flags),
+                                                  ctypes.byref(out)),
+           "tsv_tree_attention_workspace_size")
+    return out.value
+
+
+def tsv_tree_attention(h, dtype_code, q, k_cache, v_cache, kv_stride_b, kv_stride_l, kv_stride_h, out,
+                       prefix_len_host, node_offsets_host, prefix_len, node_offsets, parent, anc, B, Hq,
+                       Hkv, D, scale, workspace, workspace_bytes, status, flags=TSV_ATTN_DEFAULT,
+                       stream=None):
+    pl, plp = _host_i32(prefix_len_host)
+    no, nop = _host_i32(node_offsets_host)
+    _check(_lib.tsv_tree_attention(
+        h, int(dtype_code), _ptr(q), _ptr(k_cache), _ptr(v_cache), int(kv_stride_b), int(kv_stride_l),
+        int(kv_stride_h), _ptr(out), plp, nop, _ptr(prefix_len), _ptr(node_offsets), _ptr(parent),
+        _ptr(anc), int(B), int(Hq), int(Hkv), int(D), float(scale), _ptr(workspace),
+        int(workspace_bytes), _ptr(status), int(flags), _stream(stream)), "tsv_tree_attention")
+
+
+def tsv_tree_verify_greedy_workspace_size(h, B, N, V) -> int:
+    out = ctypes.c_size_t()
+    _check(_lib.tsv_tree_verify_greedy_workspace_size(h, int(B), int(N), int(V), ctypes.byref(out)),
+           "tsv_tree_verify_greedy_workspace_size")
+    return out.value
+
+
+def tsv_tree_verify_greedy(h, logits, V, tree_tokens, parent, node_offsets, B, N, path, accept_len, bonus,
+                           workspace, workspace_bytes, status, stream=None):
+    _check(_lib.tsv_tree_verify_greedy(
+        h, _ptr(logits), int(V), _ptr(tree_tokens), _ptr(parent), _ptr(node_offsets), int(B), int(N),
+        _ptr(path), _ptr(accept_len), _ptr(bonus), _ptr(workspace), int(workspace_bytes), _ptr(status),
+        _stream(stream)), "tsv_tree_verify_greedy")
+
+
+def tsv_tree_verify_stochastic_workspace_size(h, B, N, V) -> int:
+    out = ctypes.c_size_t()
+    _check(_lib.tsv_tree_verify_stochastic_workspace_size(h, int(B), int(N), int(V), ctypes.byref(out)),
+           "tsv_tree_verify_stochastic_workspace_size")
+    return out.value
+
+
+def tsv_tree_verify_stochastic(h, llm_logits, ssm_probs, V, tree_tokens, parent, node_offsets, u_accept,
+                               u_sample, temperature, B, N, path, accept_len, bonus, n_tried, workspace,
+                               workspace_bytes, status, stream=None):
+    _check(_lib.tsv_tree_verify_stochastic(
+        h, _ptr(llm_logits), _ptr(ssm_probs), int(V), _ptr(tree_tokens), _ptr(parent), _ptr(node_offsets),
+        _ptr(u_accept), _ptr(u_sample), float(temperature), int(B), int(N), _ptr(path), _ptr(accept_len),
+        _ptr(bonus), _ptr(n_tried), _ptr(workspace), int(workspace_bytes), _ptr(status), _stream(stream)),
+        "tsv_tree_verify_stochastic")
+
+
+# ----------------------------------------------------------------- convenience layer
+
+_HANDLES = {}
+
+
+def handle(device=None):
+    """A library handle for `device` (default: torch's current device), created once."""
+    dev = torch.cuda.current_device() if device is None else int(device)
+    if dev not in _HANDLES:
+        _HANDLES[dev] = tsv_create(dev)
+    return _HANDLES[dev]
+
+
+def _workspace(nbytes, device):
+    return torch.empty(max(int(nbytes), 1), dtype=torch.uint8, device=device)
+
+
+def tree_prepare(parent, node_offsets, stream=None):
+    """Ancestor bitsets (uint32 [N, 8] as int32), depths and per-request status."""
+    N = parent.shape[0]
+    B = node_offsets.shape[0] - 1
+    dev = parent.device
+    anc = torch.empty((N, TSV_ANC_WORDS), dtype=torch.int32, device=dev)
+    depth = torch.empty(N, dtype=torch.int32, device=dev)
+    status = torch.empty(B, dtype=torch.int32, device=dev)
+    tsv_tree_prepare(handle(dev.index), parent, node_offsets, B, anc, depth, status, stream)
+    return anc, depth, status
+
+
+def tree_attention(q, k_cache, v_cache, prefix_len_host, node_offsets_host, prefix_len, node_offsets,
+                   parent=None, anc=None, scale=0.0, flags=TSV_ATTN_DEFAULT, out=None, workspace=None,
+                   status=None, stream=None):
+    """Tree attention: q [N, Hq, D]; k_cache / v_cache [B, Lcap, Hkv, D] (or any view
+    with D contiguous); returns out [N, Hq, D] (same dtype as q) and status [B]."""
+    N, Hq, D = q.shape
+    B = len(prefix_len_host)
+    Hkv = k_cache.shape[2]
+    assert k_cache.stride() == v_cache.stride() and k_cache.stride(3) == 1
+    sb, sl, sh = k_cache.stride(0), k_cache.stride(1), k_cache.stride(2)
+    dev = q.device
+    h = handle(dev.index)
+    code = _dtype_code(q.dtype)
+    if out is None:
+        out = torch.empty_like(q)
+    if status is None:
+        status = torch.zeros(B, dtype=torch.int32, device=dev)
+    need = tsv_tree_attention_workspace_size(h, code, B, prefix_len_host, node_offsets_host, Hq, Hkv, D,
+                                             anc is not None, flags)
+    if workspace is None:
+        workspace = _workspace(need, dev)
+    tsv_tree_attention(h, code, q, k_cache, v_cache, sb, sl, sh, out, prefix_len_host, node_offsets_host,
+                       prefix_len, node_offsets, parent, anc, B, Hq, Hkv, D, scale, workspace,
+                       workspace.numel(), status, flags, stream)
+    return out, status
+
+
+def tree_verify_greedy(logits, tree_tokens, parent, node_offsets, workspace=None, stream=None, out=None):
+    """Greedy verification; returns dict(path [N], accept_len [B], bonus [B], status [B])."""
+    N, V = logits.shape
+    B = node_offsets.shape[0] - 1
+    dev = logits.device
+    h = handle(dev.index)
+    o = out or dict(path=torch.empty(N, dtype=torch.int32, device=dev),
+                    accept_len=torch.empty(B, dtype=torch.int32, device=dev),
+                    bonus=torch.empty(B, dtype=torch.int32, device=dev),
+                    status=torch.empty(B, dtype=torch.int32, device=dev))
+    if workspace is None:
+        workspace = _workspace(tsv_tree_verify_greedy_workspace_size(h, B, N, V), dev)
+    tsv_tree_verify_greedy(h, logits, V, tree_tokens, parent, node_offsets, B, N, o["path"],
+                           o["accept_len"], o["bonus"], workspace, workspace.numel(), o["status"], stream)
+    return o
+
+
+def tree_verify_stochastic(llm_logits, ssm_probs, tree_tokens, parent, node_offsets, u_accept, u_sample,
+                           temperature=1.0, workspace=None, stream=None, out=None):
+    """Multi-step speculative sampling; returns dict(path, accept_len, bonus, n_tried, status)."""
+    N, V = llm_logits.shape
+    B = node_offsets.shape[0] - 1
+    dev = llm_logits.device
+    h = handle(dev.index)
+    o = out or dict(path=torch.empty(N, dtype=torch.int32, device=dev),
+                    accept_len=torch.empty(B, dtype=torch.int32, device=dev),
+                    bonus=torch.empty(B, dtype=torch.int32, device=dev),
+                    n_tried=torch.empty(B, dtype=torch.int32, device=dev),
+                    status=torch.empty(B, dtype=torch.int32, device=dev))
+    if workspace is None:
+        workspace = _workspace(tsv_tree_verify_stochastic_workspace_size(h, B, N, V), dev)
+    tsv_tree_verify_stochastic(h, llm_logits, ssm_probs, V, tree_tokens, parent, node_offsets, u_accept,
+                               u_sample, temperature, B, N, o["path"], o["accept_len"], o["bonus"],
+                               o["n_tried"], workspace, workspace.numel(), o["status"], stream)
+    return o

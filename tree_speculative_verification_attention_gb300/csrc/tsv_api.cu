@@ -1,0 +1,371 @@
+// tsv_api.cu — the C ABI declared in include/tsv.h: argument checks, work
+// planning, tensor-map encoding and kernel launches.  No allocation happens
+// here: every buffer, scratch included, belongs to the caller.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <string.h>
+
+#include <algorithm>
+#include <new>
+
+#include "tsv_internal.h"
+
+using namespace tsv;
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+struct tsv_handle_s {
+  int device;
+  int num_sms;
+  EncodeTiledFn encode;
+  bool tc_attr_set[2];  // D = 64, 128
+};
+
+namespace {
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+inline size_t round256(size_t x) { return (x + 255) & ~(size_t)255; }
+inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Checks the host copies of the batch layout.
+tsv_status check_batch(int32_t B, const int32_t* prefix_len, const int32_t* node_offsets) {
+  if (B < 1 || B > TSV_MAX_BATCH || !prefix_len || !node_offsets) return TSV_ERR_INVALID_ARG;
+  if (node_offsets[0] != 0) return TSV_ERR_INVALID_ARG;
+  for (int b = 0; b < B; ++b) {
+    const int64_t n = (int64_t)node_offsets[b + 1] - node_offsets[b];
+    if (n < 0 || prefix_len[b] < 0) return TSV_ERR_INVALID_ARG;
+    if (n > TSV_MAX_NODES) return TSV_ERR_UNSUPPORTED;
+    if ((int64_t)prefix_len[b] + n > INT32_MAX - 2 * kBN) return TSV_ERR_UNSUPPORTED;
+  }
+  return TSV_OK;
+}
+
+// Splits every request's keys into chunks of one common length (a multiple of
+// the 64-key block) so that the CTAs fill whole waves of SMs: the estimated
+// makespan is waves * (chunk + per-CTA overhead), minimised over the chunk
+// counts that cut the longest request into 1 .. 64 pieces.
+void build_plan(AttnPlan& p, int num_sms, int32_t B, const int32_t* prefix_len,
+                const int32_t* node_offsets, int32_t Hq, int32_t Hkv, int32_t D, float scale) {
+  memset(&p, 0, sizeof(p));
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.G = Hq / Hkv;
+  p.D = D;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  int64_t lmax = 1;
+  for (int b = 0; b < B; ++b) {
+    p.prefix[b] = prefix_len[b];
+    p.node_off[b] = node_offsets[b];
+    p.nodes[b] = node_offsets[b + 1] - node_offsets[b];
+    p.mtiles[b] = (int32_t)cdiv((int64_t)p.nodes[b] * p.G, kBM);
+    lmax = std::max<int64_t>(lmax, (int64_t)p.prefix[b] + p.nodes[b]);
+  }
+  const int64_t overhead = 2 * kBN;
+  int64_t best_cost = INT64_MAX, best_chunk = cdiv(lmax, kBN) * kBN;
+  for (int pieces = 1; pieces <= 64; ++pieces) {
+    const int64_t chunk = cdiv(cdiv(lmax, pieces), kBN) * kBN;
+    int64_t units = 0;
+    for (int b = 0; b < B; ++b)
+      units += (int64_t)Hkv * p.mtiles[b] * cdiv((int64_t)p.prefix[b] + p.nodes[b], chunk);
+    const int64_t waves = cdiv(units, num_sms);
+    const int64_t cost = waves * (chunk + overhead);
+    if (cost < best_cost || (cost == best_cost && chunk > best_chunk)) {
+      best_cost = cost;
+      best_chunk = chunk;
+    }
+    if (chunk == kBN) break;
+  }
+  p.chunk_keys = (int32_t)best_chunk;
+  int64_t units = 0, rows = 0;
+  for (int b = 0; b < B; ++b) {
+    const int64_t L = (int64_t)p.prefix[b] + p.nodes[b];
+    p.n_chunks[b] = p.mtiles[b] > 0 ? (int32_t)cdiv(L, best_chunk) : 0;
+    p.unit_start[b] = (int32_t)units;
+    units += (int64_t)Hkv * p.mtiles[b] * p.n_chunks[b];
+    if (p.n_chunks[b] > 1) {
+      p.part_row[b] = rows;
+      rows += (int64_t)Hkv * p.n_chunks[b] * p.nodes[b] * p.G;
+    } else {
+      p.part_row[b] = -1;
+    }
+  }
+  p.unit_start[B] = (int32_t)units;
+  p.n_units = (int32_t)units;
+  p.part_rows_total = rows;
+}
+
+struct AttnLayout {
+  size_t anc_off, part_o_off, part_lse_off, total;
+};
+
+AttnLayout attention_layout(const AttnPlan& p, int64_t N, bool anc_given, bool use_tc) {
+  AttnLayout a{};
+  size_t off = 0;
+  a.anc_off = off;
+  if (!anc_given) off += round256((size_t)N * TSV_ANC_WORDS * sizeof(uint32_t));
+  a.part_o_off = off;
+  if (use_tc) off += round256((size_t)p.part_rows_total * p.D * sizeof(float));
+  a.part_lse_off = off;
+  if (use_tc) off += round256((size_t)p.part_rows_total * sizeof(float));
+  a.total = off;
+  return a;
+}
+
+tsv_status cuda_status(cudaError_t e) { return e == cudaSuccess ? TSV_OK : TSV_ERR_CUDA; }
+
+tsv_status encode_kv_map(tsv_handle h, CUtensorMap* map, const void* base, int64_t sb, int64_t sl,
+                         int64_t sh, int32_t B, int64_t L, int32_t Hkv, int32_t D) {
+  const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)Hkv, (cuuint64_t)L, (cuuint64_t)B};
+  const cuuint64_t strides[3] = {(cuuint64_t)sh * 2, (cuuint64_t)sl * 2, (cuuint64_t)sb * 2};
+  const cuuint32_t box[4] = {64, 1, (cuuint32_t)kBN, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUresult r = h->encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base),
+                               dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? TSV_OK : TSV_ERR_INVALID_ARG;
+}
+
+bool attention_uses_tc(tsv_dtype dtype, uint32_t flags) {
+  return dtype == TSV_BF16 && !(flags & TSV_ATTN_SIMT);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* tsv_status_string(int status) {
+  switch (status) {
+    case TSV_OK: return "ok";
+    case TSV_ERR_INVALID_ARG: return "invalid argument";
+    case TSV_ERR_BAD_TREE: return "bad tree (parent array breaks the topological convention)";
+    case TSV_ERR_UNSUPPORTED: return "unsupported shape";
+    case TSV_ERR_CUDA: return "CUDA error";
+    case TSV_ERR_TIMEOUT: return "device-side wait timed out";
+    default: return "unknown status";
+  }
+}
+
+int tsv_version(void) { return 100; }
+
+tsv_status tsv_create(tsv_handle* out, int device) {
+  if (!out) return TSV_ERR_INVALID_ARG;
+  *out = nullptr;
+  int count = 0;
+  if (cudaGetDeviceCount(&count) != cudaSuccess || device < 0 || device >= count) {
+    cudaGetLastError();
+    return TSV_ERR_CUDA;
+  }
+  if (cudaSetDevice(device) != cudaSuccess) return TSV_ERR_CUDA;
+  int major = 0, minor = 0, sms = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
+    return TSV_ERR_CUDA;
+  if (major != 10 || minor != 3) return TSV_ERR_UNSUPPORTED;  // kernels are built for sm_103a
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                       &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || fn == nullptr)
+    return TSV_ERR_CUDA;
+  tsv_handle h = new (std::nothrow) tsv_handle_s;
+  if (!h) return TSV_ERR_CUDA;
+  h->device = device;
+  h->num_sms = sms;
+  h->encode = reinterpret_cast<EncodeTiledFn>(fn);
+  h->tc_attr_set[0] = h->tc_attr_set[1] = false;
+  *out = h;
+  return TSV_OK;
+}
+
+tsv_status tsv_destroy(tsv_handle h) {
+  if (!h) return TSV_ERR_INVALID_ARG;
+  delete h;
+  return TSV_OK;
+}
+
+tsv_status tsv_tree_prepare(tsv_handle h, const int32_t* parent_d, const int32_t* node_offsets_d,
+                            int32_t B, uint32_t* anc_d, int32_t* depth_d, int32_t* status_d,
+                            void* stream) {
+  if (!h || !parent_d || !node_offsets_d || !anc_d || !status_d) return TSV_ERR_INVALID_ARG;
+  if (B < 1 || B > TSV_MAX_BATCH) return TSV_ERR_INVALID_ARG;
+  return cuda_status(launch_tree_prepare(parent_d, node_offsets_d, B, anc_d, depth_d, status_d,
+                                         static_cast<cudaStream_t>(stream)));
+}
+
+tsv_status tsv_tree_attention_workspace_size(tsv_handle h, tsv_dtype dtype, int32_t B,
+                                             const int32_t* prefix_len_host,
+                                             const int32_t* node_offsets_host, int32_t Hq,
+                                             int32_t Hkv, int32_t D, int anc_given,
+                                             uint32_t flags, size_t* bytes) {
+  if (!h || !bytes) return TSV_ERR_INVALID_ARG;
+  if (dtype != TSV_F32 && dtype != TSV_BF16) return TSV_ERR_INVALID_ARG;
+  if (Hq < 1 || Hkv < 1 || Hq % Hkv) return TSV_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return TSV_ERR_UNSUPPORTED;
+  tsv_status st = check_batch(B, prefix_len_host, node_offsets_host);
+  if (st != TSV_OK) return st;
+  AttnPlan plan;
+  build_plan(plan, h->num_sms, B, prefix_len_host, node_offsets_host, Hq, Hkv, D, 1.f);
+  *bytes = attention_layout(plan, node_offsets_host[B], anc_given != 0,
+                            attention_uses_tc(dtype, flags)).total;
+  return TSV_OK;
+}
+
+tsv_status tsv_tree_attention(tsv_handle h, tsv_dtype dtype, const void* q_d, const void* k_cache_d,
+                              const void* v_cache_d, int64_t kv_stride_b, int64_t kv_stride_l,
+                              int64_t kv_stride_h, void* out_d, const int32_t* prefix_len_host,
+                              const int32_t* node_offsets_host, const int32_t* prefix_len_d,
+                              const int32_t* node_offsets_d, const int32_t* parent_d,
+                              const uint32_t* anc_d, int32_t B, int32_t Hq, int32_t Hkv, int32_t D,
+                              float scale, void* workspace_d, size_t workspace_bytes,
+                              int32_t* status_d, uint32_t flags, void* stream) {
+  if (!h || !q_d || !k_cache_d || !v_cache_d || !out_d || !prefix_len_d || !node_offsets_d ||
+      !status_d)
+    return TSV_ERR_INVALID_ARG;
+  if (dtype != TSV_F32 && dtype != TSV_BF16) return TSV_ERR_INVALID_ARG;
+  if (flags & ~TSV_ATTN_SIMT) return TSV_ERR_INVALID_ARG;
+  if (Hq < 1 || Hkv < 1 || Hq % Hkv) return TSV_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return TSV_ERR_UNSUPPORTED;
+  if (kv_stride_b < 0 || kv_stride_l < 0 || kv_stride_h < 0) return TSV_ERR_INVALID_ARG;
+  if (!(scale >= 0.f) || isinf(scale)) return TSV_ERR_INVALID_ARG;
+  if (!anc_d && !parent_d) return TSV_ERR_INVALID_ARG;
+  tsv_status st = check_batch(B, prefix_len_host, node_offsets_host);
+  if (st != TSV_OK) return st;
+  const int64_t N = node_offsets_host[B];
+  if (N * (int64_t)Hq > INT32_MAX) return TSV_ERR_UNSUPPORTED;
+  const bool use_tc = attention_uses_tc(dtype, flags);
+  if (use_tc) {
+    if (!aligned16(q_d) || !aligned16(out_d) || !aligned16(k_cache_d) || !aligned16(v_cache_d))
+      return TSV_ERR_INVALID_ARG;
+    if (kv_stride_b % 8 || kv_stride_l % 8 || kv_stride_h % 8) return TSV_ERR_INVALID_ARG;
+  }
+  if (scale == 0.f) scale = 1.f / sqrtf((float)D);
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+
+  AttnPlan plan;
+  build_plan(plan, h->num_sms, B, prefix_len_host, node_offsets_host, Hq, Hkv, D, scale);
+  const AttnLayout lay = attention_layout(plan, N, anc_d != nullptr, use_tc);
+  if (lay.total > 0 && (!workspace_d || workspace_bytes < lay.total)) return TSV_ERR_INVALID_ARG;
+  char* ws = static_cast<char*>(workspace_d);
+  if (N == 0) return TSV_OK;
+
+  const uint32_t* anc = anc_d;
+  if (!anc) {
+    uint32_t* a = reinterpret_cast<uint32_t*>(ws + lay.anc_off);
+    st = cuda_status(launch_tree_prepare(parent_d, node_offsets_d, B, a, nullptr, status_d, cs));
+    if (st != TSV_OK) return st;
+    anc = a;
+  }
+  if (!use_tc) {
+    return cuda_status(launch_attention_simt(dtype == TSV_BF16, q_d, k_cache_d, v_cache_d,
+                                             kv_stride_b, kv_stride_l, kv_stride_h, out_d,
+                                             prefix_len_d, node_offsets_d, anc, B, (int32_t)N, Hq,
+                                             Hkv, D, scale, cs));
+  }
+  const int di = D == 64 ? 0 : 1;
+  if (!h->tc_attr_set[di]) {
+    if (attention_tc_set_attributes(D) != cudaSuccess) return TSV_ERR_CUDA;
+    h->tc_attr_set[di] = true;
+  }
+  int64_t lmax = 1;
+  for (int b = 0; b < B; ++b) lmax = std::max<int64_t>(lmax, (int64_t)plan.prefix[b] + plan.nodes[b]);
+  CUtensorMap tmk, tmv;
+  st = encode_kv_map(h, &tmk, k_cache_d, kv_stride_b, kv_stride_l, kv_stride_h, B, lmax, Hkv, D);
+  if (st != TSV_OK) return st;
+  st = encode_kv_map(h, &tmv, v_cache_d, kv_stride_b, kv_stride_l, kv_stride_h, B, lmax, Hkv, D);
+  if (st != TSV_OK) return st;
+  float* part_o = reinterpret_cast<float*>(ws + lay.part_o_off);
+  float* part_lse = reinterpret_cast<float*>(ws + lay.part_lse_off);
+  st = cuda_status(launch_attention_tc(tmk, tmv, plan, q_d, anc, out_d, part_o, part_lse, status_d,
+                                       h->num_sms, cs));
+  if (st != TSV_OK) return st;
+  return cuda_status(launch_attention_combine(plan, part_o, part_lse, out_d, cs));
+}
+
+tsv_status tsv_tree_verify_greedy_workspace_size(tsv_handle h, int32_t B, int32_t N, int64_t V,
+                                                 size_t* bytes) {
+  if (!h || !bytes || B < 1 || B > TSV_MAX_BATCH || N < 0 || V < 1 || V > INT32_MAX)
+    return TSV_ERR_INVALID_ARG;
+  const int splits = greedy_splits(V, N, h->num_sms);
+  *bytes = 2 * round256((size_t)N * splits * 4);
+  return TSV_OK;
+}
+
+tsv_status tsv_tree_verify_greedy(tsv_handle h, const float* logits_d, int64_t V,
+                                  const int32_t* tree_tokens_d, const int32_t* parent_d,
+                                  const int32_t* node_offsets_d, int32_t B, int32_t N,
+                                  int32_t* path_d, int32_t* accept_len_d, int32_t* bonus_d,
+                                  void* workspace_d, size_t workspace_bytes, int32_t* status_d,
+                                  void* stream) {
+  if (!h || !tree_tokens_d || !parent_d || !node_offsets_d || !accept_len_d || !bonus_d ||
+      !status_d)
+    return TSV_ERR_INVALID_ARG;
+  if (B < 1 || B > TSV_MAX_BATCH || N < 0 || V < 1 || V > INT32_MAX) return TSV_ERR_INVALID_ARG;
+  if (N > 0 && (!logits_d || !path_d)) return TSV_ERR_INVALID_ARG;
+  const int splits = greedy_splits(V, N, h->num_sms);
+  const size_t part = round256((size_t)N * splits * 4);
+  if (N > 0 && (!workspace_d || workspace_bytes < 2 * part)) return TSV_ERR_INVALID_ARG;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  float* pv = reinterpret_cast<float*>(workspace_d);
+  int32_t* pi = reinterpret_cast<int32_t*>(static_cast<char*>(workspace_d) + part);
+  if (N > 0) {
+    tsv_status st = cuda_status(launch_argmax_partial(logits_d, V, N, splits, pv, pi, cs));
+    if (st != TSV_OK) return st;
+  }
+  return cuda_status(launch_greedy_walk(pv, pi, splits, tree_tokens_d, parent_d, node_offsets_d, B,
+                                        path_d, accept_len_d, bonus_d, status_d, cs));
+}
+
+tsv_status tsv_tree_verify_stochastic_workspace_size(tsv_handle h, int32_t B, int32_t N, int64_t V,
+                                                     size_t* bytes) {
+  if (!h || !bytes || B < 1 || B > TSV_MAX_BATCH || N < 0 || V < 1 || V > INT32_MAX)
+    return TSV_ERR_INVALID_ARG;
+  const int splits = stats_splits(V, N, h->num_sms);
+  *bytes = round256((size_t)N * splits * 4) + round256((size_t)N * splits * 8) +
+           round256((size_t)B * 2 * (size_t)V * 4);
+  return TSV_OK;
+}
+
+tsv_status tsv_tree_verify_stochastic(tsv_handle h, const float* llm_logits_d,
+                                      const float* ssm_probs_d, int64_t V,
+                                      const int32_t* tree_tokens_d, const int32_t* parent_d,
+                                      const int32_t* node_offsets_d, const float* u_accept_d,
+                                      const float* u_sample_d, float temperature, int32_t B,
+                                      int32_t N, int32_t* path_d, int32_t* accept_len_d,
+                                      int32_t* bonus_d, int32_t* n_tried_d, void* workspace_d,
+                                      size_t workspace_bytes, int32_t* status_d, void* stream) {
+  if (!h || !tree_tokens_d || !parent_d || !node_offsets_d || !accept_len_d || !bonus_d ||
+      !status_d)
+    return TSV_ERR_INVALID_ARG;
+  if (B < 1 || B > TSV_MAX_BATCH || N < 0 || V < 1 || V > INT32_MAX) return TSV_ERR_INVALID_ARG;
+  if (!(temperature > 0.f) || isinf(temperature)) return TSV_ERR_INVALID_ARG;
+  if (N > 0 && (!llm_logits_d || !ssm_probs_d || !u_accept_d || !u_sample_d || !path_d))
+    return TSV_ERR_INVALID_ARG;
+  const int splits = stats_splits(V, N, h->num_sms);
+  const size_t pm = round256((size_t)N * splits * 4), ps = round256((size_t)N * splits * 8);
+  const size_t need = pm + ps + round256((size_t)B * 2 * (size_t)V * 4);
+  if (!workspace_d || workspace_bytes < need) return TSV_ERR_INVALID_ARG;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace_d);
+  float* part_m = reinterpret_cast<float*>(ws);
+  double* part_s = reinterpret_cast<double*>(ws + pm);
+  float* resid = reinterpret_cast<float*>(ws + pm + ps);
+  const float inv_t = 1.0f / temperature;
+  if (N > 0) {
+    tsv_status st =
+        cuda_status(launch_row_stats(llm_logits_d, V, N, splits, inv_t, part_m, part_s, cs));
+    if (st != TSV_OK) return st;
+  }
+  return cuda_status(launch_mss_walk(llm_logits_d, ssm_probs_d, V, tree_tokens_d, parent_d,
+                                     node_offsets_d, u_accept_d, u_sample_d, inv_t, B, splits,
+                                     part_m, part_s, resid, path_d, accept_len_d, bonus_d,
+                                     n_tried_d, status_d, cs));
+}
+
+}  // extern "C"

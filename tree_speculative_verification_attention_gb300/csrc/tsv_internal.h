@@ -1,0 +1,91 @@
+// tsv_internal.h — declarations shared by the library's translation units
+// (launch wrappers and the attention work plan).  Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/tsv.h"
+
+namespace tsv {
+
+constexpr int kBM = 128;  // query rows (node x head-in-group) per attention CTA = TMEM lanes
+constexpr int kBN = 64;   // keys per pipeline block
+
+// How one tsv_tree_attention call is cut into CTAs.  Passed by value as a
+// kernel parameter (no host-to-device copy, so a launch can be captured).
+// A unit (CTA) is (request b, KV head g, chunk c, M-tile mt); inside request b
+// the unit index is ((g * n_chunks + c) * mtiles + mt), so the M-tiles of one
+// KV chunk run next to each other and share its rows through L2.
+struct AttnPlan {
+  int32_t B, Hq, Hkv, G, D;
+  int32_t n_units;
+  int32_t chunk_keys;  // keys per chunk (multiple of kBN), same for every request
+  float scale_log2;    // softmax scale * log2(e)
+  int32_t unit_start[TSV_MAX_BATCH + 1];
+  int32_t n_chunks[TSV_MAX_BATCH];
+  int32_t mtiles[TSV_MAX_BATCH];
+  int32_t prefix[TSV_MAX_BATCH];
+  int32_t nodes[TSV_MAX_BATCH];
+  int32_t node_off[TSV_MAX_BATCH];
+  int64_t part_row[TSV_MAX_BATCH];  // first partial row of request b, -1 when n_chunks == 1
+  int64_t part_rows_total;
+};
+
+struct Workspace {
+  char* base;
+  size_t size;
+  size_t used;
+  void* take(size_t bytes) {
+    size_t off = (used + 255) & ~(size_t)255;
+    if (off + bytes > size) return nullptr;
+    used = off + bytes;
+    return base + off;
+  }
+};
+
+// Launch wrappers (defined next to their kernels); return the launch error.
+cudaError_t launch_tree_prepare(const int32_t* parent, const int32_t* node_offsets, int32_t B,
+                                uint32_t* anc, int32_t* depth, int32_t* status, cudaStream_t st);
+
+cudaError_t launch_attention_tc(const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
+                                const AttnPlan& plan, const void* q, const uint32_t* anc,
+                                void* out, float* part_o, float* part_lse, int32_t* status,
+                                int num_sms, cudaStream_t st);
+cudaError_t attention_tc_set_attributes(int D);
+size_t attention_tc_smem_bytes(int D);
+
+cudaError_t launch_attention_simt(bool bf16, const void* q, const void* k, const void* v,
+                                  int64_t sb, int64_t sl, int64_t sh, void* out,
+                                  const int32_t* prefix_len, const int32_t* node_offsets,
+                                  const uint32_t* anc, int32_t B, int32_t N, int32_t Hq,
+                                  int32_t Hkv, int32_t D, float scale, cudaStream_t st);
+
+cudaError_t launch_attention_combine(const AttnPlan& plan, const float* part_o,
+                                     const float* part_lse, void* out, cudaStream_t st);
+
+// Greedy verification: partial argmax over vocab slices, then the walk.
+int greedy_splits(int64_t V, int32_t N, int num_sms);
+cudaError_t launch_argmax_partial(const float* logits, int64_t V, int32_t N, int splits,
+                                  float* part_val, int32_t* part_idx, cudaStream_t st);
+cudaError_t launch_greedy_walk(const float* part_val, const int32_t* part_idx, int splits,
+                               const int32_t* tokens, const int32_t* parent,
+                               const int32_t* node_offsets, int32_t B, int32_t* path,
+                               int32_t* accept_len, int32_t* bonus, int32_t* status,
+                               cudaStream_t st);
+
+// Stochastic verification: per-row softmax statistics, then one walk CTA per request.
+int stats_splits(int64_t V, int32_t N, int num_sms);
+cudaError_t launch_row_stats(const float* logits, int64_t V, int32_t N, int splits, float inv_t,
+                             float* part_m, double* part_s, cudaStream_t st);
+cudaError_t launch_mss_walk(const float* llm_logits, const float* ssm_probs, int64_t V,
+                            const int32_t* tokens, const int32_t* parent,
+                            const int32_t* node_offsets, const float* u_acc, const float* u_smp,
+                            float inv_t, int32_t B, int splits, const float* part_m,
+                            const double* part_s, float* resid, int32_t* path,
+                            int32_t* accept_len, int32_t* bonus, int32_t* n_tried,
+                            int32_t* status, cudaStream_t st);
+
+}  // namespace tsv
