@@ -47,6 +47,7 @@ def parse_args():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default=DEFAULT_WORKLOAD)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true", help="profiling runs: skip e2e, baselines, JSON line")
     p.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU oracle sample budget")
     return p.parse_args()
 
@@ -350,30 +351,41 @@ def run_ours(args, spec):
         step(c, st)
     torch.cuda.synchronize()
     assert (states[0]["status"].cpu() == 0).all()
-    graphs, attn_graphs = [], []
+    # One graph holds one step on every input copy (R steps), so the host
+    # replays one graph per R steps and stays ahead of the GPU.
+    g_steps = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_steps, stream=stream):
+        for c, st in zip(copies, states):
+            step(c, st)
+    g_one = []
     for c, st in zip(copies, states):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
             step(c, st)
-        graphs.append(g)
-        ga = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(ga, stream=stream):
+        g_one.append(g)
+    g_attn = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_attn, stream=stream):
+        for c, st in zip(copies, states):
             attention(c, st)
-        attn_graphs.append(ga)
     torch.cuda.synchronize()
     # Kernels per step: prepare, attention (+ the split merge when the plan cuts
     # requests into chunks, i.e. when the attention needs workspace), two per
     # verification; checked against the captured graph when torch exposes it.
     attn_kernels = 1 + (1 if ws_attn > 0 else 0)
     kernels_per_step = 1 + attn_kernels + (2 if gi is not None else 0) + (2 if si is not None else 0)
-    counted = graph_kernel_count(graphs[0])
+    counted = graph_kernel_count(g_one[0])
     if counted is not None:
         assert counted == kernels_per_step, (counted, kernels_per_step)
 
     sampler = ClockSampler(local)
     sampler.start()
-    for i in range(args.warmup):
-        graphs[i % R].replay()
+    def run_steps(k):
+        for _ in range(k // R):
+            g_steps.replay()
+        for i in range(k % R):
+            g_one[i].replay()
+
+    run_steps(args.warmup)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
@@ -384,8 +396,7 @@ def run_ours(args, spec):
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t_wall0 = time.time()
     e0.record(stream)
-    for i in range(args.steps):
-        graphs[i % R].replay()
+    run_steps(args.steps)
     e1.record(stream)
     torch.cuda.synchronize()
     t_wall1 = time.time()
@@ -400,18 +411,23 @@ def run_ours(args, spec):
     value = world * N / (ms_step * 1e-3)
 
     # ---------------------------------------------------------------- attention kernel, per launch
-    reps = max(R, min(20000, args.steps))
-    torch.cuda._sleep(int(2e6))
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
-    ev[0].record(stream)
-    for i in range(reps):
-        attn_graphs[i % R].replay()
-        ev[i + 1].record(stream)
+    # Average launch duration of the attention call inside a graph of R
+    # back-to-back launches (one per input copy), events on the launching stream.
+    reps = max(1, min(2000, args.steps) // R)
+    g_attn.replay()
     torch.cuda.synchronize()
-    durs = np.array([ev[i].elapsed_time(ev[i + 1]) for i in range(reps)])
-    attn_ms = float(durs.mean())
+    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a0.record(stream)
+    for _ in range(reps):
+        g_attn.replay()
+    a1.record(stream)
+    torch.cuda.synchronize()
+    attn_ms = a0.elapsed_time(a1) / (reps * R)
     sampler.stop()
     clocks = sampler.summary(t_wall0, t_wall1)
+    if args.no_e2e:
+        print(json.dumps({"ms_per_step": ms_step, "attn_launch_ms": attn_ms}), flush=True)
+        return
 
     # ---------------------------------------------------------------- end to end
     e2e = measure_e2e(args, spec, trees, att, gi, si, h, tsv, dev, stream, ws_attn, ws_g, ws_s)

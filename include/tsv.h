@@ -36,8 +36,11 @@
  *   - Memory.  The caller owns every buffer.  Pointers marked _d are device
  *     pointers, _host are host pointers read during the call only.  Scratch
  *     memory is a caller-provided device workspace whose size the matching
- *     *_workspace_size query returns; it may be reused between calls on one
- *     stream but not shared by calls that overlap on the GPU.
+ *     *_workspace_size query returns.  Zero-fill a workspace once before its
+ *     first use (it holds completion counters); every call that completes
+ *     leaves them zero again, so it may be reused by later calls on one stream
+ *     as is (re-zero it after a TSV_ERR_TIMEOUT).  Calls that overlap on the
+ *     GPU must not share a workspace.
  *   - Streams.  `stream` is a cudaStream_t (NULL = the legacy default stream).
  *     Calls are asynchronous on it.  The return value reports only the
  *     synchronous host-side checks and launch errors; device-side results and
@@ -148,13 +151,17 @@ tsv_status tsv_tree_attention_workspace_size(tsv_handle h, tsv_dtype dtype, int3
  *   prefix_len_host, node_offsets_host  host copies (used to plan the grid);
  *   prefix_len_d, node_offsets_d        the same values on the device
  *   parent_d           int32 [N]
- *   anc_d              from tsv_tree_prepare on the same parent_d, or NULL (the
- *                      call then prepares the bitsets into its workspace)
- *   B, Hq, Hkv, D      Hq % Hkv == 0, D in {64, 128}, Hq*N rows fit in int32
+ *   anc_d              from tsv_tree_prepare on the same parent_d (16-byte
+ *                      aligned), or NULL: the bitsets are then computed from
+ *                      parent_d inside the call, which also validates the tree
+ *   B, Hq, Hkv, D      Hq % Hkv == 0, D in {64, 128}, Hq*N rows fit in int32;
+ *                      the tensor-core path also needs Hq/Hkv to divide 128
+ *                      (TSV_ERR_UNSUPPORTED otherwise)
  *   scale              softmax scale; 0 means 1/sqrt(D)
  *   workspace_d, workspace_bytes   at least tsv_tree_attention_workspace_size
- *   status_d    (out)  int32 [B] (written only when anc_d is NULL, or on a
- *                      device-side timeout)
+ *   status_d    (out)  int32 [B]: TSV_OK or TSV_ERR_BAD_TREE when anc_d is NULL
+ *                      (else left alone); TSV_ERR_TIMEOUT on a device-side
+ *                      timeout
  *   flags              TSV_ATTN_DEFAULT or TSV_ATTN_SIMT
  */
 tsv_status tsv_tree_attention(tsv_handle h, tsv_dtype dtype, const void* q_d, const void* k_cache_d,

@@ -40,8 +40,8 @@ def test_prepare_matches_oracle(tsv, n, depth, B):
 
 
 def test_prepare_flags_bad_trees(tsv):
-    par = np.array([-1, 0, 1, -1, 3, 3, 0, 1, 2], dtype=np.int32)  # requests of 3 nodes
-    par[5] = 7  # request 1: node 2 points forward
+    par = np.array([-1, 0, 1, -1, 0, 0, -1, 0, 1], dtype=np.int32)  # three requests of 3 nodes
+    par[5] = 7  # request 1: its node 2 points forward
     offs = np.array([0, 3, 6, 9], dtype=np.int32)
     anc, dep, st = tsv.tree_prepare(d(par), d(offs))
     torch.cuda.synchronize()
@@ -217,7 +217,7 @@ def test_host_side_argument_checks(tsv):
     Hkv = k.shape[2]
     out = torch.empty_like(q)
     st = torch.zeros(B, dtype=torch.int32, device=q.device)
-    ws = torch.empty(1 << 24, dtype=torch.uint8, device=q.device)
+    ws = torch.zeros(1 << 24, dtype=torch.uint8, device=q.device)
     plen, offs, par = d(trees.prefix_len), d(trees.node_offsets), d(trees.parent)
     s = k.stride()
 

@@ -42,7 +42,8 @@ def test_greedy_workloads(tsv, name):
     r = _greedy(tsv, trees, gi)
     ref = oracle.verify_greedy(gi.logits, gi.tokens, trees.parent, trees.node_offsets)
     _check_greedy(r, ref)
-    assert ref["accept_len"].sum() > 0  # the recipe makes about half the children match
+    if spec.B > 1:
+        assert ref["accept_len"].sum() > 0  # the recipe makes about half the children match
 
 
 @pytest.mark.parametrize("seed", range(12))

@@ -213,7 +213,8 @@ def handle(device=None):
 
 
 def _workspace(nbytes, device):
-    return torch.empty(max(int(nbytes), 1), dtype=torch.uint8, device=device)
+    """A zero-filled workspace (the library's completion counters start at zero)."""
+    return torch.zeros(max(int(nbytes), 1), dtype=torch.uint8, device=device)
 
 
 def tree_prepare(parent, node_offsets, stream=None):

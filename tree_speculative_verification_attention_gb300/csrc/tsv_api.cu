@@ -81,12 +81,14 @@ void build_plan(AttnPlan& p, int num_sms, int32_t B, const int32_t* prefix_len,
     if (chunk == kBN) break;
   }
   p.chunk_keys = (int32_t)best_chunk;
-  int64_t units = 0, rows = 0;
+  int64_t units = 0, rows = 0, ctrs = 0;
   for (int b = 0; b < B; ++b) {
     const int64_t L = (int64_t)p.prefix[b] + p.nodes[b];
     p.n_chunks[b] = p.mtiles[b] > 0 ? (int32_t)cdiv(L, best_chunk) : 0;
     p.unit_start[b] = (int32_t)units;
     units += (int64_t)Hkv * p.mtiles[b] * p.n_chunks[b];
+    p.ctr_base[b] = (int32_t)ctrs;
+    ctrs += (int64_t)Hkv * p.mtiles[b];
     if (p.n_chunks[b] > 1) {
       p.part_row[b] = rows;
       rows += (int64_t)Hkv * p.n_chunks[b] * p.nodes[b] * p.G;
@@ -97,17 +99,24 @@ void build_plan(AttnPlan& p, int num_sms, int32_t B, const int32_t* prefix_len,
   p.unit_start[B] = (int32_t)units;
   p.n_units = (int32_t)units;
   p.part_rows_total = rows;
+  p.n_counters = (int32_t)ctrs;
 }
 
+// Workspace of one attention call.  Tensor-core path: merge counters first
+// (they must be zero before the first call on a workspace; every completed
+// call leaves them zero), then the split partials.  CUDA-core path without
+// prepared bitsets: the bitsets.
 struct AttnLayout {
-  size_t anc_off, part_o_off, part_lse_off, total;
+  size_t ctr_off, anc_off, part_o_off, part_lse_off, total;
 };
 
 AttnLayout attention_layout(const AttnPlan& p, int64_t N, bool anc_given, bool use_tc) {
   AttnLayout a{};
   size_t off = 0;
+  a.ctr_off = off;
+  if (use_tc && p.part_rows_total > 0) off += round256((size_t)p.n_counters * sizeof(int32_t));
   a.anc_off = off;
-  if (!anc_given) off += round256((size_t)N * TSV_ANC_WORDS * sizeof(uint32_t));
+  if (!anc_given && !use_tc) off += round256((size_t)N * TSV_ANC_WORDS * sizeof(uint32_t));
   a.part_o_off = off;
   if (use_tc) off += round256((size_t)p.part_rows_total * p.D * sizeof(float));
   a.part_lse_off = off;
@@ -126,6 +135,21 @@ tsv_status encode_kv_map(tsv_handle h, CUtensorMap* map, const void* base, int64
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   const CUresult r = h->encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base),
                                dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? TSV_OK : TSV_ERR_INVALID_ARG;
+}
+
+// Q [N, Hq, D] as a 3-D map (D, Hq, N); a box of (64, G, 128/G) is one
+// 128-row tile whose row r is (node r / G, head-in-group r % G).
+tsv_status encode_q_map(tsv_handle h, CUtensorMap* map, const void* q, int64_t N, int32_t Hq,
+                        int32_t G, int32_t D) {
+  const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)Hq, (cuuint64_t)N};
+  const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)Hq * D * 2};
+  const cuuint32_t box[3] = {64, (cuuint32_t)G, (cuuint32_t)(kBM / G)};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = h->encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims,
+                               strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? TSV_OK : TSV_ERR_INVALID_ARG;
@@ -241,9 +265,11 @@ tsv_status tsv_tree_attention(tsv_handle h, tsv_dtype dtype, const void* q_d, co
   if (N * (int64_t)Hq > INT32_MAX) return TSV_ERR_UNSUPPORTED;
   const bool use_tc = attention_uses_tc(dtype, flags);
   if (use_tc) {
-    if (!aligned16(q_d) || !aligned16(out_d) || !aligned16(k_cache_d) || !aligned16(v_cache_d))
+    if (!aligned16(q_d) || !aligned16(out_d) || !aligned16(k_cache_d) || !aligned16(v_cache_d) ||
+        (anc_d && !aligned16(anc_d)))
       return TSV_ERR_INVALID_ARG;
     if (kv_stride_b % 8 || kv_stride_l % 8 || kv_stride_h % 8) return TSV_ERR_INVALID_ARG;
+    if (kBM % (Hq / Hkv) != 0) return TSV_ERR_UNSUPPORTED;  // a tile holds whole GQA groups
   }
   if (scale == 0.f) scale = 1.f / sqrtf((float)D);
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
@@ -255,14 +281,14 @@ tsv_status tsv_tree_attention(tsv_handle h, tsv_dtype dtype, const void* q_d, co
   char* ws = static_cast<char*>(workspace_d);
   if (N == 0) return TSV_OK;
 
-  const uint32_t* anc = anc_d;
-  if (!anc) {
-    uint32_t* a = reinterpret_cast<uint32_t*>(ws + lay.anc_off);
-    st = cuda_status(launch_tree_prepare(parent_d, node_offsets_d, B, a, nullptr, status_d, cs));
-    if (st != TSV_OK) return st;
-    anc = a;
-  }
   if (!use_tc) {
+    const uint32_t* anc = anc_d;
+    if (!anc) {
+      uint32_t* a = reinterpret_cast<uint32_t*>(ws + lay.anc_off);
+      st = cuda_status(launch_tree_prepare(parent_d, node_offsets_d, B, a, nullptr, status_d, cs));
+      if (st != TSV_OK) return st;
+      anc = a;
+    }
     return cuda_status(launch_attention_simt(dtype == TSV_BF16, q_d, k_cache_d, v_cache_d,
                                              kv_stride_b, kv_stride_l, kv_stride_h, out_d,
                                              prefix_len_d, node_offsets_d, anc, B, (int32_t)N, Hq,
@@ -275,17 +301,18 @@ tsv_status tsv_tree_attention(tsv_handle h, tsv_dtype dtype, const void* q_d, co
   }
   int64_t lmax = 1;
   for (int b = 0; b < B; ++b) lmax = std::max<int64_t>(lmax, (int64_t)plan.prefix[b] + plan.nodes[b]);
-  CUtensorMap tmk, tmv;
+  CUtensorMap tmq, tmk, tmv;
+  st = encode_q_map(h, &tmq, q_d, N, Hq, Hq / Hkv, D);
+  if (st != TSV_OK) return st;
   st = encode_kv_map(h, &tmk, k_cache_d, kv_stride_b, kv_stride_l, kv_stride_h, B, lmax, Hkv, D);
   if (st != TSV_OK) return st;
   st = encode_kv_map(h, &tmv, v_cache_d, kv_stride_b, kv_stride_l, kv_stride_h, B, lmax, Hkv, D);
   if (st != TSV_OK) return st;
+  int32_t* counters = reinterpret_cast<int32_t*>(ws + lay.ctr_off);
   float* part_o = reinterpret_cast<float*>(ws + lay.part_o_off);
   float* part_lse = reinterpret_cast<float*>(ws + lay.part_lse_off);
-  st = cuda_status(launch_attention_tc(tmk, tmv, plan, q_d, anc, out_d, part_o, part_lse, status_d,
-                                       h->num_sms, cs));
-  if (st != TSV_OK) return st;
-  return cuda_status(launch_attention_combine(plan, part_o, part_lse, out_d, cs));
+  return cuda_status(launch_attention_tc(tmq, tmk, tmv, plan, parent_d, anc_d, out_d, part_o,
+                                         part_lse, counters, status_d, cs));
 }
 
 tsv_status tsv_tree_verify_greedy_workspace_size(tsv_handle h, int32_t B, int32_t N, int64_t V,
@@ -293,7 +320,7 @@ tsv_status tsv_tree_verify_greedy_workspace_size(tsv_handle h, int32_t B, int32_
   if (!h || !bytes || B < 1 || B > TSV_MAX_BATCH || N < 0 || V < 1 || V > INT32_MAX)
     return TSV_ERR_INVALID_ARG;
   const int splits = greedy_splits(V, N, h->num_sms);
-  *bytes = 2 * round256((size_t)N * splits * 4);
+  *bytes = round256((size_t)B * 4) + 2 * round256((size_t)N * splits * 4);
   return TSV_OK;
 }
 
@@ -309,17 +336,19 @@ tsv_status tsv_tree_verify_greedy(tsv_handle h, const float* logits_d, int64_t V
   if (B < 1 || B > TSV_MAX_BATCH || N < 0 || V < 1 || V > INT32_MAX) return TSV_ERR_INVALID_ARG;
   if (N > 0 && (!logits_d || !path_d)) return TSV_ERR_INVALID_ARG;
   const int splits = greedy_splits(V, N, h->num_sms);
-  const size_t part = round256((size_t)N * splits * 4);
-  if (N > 0 && (!workspace_d || workspace_bytes < 2 * part)) return TSV_ERR_INVALID_ARG;
+  const size_t ctr = round256((size_t)B * 4), part = round256((size_t)N * splits * 4);
+  if (!workspace_d || workspace_bytes < ctr + 2 * part) return TSV_ERR_INVALID_ARG;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  float* pv = reinterpret_cast<float*>(workspace_d);
-  int32_t* pi = reinterpret_cast<int32_t*>(static_cast<char*>(workspace_d) + part);
-  if (N > 0) {
-    tsv_status st = cuda_status(launch_argmax_partial(logits_d, V, N, splits, pv, pi, cs));
-    if (st != TSV_OK) return st;
-  }
-  return cuda_status(launch_greedy_walk(pv, pi, splits, tree_tokens_d, parent_d, node_offsets_d, B,
-                                        path_d, accept_len_d, bonus_d, status_d, cs));
+  char* ws = static_cast<char*>(workspace_d);
+  int32_t* counters = reinterpret_cast<int32_t*>(ws);
+  float* pv = reinterpret_cast<float*>(ws + ctr);
+  int32_t* pi = reinterpret_cast<int32_t*>(ws + ctr + part);
+  if (N == 0)
+    return cuda_status(launch_greedy_walk(pv, pi, splits, tree_tokens_d, parent_d, node_offsets_d, B,
+                                          path_d, accept_len_d, bonus_d, status_d, cs));
+  return cuda_status(launch_greedy_verify(logits_d, V, N, splits, tree_tokens_d, parent_d,
+                                          node_offsets_d, B, pv, pi, counters, path_d, accept_len_d,
+                                          bonus_d, status_d, cs));
 }
 
 tsv_status tsv_tree_verify_stochastic_workspace_size(tsv_handle h, int32_t B, int32_t N, int64_t V,

@@ -12,17 +12,23 @@
 // query rows are (node, head-in-group) pairs: all query heads that share KV
 // head g sit in the same tile, so each streamed K/V row serves every tree node
 // and every grouped head at once.  Warp roles (192 threads):
-//   warp 4        TMA producer: K and V blocks of 64 rows x D, 128-byte
-//                 swizzled, into a ring of kStages shared-memory stages.
-//   warp 5        tcgen05 issuer: S = Q K^T into TMEM (double-buffered), then
-//                 O += P V into a TMEM accumulator; also owns TMEM allocation.
-//   warps 0-3     one thread per query row (= TMEM lane): reads S, applies the
-//                 ancestor-bitset mask on the tree part of the keys, online
-//                 softmax in base 2 with a lazily moved reference maximum,
-//                 writes P (bf16) to shared memory, rescales O in TMEM when
-//                 the reference moves, and finally normalises O and stores the
-//                 output (one chunk) or a partial result + log2-sum-exp.
-// attn_combine_kernel merges the partials of requests cut into several chunks.
+//   warp 4        TMA producer: the Q tile first, then K and V blocks of 64
+//                 rows x D, 128-byte swizzled, into a ring of kStages stages.
+//                 It starts right after the barriers exist, so the first
+//                 loads overlap everything else the CTA sets up.
+//   warp 5        tcgen05 issuer: S = Q K^T into TMEM (two buffers), then
+//                 O += P V into a TMEM accumulator; owns TMEM allocation.
+//   warps 0-3     one thread per query row (= TMEM lane).  Set-up: the
+//                 ancestor bitsets of the tile's nodes, read from the
+//                 prepared array or computed here from parent[] by pointer
+//                 jumping.  Loop: read S, mask the tree part of the keys with
+//                 the bitset, online softmax in base 2 with a lazily moved
+//                 reference maximum, write P (bf16, two buffers) to shared
+//                 memory, rescale O in TMEM when the reference moves.  End:
+//                 normalise and store the output; when the request's keys are
+//                 split over several CTAs, store a partial + log2-sum-exp and
+//                 let the last CTA of the group (atomic counter, no waiting)
+//                 merge the partials into the output.
 #include <cuda_bf16.h>
 #include <math.h>
 
@@ -37,25 +43,37 @@ struct TcCfg {
   static constexpr int kStages = (D == 128) ? 4 : 8;   // K/V ring depth
   static constexpr int kQBytes = kBM * D * 2;
   static constexpr int kTileBytes = kBN * D * 2;       // one K (or V) block
-  static constexpr int kPBytes = kBM * kBN * 2;
+  static constexpr int kPBytes = kBM * kBN * 2;        // one P buffer
   static constexpr int kAncWords = TSV_ANC_WORDS + 2;  // two zero words past the end
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kOffQ + kQBytes;
   static constexpr int kOffV = kOffK + kStages * kTileBytes;
   static constexpr int kOffP = kOffV + kStages * kTileBytes;
-  static constexpr int kOffAnc = kOffP + kPBytes;
+  static constexpr int kOffAnc = kOffP + 2 * kPBytes;
   static constexpr int kOffBar = kOffAnc + kBM * kAncWords * 4;
-  static constexpr int kNumBars = 2 * kStages + 5;  // kv_full, kv_empty, s_full[2], p_full, pv_done, mma_done
+  // q_full, kv_full[S], kv_empty[S], s_full[2], p_full[2], pv_done[2], mma_done
+  static constexpr int kNumBars = 1 + 2 * kStages + 7;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + slack to align the base to 1024
   static constexpr uint32_t kTmemCols = 256;               // S0 | S1 | O
   static_assert(kOffK % 1024 == 0 && kOffV % 1024 == 0 && kOffP % 1024 == 0, "swizzle atoms");
   static_assert(kOffBar % 8 == 0, "mbarrier alignment");
   static_assert(2 * kBN + D <= (int)kTmemCols, "TMEM columns");
+  // Pointer-jumping scratch (two bitset buffers + two jump buffers) reuses the P buffers.
+  static_assert(2 * TSV_MAX_NODES * TSV_ANC_WORDS * 4 + 2 * TSV_MAX_NODES * 4 <= 2 * kPBytes,
+                "ancestor scratch");
 };
 
 constexpr int kTcThreads = 192;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: P stays below 2^8 between rescales
+
+// Named barriers (0 is __syncthreads).
+constexpr int kBarSetup = 1;    // warps 0-3 + warp 5: TMEM address published
+constexpr int kBarSoftmax = 2;  // warps 0-3
+
+__device__ __forceinline__ void named_bar(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
 
 // Visibility of the 64 keys key0 .. key0+63 for one query row, given o =
 // key0 - P (its tree index of column 0, may be negative) and the row's
@@ -74,14 +92,56 @@ __device__ __forceinline__ uint64_t block_visibility(const uint32_t* arow, int o
   return (tb << pre) | ((1ull << pre) - 1ull);
 }
 
+// Ancestor bitsets of all n nodes of a request, computed by the 128 softmax
+// threads from parent[] (topological order) by pointer jumping: after round k
+// each node holds its ancestors within distance 2^k.  Returns the buffer that
+// holds the result; *bad is set when parent[] breaks the convention.
+__device__ __forceinline__ const uint32_t* ancestors_by_pointer_jumping(
+    const int32_t* __restrict__ par, int n, uint32_t* scratch, int* bad) {
+  uint32_t* const A0 = scratch;
+  uint32_t* const A1 = scratch + TSV_MAX_NODES * TSV_ANC_WORDS;
+  int32_t* const J0 = reinterpret_cast<int32_t*>(scratch + 2 * TSV_MAX_NODES * TSV_ANC_WORDS);
+  int32_t* const J1 = J0 + TSV_MAX_NODES;
+  const int tid = threadIdx.x;
+  for (int i = tid; i < n; i += 128) {
+    const int p = __ldg(par + i);
+    const bool ok = p >= -1 && p < i;
+    if (!ok) atomicOr(bad, 1);
+    const int pp = ok ? p : -1;
+#pragma unroll
+    for (int w = 0; w < TSV_ANC_WORDS; ++w) A0[i * TSV_ANC_WORDS + w] = 0u;
+    A0[i * TSV_ANC_WORDS + (i >> 5)] |= 1u << (i & 31);
+    if (pp >= 0) A0[i * TSV_ANC_WORDS + (pp >> 5)] |= 1u << (pp & 31);
+    J0[i] = pp;
+  }
+  const int rounds = n > 1 ? 32 - __clz(n - 1) : 0;
+  for (int r = 0; r < rounds; ++r) {
+    named_bar(kBarSoftmax, 128);
+    const uint32_t* Ac = (r & 1) ? A1 : A0;
+    uint32_t* An = (r & 1) ? A0 : A1;
+    const int32_t* Jc = (r & 1) ? J1 : J0;
+    int32_t* Jn = (r & 1) ? J0 : J1;
+    for (int i = tid; i < n; i += 128) {
+      const int j = Jc[i];
+#pragma unroll
+      for (int w = 0; w < TSV_ANC_WORDS; ++w)
+        An[i * TSV_ANC_WORDS + w] = Ac[i * TSV_ANC_WORDS + w] | (j >= 0 ? Ac[j * TSV_ANC_WORDS + w] : 0u);
+      Jn[i] = j >= 0 ? Jc[j] : -1;
+    }
+  }
+  named_bar(kBarSoftmax, 128);
+  return (rounds & 1) ? A1 : A0;
+}
+
 template <int D>
 __global__ void __launch_bounds__(kTcThreads, 1)
-    tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
+    tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
+                        const __grid_constant__ CUtensorMap tmap_k,
                         const __grid_constant__ CUtensorMap tmap_v,
-                        const __grid_constant__ AttnPlan plan, const __nv_bfloat16* __restrict__ q,
+                        const __grid_constant__ AttnPlan plan, const int32_t* __restrict__ parent,
                         const uint32_t* __restrict__ anc, __nv_bfloat16* __restrict__ out,
                         float* __restrict__ part_o, float* __restrict__ part_lse,
-                        int32_t* __restrict__ status) {
+                        int32_t* __restrict__ counters, int32_t* __restrict__ status) {
   using C = TcCfg<D>;
   constexpr int S = C::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -92,14 +152,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint8_t* sP = smem + C::kOffP;
   uint32_t* sAnc = reinterpret_cast<uint32_t*>(smem + C::kOffAnc);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
-  uint64_t* kv_full = bars;
-  uint64_t* kv_empty = bars + S;
-  uint64_t* s_full = bars + 2 * S;
+  uint64_t* q_full = bars;
+  uint64_t* kv_full = bars + 1;
+  uint64_t* kv_empty = kv_full + S;
+  uint64_t* s_full = kv_empty + S;
   uint64_t* p_full = s_full + 2;
-  uint64_t* pv_done = p_full + 1;
-  uint64_t* mma_done = pv_done + 1;
+  uint64_t* pv_done = p_full + 2;
+  uint64_t* mma_done = pv_done + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   int* abort_flag = reinterpret_cast<int*>(smem + C::kOffMisc + 4);
+  int* bad_tree = reinterpret_cast<int*>(smem + C::kOffMisc + 8);
+  int* last_cta = reinterpret_cast<int*>(smem + C::kOffMisc + 12);
   volatile int* abort_v = abort_flag;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -128,61 +191,35 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int nblk = (k_end - k_begin + kBN - 1) / kBN;
 
   if (tid == 0) {
+    mbar_init(q_full, 1);
     for (int s = 0; s < S; ++s) {
       mbar_init(&kv_full[s], 1);
       mbar_init(&kv_empty[s], 1);
     }
-    mbar_init(&s_full[0], 1);
-    mbar_init(&s_full[1], 1);
-    mbar_init(p_full, 128);  // every softmax thread arrives
-    mbar_init(pv_done, 1);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&s_full[x], 1);
+      mbar_init(&p_full[x], 128);  // every softmax thread arrives
+      mbar_init(&pv_done[x], 1);
+    }
     mbar_init(mma_done, 1);
     *abort_flag = 0;
+    *bad_tree = 0;
     mbar_fence_init();
   }
-  if (warp == 5) {
-    tmem_alloc(tmem_slot, C::kTmemCols);
-    tmem_relinquish();
-  }
-  if (warp == 4 && lane == 0) {
-    tma_prefetch_desc(&tmap_k);
-    tma_prefetch_desc(&tmap_v);
-  }
-
-  // Q tile (rows past the request are zero) in the 128-byte-swizzled K-major
-  // layout the MMA reads: row r, 16-byte chunk c8 of column group hf at
-  // hf*kBM*128 + r*128 + (c8 ^ (r & 7))*16.
-  for (int idx = tid; idx < kBM * (D / 8); idx += kTcThreads) {
-    const int r = idx / (D / 8), ch = idx % (D / 8);
-    uint4 val = make_uint4(0u, 0u, 0u, 0u);
-    if (r < rows_valid) {
-      const int gr = row0 + r;
-      const int node = gr / G, hr = gr - node * G;
-      const uint4* src = reinterpret_cast<const uint4*>(
-          q + ((size_t)(off + node) * plan.Hq + (size_t)g * G + hr) * D);
-      val = __ldg(src + ch);
-    }
-    const int hf = ch >> 3, c8 = ch & 7;
-    *reinterpret_cast<uint4*>(sQ + hf * (kBM * 128) + r * 128 + ((c8 ^ (r & 7)) << 4)) = val;
-  }
-  for (int idx = tid; idx < kBM * C::kAncWords; idx += kTcThreads) {
-    const int r = idx / C::kAncWords, w = idx % C::kAncWords;
-    uint32_t val = 0u;
-    if (r < rows_valid && w < TSV_ANC_WORDS) {
-      const int node = (row0 + r) / G;
-      val = anc[(size_t)(off + node) * TSV_ANC_WORDS + w];
-    }
-    sAnc[idx] = val;
-  }
-  fence_proxy_async_smem();
-  tc_fence_before();
   __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
 
   if (warp == 4) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
+      tma_prefetch_desc(&tmap_q);
+      tma_prefetch_desc(&tmap_k);
+      tma_prefetch_desc(&tmap_v);
+      // Q tile: box (64 d, G heads, 128/G nodes) lands as 128 rows r = node*G + head.
+      mbar_arrive_expect_tx(q_full, C::kQBytes);
+#pragma unroll
+      for (int hf = 0; hf < C::kHalves; ++hf)
+        tma_load_3d(sQ + hf * (kBM * 128), &tmap_q, q_full, hf * 64, g * G, off + row0 / G,
+                    l2_policy_evict_first());
       const uint64_t pol = mtiles > 1 ? l2_policy_evict_last() : l2_policy_evict_first();
       int issued = 0;
       for (int j = 0; j < nblk; ++j) {
@@ -200,12 +237,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         ++issued;
       }
       if (*abort_v) {  // let copies still in flight land before the CTA exits
+        mbar_wait(q_full, 0, nullptr);
         for (int j = (issued > S ? issued - S : 0); j < issued; ++j)
           mbar_wait(&kv_full[j % S], (j / S) & 1, nullptr);
       }
     }
   } else if (warp == 5) {
     // ------------------------------------------------------------ MMA issuer
+    tmem_alloc(tmem_slot, C::kTmemCols);
+    tmem_relinquish();
+    tc_fence_before();
+    named_bar(kBarSetup, 160);
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16_f32(kBM, kBN, 0);
       constexpr uint32_t idPV = idesc_bf16_f32(kBM, D, 1);
@@ -224,14 +268,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       };
       auto issue_pv = [&](int j) {
         const int st = j % S;
+        const uint32_t pbuf = pa + (uint32_t)((j & 1) * C::kPBytes);
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk) {
           const uint32_t bo = st * C::kTileBytes + kk * 16 * 128;
-          umma_bf16(tO, sdesc_sw128(pa + kk * 32, 16, 1024),
+          umma_bf16(tO, sdesc_sw128(pbuf + kk * 32, 16, 1024),
                     sdesc_sw128(va + bo, kBN * 128, 1024), idPV, (j > 0 || kk > 0) ? 1u : 0u);
         }
       };
-      bool ok = nblk > 0 && mbar_wait(&kv_full[0], 0, abort_v);
+      bool ok = nblk > 0 && mbar_wait(q_full, 0, abort_v) && mbar_wait(&kv_full[0], 0, abort_v);
       if (ok) {
         tc_fence_after();
         issue_s(0);
@@ -244,10 +289,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           issue_s(j + 1);
           umma_commit(&s_full[(j + 1) & 1]);
         }
-        if (!mbar_wait(p_full, j & 1, abort_v)) break;
+        if (!mbar_wait(&p_full[j & 1], (j >> 1) & 1, abort_v)) break;
         tc_fence_after();
         issue_pv(j);
-        umma_commit(pv_done);
+        umma_commit(&pv_done[j & 1]);
         umma_commit(&kv_empty[j % S]);
       }
       umma_commit(mma_done);  // every MMA of this CTA has finished before TMEM is freed
@@ -257,6 +302,35 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // ------------------------------------------------------------ softmax
     const int r = tid;
     const bool valid = r < rows_valid;
+    // Ancestor bitsets of the tile's rows.
+    if (anc != nullptr) {
+      if (valid) {
+        const uint4* src = reinterpret_cast<const uint4*>(anc + (size_t)(off + (row0 + r) / G) * TSV_ANC_WORDS);
+        const uint4 a0 = __ldg(src), a1 = __ldg(src + 1);
+        uint32_t* dst = sAnc + r * C::kAncWords;
+        dst[0] = a0.x; dst[1] = a0.y; dst[2] = a0.z; dst[3] = a0.w;
+        dst[4] = a1.x; dst[5] = a1.y; dst[6] = a1.z; dst[7] = a1.w;
+        dst[8] = 0u; dst[9] = 0u;
+      }
+    } else {
+      const uint32_t* A = ancestors_by_pointer_jumping(parent + off, n,
+                                                       reinterpret_cast<uint32_t*>(sP), bad_tree);
+      const bool bad = *bad_tree != 0;
+      if (valid) {
+        const int node = (row0 + r) / G;
+        uint32_t* dst = sAnc + r * C::kAncWords;
+#pragma unroll
+        for (int w = 0; w < TSV_ANC_WORDS; ++w) dst[w] = bad ? 0u : A[node * TSV_ANC_WORDS + w];
+        dst[8] = 0u;
+        dst[9] = 0u;
+      }
+      if (local == 0 && tid == 0) status[b] = bad ? TSV_ERR_BAD_TREE : TSV_OK;
+      named_bar(kBarSoftmax, 128);  // scratch (the P buffers) free again
+    }
+    tc_fence_before();
+    named_bar(kBarSetup, 160);
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
     const uint32_t* arow = sAnc + r * C::kAncWords;
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
     const float sl2 = plan.scale_log2;
@@ -304,22 +378,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         pk[e >> 1] = pack_bf16x2(p0, p1);
       }
       l = l * alpha + psum;
-      if (j > 0) {  // PV of the previous block done: P buffer free, O stable
-        ok = __all_sync(0xffffffffu, mbar_wait(pv_done, (j - 1) & 1, abort_v));
+      // P buffer j&1 was last read by PV(j-2); O must hold PV(j-1) before a rescale.
+      if (j >= 2) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&pv_done[j & 1], ((j - 2) >> 1) & 1, abort_v));
+        if (!ok) break;
+      }
+      if (j >= 1 && __any_sync(0xffffffffu, resc)) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort_v));
         if (!ok) break;
         tc_fence_after();
-        if (__any_sync(0xffffffffu, resc)) {
 #pragma unroll 1
-          for (int cc = 0; cc < D; cc += 32) {
-            float o[32];
-            tmem_ld32(tmem + lane_base + (uint32_t)(2 * kBN + cc), o);
+        for (int cc = 0; cc < D; cc += 32) {
+          float o[32];
+          tmem_ld32(tmem + lane_base + (uint32_t)(2 * kBN + cc), o);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] *= alpha;
-            tmem_st32(tmem + lane_base + (uint32_t)(2 * kBN + cc), o);
-          }
+          for (int e = 0; e < 32; ++e) o[e] *= alpha;
+          tmem_st32(tmem + lane_base + (uint32_t)(2 * kBN + cc), o);
         }
       }
-      uint8_t* prow = sP + r * 128;
+      uint8_t* prow = sP + (j & 1) * C::kPBytes + r * 128;
 #pragma unroll
       for (int c8 = 0; c8 < 8; ++c8)
         *reinterpret_cast<uint4*>(prow + ((c8 ^ (r & 7)) << 4)) =
@@ -339,9 +416,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(p_full);
+      mbar_arrive(&p_full[j & 1]);
     }
-    if (ok && nblk > 0) ok = __all_sync(0xffffffffu, mbar_wait(pv_done, (nblk - 1) & 1, abort_v));
+    if (ok && nblk > 0)
+      ok = __all_sync(0xffffffffu,
+                      mbar_wait(&pv_done[(nblk - 1) & 1], ((nblk - 1) >> 1) & 1, abort_v));
     if (ok && nblk > 0) {
       tc_fence_after();
       const int gr = row0 + r;
@@ -365,7 +444,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
         }
       } else {
-        const int64_t prow_i = plan.part_row[b] + (int64_t)(g * nch + c) * R + gr;
+        // Partial of this chunk, then the group's last CTA merges all chunks.
+        const int64_t base0 = plan.part_row[b] + (int64_t)g * nch * R;
+        const int64_t prow_i = base0 + (int64_t)c * R + gr;
         float* dst = part_o + prow_i * D;
 #pragma unroll 1
         for (int cc = 0; cc < D; cc += 32) {
@@ -380,6 +461,49 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
         }
         if (valid) part_lse[prow_i] = l > 0.f ? m_ref + log2f(l) : -INFINITY;
+        __threadfence();
+        named_bar(kBarSoftmax, 128);
+        int32_t* ctr = counters + plan.ctr_base[b] + g * mtiles + mt;
+        if (tid == 0) *last_cta = atomicAdd(ctr, 1) == nch - 1;
+        named_bar(kBarSoftmax, 128);
+        if (*last_cta) {
+          __threadfence();
+          // Warp w merges rows w, w+4, ...; each lane owns D/32 columns.
+          constexpr int E = D / 32;
+          for (int rr = warp; rr < rows_valid; rr += 4) {
+            const int grr = row0 + rr;
+            float M = -INFINITY;
+            for (int cc = 0; cc < nch; ++cc) M = fmaxf(M, __ldcg(part_lse + base0 + (int64_t)cc * R + grr));
+            float acc[E], wsum = 0.f;
+#pragma unroll
+            for (int e = 0; e < E; ++e) acc[e] = 0.f;
+            for (int cc = 0; cc < nch; ++cc) {
+              const int64_t pr = base0 + (int64_t)cc * R + grr;
+              const float lse = __ldcg(part_lse + pr);
+              if (lse == -INFINITY) continue;
+              const float w = fast_exp2(lse - M);
+              wsum += w;
+              const float* src = part_o + pr * D + lane * E;
+              if constexpr (E == 4) {
+                const float4 v = __ldcg(reinterpret_cast<const float4*>(src));
+                acc[0] += w * v.x; acc[1] += w * v.y; acc[2] += w * v.z; acc[3] += w * v.w;
+              } else {
+                const float2 v = __ldcg(reinterpret_cast<const float2*>(src));
+                acc[0] += w * v.x; acc[1] += w * v.y;
+              }
+            }
+            const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+            const int nd = grr / G, hh = g * G + (grr - nd * G);
+            __nv_bfloat16* o = out + ((size_t)(off + nd) * plan.Hq + hh) * D + lane * E;
+            if constexpr (E == 4) {
+              *reinterpret_cast<uint2*>(o) =
+                  make_uint2(pack_bf16x2(acc[0] * inv, acc[1] * inv), pack_bf16x2(acc[2] * inv, acc[3] * inv));
+            } else {
+              *reinterpret_cast<uint32_t*>(o) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+            }
+          }
+          if (tid == 0) *ctr = 0;  // leave the counter zeroed for the next call
+        }
       }
     }
   }
@@ -389,43 +513,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (tid == 0 && *abort_v) status[b] = TSV_ERR_TIMEOUT;
   if (warp == 5) {
     tc_fence_after();
-    tmem_dealloc(tmem, C::kTmemCols);
-  }
-}
-
-// Merges the per-chunk partials of one (request, KV head): out = sum_c w_c o_c
-// / sum_c w_c with w_c = 2^(lse_c - max lse).
-__global__ void __launch_bounds__(256)
-    attn_combine_kernel(const __grid_constant__ AttnPlan plan, const float* __restrict__ part_o,
-                        const float* __restrict__ part_lse, __nv_bfloat16* __restrict__ out) {
-  const int b = blockIdx.z, g = blockIdx.y;
-  const int nch = plan.n_chunks[b];
-  if (nch <= 1) return;
-  const int D = plan.D, G = plan.G, R = plan.nodes[b] * G, off = plan.node_off[b];
-  const int D4 = D / 4;
-  const int64_t base0 = plan.part_row[b] + (int64_t)g * nch * R;
-  for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < R * D4; e += gridDim.x * blockDim.x) {
-    const int r = e / D4, d4 = e - (e / D4) * D4;
-    float M = -INFINITY;
-    for (int cc = 0; cc < nch; ++cc) M = fmaxf(M, part_lse[base0 + (int64_t)cc * R + r]);
-    float wsum = 0.f;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int cc = 0; cc < nch; ++cc) {
-      const int64_t pr = base0 + (int64_t)cc * R + r;
-      const float lse = part_lse[pr];
-      if (lse == -INFINITY) continue;
-      const float w = exp2f(lse - M);
-      const float4 o = reinterpret_cast<const float4*>(part_o + pr * D)[d4];
-      wsum += w;
-      acc.x += w * o.x;
-      acc.y += w * o.y;
-      acc.z += w * o.z;
-      acc.w += w * o.w;
-    }
-    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-    const int node = r / G, h = g * G + (r - node * G);
-    uint2 v = make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
-    *reinterpret_cast<uint2*>(out + ((size_t)(off + node) * plan.Hq + h) * D + d4 * 4) = v;
+    tmem_dealloc(*tmem_slot, C::kTmemCols);
   }
 }
 
@@ -441,35 +529,19 @@ cudaError_t attention_tc_set_attributes(int D) {
                               TcCfg<128>::kSmemBytes);
 }
 
-cudaError_t launch_attention_tc(const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
-                                const AttnPlan& plan, const void* q, const uint32_t* anc,
-                                void* out, float* part_o, float* part_lse, int32_t* status,
-                                int num_sms, cudaStream_t st) {
-  (void)num_sms;
+cudaError_t launch_attention_tc(const CUtensorMap& tmap_q, const CUtensorMap& tmap_k,
+                                const CUtensorMap& tmap_v, const AttnPlan& plan,
+                                const int32_t* parent, const uint32_t* anc, void* out,
+                                float* part_o, float* part_lse, int32_t* counters,
+                                int32_t* status, cudaStream_t st) {
   if (plan.n_units == 0) return cudaSuccess;
-  const __nv_bfloat16* qb = static_cast<const __nv_bfloat16*>(q);
   __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(out);
   if (plan.D == 64)
     tree_attn_tc_kernel<64><<<plan.n_units, kTcThreads, TcCfg<64>::kSmemBytes, st>>>(
-        tmap_k, tmap_v, plan, qb, anc, ob, part_o, part_lse, status);
+        tmap_q, tmap_k, tmap_v, plan, parent, anc, ob, part_o, part_lse, counters, status);
   else
     tree_attn_tc_kernel<128><<<plan.n_units, kTcThreads, TcCfg<128>::kSmemBytes, st>>>(
-        tmap_k, tmap_v, plan, qb, anc, ob, part_o, part_lse, status);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_attention_combine(const AttnPlan& plan, const float* part_o,
-                                     const float* part_lse, void* out, cudaStream_t st) {
-  if (plan.part_rows_total == 0) return cudaSuccess;
-  int max_r = 0;
-  for (int b = 0; b < plan.B; ++b)
-    if (plan.n_chunks[b] > 1 && plan.nodes[b] * plan.G > max_r) max_r = plan.nodes[b] * plan.G;
-  const int elems = max_r * (plan.D / 4);
-  int gx = (elems + 255) / 256;
-  if (gx > 64) gx = 64;
-  dim3 grid(gx, plan.Hkv, plan.B);
-  attn_combine_kernel<<<grid, 256, 0, st>>>(plan, part_o, part_lse,
-                                            static_cast<__nv_bfloat16*>(out));
+        tmap_q, tmap_k, tmap_v, plan, parent, anc, ob, part_o, part_lse, counters, status);
   return cudaGetLastError();
 }
 

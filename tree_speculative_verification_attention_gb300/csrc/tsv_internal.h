@@ -31,7 +31,9 @@ struct AttnPlan {
   int32_t nodes[TSV_MAX_BATCH];
   int32_t node_off[TSV_MAX_BATCH];
   int64_t part_row[TSV_MAX_BATCH];  // first partial row of request b, -1 when n_chunks == 1
+  int32_t ctr_base[TSV_MAX_BATCH];  // first merge counter of request b (one per KV head x M-tile)
   int64_t part_rows_total;
+  int32_t n_counters;
 };
 
 struct Workspace {
@@ -50,10 +52,11 @@ struct Workspace {
 cudaError_t launch_tree_prepare(const int32_t* parent, const int32_t* node_offsets, int32_t B,
                                 uint32_t* anc, int32_t* depth, int32_t* status, cudaStream_t st);
 
-cudaError_t launch_attention_tc(const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
-                                const AttnPlan& plan, const void* q, const uint32_t* anc,
-                                void* out, float* part_o, float* part_lse, int32_t* status,
-                                int num_sms, cudaStream_t st);
+cudaError_t launch_attention_tc(const CUtensorMap& tmap_q, const CUtensorMap& tmap_k,
+                                const CUtensorMap& tmap_v, const AttnPlan& plan,
+                                const int32_t* parent, const uint32_t* anc, void* out,
+                                float* part_o, float* part_lse, int32_t* counters,
+                                int32_t* status, cudaStream_t st);
 cudaError_t attention_tc_set_attributes(int D);
 size_t attention_tc_smem_bytes(int D);
 
@@ -63,13 +66,14 @@ cudaError_t launch_attention_simt(bool bf16, const void* q, const void* k, const
                                   const uint32_t* anc, int32_t B, int32_t N, int32_t Hq,
                                   int32_t Hkv, int32_t D, float scale, cudaStream_t st);
 
-cudaError_t launch_attention_combine(const AttnPlan& plan, const float* part_o,
-                                     const float* part_lse, void* out, cudaStream_t st);
-
-// Greedy verification: partial argmax over vocab slices, then the walk.
+// Greedy verification: argmax over vocab slices, the last CTA of a request walks.
 int greedy_splits(int64_t V, int32_t N, int num_sms);
-cudaError_t launch_argmax_partial(const float* logits, int64_t V, int32_t N, int splits,
-                                  float* part_val, int32_t* part_idx, cudaStream_t st);
+cudaError_t launch_greedy_verify(const float* logits, int64_t V, int32_t N, int splits,
+                                 const int32_t* tokens, const int32_t* parent,
+                                 const int32_t* node_offsets, int32_t B, float* part_val,
+                                 int32_t* part_idx, int32_t* counters, int32_t* path,
+                                 int32_t* accept_len, int32_t* bonus, int32_t* status,
+                                 cudaStream_t st);
 cudaError_t launch_greedy_walk(const float* part_val, const int32_t* part_idx, int splits,
                                const int32_t* tokens, const int32_t* parent,
                                const int32_t* node_offsets, int32_t B, int32_t* path,

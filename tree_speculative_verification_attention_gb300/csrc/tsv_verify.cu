@@ -2,13 +2,13 @@
 //
 // Greedy (SpecInfer §4 Token Tree Verification; §6: the output equals
 // incremental decoding):
-//   argmax_partial_kernel  grid (splits, N): each CTA streams one vocab slice
+//   greedy_verify_kernel   grid (splits, N): each CTA streams one vocab slice
 //                          of one logits row with 16-byte loads and reduces
-//                          (max, lowest index) with warp shuffles.
-//   greedy_walk_kernel     grid B: merges the slices per row, then marks for
-//                          every node u its next node = the lowest-index child
-//                          whose token is argmax(u), and follows those links
-//                          from the root.
+//                          (max, lowest index) with warp shuffles; the last
+//                          CTA of each request merges the slices per row, marks
+//                          for every node u its next node = the lowest-index
+//                          child whose token is argmax(u), and follows those
+//                          links from the root.
 // Stochastic, multi-step speculative sampling (SpecInfer §1 Correctness, §4
 // Token Verification):
 //   row_stats_kernel       grid (splits, N): per row max and compensated
@@ -60,10 +60,10 @@ __device__ __forceinline__ int64_t slice_len(int64_t V, int splits) {
 
 }  // namespace
 
-__global__ void __launch_bounds__(kArgmaxThreads)
-    argmax_partial_kernel(const float* __restrict__ logits, int64_t V, int splits,
-                          float* __restrict__ part_val, int32_t* __restrict__ part_idx) {
-  const int row = blockIdx.y, s = blockIdx.x;
+// Argmax (lowest index on ties) of vocab slice s of logits row `row`, reduced
+// over the CTA; the result is valid in thread 0.  `red` holds one entry per warp.
+__device__ __forceinline__ ArgMax slice_argmax(const float* __restrict__ logits, int64_t V, int splits,
+                                               int row, int s, ArgMax* red) {
   const int64_t per = slice_len(V, splits);
   const int64_t lo = (int64_t)s * per;
   const int64_t hi = min(V, lo + per);
@@ -100,18 +100,14 @@ __global__ void __launch_bounds__(kArgmaxThreads)
       best = better(best, ArgMax{__ldcs(x + k), (int32_t)k});
   }
   best = warp_argmax(best);
-  __shared__ ArgMax red[kArgmaxThreads / 32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (lane == 0) red[warp] = best;
   __syncthreads();
   if (warp == 0) {
     best = lane < kArgmaxThreads / 32 ? red[lane] : ArgMax{-INFINITY, INT32_MAX};
     best = warp_argmax(best);
-    if (lane == 0) {
-      part_val[(size_t)row * splits + s] = best.v;
-      part_idx[(size_t)row * splits + s] = best.i;
-    }
   }
+  return best;
 }
 
 // Validates one request's tree for verification: a single root at node 0,
@@ -141,19 +137,16 @@ __device__ void fail_request(int32_t* path, int n, int32_t* accept_len, int32_t*
   }
 }
 
-__global__ void __launch_bounds__(TSV_MAX_NODES)
-    greedy_walk_kernel(const float* __restrict__ part_val, const int32_t* __restrict__ part_idx,
-                       int splits, const int32_t* __restrict__ tokens,
-                       const int32_t* __restrict__ parent, const int32_t* __restrict__ node_offsets,
-                       int32_t* __restrict__ path, int32_t* __restrict__ accept_len,
-                       int32_t* __restrict__ bonus, int32_t* __restrict__ status) {
-  __shared__ int32_t am[TSV_MAX_NODES];
-  __shared__ int32_t nxt[TSV_MAX_NODES];
-  __shared__ int bad, len_s;
-  const int b = blockIdx.x;
-  const int off = node_offsets[b];
-  const int n = node_offsets[b + 1] - off;
-  const int code = validate_verify_tree(parent + off, n, &bad);
+// The greedy walk of request b from its per-slice argmax partials: every
+// child c whose token equals argmax(parent(c)) proposes itself to its parent
+// with atomicMin (lowest index wins), then the chain is followed from the root.
+// Run by one whole CTA of up to 256 threads.
+__device__ void greedy_walk_request(int b, int off, int n, const float* part_val,
+                                    const int32_t* part_idx, int splits, const int32_t* tokens,
+                                    const int32_t* parent, int32_t* path, int32_t* accept_len,
+                                    int32_t* bonus, int32_t* status, int* sh_bad, int32_t* am,
+                                    int32_t* nxt, int* len_s) {
+  const int code = validate_verify_tree(parent + off, n, sh_bad);
   if (code) {
     fail_request(path + off, n, accept_len + b, bonus + b, nullptr, status + b, code);
     return;
@@ -162,7 +155,7 @@ __global__ void __launch_bounds__(TSV_MAX_NODES)
     ArgMax best{-INFINITY, INT32_MAX};
     for (int s = 0; s < splits; ++s) {
       const size_t k = (size_t)(off + u) * splits + s;
-      best = better(best, ArgMax{part_val[k], part_idx[k]});
+      best = better(best, ArgMax{__ldcg(part_val + k), __ldcg(part_idx + k)});
     }
     am[u] = best.i;
     nxt[u] = INT32_MAX;
@@ -183,10 +176,78 @@ __global__ void __launch_bounds__(TSV_MAX_NODES)
     accept_len[b] = len - 1;
     bonus[b] = am[u];
     status[b] = TSV_OK;
-    len_s = len;
+    *len_s = len;
   }
   __syncthreads();
-  for (int i = len_s + threadIdx.x; i < n; i += blockDim.x) path[off + i] = -1;
+  for (int i = *len_s + threadIdx.x; i < n; i += blockDim.x) path[off + i] = -1;
+}
+
+// Walk-only kernel: one CTA per request (used when N == 0, where no argmax CTA exists).
+__global__ void __launch_bounds__(TSV_MAX_NODES)
+    greedy_walk_kernel(const float* __restrict__ part_val, const int32_t* __restrict__ part_idx,
+                       int splits, const int32_t* __restrict__ tokens,
+                       const int32_t* __restrict__ parent, const int32_t* __restrict__ node_offsets,
+                       int32_t* __restrict__ path, int32_t* __restrict__ accept_len,
+                       int32_t* __restrict__ bonus, int32_t* __restrict__ status) {
+  __shared__ int32_t am[TSV_MAX_NODES];
+  __shared__ int32_t nxt[TSV_MAX_NODES];
+  __shared__ int bad, len_s;
+  const int b = blockIdx.x;
+  const int off = node_offsets[b];
+  greedy_walk_request(b, off, node_offsets[b + 1] - off, part_val, part_idx, splits, tokens, parent,
+                      path, accept_len, bonus, status, &bad, am, nxt, &len_s);
+}
+
+// Fused greedy verification: grid (splits, N).  Each CTA reduces one vocab
+// slice of one row; the last CTA to finish among a request's rows x slices
+// (atomic counter, no waiting) walks that request's tree.  CTA (0, 0) also
+// reports requests that own no rows.  Counters start at zero and are reset.
+__global__ void __launch_bounds__(kArgmaxThreads)
+    greedy_verify_kernel(const float* __restrict__ logits, int64_t V, int splits,
+                         const int32_t* __restrict__ tokens, const int32_t* __restrict__ parent,
+                         const int32_t* __restrict__ node_offsets, int B,
+                         float* __restrict__ part_val, int32_t* __restrict__ part_idx,
+                         int32_t* __restrict__ counters, int32_t* __restrict__ path,
+                         int32_t* __restrict__ accept_len, int32_t* __restrict__ bonus,
+                         int32_t* __restrict__ status) {
+  __shared__ int32_t offs[TSV_MAX_BATCH + 1];
+  __shared__ int32_t am[TSV_MAX_NODES];
+  __shared__ int32_t nxt[TSV_MAX_NODES];
+  __shared__ ArgMax red[kArgmaxThreads / 32];
+  __shared__ int bad, len_s, last;
+  const int row = blockIdx.y, s = blockIdx.x;
+  for (int i = threadIdx.x; i <= B; i += blockDim.x) offs[i] = node_offsets[i];
+  const ArgMax best = slice_argmax(logits, V, splits, row, s, red);
+  if (threadIdx.x == 0) {
+    part_val[(size_t)row * splits + s] = best.v;
+    part_idx[(size_t)row * splits + s] = best.i;
+  }
+  __syncthreads();  // offs loaded
+  int lo = 0, hi = B;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (offs[mid] <= row) lo = mid; else hi = mid;
+  }
+  while (lo + 1 < B && offs[lo + 1] <= row) ++lo;  // skip empty requests sharing the offset
+  const int b = lo;
+  const int off = offs[b], n = offs[b + 1] - off;
+  if (row == 0 && s == 0) {
+    for (int e = threadIdx.x; e < B; e += blockDim.x)
+      if (offs[e + 1] == offs[e]) {
+        accept_len[e] = 0;
+        bonus[e] = -1;
+        status[e] = TSV_ERR_BAD_TREE;
+      }
+  }
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) last = atomicAdd(counters + b, 1) == n * splits - 1;
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  greedy_walk_request(b, off, n, part_val, part_idx, splits, tokens, parent, path, accept_len, bonus,
+                      status, &bad, am, nxt, &len_s);
+  if (threadIdx.x == 0) counters[b] = 0;
 }
 
 int greedy_splits(int64_t V, int32_t N, int num_sms) {
@@ -196,10 +257,16 @@ int greedy_splits(int64_t V, int32_t N, int num_sms) {
   return (int)(s < 1 ? 1 : s);
 }
 
-cudaError_t launch_argmax_partial(const float* logits, int64_t V, int32_t N, int splits,
-                                  float* part_val, int32_t* part_idx, cudaStream_t st) {
+cudaError_t launch_greedy_verify(const float* logits, int64_t V, int32_t N, int splits,
+                                 const int32_t* tokens, const int32_t* parent,
+                                 const int32_t* node_offsets, int32_t B, float* part_val,
+                                 int32_t* part_idx, int32_t* counters, int32_t* path,
+                                 int32_t* accept_len, int32_t* bonus, int32_t* status,
+                                 cudaStream_t st) {
   dim3 grid(splits, N);
-  argmax_partial_kernel<<<grid, kArgmaxThreads, 0, st>>>(logits, V, splits, part_val, part_idx);
+  greedy_verify_kernel<<<grid, kArgmaxThreads, 0, st>>>(logits, V, splits, tokens, parent,
+                                                        node_offsets, B, part_val, part_idx,
+                                                        counters, path, accept_len, bonus, status);
   return cudaGetLastError();
 }
 
