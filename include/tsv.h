@@ -71,7 +71,8 @@ typedef enum {
   TSV_ERR_BAD_TREE = 2,
   TSV_ERR_UNSUPPORTED = 3,
   TSV_ERR_CUDA = 4,
-  TSV_ERR_TIMEOUT = 5
+  TSV_ERR_TIMEOUT = 5,
+  TSV_ERR_SCRATCH_LIMIT = 6  /* the call needs more than the fixed scratch of a _noalloc entry point */
 } tsv_status;
 
 typedef enum { TSV_F32 = 0, TSV_BF16 = 1 } tsv_dtype;
@@ -233,6 +234,32 @@ tsv_status tsv_tree_verify_stochastic(tsv_handle h, const float* llm_logits_d,
                                       int32_t N, int32_t* path_d, int32_t* accept_len_d,
                                       int32_t* bonus_d, int32_t* n_tried_d, void* workspace_d,
                                       size_t workspace_bytes, int32_t* status_d, void* stream);
+
+/*
+ * tsv_tree_verify_greedy_noalloc — the same greedy verification as
+ * tsv_tree_verify_greedy, for callers that cannot provide device scratch
+ * memory: code running where it may not allocate (an engine or plugin whose
+ * allocator owns all device memory, a latency-critical loop that must never
+ * enter the CUDA allocator) or a binding with no device-memory management of
+ * its own.  The pages describe no such interface; it has no counterpart there.
+ *   Arguments and outputs as in tsv_tree_verify_greedy, without the workspace.
+ *   Scratch: one fixed 1 MiB array in device memory, allocated when the library
+ *   is loaded and held by every GPU that loads it until the process exits; this
+ *   call allocates and frees nothing.  A shape whose scratch would exceed it
+ *   returns TSV_ERR_SCRATCH_LIMIT (no shape within TSV_MAX_BATCH x
+ *   TSV_MAX_NODES does).
+ *   The first call on a device looks up the array's device address (a host-side
+ *   set-up step, with that device current); make that first call before any
+ *   stream capture.
+ *   All calls on a device share the array: each call clears the part that must
+ *   start at zero on its stream, but calls that overlap on the GPU (streams not
+ *   ordered with each other) race on it and give wrong results.
+ */
+tsv_status tsv_tree_verify_greedy_noalloc(tsv_handle h, const float* logits_d, int64_t V,
+                                          const int32_t* tree_tokens_d, const int32_t* parent_d,
+                                          const int32_t* node_offsets_d, int32_t B, int32_t N,
+                                          int32_t* path_d, int32_t* accept_len_d, int32_t* bonus_d,
+                                          int32_t* status_d, void* stream);
 
 #ifdef __cplusplus
 }

@@ -1,0 +1,72 @@
+"""The no-allocation greedy verification entry point.
+
+tsv_tree_verify_greedy_noalloc serves callers that cannot hand the library a
+device workspace (an engine whose allocator owns all device memory, a loop that
+must never enter the allocator): its scratch is a fixed array inside the
+library.  Called through the C ABI, it must give exactly what
+tsv_tree_verify_greedy gives with a caller-provided workspace, on two calls in
+a row (the shared scratch keeps the previous call's contents).  This file is
+collected last so that a failure here stops a -x run only after every other test.
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+def _inputs(spec):
+    trees = W.make_trees(spec)
+    gi = W.make_greedy_inputs(spec, trees)
+    d = lambda x: torch.as_tensor(np.ascontiguousarray(x)).cuda()
+    return trees, dict(logits=d(gi.logits), tokens=d(gi.tokens), parent=d(trees.parent),
+                       offs=d(trees.node_offsets))
+
+
+def _outputs(N, B):
+    z = lambda n: torch.full((n,), -7, dtype=torch.int32, device="cuda")
+    return dict(path=z(N), accept_len=z(B), bonus=z(B), status=z(B))
+
+
+def _with_workspace(tsv, h, x, B, N, V):
+    o = _outputs(N, B)
+    ws = torch.zeros(tsv.tsv_tree_verify_greedy_workspace_size(h, B, N, V), dtype=torch.uint8,
+                     device="cuda")
+    tsv.tsv_tree_verify_greedy(h, x["logits"], V, x["tokens"], x["parent"], x["offs"], B, N, o["path"],
+                               o["accept_len"], o["bonus"], ws, ws.numel(), o["status"])
+    return o
+
+
+def _no_alloc(tsv, h, x, B, N, V):
+    o = _outputs(N, B)
+    tsv.tsv_tree_verify_greedy_noalloc(h, x["logits"], V, x["tokens"], x["parent"], x["offs"], B, N,
+                                       o["path"], o["accept_len"], o["bonus"], o["status"])
+    return o
+
+
+def test_no_alloc_matches_workspace_entry_on_consecutive_calls(tsv):
+    h = tsv.handle()
+    specs = [W.SPECS["batch32-P2048-n16"], W.SPECS["llama7b-layer-P1024-n20"]]
+    for spec in specs:  # two different batches, each verified twice in a row
+        trees, x = _inputs(spec)
+        B, N, V = spec.B, int(trees.node_offsets[-1]), spec.V
+        ref = _with_workspace(tsv, h, x, B, N, V)
+        first = _no_alloc(tsv, h, x, B, N, V)
+        second = _no_alloc(tsv, h, x, B, N, V)
+        torch.cuda.synchronize()
+        assert (ref["status"].cpu() == 0).all()
+        for k in ref:  # integer outputs: bit-exact
+            assert torch.equal(first[k], ref[k]), k
+            assert torch.equal(second[k], ref[k]), k
+
+
+def test_no_alloc_rejects_what_the_scratch_cannot_hold(tsv):
+    h = tsv.handle()
+    x = dict(logits=None, tokens=None, parent=None, offs=None)
+    o = _outputs(1, 1)
+    with pytest.raises(tsv.TSVError) as e:  # B beyond the library's maximum: rejected before launch
+        tsv.tsv_tree_verify_greedy_noalloc(h, None, 10, None, None, None, 1000, 0, None, o["accept_len"],
+                                           o["bonus"], o["status"])
+    assert e.value.code in (tsv.TSV_ERR_INVALID_ARG, tsv.TSV_ERR_SCRATCH_LIMIT)

@@ -25,7 +25,8 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libtsv.so")
 
-TSV_OK, TSV_ERR_INVALID_ARG, TSV_ERR_BAD_TREE, TSV_ERR_UNSUPPORTED, TSV_ERR_CUDA, TSV_ERR_TIMEOUT = range(6)
+(TSV_OK, TSV_ERR_INVALID_ARG, TSV_ERR_BAD_TREE, TSV_ERR_UNSUPPORTED, TSV_ERR_CUDA, TSV_ERR_TIMEOUT,
+ TSV_ERR_SCRATCH_LIMIT) = range(7)
 TSV_F32, TSV_BF16 = 0, 1
 TSV_ATTN_DEFAULT, TSV_ATTN_SIMT = 0, 1
 TSV_MAX_NODES, TSV_MAX_BATCH, TSV_ANC_WORDS = 256, 128, 8
@@ -35,6 +36,7 @@ EXPORTED = (
     "tsv_tree_attention_workspace_size", "tsv_tree_attention",
     "tsv_tree_verify_greedy_workspace_size", "tsv_tree_verify_greedy",
     "tsv_tree_verify_stochastic_workspace_size", "tsv_tree_verify_stochastic",
+    "tsv_tree_verify_greedy_noalloc",
 )
 
 
@@ -68,6 +70,8 @@ def _load():
         "tsv_tree_verify_greedy_workspace_size": (ctypes.c_int, [vp, i32, i32, i64, szp]),
         "tsv_tree_verify_greedy": (
             ctypes.c_int, [vp, vp, i64, vp, vp, vp, i32, i32, vp, vp, vp, vp, sz, vp, vp]),
+        "tsv_tree_verify_greedy_noalloc": (
+            ctypes.c_int, [vp, vp, i64, vp, vp, vp, i32, i32, vp, vp, vp, vp, vp]),
         "tsv_tree_verify_stochastic_workspace_size": (ctypes.c_int, [vp, i32, i32, i64, szp]),
         "tsv_tree_verify_stochastic": (
             ctypes.c_int, [vp, vp, vp, i64, vp, vp, vp, vp, vp, f32, i32, i32, vp, vp, vp, vp, vp, sz,
@@ -180,6 +184,17 @@ def tsv_tree_verify_greedy(h, logits, V, tree_tokens, parent, node_offsets, B, N
         h, _ptr(logits), int(V), _ptr(tree_tokens), _ptr(parent), _ptr(node_offsets), int(B), int(N),
         _ptr(path), _ptr(accept_len), _ptr(bonus), _ptr(workspace), int(workspace_bytes), _ptr(status),
         _stream(stream)), "tsv_tree_verify_greedy")
+
+
+def tsv_tree_verify_greedy_noalloc(h, logits, V, tree_tokens, parent, node_offsets, B, N, path, accept_len,
+                                   bonus, status, stream=None):
+    """Greedy verification with the library's fixed device scratch (no workspace
+    argument): for callers that cannot allocate device memory.  Calls that overlap
+    on the GPU share that scratch and must not run concurrently."""
+    _check(_lib.tsv_tree_verify_greedy_noalloc(
+        h, _ptr(logits), int(V), _ptr(tree_tokens), _ptr(parent), _ptr(node_offsets), int(B), int(N),
+        _ptr(path), _ptr(accept_len), _ptr(bonus), _ptr(status), _stream(stream)),
+        "tsv_tree_verify_greedy_noalloc")
 
 
 def tsv_tree_verify_stochastic_workspace_size(h, B, N, V) -> int:

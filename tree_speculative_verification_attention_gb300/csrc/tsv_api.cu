@@ -171,6 +171,7 @@ const char* tsv_status_string(int status) {
     case TSV_ERR_UNSUPPORTED: return "unsupported shape";
     case TSV_ERR_CUDA: return "CUDA error";
     case TSV_ERR_TIMEOUT: return "device-side wait timed out";
+    case TSV_ERR_SCRATCH_LIMIT: return "shape needs more than the fixed scratch of the no-allocation entry point";
     default: return "unknown status";
   }
 }

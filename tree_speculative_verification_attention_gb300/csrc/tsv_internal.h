@@ -80,6 +80,10 @@ cudaError_t launch_greedy_walk(const float* part_val, const int32_t* part_idx, i
                                int32_t* accept_len, int32_t* bonus, int32_t* status,
                                cudaStream_t st);
 
+// Bytes of the per-request completion counters at the start of a greedy
+// verification workspace (the layout tsv_tree_verify_greedy uses).
+inline size_t greedy_counter_bytes(int32_t B) { return ((size_t)B * 4 + 255) & ~(size_t)255; }
+
 // Stochastic verification: per-row softmax statistics, then one walk CTA per request.
 int stats_splits(int64_t V, int32_t N, int num_sms);
 cudaError_t launch_row_stats(const float* logits, int64_t V, int32_t N, int splits, float inv_t,

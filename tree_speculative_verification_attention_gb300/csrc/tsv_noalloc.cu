@@ -1,0 +1,78 @@
+// tsv_noalloc.cu — greedy tree verification without a caller-provided workspace.
+//
+// Some callers cannot hand this library a device buffer: code that runs where
+// allocation is not allowed or not possible (inside an engine or plugin whose
+// allocator owns all device memory, a real-time loop that must never enter the
+// CUDA allocator, a host language binding without device-memory management).
+// tsv_tree_verify_greedy_noalloc serves them: its scratch (per-slice argmax
+// partials and per-request completion counters) lives in one file-scope
+// __device__ array of fixed size, which every GPU that loads the library keeps
+// until the process exits.  The caller still passes every input and output.
+//
+// The array is shared by all calls on a device and keeps the last call's
+// contents: the counters, which must start at zero, are cleared on the stream
+// at the start of every call.  Calls whose work overlaps on the GPU (different
+// streams, no ordering between them) race on the array and give wrong results.
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "tsv_internal.h"
+
+namespace {
+
+// Fixed scratch: enough for TSV_MAX_BATCH requests of TSV_MAX_NODES rows at any
+// vocabulary size (the slice partials need at most (N + 2 * SM count) entries).
+constexpr size_t kNoallocScratchBytes = size_t(1) << 20;
+constexpr int kMaxDevices = 64;
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
+
+// Device address of g_noalloc_scratch, looked up once per device.  In host
+// code the symbol itself is only a host-side stand-in for the device array, so
+// the kernel must be given the address cudaGetSymbolAddress returns.
+std::mutex g_scratch_mutex;
+void* g_scratch_ptr[kMaxDevices] = {};
+
+tsv_status scratch_address(int device, void** out) {
+  if (device < 0 || device >= kMaxDevices) return TSV_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_scratch_mutex);
+  if (g_scratch_ptr[device] == nullptr) {
+    int prev = -1;
+    if (cudaGetDevice(&prev) != cudaSuccess) return TSV_ERR_CUDA;
+    if (prev != device && cudaSetDevice(device) != cudaSuccess) return TSV_ERR_CUDA;
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (prev != device) cudaSetDevice(prev);
+    if (e != cudaSuccess || p == nullptr) return TSV_ERR_CUDA;
+    g_scratch_ptr[device] = p;
+  }
+  *out = g_scratch_ptr[device];
+  return TSV_OK;
+}
+
+}  // namespace
+
+extern "C" tsv_status tsv_tree_verify_greedy_noalloc(
+    tsv_handle h, const float* logits_d, int64_t V, const int32_t* tree_tokens_d,
+    const int32_t* parent_d, const int32_t* node_offsets_d, int32_t B, int32_t N, int32_t* path_d,
+    int32_t* accept_len_d, int32_t* bonus_d, int32_t* status_d, void* stream) {
+  if (!h) return TSV_ERR_INVALID_ARG;
+  size_t need = 0;
+  tsv_status st = tsv_tree_verify_greedy_workspace_size(h, B, N, V, &need);
+  if (st != TSV_OK) return st;
+  if (need > kNoallocScratchBytes) return TSV_ERR_SCRATCH_LIMIT;
+  int device = -1;
+  if (cudaGetDevice(&device) != cudaSuccess) return TSV_ERR_CUDA;
+  void* scratch = nullptr;
+  st = scratch_address(device, &scratch);
+  if (st != TSV_OK) return st;
+  // The workspace of greedy verification starts with B int32 completion
+  // counters (tsv_tree_verify_greedy's layout); they must be zero.
+  const size_t counter_bytes = tsv::greedy_counter_bytes(B);
+  if (cudaMemsetAsync(scratch, 0, counter_bytes, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return TSV_ERR_CUDA;
+  return tsv_tree_verify_greedy(h, logits_d, V, tree_tokens_d, parent_d, node_offsets_d, B, N, path_d,
+                                accept_len_d, bonus_d, scratch, kNoallocScratchBytes, status_d,
+                                stream);
+}
