@@ -309,7 +309,7 @@ def run_ours(args, spec):
     h = tsv.handle(local)
     ws_attn = tsv.tsv_tree_attention_workspace_size(h, tsv.TSV_BF16 if spec.dtype == "bf16" else tsv.TSV_F32,
                                                     B, trees.prefix_len, trees.node_offsets, spec.Hq,
-                                                    spec.Hkv, spec.D, True)
+                                                    spec.Hkv, spec.D, False)
     ws_g = tsv.tsv_tree_verify_greedy_workspace_size(h, B, N, spec.V)
     ws_s = tsv.tsv_tree_verify_stochastic_workspace_size(h, B, N, spec.V)
     ws_bytes = max(ws_attn, 1) + max(ws_g, 1) + max(ws_s, 1) + 3 * 256
@@ -331,12 +331,13 @@ def run_ours(args, spec):
         return st
 
     def attention(c, st):
+        # The kernel builds the ancestor masks from parent[] itself (and
+        # validates the tree), so tree preparation runs inside this launch.
         tsv.tree_attention(c["q"], c["k"], c["v"], trees.prefix_len, trees.node_offsets, c["plen"],
-                           c["offs"], parent=c["parent"], anc=st["anc"], out=st["out"],
+                           c["offs"], parent=c["parent"], anc=None, out=st["out"],
                            workspace=st["ws_attn"], status=st["status"])
 
     def step(c, st):
-        tsv.tsv_tree_prepare(h, c["parent"], c["offs"], B, st["anc"], st["depth"], st["status"])
         attention(c, st)
         if gi is not None:
             tsv.tree_verify_greedy(c["logits"], c["gtok"], c["parent"], c["offs"], workspace=st["ws_g"],
@@ -368,11 +369,11 @@ def run_ours(args, spec):
         for c, st in zip(copies, states):
             attention(c, st)
     torch.cuda.synchronize()
-    # Kernels per step: prepare, attention (+ the split merge when the plan cuts
-    # requests into chunks, i.e. when the attention needs workspace), two per
-    # verification; checked against the captured graph when torch exposes it.
-    attn_kernels = 1 + (1 if ws_attn > 0 else 0)
-    kernels_per_step = 1 + attn_kernels + (2 if gi is not None else 0) + (2 if si is not None else 0)
+    # Kernels per step: one attention launch (masks built inside, splits merged
+    # inside), one for greedy verification, two for stochastic verification;
+    # checked against the captured graph when torch exposes it.
+    attn_kernels = 1
+    kernels_per_step = attn_kernels + (1 if gi is not None else 0) + (2 if si is not None else 0)
     counted = graph_kernel_count(g_one[0])
     if counted is not None:
         assert counted == kernels_per_step, (counted, kernels_per_step)
@@ -437,9 +438,11 @@ def run_ours(args, spec):
     abytes = attention_bytes(spec, trees)
     achieved = abytes / (attn_ms * 1e-3) / 1e9
     traffic = recorded_traffic(spec.name)
+    keys_kernel = all(int(n) * (spec.Hq // spec.Hkv) <= 64 for n in np.diff(trees.node_offsets)) and \
+        64 % (spec.Hq // spec.Hkv) == 0
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "traffic": traffic,
-                "kernel": "tree_attn_tc_kernel" + (" + attn_combine_kernel" if attn_kernels > 1 else ""),
+                "kernel": "tree_attn_keys_kernel" if keys_kernel else "tree_attn_tc_kernel",
                 "launch_ms": attn_ms, "algorithmic_bytes": abytes, "peak_kind": peak_kind + " hbm_gbs"}
     step_bytes = abytes + verify_bytes(spec, trees)
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -516,9 +519,8 @@ def measure_e2e(args, spec, trees, att, gi, si, h, tsv, dev, stream, ws_attn, ws
     def step():
         for k in host:
             d[k].copy_(host[k], non_blocking=True)
-        tsv.tsv_tree_prepare(h, d["parent"], d["offs"], B, anc, None, status)
         tsv.tree_attention(d["q"], d["k"], d["v"], trees.prefix_len, trees.node_offsets, d["plen"], d["offs"],
-                           parent=d["parent"], anc=anc, out=out, workspace=wsa, status=status)
+                           parent=d["parent"], anc=None, out=out, workspace=wsa, status=status)
         out_h.copy_(out, non_blocking=True)
         if gi is not None:
             tsv.tree_verify_greedy(d["logits"], d["gtok"], d["parent"], d["offs"], workspace=wsg, out=res)

@@ -22,7 +22,8 @@ struct tsv_handle_s {
   int device;
   int num_sms;
   EncodeTiledFn encode;
-  bool tc_attr_set[2];  // D = 64, 128
+  bool tc_attr_set[2];    // rows-on-lanes kernel, D = 64, 128
+  bool keys_attr_set[2];  // keys-on-lanes kernel, D = 64, 128
 };
 
 namespace {
@@ -102,6 +103,73 @@ void build_plan(AttnPlan& p, int num_sms, int32_t B, const int32_t* prefix_len,
   p.n_counters = (int32_t)ctrs;
 }
 
+// Plan of the keys-on-lanes kernel (every request at most 64 query rows per
+// KV head): each request's keys are cut into the same number K of chunks (K in
+// 1 .. 8, the cluster size), chunk length ceil(L_b / K) rounded up to the
+// 128-key block.  K minimises the estimated makespan max(waves x longest unit,
+// total work / SMs), in keys plus a per-unit overhead of two blocks; ties go to
+// the smaller cluster.
+void build_plan_keys(AttnPlan& p, int num_sms, int32_t B, const int32_t* prefix_len,
+                     const int32_t* node_offsets, int32_t Hq, int32_t Hkv, int32_t D, float scale) {
+  memset(&p, 0, sizeof(p));
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.G = Hq / Hkv;
+  p.D = D;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.keys_kernel = 1;
+  for (int b = 0; b < B; ++b) {
+    p.prefix[b] = prefix_len[b];
+    p.node_off[b] = node_offsets[b];
+    p.nodes[b] = node_offsets[b + 1] - node_offsets[b];
+    p.mtiles[b] = (int32_t)cdiv((int64_t)p.nodes[b] * p.G, kKeysTileRows);
+  }
+  const int64_t overhead = 2 * kKeysBlockKeys;
+  int best_k = 1;
+  double best_est = 1e300;
+  for (int K = 1; K <= 8; ++K) {
+    double total = 0, longest = 0;
+    int64_t units = 0;
+    for (int b = 0; b < B; ++b) {
+      if (p.mtiles[b] == 0) continue;
+      const int64_t L = (int64_t)p.prefix[b] + p.nodes[b];
+      const int64_t clen = cdiv(cdiv(L, K), kKeysBlockKeys) * kKeysBlockKeys;
+      const double unit_cost = (double)(clen + overhead);
+      units += (int64_t)Hkv * p.mtiles[b] * K;
+      total += unit_cost * (double)Hkv * p.mtiles[b] * K;
+      longest = std::max(longest, unit_cost);
+    }
+    const double est = std::max((double)cdiv(units, num_sms) * longest, total / num_sms);
+    if (est < best_est) {
+      best_est = est;
+      best_k = K;
+    }
+  }
+  p.cluster = best_k;
+  int64_t units = 0;
+  for (int b = 0; b < B; ++b) {
+    const int64_t L = (int64_t)p.prefix[b] + p.nodes[b];
+    p.chunk_len[b] = (int32_t)(cdiv(cdiv(L, best_k), kKeysBlockKeys) * kKeysBlockKeys);
+    p.n_chunks[b] = p.mtiles[b] > 0 ? best_k : 0;
+    p.unit_start[b] = (int32_t)units;
+    units += (int64_t)Hkv * p.mtiles[b] * p.n_chunks[b];
+    p.part_row[b] = -1;
+  }
+  p.unit_start[B] = (int32_t)units;
+  p.n_units = (int32_t)units;
+}
+
+// The keys-on-lanes kernel serves batches whose requests all have at most 64
+// query rows per KV head (GQA group dividing 64).
+bool use_keys_kernel(int32_t B, const int32_t* node_offsets, int32_t Hq, int32_t Hkv) {
+  const int32_t G = Hq / Hkv;
+  if (kKeysTileRows % G != 0) return false;
+  for (int b = 0; b < B; ++b)
+    if ((int64_t)(node_offsets[b + 1] - node_offsets[b]) * G > kKeysTileRows) return false;
+  return true;
+}
+
 // Workspace of one attention call.  Tensor-core path: merge counters first
 // (they must be zero before the first call on a workspace; every completed
 // call leaves them zero), then the split partials.  CUDA-core path without
@@ -128,10 +196,10 @@ AttnLayout attention_layout(const AttnPlan& p, int64_t N, bool anc_given, bool u
 tsv_status cuda_status(cudaError_t e) { return e == cudaSuccess ? TSV_OK : TSV_ERR_CUDA; }
 
 tsv_status encode_kv_map(tsv_handle h, CUtensorMap* map, const void* base, int64_t sb, int64_t sl,
-                         int64_t sh, int32_t B, int64_t L, int32_t Hkv, int32_t D) {
+                         int64_t sh, int32_t B, int64_t L, int32_t Hkv, int32_t D, int box_rows) {
   const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)Hkv, (cuuint64_t)L, (cuuint64_t)B};
   const cuuint64_t strides[3] = {(cuuint64_t)sh * 2, (cuuint64_t)sl * 2, (cuuint64_t)sb * 2};
-  const cuuint32_t box[4] = {64, 1, (cuuint32_t)kBN, 1};
+  const cuuint32_t box[4] = {64, 1, (cuuint32_t)box_rows, 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   const CUresult r = h->encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base),
                                dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -140,13 +208,13 @@ tsv_status encode_kv_map(tsv_handle h, CUtensorMap* map, const void* base, int64
   return r == CUDA_SUCCESS ? TSV_OK : TSV_ERR_INVALID_ARG;
 }
 
-// Q [N, Hq, D] as a 3-D map (D, Hq, N); a box of (64, G, 128/G) is one
-// 128-row tile whose row r is (node r / G, head-in-group r % G).
+// Q [N, Hq, D] as a 3-D map (D, Hq, N); a box of (64, G, tile_rows/G) is one
+// tile whose row r is (node r / G, head-in-group r % G).
 tsv_status encode_q_map(tsv_handle h, CUtensorMap* map, const void* q, int64_t N, int32_t Hq,
-                        int32_t G, int32_t D) {
+                        int32_t G, int32_t D, int tile_rows) {
   const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)Hq, (cuuint64_t)N};
   const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)Hq * D * 2};
-  const cuuint32_t box[3] = {64, (cuuint32_t)G, (cuuint32_t)(kBM / G)};
+  const cuuint32_t box[3] = {64, (cuuint32_t)G, (cuuint32_t)(tile_rows / G)};
   const cuuint32_t estr[3] = {1, 1, 1};
   const CUresult r = h->encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims,
                                strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -205,6 +273,7 @@ tsv_status tsv_create(tsv_handle* out, int device) {
   h->num_sms = sms;
   h->encode = reinterpret_cast<EncodeTiledFn>(fn);
   h->tc_attr_set[0] = h->tc_attr_set[1] = false;
+  h->keys_attr_set[0] = h->keys_attr_set[1] = false;
   *out = h;
   return TSV_OK;
 }
@@ -236,9 +305,12 @@ tsv_status tsv_tree_attention_workspace_size(tsv_handle h, tsv_dtype dtype, int3
   tsv_status st = check_batch(B, prefix_len_host, node_offsets_host);
   if (st != TSV_OK) return st;
   AttnPlan plan;
-  build_plan(plan, h->num_sms, B, prefix_len_host, node_offsets_host, Hq, Hkv, D, 1.f);
-  *bytes = attention_layout(plan, node_offsets_host[B], anc_given != 0,
-                            attention_uses_tc(dtype, flags)).total;
+  const bool use_tc = attention_uses_tc(dtype, flags);
+  if (use_tc && use_keys_kernel(B, node_offsets_host, Hq, Hkv))
+    build_plan_keys(plan, h->num_sms, B, prefix_len_host, node_offsets_host, Hq, Hkv, D, 1.f);
+  else
+    build_plan(plan, h->num_sms, B, prefix_len_host, node_offsets_host, Hq, Hkv, D, 1.f);
+  *bytes = attention_layout(plan, node_offsets_host[B], anc_given != 0, use_tc).total;
   return TSV_OK;
 }
 
@@ -265,18 +337,22 @@ tsv_status tsv_tree_attention(tsv_handle h, tsv_dtype dtype, const void* q_d, co
   const int64_t N = node_offsets_host[B];
   if (N * (int64_t)Hq > INT32_MAX) return TSV_ERR_UNSUPPORTED;
   const bool use_tc = attention_uses_tc(dtype, flags);
+  const bool use_keys = use_tc && use_keys_kernel(B, node_offsets_host, Hq, Hkv);
   if (use_tc) {
     if (!aligned16(q_d) || !aligned16(out_d) || !aligned16(k_cache_d) || !aligned16(v_cache_d) ||
         (anc_d && !aligned16(anc_d)))
       return TSV_ERR_INVALID_ARG;
     if (kv_stride_b % 8 || kv_stride_l % 8 || kv_stride_h % 8) return TSV_ERR_INVALID_ARG;
-    if (kBM % (Hq / Hkv) != 0) return TSV_ERR_UNSUPPORTED;  // a tile holds whole GQA groups
+    if (!use_keys && kBM % (Hq / Hkv) != 0) return TSV_ERR_UNSUPPORTED;  // a tile holds whole GQA groups
   }
   if (scale == 0.f) scale = 1.f / sqrtf((float)D);
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
 
   AttnPlan plan;
-  build_plan(plan, h->num_sms, B, prefix_len_host, node_offsets_host, Hq, Hkv, D, scale);
+  if (use_keys)
+    build_plan_keys(plan, h->num_sms, B, prefix_len_host, node_offsets_host, Hq, Hkv, D, scale);
+  else
+    build_plan(plan, h->num_sms, B, prefix_len_host, node_offsets_host, Hq, Hkv, D, scale);
   const AttnLayout lay = attention_layout(plan, N, anc_d != nullptr, use_tc);
   if (lay.total > 0 && (!workspace_d || workspace_bytes < lay.total)) return TSV_ERR_INVALID_ARG;
   char* ws = static_cast<char*>(workspace_d);
@@ -296,19 +372,28 @@ tsv_status tsv_tree_attention(tsv_handle h, tsv_dtype dtype, const void* q_d, co
                                              Hkv, D, scale, cs));
   }
   const int di = D == 64 ? 0 : 1;
+  int64_t lmax = 1;
+  for (int b = 0; b < B; ++b) lmax = std::max<int64_t>(lmax, (int64_t)plan.prefix[b] + plan.nodes[b]);
+  CUtensorMap tmq, tmk, tmv;
+  const int tile_rows = use_keys ? kKeysTileRows : kBM;
+  const int box_rows = use_keys ? kKeysBlockKeys : kBN;
+  st = encode_q_map(h, &tmq, q_d, N, Hq, Hq / Hkv, D, tile_rows);
+  if (st != TSV_OK) return st;
+  st = encode_kv_map(h, &tmk, k_cache_d, kv_stride_b, kv_stride_l, kv_stride_h, B, lmax, Hkv, D, box_rows);
+  if (st != TSV_OK) return st;
+  st = encode_kv_map(h, &tmv, v_cache_d, kv_stride_b, kv_stride_l, kv_stride_h, B, lmax, Hkv, D, box_rows);
+  if (st != TSV_OK) return st;
+  if (use_keys) {
+    if (!h->keys_attr_set[di]) {
+      if (attention_keys_set_attributes(D) != cudaSuccess) return TSV_ERR_CUDA;
+      h->keys_attr_set[di] = true;
+    }
+    return cuda_status(launch_attention_keys(tmq, tmk, tmv, plan, parent_d, anc_d, out_d, status_d, cs));
+  }
   if (!h->tc_attr_set[di]) {
     if (attention_tc_set_attributes(D) != cudaSuccess) return TSV_ERR_CUDA;
     h->tc_attr_set[di] = true;
   }
-  int64_t lmax = 1;
-  for (int b = 0; b < B; ++b) lmax = std::max<int64_t>(lmax, (int64_t)plan.prefix[b] + plan.nodes[b]);
-  CUtensorMap tmq, tmk, tmv;
-  st = encode_q_map(h, &tmq, q_d, N, Hq, Hq / Hkv, D);
-  if (st != TSV_OK) return st;
-  st = encode_kv_map(h, &tmk, k_cache_d, kv_stride_b, kv_stride_l, kv_stride_h, B, lmax, Hkv, D);
-  if (st != TSV_OK) return st;
-  st = encode_kv_map(h, &tmv, v_cache_d, kv_stride_b, kv_stride_l, kv_stride_h, B, lmax, Hkv, D);
-  if (st != TSV_OK) return st;
   int32_t* counters = reinterpret_cast<int32_t*>(ws + lay.ctr_off);
   float* part_o = reinterpret_cast<float*>(ws + lay.part_o_off);
   float* part_lse = reinterpret_cast<float*>(ws + lay.part_lse_off);

@@ -34,6 +34,12 @@ struct AttnPlan {
   int32_t ctr_base[TSV_MAX_BATCH];  // first merge counter of request b (one per KV head x M-tile)
   int64_t part_rows_total;
   int32_t n_counters;
+  // Keys-on-lanes kernel: every request is cut into n_chunks[b] == cluster
+  // chunks of chunk_len[b] keys (a multiple of 128); the chunks of one (KV
+  // head, M-tile) group are consecutive units and form one cluster.
+  int32_t chunk_len[TSV_MAX_BATCH];
+  int32_t cluster;
+  int32_t keys_kernel;  // 1: keys-on-lanes kernel, 0: rows-on-lanes kernel
 };
 
 struct Workspace {
@@ -59,6 +65,15 @@ cudaError_t launch_attention_tc(const CUtensorMap& tmap_q, const CUtensorMap& tm
                                 int32_t* status, cudaStream_t st);
 cudaError_t attention_tc_set_attributes(int D);
 size_t attention_tc_smem_bytes(int D);
+
+constexpr int kKeysBlockKeys = 128;  // keys per block of the keys-on-lanes kernel
+constexpr int kKeysTileRows = 64;    // query rows per CTA of the keys-on-lanes kernel
+cudaError_t launch_attention_keys(const CUtensorMap& tmap_q, const CUtensorMap& tmap_k,
+                                  const CUtensorMap& tmap_v, const AttnPlan& plan,
+                                  const int32_t* parent, const uint32_t* anc, void* out,
+                                  int32_t* status, cudaStream_t st);
+cudaError_t attention_keys_set_attributes(int D);
+size_t attention_keys_smem_bytes(int D);
 
 cudaError_t launch_attention_simt(bool bf16, const void* q, const void* k, const void* v,
                                   int64_t sb, int64_t sl, int64_t sh, void* out,
