@@ -440,9 +440,11 @@ def run_ours(args, spec):
     traffic = recorded_traffic(spec.name)
     keys_kernel = all(int(n) * (spec.Hq // spec.Hkv) <= 64 for n in np.diff(trees.node_offsets)) and \
         64 % (spec.Hq // spec.Hkv) == 0
+    kernel_name = ("tree_attn_simt_kernel" if spec.dtype != "bf16" else
+                   "tree_attn_keys_kernel" if keys_kernel else "tree_attn_tc_kernel")
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "traffic": traffic,
-                "kernel": "tree_attn_keys_kernel" if keys_kernel else "tree_attn_tc_kernel",
+                "kernel": kernel_name,
                 "launch_ms": attn_ms, "algorithmic_bytes": abytes, "peak_kind": peak_kind + " hbm_gbs"}
     step_bytes = abytes + verify_bytes(spec, trees)
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
