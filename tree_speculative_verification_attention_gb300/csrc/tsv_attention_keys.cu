@@ -24,13 +24,16 @@
 //
 // When a request's keys are split into K chunks (K <= 8), the K CTAs of a
 // chunk group form one cluster: each leaves its normalised partial and
-// log2-sum-exp in its own shared memory and CTA rank 0 merges them through
-// distributed shared memory (weights first, then 16-byte loads kept in
-// flight together) — no global partials, no atomics, no second kernel.
+// log2-sum-exp in its own shared memory, and CTA rank c merges the c-th
+// share of the rows through distributed shared memory (weights first, then
+// 16-byte loads kept in flight together) — no global partials, no atomics,
+// no second kernel.
 //
 // Warp roles (320 threads): warps 0-7 key lanes (softmax, P^T, epilogue),
-// warp 8 TMA producer (Q tile, then K/V blocks of 128 keys into a 2-stage
-// ring), warp 9 tcgen05 issuer and TMEM owner.
+// warp 8 TMA producer (Q tile, then K/V blocks of 128 keys into a 3-stage
+// ring), warp 9 tcgen05 issuer and TMEM owner.  P^T of a block is written
+// over that block's K tile, which S^T has finished reading, so the ring
+// needs no separate P buffers and three 64 KB stages fit next to Q.
 #include "tsv_attention_common.cuh"
 
 namespace tsv {
@@ -48,17 +51,16 @@ constexpr int kBarKeys = 2;                  // key lanes
 template <int D>
 struct KeysCfg {
   static constexpr int kHalves = D / 64;
-  static constexpr int kStages = 2;
+  static constexpr int kStages = 3;
   static constexpr int kQBytes = kKeysRows * D * 2;
   static constexpr int kKTile = kKeysBlock * D * 2;
   static constexpr int kVTile = kKeysBlock * 128 * 2;  // always 128 d: upper half zero when D = 64
   static constexpr int kStageBytes = kKTile + kVTile;
-  static constexpr int kPBytes = kKeysBlock * kKeysRows * 2;
-  static constexpr int kOnesBytes = 128 * 128;  // 128 rows x 64 bf16 ones
+  static constexpr int kPBytes = kKeysBlock * kKeysRows * 2;  // P^T, written over the K tile
+  static constexpr int kOnesBytes = 1024;  // one 8-row atom of bf16 ones, read by every row group
   static constexpr int kOffQ = 0;
   static constexpr int kOffStage = kOffQ + kQBytes;
-  static constexpr int kOffP = kOffStage + kStages * kStageBytes;
-  static constexpr int kOffOnes = kOffP + 2 * kPBytes;
+  static constexpr int kOffOnes = kOffStage + kStages * kStageBytes;
   static constexpr int kOffDesc = kOffOnes + kOnesBytes;        // uint32 [64][2]
   static constexpr int kOffPar = kOffDesc + kKeysMaxTree * 8;   // int32 [64]
   static constexpr int kOffMref = kOffPar + kKeysMaxTree * 4;   // float [64]
@@ -72,7 +74,8 @@ struct KeysCfg {
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemBytes = kOffMisc + 32 + 1024;
   static constexpr uint32_t kTmemCols = 256;  // S0 | S1 | O^T | L^T, 64 columns each
-  static_assert(kOffStage % 1024 == 0 && kOffP % 1024 == 0 && kOffOnes % 1024 == 0, "atoms");
+  static_assert(kOffStage % 1024 == 0 && kStageBytes % 1024 == 0 && kOffOnes % 1024 == 0, "atoms");
+  static_assert(kPBytes <= kKTile, "P^T fits in the K tile it replaces");
   static_assert(kOffBar % 8 == 0, "mbarrier alignment");
   static_assert(kKeysRows * D * 4 <= kStageBytes, "partial fits in a stage");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory");
@@ -92,7 +95,6 @@ __global__ void __launch_bounds__(kKeysThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem + C::kOffQ;
   uint8_t* sStage = smem + C::kOffStage;
-  uint8_t* sP = smem + C::kOffP;
   uint8_t* sOnes = smem + C::kOffOnes;
   uint32_t* sDesc = reinterpret_cast<uint32_t*>(smem + C::kOffDesc);
   int32_t* sPar = reinterpret_cast<int32_t*>(smem + C::kOffPar);
@@ -203,7 +205,7 @@ __global__ void __launch_bounds__(kKeysThreads, 1)
       constexpr uint32_t idO = idesc_bf16_f32_ab(128, kKeysRows, 1, 1);
       constexpr uint32_t idL = idesc_bf16_f32_ab(128, kKeysRows, 0, 1);
       const uint32_t tO = tmem + 2 * kKeysRows, tL = tmem + 3 * kKeysRows;
-      const uint32_t qa = smem_u32(sQ), sa = smem_u32(sStage), pa = smem_u32(sP), oa = smem_u32(sOnes);
+      const uint32_t qa = smem_u32(sQ), sa = smem_u32(sStage), oa = smem_u32(sOnes);
       auto issue_s = [&](int j) {
         const uint32_t ka = sa + (uint32_t)((j % S) * C::kStageBytes);
         const uint32_t dst = tmem + (uint32_t)((j & 1) * kKeysRows);
@@ -216,14 +218,15 @@ __global__ void __launch_bounds__(kKeysThreads, 1)
         }
       };
       auto issue_pv = [&](int j) {
-        const uint32_t va = sa + (uint32_t)((j % S) * C::kStageBytes + C::kKTile);
-        const uint32_t pb = pa + (uint32_t)((j & 1) * C::kPBytes);
+        const uint32_t pb = sa + (uint32_t)((j % S) * C::kStageBytes);  // P^T over K(j)
+        const uint32_t va = pb + (uint32_t)C::kKTile;
 #pragma unroll
         for (int kk = 0; kk < kKeysBlock / 16; ++kk) {
           const uint64_t bdesc = sdesc_sw128(pb + kk * 2048, kKeysBlock * 128, 1024);
           const uint32_t acc = (j > 0 || kk > 0) ? 1u : 0u;
           umma_bf16(tO, sdesc_sw128(va + kk * 2048, kKeysBlock * 128, 1024), bdesc, idO, acc);
-          umma_bf16(tL, sdesc_sw128(oa + (kk & 3) * 32, 16, 1024), bdesc, idL, acc);
+          // Row-group stride 0: all 16 groups of 8 rows read the same atom of ones.
+          umma_bf16(tL, sdesc_sw128(oa + (kk & 3) * 32, 16, 0), bdesc, idL, acc);
         }
       };
       bool ok = nblk > 0 && mbar_wait(q_full, 0, abort_v) && mbar_wait(&kv_full[0], 0, abort_v);
@@ -324,9 +327,10 @@ __global__ void __launch_bounds__(kKeysThreads, 1)
       if (!full_vis && key < k_end)
         vis = (uint64_t)sDesc[2 * (key - P)] | ((uint64_t)sDesc[2 * (key - P) + 1] << 32);
       const uint32_t s_col = tmem + lane_base + (uint32_t)((j & 1) * kKeysRows);
-      float over = -INFINITY;
+      // The first block always moves the maxima (they start at -inf): skip the test.
+      float over = j == 0 ? INFINITY : -INFINITY;
 #pragma unroll 1
-      for (int g16 = 0; g16 < ngrp; ++g16) {
+      for (int g16 = 0; j > 0 && g16 < ngrp; ++g16) {
         const int c0 = g16 * 16 + h * 8;
         float sv[8];
         tmem_ld8(s_col + c0, sv);
@@ -348,19 +352,30 @@ __global__ void __launch_bounds__(kKeysThreads, 1)
       }
       if (any_over) {
         // Move the reference maxima: per-row max over this block's visible keys.
+        // Transposed warp reduction: each xor step halves the values a lane
+        // keeps, so 8 rows x 32 lanes take 4 + 2 + 1 + 2 shuffles, after which
+        // lane l holds the maximum of row c0 + ((l >> 2) & 7).
 #pragma unroll 1
         for (int g16 = 0; g16 < ngrp; ++g16) {
           const int c0 = g16 * 16 + h * 8;
           float sv[8];
           tmem_ld8(s_col + c0, sv);
           const uint32_t vm = full_vis ? 0xFFu : (uint32_t)(vis >> c0) & 0xFFu;
+          float v[8];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            float v = ((vm >> e) & 1u) ? sv[e] * sl2 : -INFINITY;
+          for (int e = 0; e < 8; ++e) v[e] = ((vm >> e) & 1u) ? sv[e] * sl2 : -INFINITY;
+          const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
+          float w4[4], w2[2];
 #pragma unroll
-            for (int o2 = 16; o2 > 0; o2 >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o2));
-            if (lane == 0) sWmax[lg * kKeysRows + c0 + e] = v;
-          }
+          for (int i = 0; i < 4; ++i)
+            w4[i] = fmaxf(b4 ? v[i + 4] : v[i], __shfl_xor_sync(0xffffffffu, b4 ? v[i] : v[i + 4], 16));
+#pragma unroll
+          for (int i = 0; i < 2; ++i)
+            w2[i] = fmaxf(b3 ? w4[i + 2] : w4[i], __shfl_xor_sync(0xffffffffu, b3 ? w4[i] : w4[i + 2], 8));
+          float w1 = fmaxf(b2 ? w2[1] : w2[0], __shfl_xor_sync(0xffffffffu, b2 ? w2[0] : w2[1], 4));
+          w1 = fmaxf(w1, __shfl_xor_sync(0xffffffffu, w1, 2));
+          w1 = fmaxf(w1, __shfl_xor_sync(0xffffffffu, w1, 1));
+          if ((lane & 3) == 0) sWmax[lg * kKeysRows + c0 + (lane >> 2)] = w1;
         }
         named_bar(kBarKeys, kKeysLaneThreads);
         if (t < rows_valid) {
@@ -393,10 +408,8 @@ __global__ void __launch_bounds__(kKeysThreads, 1)
           }
         }
       }
-      // P^T buffer j&1 was last read by PV(j-2).
-      if (j >= 2 && !__all_sync(0xffffffffu, mbar_wait(&pv_done[j & 1], ((j - 2) >> 1) & 1, abort_v)))
-        *fail_flag = 1;
-      uint8_t* prow = sP + (j & 1) * C::kPBytes + kl * 128;
+      // P^T goes over the K tile of this block: S^T(j) has finished reading it.
+      uint8_t* prow = sStage + (j % S) * C::kStageBytes + kl * 128;
 #pragma unroll 1
       for (int g16 = 0; g16 < ngrp; ++g16) {
         const int c0 = g16 * 16 + h * 8;
@@ -472,15 +485,18 @@ __global__ void __launch_bounds__(kKeysThreads, 1)
   __syncwarp();
   if (nch > 1) {
     cluster_sync_all();  // every partial of the group is in its CTA's shared memory
-    if (c == 0 && warp < 8) {
+    if (warp < 8) {
+      // Rank c merges rows [r_lo, r_hi) of the tile.
       const int t = tid;
+      const int r_lo = (c * rows_valid) / nch, r_hi = ((c + 1) * rows_valid) / nch;
+      const int nr = r_hi - r_lo;
       // Weights of the chunks for every row.
-      for (int i = t; i < nch * rows_valid; i += kKeysLaneThreads) {
-        const int cc = i / rows_valid, r = i - cc * rows_valid;
+      for (int i = t; i < nch * nr; i += kKeysLaneThreads) {
+        const int cc = i / nr, r = r_lo + (i - cc * nr);
         sWts[cc * kKeysRows + r] = ld_dsmem_f32(mapa_shared(smem_u32(sLse + r), cc));
       }
       named_bar(kBarKeys, kKeysLaneThreads);
-      if (t < rows_valid) {
+      if (t >= r_lo && t < r_hi) {
         float M = -INFINITY;
         for (int cc = 0; cc < nch; ++cc) M = fmaxf(M, sWts[cc * kKeysRows + t]);
         float wsum = 0.f;
@@ -497,8 +513,8 @@ __global__ void __launch_bounds__(kKeysThreads, 1)
       // out[row][4 d] = sum over chunks of weight x partial, 16-byte remote loads.
       constexpr int D4 = D / 4;
       const uint32_t part_s = smem_u32(sStage);
-      for (int i = t; i < rows_valid * D4; i += kKeysLaneThreads) {
-        const int r = i / D4, d4 = i - r * D4;
+      for (int i = t; i < nr * D4; i += kKeysLaneThreads) {
+        const int r = r_lo + i / D4, d4 = i % D4;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
         float4 v[8];
 #pragma unroll
@@ -519,7 +535,7 @@ __global__ void __launch_bounds__(kKeysThreads, 1)
         *reinterpret_cast<uint2*>(o) = make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
       }
     }
-    cluster_sync_all();  // peers keep their shared memory until rank 0 has read it
+    cluster_sync_all();  // every CTA keeps its shared memory until its peers have read it
   }
 
   tc_fence_before();
