@@ -370,10 +370,10 @@ def run_ours(args, spec):
             attention(c, st)
     torch.cuda.synchronize()
     # Kernels per step: one attention launch (masks built inside, splits merged
-    # inside), one for greedy verification, two for stochastic verification;
+    # inside), one for greedy verification, one for stochastic verification;
     # checked against the captured graph when torch exposes it.
     attn_kernels = 1
-    kernels_per_step = attn_kernels + (1 if gi is not None else 0) + (2 if si is not None else 0)
+    kernels_per_step = attn_kernels + (1 if gi is not None else 0) + (1 if si is not None else 0)
     counted = graph_kernel_count(g_one[0])
     if counted is not None:
         assert counted == kernels_per_step, (counted, kernels_per_step)

@@ -441,9 +441,8 @@ tsv_status tsv_tree_verify_stochastic_workspace_size(tsv_handle h, int32_t B, in
                                                      size_t* bytes) {
   if (!h || !bytes || B < 1 || B > TSV_MAX_BATCH || N < 0 || V < 1 || V > INT32_MAX)
     return TSV_ERR_INVALID_ARG;
-  const int splits = stats_splits(V, N, h->num_sms);
-  *bytes = round256((size_t)N * splits * 4) + round256((size_t)N * splits * 8) +
-           round256((size_t)B * 2 * (size_t)V * 4);
+  (void)N;
+  *bytes = round256((size_t)B * 2 * (size_t)V * 4);  // two residual rows per request
   return TSV_OK;
 }
 
@@ -462,25 +461,13 @@ tsv_status tsv_tree_verify_stochastic(tsv_handle h, const float* llm_logits_d,
   if (!(temperature > 0.f) || isinf(temperature)) return TSV_ERR_INVALID_ARG;
   if (N > 0 && (!llm_logits_d || !ssm_probs_d || !u_accept_d || !u_sample_d || !path_d))
     return TSV_ERR_INVALID_ARG;
-  const int splits = stats_splits(V, N, h->num_sms);
-  const size_t pm = round256((size_t)N * splits * 4), ps = round256((size_t)N * splits * 8);
-  const size_t need = pm + ps + round256((size_t)B * 2 * (size_t)V * 4);
+  const size_t need = round256((size_t)B * 2 * (size_t)V * 4);
   if (!workspace_d || workspace_bytes < need) return TSV_ERR_INVALID_ARG;
-  cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  char* ws = static_cast<char*>(workspace_d);
-  float* part_m = reinterpret_cast<float*>(ws);
-  double* part_s = reinterpret_cast<double*>(ws + pm);
-  float* resid = reinterpret_cast<float*>(ws + pm + ps);
-  const float inv_t = 1.0f / temperature;
-  if (N > 0) {
-    tsv_status st =
-        cuda_status(launch_row_stats(llm_logits_d, V, N, splits, inv_t, part_m, part_s, cs));
-    if (st != TSV_OK) return st;
-  }
-  return cuda_status(launch_mss_walk(llm_logits_d, ssm_probs_d, V, tree_tokens_d, parent_d,
-                                     node_offsets_d, u_accept_d, u_sample_d, inv_t, B, splits,
-                                     part_m, part_s, resid, path_d, accept_len_d, bonus_d,
-                                     n_tried_d, status_d, cs));
+  float* resid = static_cast<float*>(workspace_d);
+  return cuda_status(launch_mss_verify(llm_logits_d, ssm_probs_d, V, tree_tokens_d, parent_d,
+                                       node_offsets_d, u_accept_d, u_sample_d, 1.0f / temperature,
+                                       B, resid, path_d, accept_len_d, bonus_d, n_tried_d,
+                                       status_d, static_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

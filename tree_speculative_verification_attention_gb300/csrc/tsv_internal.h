@@ -99,16 +99,14 @@ cudaError_t launch_greedy_walk(const float* part_val, const int32_t* part_idx, i
 // verification workspace (the layout tsv_tree_verify_greedy uses).
 inline size_t greedy_counter_bytes(int32_t B) { return ((size_t)B * 4 + 255) & ~(size_t)255; }
 
-// Stochastic verification: per-row softmax statistics, then one walk CTA per request.
-int stats_splits(int64_t V, int32_t N, int num_sms);
-cudaError_t launch_row_stats(const float* logits, int64_t V, int32_t N, int splits, float inv_t,
-                             float* part_m, double* part_s, cudaStream_t st);
-cudaError_t launch_mss_walk(const float* llm_logits, const float* ssm_probs, int64_t V,
-                            const int32_t* tokens, const int32_t* parent,
-                            const int32_t* node_offsets, const float* u_acc, const float* u_smp,
-                            float inv_t, int32_t B, int splits, const float* part_m,
-                            const double* part_s, float* resid, int32_t* path,
-                            int32_t* accept_len, int32_t* bonus, int32_t* n_tried,
-                            int32_t* status, cudaStream_t st);
+// Stochastic verification: one cluster of mss_cluster_size(V) CTAs per
+// request, each owning a slice of the vocabulary.
+int mss_cluster_size(int64_t V);
+cudaError_t launch_mss_verify(const float* llm_logits, const float* ssm_probs, int64_t V,
+                              const int32_t* tokens, const int32_t* parent,
+                              const int32_t* node_offsets, const float* u_acc, const float* u_smp,
+                              float inv_t, int32_t B, float* resid, int32_t* path,
+                              int32_t* accept_len, int32_t* bonus, int32_t* n_tried,
+                              int32_t* status, cudaStream_t st);
 
 }  // namespace tsv

@@ -11,14 +11,14 @@
 //                          links from the root.
 // Stochastic, multi-step speculative sampling (SpecInfer §1 Correctness, §4
 // Token Verification):
-//   row_stats_kernel       grid (splits, N): per row max and compensated
-//                          sum of exp(l/T - max) over a vocab slice.
-//   mss_walk_kernel        grid B, 1024 threads: the sequential walk.  An
-//                          accept test needs only p(x) and q(x); a rejection
-//                          makes one vocab-wide pass that writes the residual
-//                          max(0, p - q) into the workspace and sums it; the
-//                          bonus token is drawn by a block-wide inverse-CDF
-//                          scan.
+//   mss_verify_kernel      one cluster of up to 8 CTAs per request, each CTA
+//                          owning a slice of the vocabulary.  The walk is
+//                          sequential; every vocab-wide step in it is split
+//                          over the cluster: the softmax statistics of each
+//                          row the walk visits (only those rows are read), the
+//                          residual pass max(0, p - q) after a rejection, and
+//                          the inverse-CDF draw of the bonus token.  Partial
+//                          results meet in distributed shared memory.
 #include <float.h>
 #include <math.h>
 
@@ -284,8 +284,11 @@ cudaError_t launch_greedy_walk(const float* part_val, const int32_t* part_idx, i
 
 namespace {
 
-constexpr int kStatsThreads = 256;
-constexpr int kWalkThreads = 1024;
+constexpr int kMssThreads = 256;
+constexpr int kMssWarps = kMssThreads / 32;
+constexpr int kMssMaxCluster = 8;
+constexpr int64_t kMssMinSlice = 4096;  // vocab entries per CTA at least
+constexpr int kMssGroups = 4;           // 4-float groups in flight per thread
 
 // exp(a - m) with the subtraction's rounding error folded back in (TwoSum:
 // a - m = d + err exactly), so the result is as accurate as expf itself even
@@ -303,79 +306,94 @@ __device__ __forceinline__ double warp_sum_d(double v) {
   return v;
 }
 
-// Block-wide sum in fp64 (every thread gets the result).  `scratch` holds 32 doubles.
-__device__ double block_sum_d(double v, double* scratch) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
-  v = warp_sum_d(v);
+// Block-wide sums of three fp64 values (every thread gets them); red holds 3 x 32 doubles.
+__device__ void block_sum3(double& a, double& b, double& c, double* red) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  a = warp_sum_d(a);
+  b = warp_sum_d(b);
+  c = warp_sum_d(c);
+  __syncthreads();  // red is free
+  if (lane == 0) {
+    red[warp] = a;
+    red[32 + warp] = b;
+    red[64 + warp] = c;
+  }
   __syncthreads();
-  if (lane == 0) scratch[warp] = v;
-  __syncthreads();
-  double t = lane < nw ? scratch[lane] : 0.0;
-  t = warp_sum_d(t);
-  return t;
+  a = warp_sum_d(lane < kMssWarps ? red[lane] : 0.0);
+  b = warp_sum_d(lane < kMssWarps ? red[32 + lane] : 0.0);
+  c = warp_sum_d(lane < kMssWarps ? red[64 + lane] : 0.0);
 }
+
+__device__ float block_max(float v, double* red) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  float* r = reinterpret_cast<float*>(red);
+  __syncthreads();
+  if (lane == 0) r[warp] = v;
+  __syncthreads();
+  v = lane < kMssWarps ? r[lane] : -INFINITY;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+__device__ __forceinline__ double ld_dsmem_f64(uint32_t addr) {
+  double v;
+  asm volatile("ld.shared::cluster.f64 %0, [%1];" : "=d"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+// Four consecutive floats at p[y] (16-byte load when rows are 16-byte aligned).
+template <int kind>  // 0: read-only, 1: streamed once, 2: read-write scratch
+__device__ __forceinline__ float4 load4(const float* p, int64_t y, bool vec) {
+  if (vec) {
+    const float4* q = reinterpret_cast<const float4*>(p + y);
+    return kind == 0 ? __ldg(q) : kind == 1 ? __ldcs(q) : *q;
+  }
+  return make_float4(p[y], p[y + 1], p[y + 2], p[y + 3]);
+}
+
+__device__ __forceinline__ float at(const float4& v, int e) {
+  return e == 0 ? v.x : e == 1 ? v.y : e == 2 ? v.z : v.w;
+}
+
+// The CTA's vocabulary slice is visited in 4-float groups: thread t takes
+// groups t, t + T, t + 2T, ... (T threads), kMssGroups groups per round so that
+// their loads are in flight together.  body(y, four floats ...) sees full
+// groups; a ragged end (hi - lo not a multiple of 4) goes element by element.
+struct Slice {
+  int64_t lo, hi;
+};
 
 }  // namespace
 
-__global__ void __launch_bounds__(kStatsThreads)
-    row_stats_kernel(const float* __restrict__ logits, int64_t V, int splits, float inv_t,
-                     float* __restrict__ part_m, double* __restrict__ part_s) {
-  const int row = blockIdx.y, s = blockIdx.x;
-  const int64_t per = slice_len(V, splits);
-  const int64_t lo = (int64_t)s * per, hi = min(V, lo + per);
-  const float* x = logits + (size_t)row * (size_t)V;
-  // Pass 1: max of the slice.
-  float m = -INFINITY;
-  for (int64_t k = lo + threadIdx.x; k < hi; k += kStatsThreads) m = fmaxf(m, __ldg(x + k) * inv_t);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-  __shared__ float redm[kStatsThreads / 32];
-  __shared__ double reds[32];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (lane == 0) redm[warp] = m;
-  __syncthreads();
-  m = -INFINITY;
-#pragma unroll
-  for (int w = 0; w < kStatsThreads / 32; ++w) m = fmaxf(m, redm[w]);
-  // Pass 2 (the slice is now in L1/L2): compensated sum of exp(z - m).
-  CompSum acc;
-  for (int64_t k = lo + threadIdx.x; k < hi; k += kStatsThreads)
-    acc.add(exp_diff(__ldg(x + k) * inv_t, m));
-  const double tot = block_sum_d(acc.value(), reds);
-  if (threadIdx.x == 0) {
-    part_m[(size_t)row * splits + s] = m;
-    part_s[(size_t)row * splits + s] = tot;
-  }
-}
-
-int stats_splits(int64_t V, int32_t N, int num_sms) { return greedy_splits(V, N, num_sms); }
-
-cudaError_t launch_row_stats(const float* logits, int64_t V, int32_t N, int splits, float inv_t,
-                             float* part_m, double* part_s, cudaStream_t st) {
-  dim3 grid(splits, N);
-  row_stats_kernel<<<grid, kStatsThreads, 0, st>>>(logits, V, splits, inv_t, part_m, part_s);
-  return cudaGetLastError();
-}
-
-__global__ void __launch_bounds__(kWalkThreads)
-    mss_walk_kernel(const float* __restrict__ llm_logits, const float* __restrict__ ssm_probs,
-                    int64_t V, const int32_t* __restrict__ tokens,
-                    const int32_t* __restrict__ parent, const int32_t* __restrict__ node_offsets,
-                    const float* __restrict__ u_acc, const float* __restrict__ u_smp, float inv_t,
-                    int splits, const float* __restrict__ part_m, const double* __restrict__ part_s,
-                    float* __restrict__ resid_all, int32_t* __restrict__ path,
-                    int32_t* __restrict__ accept_len, int32_t* __restrict__ bonus,
-                    int32_t* __restrict__ n_tried, int32_t* __restrict__ status) {
+// Multi-step speculative sampling: one cluster of `ncl` CTAs per request, CTA
+// rank r owning vocab slice r.  All walk decisions are taken identically by
+// every CTA from values every CTA holds: the children and tokens, the row
+// statistics and residual sums (combined in rank order through distributed
+// shared memory), and p at the next child's token, which the residual pass of
+// the CTA owning that token publishes with the sums.  A CTA therefore reads
+// and writes only its own slice of the logits, proposals and residual rows.
+__global__ void __launch_bounds__(kMssThreads, 2)
+    mss_verify_kernel(const float* __restrict__ llm_logits, const float* __restrict__ ssm_probs,
+                      int64_t V, const int32_t* __restrict__ tokens,
+                      const int32_t* __restrict__ parent, const int32_t* __restrict__ node_offsets,
+                      const float* __restrict__ u_acc, const float* __restrict__ u_smp, float inv_t,
+                      int ncl, int vec, float* __restrict__ resid_all, int32_t* __restrict__ path,
+                      int32_t* __restrict__ accept_len, int32_t* __restrict__ bonus,
+                      int32_t* __restrict__ n_tried, int32_t* __restrict__ status) {
   __shared__ int32_t first_child[TSV_MAX_NODES];
   __shared__ int32_t next_sib[TSV_MAX_NODES];
-  __shared__ float row_m[TSV_MAX_NODES];
-  __shared__ double row_s[TSV_MAX_NODES];
-  __shared__ double scratch[32];
-  __shared__ double scan_s[kWalkThreads / 32];
+  __shared__ double red[96];
+  __shared__ double scan_s[kMssWarps];
+  __shared__ __align__(16) double pub[2][4];  // exchange slots, alternating
   __shared__ int bad;
   __shared__ int pick_s, last_s;
-  const int b = blockIdx.x;
+  const int b = blockIdx.x / ncl;
+  const int rank = blockIdx.x - b * ncl;  // == %cluster_ctarank for 1-D clusters of ncl
   const int tid = threadIdx.x;
+  const int T = blockDim.x;
   if (tid == 0) {
     pick_s = INT32_MAX;
     last_s = -1;
@@ -384,26 +402,28 @@ __global__ void __launch_bounds__(kWalkThreads)
   const int n = node_offsets[b + 1] - off;
   const int code = validate_verify_tree(parent + off, n, &bad);
   if (code) {
-    fail_request(path + off, n, accept_len + b, bonus + b, n_tried ? n_tried + b : nullptr,
-                 status + b, code);
-    return;
+    if (rank == 0)
+      fail_request(path + off, n, accept_len + b, bonus + b, n_tried ? n_tried + b : nullptr,
+                   status + b, code);
+    return;  // uniform over the cluster: every CTA sees the same tree
   }
   const int32_t* par = parent + off;
   // Tokens index the vocabulary rows: reject out-of-range ones before any access.
-  for (int c = 1 + tid; c < n; c += blockDim.x) {
+  for (int c = 1 + tid; c < n; c += T) {
     const int x = tokens[off + c];
     if (x < 0 || (int64_t)x >= V) atomicMax(&bad, TSV_ERR_INVALID_ARG);
   }
   __syncthreads();
   if (bad) {
-    fail_request(path + off, n, accept_len + b, bonus + b, n_tried ? n_tried + b : nullptr,
-                 status + b, bad);
+    if (rank == 0)
+      fail_request(path + off, n, accept_len + b, bonus + b, n_tried ? n_tried + b : nullptr,
+                   status + b, bad);
     return;
   }
   // Sibling lists in increasing index order.
-  for (int c = tid; c < n; c += blockDim.x) first_child[c] = INT32_MAX;
+  for (int c = tid; c < n; c += T) first_child[c] = INT32_MAX;
   __syncthreads();
-  for (int c = 1 + tid; c < n; c += blockDim.x) {
+  for (int c = 1 + tid; c < n; c += T) {
     const int p = par[c];
     atomicMin(&first_child[p], c);
     int nx = -1;
@@ -415,86 +435,224 @@ __global__ void __launch_bounds__(kWalkThreads)
     }
     next_sib[c] = nx;
   }
-  // Row statistics of every node: merge the vocab slices.
-  for (int u = tid; u < n; u += blockDim.x) {
-    float m = -INFINITY;
-    for (int s = 0; s < splits; ++s) m = fmaxf(m, part_m[(size_t)(off + u) * splits + s]);
-    double sum = 0.0;
-    for (int s = 0; s < splits; ++s) {
-      const size_t k = (size_t)(off + u) * splits + s;
-      if (part_m[k] != -INFINITY) sum += part_s[k] * (double)exp_diff(part_m[k], m);
-    }
-    row_m[u] = m;
-    row_s[u] = sum;
-  }
   __syncthreads();
 
+  // This CTA's slice (a multiple of 4 long, so 16-byte aligned rows stay aligned).
+  const int64_t per = (((V + ncl - 1) / ncl) + 3) & ~int64_t(3);
+  const int64_t lo = min(V, (int64_t)rank * per), hi = min(V, lo + per);
+  const int64_t n4 = (hi - lo) >> 2;  // full groups
   float* resid[2] = {resid_all + (size_t)b * 2 * (size_t)V, resid_all + ((size_t)b * 2 + 1) * (size_t)V};
+  int xk = 0;  // exchanges so far (the same count in every CTA)
+  // Publishes three values, waits for the cluster, returns the rank-ordered
+  // sums of slots 0..2 over the cluster (slot 0 may instead be max-combined).
+  auto exchange = [&](double v0, double v1, double v2) {
+    if (tid == 0) {
+      pub[xk & 1][0] = v0;
+      pub[xk & 1][1] = v1;
+      pub[xk & 1][2] = v2;
+    }
+    cluster_sync_all();
+  };
+  auto peer = [&](int slot, int r) {
+    return ld_dsmem_f64(mapa_shared(smem_u32(&pub[xk & 1][slot]), (uint32_t)r));
+  };
+  const int lane = tid & 31;
+
+  // Row statistics of node u's logits: m = max(l / T), s = sum exp(l / T - m).
+  float m_u = 0.f, inv_s = 0.f;
+  auto row_stats = [&](int u) {
+    const float* lrow = llm_logits + (size_t)(off + u) * (size_t)V;
+    float m = -INFINITY;
+    for (int64_t g0 = tid; g0 < n4; g0 += (int64_t)T * kMssGroups) {
+      float4 v[kMssGroups];
+#pragma unroll
+      for (int k = 0; k < kMssGroups; ++k) {
+        const int64_t g = g0 + (int64_t)k * T;
+        if (g < n4) v[k] = load4<0>(lrow, lo + 4 * g, vec);
+      }
+#pragma unroll
+      for (int k = 0; k < kMssGroups; ++k)
+        if (g0 + (int64_t)k * T < n4)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) m = fmaxf(m, at(v[k], e) * inv_t);
+    }
+    for (int64_t y = lo + 4 * n4 + tid; y < hi; y += T) m = fmaxf(m, lrow[y] * inv_t);
+    m = block_max(m, red);
+    CompSum acc;
+    for (int64_t g0 = tid; g0 < n4; g0 += (int64_t)T * kMssGroups) {
+      float4 v[kMssGroups];
+#pragma unroll
+      for (int k = 0; k < kMssGroups; ++k) {
+        const int64_t g = g0 + (int64_t)k * T;
+        if (g < n4) v[k] = load4<0>(lrow, lo + 4 * g, vec);
+      }
+#pragma unroll
+      for (int k = 0; k < kMssGroups; ++k)
+        if (g0 + (int64_t)k * T < n4)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) acc.add(exp_diff(at(v[k], e) * inv_t, m));
+    }
+    for (int64_t y = lo + 4 * n4 + tid; y < hi; y += T) acc.add(exp_diff(lrow[y] * inv_t, m));
+    double s = acc.value(), z1 = 0.0, z2 = 0.0;
+    block_sum3(s, z1, z2, red);
+    exchange((double)m, s, 0.0);
+    // Combine in rank order (identical in every CTA): M = max m_r, S = sum s_r e^(m_r - M).
+    const double mine_m = lane < ncl ? peer(0, lane) : -INFINITY;
+    const double mine_s = lane < ncl ? peer(1, lane) : 0.0;
+    float M = -INFINITY;
+    for (int r = 0; r < ncl; ++r) M = fmaxf(M, (float)__shfl_sync(0xffffffffu, mine_m, r));
+    double S = 0.0;
+    for (int r = 0; r < ncl; ++r) {
+      const float mr = (float)__shfl_sync(0xffffffffu, mine_m, r);
+      const double sr = __shfl_sync(0xffffffffu, mine_s, r);
+      if (mr != -INFINITY) S += sr * (double)exp_diff(mr, M);
+    }
+    ++xk;
+    m_u = M;
+    inv_s = (float)(1.0 / S);
+  };
+
   int u = 0, len = 1, cur = 0, tried = 0;
   bool from_resid = false;  // false: p = softmax(row u); true: p = resid[cur] / Z
+  bool px_known = false;    // p at the current child's token came with the last exchange
+  float px_next = 0.f;
   double Z = 0.0;
-  if (tid == 0) path[off] = 0;
+  if (rank == 0 && tid == 0) path[off] = 0;
+  row_stats(0);
   while (true) {
     int accepted = -1;
     int c = first_child[u];
     if (c == INT32_MAX) c = -1;
     const float* lrow = llm_logits + (size_t)(off + u) * (size_t)V;
-    const float m_u = row_m[u];
-    const float inv_s = (float)(1.0 / row_s[u]);
-    while (c >= 0 && accepted < 0) {
+    while (c >= 0) {
       const int x = tokens[off + c];
       const float* q = ssm_probs + (size_t)(off + c) * (size_t)V;
-      const float inv_z = (float)(1.0 / Z);
       // p(x) of the current distribution (fp32, ~2 ulp), compared in fp64.
-      const float px = from_resid ? resid[cur][x] * inv_z
-                                  : exp_diff(__ldg(lrow + x) * inv_t, m_u) * inv_s;
+      const float px = px_known ? px_next : exp_diff(__ldg(lrow + x) * inv_t, m_u) * inv_s;
       ++tried;
       if ((double)__ldg(u_acc + off + c) * (double)__ldg(q + x) < (double)px) {
         accepted = c;
         break;
       }
-      // Rejected: residual pass over the vocabulary, r = max(0, p - q).
+      // Rejected: residual pass over the slice, r = max(0, p - q).  The owner
+      // of the next child's token records r and p there for the exchange.
+      const int cn = next_sib[c];
+      const int64_t xn = cn >= 0 ? (int64_t)tokens[off + cn] : -1;
       const int nxt = cur ^ 1;
+      const float inv_z = (float)(1.0 / Z);
+      const float* rin = resid[cur];
+      float* rout = resid[nxt];
       CompSum acc;
-      for (int64_t y = tid; y < V; y += blockDim.x) {
-        const float py = from_resid ? resid[cur][y] * inv_z
-                                    : exp_diff(__ldg(lrow + y) * inv_t, m_u) * inv_s;
-        const float r = fmaxf(py - __ldcs(q + y), 0.0f);
-        resid[nxt][y] = r;
-        acc.add(r);
+      double r_x = 0.0, p_x = 0.0;
+      for (int64_t g0 = tid; g0 < n4; g0 += (int64_t)T * kMssGroups) {
+        float4 a[kMssGroups], qq[kMssGroups];
+#pragma unroll
+        for (int k = 0; k < kMssGroups; ++k) {
+          const int64_t g = g0 + (int64_t)k * T;
+          if (g < n4) {
+            a[k] = from_resid ? load4<2>(rin, lo + 4 * g, vec) : load4<0>(lrow, lo + 4 * g, vec);
+            qq[k] = load4<1>(q, lo + 4 * g, vec);
+          }
+        }
+#pragma unroll
+        for (int k = 0; k < kMssGroups; ++k) {
+          const int64_t g = g0 + (int64_t)k * T;
+          if (g < n4) {
+            const int64_t y = lo + 4 * g;
+            float r[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float py = from_resid ? at(a[k], e) * inv_z : exp_diff(at(a[k], e) * inv_t, m_u) * inv_s;
+              r[e] = fmaxf(py - at(qq[k], e), 0.0f);
+              acc.add(r[e]);
+              if (y + e == xn) {
+                r_x = r[e];
+                p_x = py;
+              }
+            }
+            if (vec) {
+              *reinterpret_cast<float4*>(rout + y) = make_float4(r[0], r[1], r[2], r[3]);
+            } else {
+#pragma unroll
+              for (int e = 0; e < 4; ++e) rout[y + e] = r[e];
+            }
+          }
+        }
       }
-      const double Znew = block_sum_d(acc.value(), scratch);
+      for (int64_t y = lo + 4 * n4 + tid; y < hi; y += T) {
+        const float py = from_resid ? rin[y] * inv_z : exp_diff(__ldg(lrow + y) * inv_t, m_u) * inv_s;
+        const float r = fmaxf(py - __ldcs(q + y), 0.0f);
+        rout[y] = r;
+        acc.add(r);
+        if (y == xn) {
+          r_x = r;
+          p_x = py;
+        }
+      }
+      double zs = acc.value();
+      block_sum3(zs, r_x, p_x, red);
+      exchange(zs, r_x, p_x);
+      double zr = lane < ncl ? peer(0, lane) : 0.0;
+      double rr = lane < ncl ? peer(1, lane) : 0.0;
+      double pr = lane < ncl ? peer(2, lane) : 0.0;
+      double Znew = 0.0, rxn = 0.0, pxn = 0.0;
+      for (int r = 0; r < ncl; ++r) {
+        Znew += __shfl_sync(0xffffffffu, zr, r);
+        rxn += __shfl_sync(0xffffffffu, rr, r);  // one owner, the rest add zeros
+        pxn += __shfl_sync(0xffffffffu, pr, r);
+      }
+      ++xk;
       if (Znew > 0.0) {  // else p = q up to rounding: keep p
         cur = nxt;
         Z = Znew;
         from_resid = true;
+        px_next = (float)rxn * (float)(1.0 / Znew);
+      } else {
+        px_next = (float)pxn;
       }
-      __syncthreads();  // residual row complete before anyone reads it
-      c = next_sib[c];
+      px_known = true;
+      c = cn;
     }
     if (accepted < 0) break;
     u = accepted;
-    if (tid == 0) path[off + len] = u;
+    if (rank == 0 && tid == 0) path[off + len] = u;
     ++len;
     from_resid = false;
+    px_known = false;
+    row_stats(u);
   }
+
   // Bonus token: smallest y with cumsum(w)[y] > u_smp[u] * sum(w), w = the
-  // unnormalised current distribution.  Each thread owns a contiguous slice.
+  // unnormalised current distribution.  Each thread owns a contiguous run of
+  // its CTA's slice; runs and slices are in vocabulary order.
   {
     const float* lrow = llm_logits + (size_t)(off + u) * (size_t)V;
-    const float m_u = row_m[u];
-    const int64_t per = (V + blockDim.x - 1) / blockDim.x;
-    const int64_t lo = (int64_t)tid * per, hi = min(V, lo + per);
+    const float* rin = resid[cur];
+    const int64_t per_t = ((((hi - lo) + T - 1) / T) + 3) & ~int64_t(3);
+    const int64_t tlo = min(hi, lo + (int64_t)tid * per_t), thi = min(hi, tlo + per_t);
+    auto weight = [&](float a) { return from_resid ? a : exp_diff(a * inv_t, m_u); };
     CompSum acc;
     int64_t last_pos = -1;
-    for (int64_t y = lo; y < hi; ++y) {
-      const float w = from_resid ? resid[cur][y] : exp_diff(__ldg(lrow + y) * inv_t, m_u);
-      acc.add(w);
-      if (w > 0.0f) last_pos = y;
+    {
+      int64_t y = tlo;
+      for (; y + 4 <= thi; y += 4) {
+        const float4 a = from_resid ? load4<2>(rin, y, vec) : load4<0>(lrow, y, vec);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float w = weight(at(a, e));
+          acc.add(w);
+          if (w > 0.0f) last_pos = y + e;
+        }
+      }
+      for (; y < thi; ++y) {
+        const float w = weight(from_resid ? rin[y] : lrow[y]);
+        acc.add(w);
+        if (w > 0.0f) last_pos = y;
+      }
     }
     const double mine = acc.value();
-    // Exclusive prefix over threads (fp64): warp scan, then across warps.
-    const int warp = tid >> 5, lane = tid & 31;
+    // Exclusive prefix over the CTA's threads (fp64): warp scan, then across warps.
+    const int warp = tid >> 5;
     double incl = mine;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -504,52 +662,85 @@ __global__ void __launch_bounds__(kWalkThreads)
     if (lane == 31) scan_s[warp] = incl;
     if (last_pos >= 0) atomicMax(&last_s, (int)last_pos);
     __syncthreads();
-    double wbase = 0.0, total = 0.0;
-    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) {
+    double wbase = 0.0, cta_total = 0.0;
+    for (int w = 0; w < kMssWarps; ++w) {
       if (w < warp) wbase += scan_s[w];
-      total += scan_s[w];
+      cta_total += scan_s[w];
     }
-    const double excl = wbase + incl - mine;
+    exchange(cta_total, (double)last_s, 0.0);
+    const double tr = lane < ncl ? peer(0, lane) : 0.0;
+    const double lr = lane < ncl ? peer(1, lane) : -1.0;
+    double base = 0.0, total = 0.0, last_all = -1.0;
+    for (int r = 0; r < ncl; ++r) {
+      const double t = __shfl_sync(0xffffffffu, tr, r);
+      if (r < rank) base += t;
+      total += t;
+      last_all = fmax(last_all, __shfl_sync(0xffffffffu, lr, r));
+    }
+    ++xk;
+    const double excl = base + wbase + incl - mine;
     const double target = (double)__ldg(u_smp + off + u) * total;
     if (mine > 0.0 && excl <= target && target < excl + mine) {
-      // This slice holds the crossing; walk it in order.
+      // This run holds the crossing; walk it in order.
       int64_t pick = -1;
       CompSum run;
-      for (int64_t y = lo; y < hi; ++y) {
-        const float w = from_resid ? resid[cur][y] : exp_diff(__ldg(lrow + y) * inv_t, m_u);
+      for (int64_t y = tlo; y < thi; ++y) {
+        const float w = weight(from_resid ? rin[y] : lrow[y]);
         run.add(w);
         if (excl + run.value() > target) {
           pick = y;
           break;
         }
       }
-      if (pick < 0) pick = last_pos;  // rounding inside the slice
+      if (pick < 0) pick = last_pos;  // rounding inside the run
       atomicMin(&pick_s, (int)pick);
     }
     __syncthreads();
-    if (tid == 0) {
+    exchange((double)pick_s, 0.0, 0.0);
+    if (rank == 0 && tid == 0) {
+      int pick = INT32_MAX;
+      for (int r = 0; r < ncl; ++r) pick = min(pick, (int)peer(0, r));
       // No crossing (rounding left the target at the total): last positive entry.
-      bonus[b] = pick_s != INT32_MAX ? pick_s : last_s;
+      bonus[b] = pick != INT32_MAX ? pick : (int)last_all;
       accept_len[b] = len - 1;
       if (n_tried) n_tried[b] = tried;
       status[b] = TSV_OK;
     }
+    cluster_sync_all();  // peers keep their exchange slots until rank 0 has read them
   }
-  for (int i = len + tid; i < n; i += blockDim.x) path[off + i] = -1;
+  if (rank == 0)
+    for (int i = len + tid; i < n; i += T) path[off + i] = -1;
 }
 
-cudaError_t launch_mss_walk(const float* llm_logits, const float* ssm_probs, int64_t V,
-                            const int32_t* tokens, const int32_t* parent,
-                            const int32_t* node_offsets, const float* u_acc, const float* u_smp,
-                            float inv_t, int32_t B, int splits, const float* part_m,
-                            const double* part_s, float* resid, int32_t* path,
-                            int32_t* accept_len, int32_t* bonus, int32_t* n_tried,
-                            int32_t* status, cudaStream_t st) {
-  mss_walk_kernel<<<B, kWalkThreads, 0, st>>>(llm_logits, ssm_probs, V, tokens, parent,
-                                              node_offsets, u_acc, u_smp, inv_t, splits, part_m,
-                                              part_s, resid, path, accept_len, bonus, n_tried,
-                                              status);
-  return cudaGetLastError();
+int mss_cluster_size(int64_t V) {
+  const int64_t c = (V + kMssMinSlice - 1) / kMssMinSlice;
+  return (int)(c < 1 ? 1 : (c > kMssMaxCluster ? kMssMaxCluster : c));
+}
+
+cudaError_t launch_mss_verify(const float* llm_logits, const float* ssm_probs, int64_t V,
+                              const int32_t* tokens, const int32_t* parent,
+                              const int32_t* node_offsets, const float* u_acc, const float* u_smp,
+                              float inv_t, int32_t B, float* resid, int32_t* path,
+                              int32_t* accept_len, int32_t* bonus, int32_t* n_tried,
+                              int32_t* status, cudaStream_t st) {
+  const int ncl = mss_cluster_size(V);
+  const int vec = (V % 4 == 0) && ((reinterpret_cast<uintptr_t>(llm_logits) |
+                                    reinterpret_cast<uintptr_t>(ssm_probs) |
+                                    reinterpret_cast<uintptr_t>(resid)) & 15) == 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(B * ncl));
+  cfg.blockDim = dim3(kMssThreads);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)ncl;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, mss_verify_kernel, llm_logits, ssm_probs, V, tokens, parent,
+                            node_offsets, u_acc, u_smp, inv_t, ncl, vec, resid, path, accept_len,
+                            bonus, n_tried, status);
 }
 
 }  // namespace tsv
