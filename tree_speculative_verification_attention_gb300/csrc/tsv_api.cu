@@ -48,8 +48,7 @@ tsv_status check_batch(int32_t B, const int32_t* prefix_len, const int32_t* node
 // Splits every request's keys into chunks of one common length (a multiple of
 // the 64-key block) so that the CTAs fill whole waves of SMs: the estimated
 // makespan is waves * (chunk + per-CTA overhead), minimised over the chunk
-// counts that cut the longest request into 1 .. 64 pieces.  A CTA takes two
-// 128-row M-tiles of one (request, KV head, chunk).
+// counts that cut the longest request into 1 .. 64 pieces.
 void build_plan(AttnPlan& p, int num_sms, int32_t B, const int32_t* prefix_len,
                 const int32_t* node_offsets, int32_t Hq, int32_t Hkv, int32_t D, float scale) {
   memset(&p, 0, sizeof(p));
@@ -73,7 +72,7 @@ void build_plan(AttnPlan& p, int num_sms, int32_t B, const int32_t* prefix_len,
     const int64_t chunk = cdiv(cdiv(lmax, pieces), kBN) * kBN;
     int64_t units = 0;
     for (int b = 0; b < B; ++b)
-      units += (int64_t)Hkv * cdiv(p.mtiles[b], 2) * cdiv((int64_t)p.prefix[b] + p.nodes[b], chunk);
+      units += (int64_t)Hkv * p.mtiles[b] * cdiv((int64_t)p.prefix[b] + p.nodes[b], chunk);
     const int64_t waves = cdiv(units, num_sms);
     const int64_t cost = waves * (chunk + overhead);
     if (cost < best_cost || (cost == best_cost && chunk > best_chunk)) {
@@ -88,9 +87,9 @@ void build_plan(AttnPlan& p, int num_sms, int32_t B, const int32_t* prefix_len,
     const int64_t L = (int64_t)p.prefix[b] + p.nodes[b];
     p.n_chunks[b] = p.mtiles[b] > 0 ? (int32_t)cdiv(L, best_chunk) : 0;
     p.unit_start[b] = (int32_t)units;
-    units += (int64_t)Hkv * cdiv(p.mtiles[b], 2) * p.n_chunks[b];
+    units += (int64_t)Hkv * p.mtiles[b] * p.n_chunks[b];
     p.ctr_base[b] = (int32_t)ctrs;
-    ctrs += (int64_t)Hkv * cdiv(p.mtiles[b], 2);
+    ctrs += (int64_t)Hkv * p.mtiles[b];
     if (p.n_chunks[b] > 1) {
       p.part_row[b] = rows;
       rows += (int64_t)Hkv * p.n_chunks[b] * p.nodes[b] * p.G;

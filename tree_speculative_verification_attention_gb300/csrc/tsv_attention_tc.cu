@@ -9,28 +9,33 @@
 // Implementation) becomes a split of each request's keys into chunks whose
 // partial results are merged by log-sum-exp.
 //
-// One CTA = one unit (request b, KV head g, key chunk c, pair of M-tiles).
-// The 128 query rows of an M-tile are (node, head-in-group) pairs: all query
-// heads that share KV head g sit in the same tiles, and the two tiles of a
-// CTA read every streamed K/V block once from shared memory, so each K/V row
-// serves up to 256 query rows.  Warp roles (320 threads):
-//   warp 8        TMA producer: the Q tiles first, then K and V blocks of 64
-//                 rows x D, 128-byte swizzled, into a ring of kStages stages.
-//   warp 9        tcgen05 issuer and TMEM owner (512 columns: per tile two S
-//                 buffers and the O accumulator).  Per block: S_t = Q_t K^T
-//                 for both tiles, then O_t += P_t V with P_t read from TMEM.
-//   warps 0-3,    softmax warpgroup of tile 0 and tile 1: one thread per query
-//   warps 4-7     row (= TMEM lane).  Set-up: the ancestor bitset of the row's
-//                 node (prepared, or by walking parent[] up to the root).
-//                 Loop: read S, mask the tree part of the keys with the bitset,
-//                 online softmax in base 2 with a lazily moved reference
-//                 maximum, P in bf16 written back over S in TMEM, O rescaled in
-//                 TMEM when the reference moves.  End: normalise and store the
-//                 output; when a request's keys are split over several CTAs,
+// One CTA = one unit (request b, KV head g, key chunk c, M-tile mt).  Its 128
+// query rows are (node, head-in-group) pairs: all query heads that share KV
+// head g sit in the same tiles, so each streamed K/V row serves every tree
+// node and every grouped head at once.  Keys go in blocks of 128, so both
+// MMAs of a block have N >= 128 (smaller N runs the tensor pipe below its
+// rate).  Warp roles (320 threads):
+//   warp 8        TMA producer.  Lane 0: the Q tile, then K blocks into a
+//                 3-stage ring, each released as soon as S has read it; lane
+//                 1: V blocks into a 2-stage ring, released after PV.
+//   warp 9        tcgen05 issuer and TMEM owner (S0 | S1 | O0 | O1): S(j+1) =
+//                 Q K^T is issued before PV(j), so the next scores are ready
+//                 when the softmax of a block ends; O_h += P_h V_h reads P_h
+//                 from TMEM, one accumulator per key half.
+//   warps 0-7     softmax.  Warp w serves the rows on TMEM lanes 32(w%4).. and
+//                 key half h = w/4 (64 keys) of every block.  The two halves
+//                 of a row are independent online softmaxes (own reference
+//                 maximum, row sum and O accumulator), so no barrier is needed
+//                 inside the loop; they are combined once at the end.  Set-up:
+//                 the ancestor bitset of the row's node (prepared, or by
+//                 walking parent[] up to the root).  Loop: read S, mask the
+//                 tree part of the keys with the bitset, base-2 softmax with a
+//                 lazily moved reference maximum, P in bf16 written back over
+//                 the thread's own S columns, O_h rescaled in TMEM when the
+//                 reference moves.  End: combine the halves, normalise and
+//                 store; when a request's keys are split over several CTAs,
 //                 store a partial + log2-sum-exp and let the last CTA of the
 //                 group (atomic counter, no waiting) merge the partials.
-// Two softmax warpgroups put two warps on each SM sub-partition, so one
-// warp's exponentials overlap the other's TMEM traffic and waits.
 #include <cuda_bf16.h>
 #include <math.h>
 
@@ -38,35 +43,39 @@
 
 namespace tsv {
 
-constexpr int kTcSoftmaxThreads = 256;  // two warpgroups, one per M-tile
+constexpr int kTcSoftmaxThreads = 256;
 constexpr int kTcThreads = kTcSoftmaxThreads + 64;
 constexpr int kTcProducerWarp = 8, kTcMmaWarp = 9;
+constexpr int kHalfKeys = kBN / 2;         // keys of a block per softmax thread
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: P stays below 2^8 between rescales
 constexpr int kBarTcSetup = 1;             // softmax warps + MMA warp
-constexpr int kBarTcSoftmax = 2;           // both softmax warpgroups
+constexpr int kBarTcSoftmax = 2;           // softmax warps
 
 template <int D>
 struct TcCfg {
-  static constexpr int kHalves = D / 64;               // 128-byte column groups per row
-  static constexpr int kStages = (D == 128) ? 4 : 8;   // K/V ring depth
-  static constexpr int kQTile = kBM * D * 2;           // one M-tile of Q
-  static constexpr int kTileBytes = kBN * D * 2;       // one K (or V) block
+  static constexpr int kHalves = D / 64;      // 128-byte column groups per row
+  static constexpr int kKStages = 3, kVStages = 2;
+  static constexpr int kQBytes = kBM * D * 2;
+  static constexpr int kTileBytes = kBN * D * 2;  // one K (or V) block
   static constexpr int kAncWords = TSV_ANC_WORDS + 2;  // two zero words past the end
   static constexpr int kOffQ = 0;
-  static constexpr int kOffK = kOffQ + 2 * kQTile;
-  static constexpr int kOffV = kOffK + kStages * kTileBytes;
-  static constexpr int kOffAnc = kOffV + kStages * kTileBytes;
-  static constexpr int kOffPar = kOffAnc + 2 * kBM * kAncWords * 4;
-  static constexpr int kOffBar = kOffPar + TSV_MAX_NODES * 4;
-  // q_full, kv_full[S], kv_empty[S], per tile s_full[2] p_full[2] pv_done[2], mma_done
-  static constexpr int kNumBars = 1 + 2 * kStages + 12 + 1;
+  static constexpr int kOffK = kOffQ + kQBytes;
+  static constexpr int kOffV = kOffK + kKStages * kTileBytes;
+  static constexpr int kOffAnc = kOffV + kVStages * kTileBytes;
+  static constexpr int kOffPar = kOffAnc + kBM * kAncWords * 4;
+  static constexpr int kOffX = kOffPar + TSV_MAX_NODES * 4;  // float [4][128]: per-half row values
+  static constexpr int kOffBar = kOffX + 4 * kBM * 4;
+  // q_full, k_full[3], k_empty[3], v_full[2], v_empty[2], s_full[2],
+  // p_full[half][2], pv_done[half][2], mma_done
+  static constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + 2 + 4 + 4 + 1;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + slack to align the base to 1024
-  static constexpr uint32_t kTileCols = 256;               // S0 | S1 | O per tile
-  static constexpr uint32_t kTmemCols = 2 * kTileCols;
+  static constexpr uint32_t kColO = 2 * kBN;               // S0 | S1 | O0 | O1 (D columns each)
+  static constexpr uint32_t kTmemCols = 512;
   static_assert(kOffK % 1024 == 0 && kOffV % 1024 == 0 && kTileBytes % 1024 == 0, "swizzle atoms");
   static_assert(kOffBar % 8 == 0, "mbarrier alignment");
-  static_assert(2 * kBN + D <= (int)kTileCols, "TMEM columns");
+  static_assert(kColO + 2 * D <= kTmemCols, "TMEM columns");
+  static_assert(kKStages * kTileBytes >= (64 + 1) * kBM * 4, "merge weights fit in the K ring");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 };
 
@@ -80,7 +89,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         float* __restrict__ part_o, float* __restrict__ part_lse,
                         int32_t* __restrict__ counters, int32_t* __restrict__ status) {
   using C = TcCfg<D>;
-  constexpr int S = C::kStages;
+  constexpr int SK = C::kKStages, SV = C::kVStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem + C::kOffQ;
@@ -88,12 +97,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint8_t* sV = smem + C::kOffV;
   uint32_t* sAnc = reinterpret_cast<uint32_t*>(smem + C::kOffAnc);
   int32_t* sPar = reinterpret_cast<int32_t*>(smem + C::kOffPar);
+  float* sX = reinterpret_cast<float*>(smem + C::kOffX);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
   uint64_t* q_full = bars;
-  uint64_t* kv_full = bars + 1;
-  uint64_t* kv_empty = kv_full + S;
-  uint64_t* tile_bars = kv_empty + S;  // tile t: s_full[2], p_full[2], pv_done[2] at 6t
-  uint64_t* mma_done = tile_bars + 12;
+  uint64_t* k_full = q_full + 1;
+  uint64_t* k_empty = k_full + SK;
+  uint64_t* v_full = k_empty + SK;
+  uint64_t* v_empty = v_full + SV;
+  uint64_t* s_full = v_empty + SV;
+  uint64_t* p_full = s_full + 2;   // [half][2]
+  uint64_t* pv_done = p_full + 4;  // [half][2]
+  uint64_t* mma_done = pv_done + 4;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   int* abort_flag = reinterpret_cast<int*>(smem + C::kOffMisc + 4);
   int* last_cta = reinterpret_cast<int*>(smem + C::kOffMisc + 8);
@@ -111,31 +125,34 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int b = lo;
   const int local = unit - plan.unit_start[b];
   const int mtiles = plan.mtiles[b], nch = plan.n_chunks[b];
-  const int npairs = (mtiles + 1) >> 1;
-  const int pr = local % npairs;
-  const int cg = local / npairs;
+  const int mt = local % mtiles;
+  const int cg = local / mtiles;
   const int c = cg % nch;
   const int g = cg / nch;
   const int G = plan.G;
   const int P = plan.prefix[b], n = plan.nodes[b], off = plan.node_off[b];
   const int R = n * G;
-  const int ntiles = min(2, mtiles - 2 * pr);  // 1 or 2
+  const int row0 = mt * kBM;
+  const int rows_valid = min(kBM, R - row0);
   const int k_begin = c * plan.chunk_keys;
   const int k_end = min(P + n, k_begin + plan.chunk_keys);
   const int nblk = (k_end - k_begin + kBN - 1) / kBN;
 
   if (tid == 0) {
     mbar_init(q_full, 1);
-    for (int s = 0; s < S; ++s) {
-      mbar_init(&kv_full[s], 1);
-      mbar_init(&kv_empty[s], 1);
+    for (int s = 0; s < SK; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);
     }
-    for (int t = 0; t < 2; ++t)
-      for (int x = 0; x < 2; ++x) {
-        mbar_init(&tile_bars[6 * t + x], 1);        // s_full
-        mbar_init(&tile_bars[6 * t + 2 + x], 128);  // p_full: every softmax thread of the tile
-        mbar_init(&tile_bars[6 * t + 4 + x], 1);    // pv_done
-      }
+    for (int s = 0; s < SV; ++s) {
+      mbar_init(&v_full[s], 1);
+      mbar_init(&v_empty[s], 1);
+    }
+    for (int x = 0; x < 2; ++x) mbar_init(&s_full[x], 1);
+    for (int x = 0; x < 4; ++x) {
+      mbar_init(&p_full[x], kTcSoftmaxThreads / 2);  // every thread of the key half
+      mbar_init(&pv_done[x], 1);
+    }
     mbar_init(mma_done, 1);
     *abort_flag = 0;
     mbar_fence_init();
@@ -144,38 +161,48 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   if (warp == kTcProducerWarp) {
     // ------------------------------------------------------------ producer
+    const uint64_t pol = mtiles > 1 ? l2_policy_evict_last() : l2_policy_evict_first();
     if (lane == 0) {
       tma_prefetch_desc(&tmap_q);
       tma_prefetch_desc(&tmap_k);
-      tma_prefetch_desc(&tmap_v);
-      // Q tile t: box (64 d, G heads, 128/G nodes) lands as 128 rows r = node*G + head.
-      mbar_arrive_expect_tx(q_full, ntiles * C::kQTile);
-      for (int t = 0; t < ntiles; ++t)
+      // Q tile: box (64 d, G heads, 128/G nodes) lands as 128 rows r = node*G + head.
+      mbar_arrive_expect_tx(q_full, C::kQBytes);
 #pragma unroll
-        for (int hf = 0; hf < C::kHalves; ++hf)
-          tma_load_3d(sQ + t * C::kQTile + hf * (kBM * 128), &tmap_q, q_full, hf * 64, g * G,
-                      off + (2 * pr + t) * kBM / G, l2_policy_evict_first());
-      const uint64_t pol = npairs > 1 ? l2_policy_evict_last() : l2_policy_evict_first();
+      for (int hf = 0; hf < C::kHalves; ++hf)
+        tma_load_3d(sQ + hf * (kBM * 128), &tmap_q, q_full, hf * 64, g * G, off + row0 / G,
+                    l2_policy_evict_first());
       int issued = 0;
       for (int j = 0; j < nblk; ++j) {
-        const int st = j % S;
-        if (j >= S && !mbar_wait(&kv_empty[st], ((j / S) - 1) & 1, abort_v)) break;
-        mbar_arrive_expect_tx(&kv_full[st], 2 * C::kTileBytes);
-        const int key0 = k_begin + j * kBN;
+        const int st = j % SK;
+        if (j >= SK && !mbar_wait(&k_empty[st], ((j / SK) - 1) & 1, abort_v)) break;
+        mbar_arrive_expect_tx(&k_full[st], C::kTileBytes);
 #pragma unroll
-        for (int hf = 0; hf < C::kHalves; ++hf) {
-          tma_load_4d(sK + st * C::kTileBytes + hf * (kBN * 128), &tmap_k, &kv_full[st], hf * 64, g,
-                      key0, b, pol);
-          tma_load_4d(sV + st * C::kTileBytes + hf * (kBN * 128), &tmap_v, &kv_full[st], hf * 64, g,
-                      key0, b, pol);
-        }
+        for (int hf = 0; hf < C::kHalves; ++hf)
+          tma_load_4d(sK + st * C::kTileBytes + hf * (kBN * 128), &tmap_k, &k_full[st], hf * 64, g,
+                      k_begin + j * kBN, b, pol);
         ++issued;
       }
       if (*abort_v) {  // let copies still in flight land before the CTA exits
         mbar_wait(q_full, 0, nullptr);
-        for (int j = (issued > S ? issued - S : 0); j < issued; ++j)
-          mbar_wait(&kv_full[j % S], (j / S) & 1, nullptr);
+        for (int j = (issued > SK ? issued - SK : 0); j < issued; ++j)
+          mbar_wait(&k_full[j % SK], (j / SK) & 1, nullptr);
       }
+    } else if (lane == 1) {
+      tma_prefetch_desc(&tmap_v);
+      int issued = 0;
+      for (int j = 0; j < nblk; ++j) {
+        const int st = j % SV;
+        if (j >= SV && !mbar_wait(&v_empty[st], ((j / SV) - 1) & 1, abort_v)) break;
+        mbar_arrive_expect_tx(&v_full[st], C::kTileBytes);
+#pragma unroll
+        for (int hf = 0; hf < C::kHalves; ++hf)
+          tma_load_4d(sV + st * C::kTileBytes + hf * (kBN * 128), &tmap_v, &v_full[st], hf * 64, g,
+                      k_begin + j * kBN, b, pol);
+        ++issued;
+      }
+      if (*abort_v)
+        for (int j = (issued > SV ? issued - SV : 0); j < issued; ++j)
+          mbar_wait(&v_full[j % SV], (j / SV) & 1, nullptr);
     }
   } else if (warp == kTcMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
@@ -193,69 +220,67 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const uint64_t dq = sdesc_sw128(smem_u32(sQ), 16, 1024);
       const uint64_t dk = sdesc_sw128(smem_u32(sK), 16, 1024);
       const uint64_t dv = sdesc_sw128(smem_u32(sV), kBN * 128, 1024);
-      auto issue_s = [&](int t, int j) {
-        const uint32_t dst = tmem + t * C::kTileCols + (uint32_t)((j & 1) * kBN);
-        const uint64_t da = dq + (uint64_t)((t * C::kQTile) >> 4);
-        const uint64_t db = dk + (uint64_t)(((j % S) * C::kTileBytes) >> 4);
+      auto issue_s = [&](int j) {
+        const uint32_t dst = tmem + (uint32_t)((j & 1) * kBN);
+        const uint64_t db = dk + (uint64_t)(((j % SK) * C::kTileBytes) >> 4);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t ao = ((kk >> 2) * (kBM * 128) + (kk & 3) * 32) >> 4;
           const uint32_t bo = ((kk >> 2) * (kBN * 128) + (kk & 3) * 32) >> 4;
-          umma_bf16(dst, da + ao, db + bo, idS, kk > 0 ? 1u : 0u);
+          umma_bf16(dst, dq + ao, db + bo, idS, kk > 0 ? 1u : 0u);
         }
-        umma_commit(&tile_bars[6 * t + (j & 1)]);
+        umma_commit(&s_full[j & 1]);
+        umma_commit(&k_empty[j % SK]);  // K(j) is free once S(j) has read it
       };
-      auto issue_pv = [&](int t, int j) {
-        const uint32_t pa = tmem + t * C::kTileCols + (uint32_t)((j & 1) * kBN);  // P over S(j)
-        const uint32_t tO = tmem + t * C::kTileCols + 2 * kBN;
-        const uint64_t db = dv + (uint64_t)(((j % S) * C::kTileBytes) >> 4);
+      auto issue_pv = [&](int h, int j) {
+        // P_h sits over the first 32 of key half h's 64 S columns; V_h is rows
+        // 64h .. 64h+63 of the V block.
+        const uint32_t pa = tmem + (uint32_t)((j & 1) * kBN + h * kHalfKeys);
+        const uint64_t db = dv + (uint64_t)(((j % SV) * C::kTileBytes + h * kHalfKeys * 128) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk)
-          umma_bf16_ts(tO, pa + kk * 8, db + (uint32_t)((kk * 16 * 128) >> 4), idPV,
+        for (int kk = 0; kk < kHalfKeys / 16; ++kk)
+          umma_bf16_ts(tmem + C::kColO + h * D, pa + kk * 8, db + (uint32_t)((kk * 16 * 128) >> 4), idPV,
                        (j > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(&tile_bars[6 * t + 4 + (j & 1)]);
+        umma_commit(&pv_done[2 * h + (j & 1)]);
       };
-      bool ok = nblk > 0 && mbar_wait(q_full, 0, abort_v) && mbar_wait(&kv_full[0], 0, abort_v);
+      bool ok = nblk > 0 && mbar_wait(q_full, 0, abort_v) && mbar_wait(&k_full[0], 0, abort_v);
       if (ok) {
         tc_fence_after();
-        for (int t = 0; t < ntiles; ++t) issue_s(t, 0);
+        issue_s(0);
       }
       for (int j = 0; ok && j < nblk; ++j) {
         if (j + 1 < nblk) {
-          if (!mbar_wait(&kv_full[(j + 1) % S], ((j + 1) / S) & 1, abort_v)) break;
+          if (!mbar_wait(&k_full[(j + 1) % SK], ((j + 1) / SK) & 1, abort_v)) break;
           tc_fence_after();
-          for (int t = 0; t < ntiles; ++t) issue_s(t, j + 1);
+          issue_s(j + 1);
         }
-        for (int t = 0; ok && t < ntiles; ++t) {
-          if (!mbar_wait(&tile_bars[6 * t + 2 + (j & 1)], (j >> 1) & 1, abort_v)) {
+        if (!mbar_wait(&v_full[j % SV], (j / SV) & 1, abort_v)) break;
+        for (int h = 0; ok && h < 2; ++h) {
+          if (!mbar_wait(&p_full[2 * h + (j & 1)], (j >> 1) & 1, abort_v)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          issue_pv(t, j);
+          issue_pv(h, j);
         }
-        if (ok) umma_commit(&kv_empty[j % S]);
+        if (ok) umma_commit(&v_empty[j % SV]);
       }
       umma_commit(mma_done);  // every MMA of this CTA has finished before TMEM is freed
       mbar_wait(mma_done, 0, nullptr);
     }
   } else {
     // ------------------------------------------------------------ softmax
-    const int t = warp >> 2;  // M-tile of this warpgroup
-    const int r = tid & 127;  // row within the tile = TMEM lane
-    const int row0 = (2 * pr + t) * kBM;
-    const bool tile_on = t < ntiles;
-    const int rows_valid = tile_on ? min(kBM, R - row0) : 0;
+    const int hk = warp >> 2;       // key half of every block
+    const int r = tid & (kBM - 1);  // row = TMEM lane
     const bool valid = r < rows_valid;
-    uint64_t* s_full = tile_bars + 6 * t;
-    uint64_t* p_full = s_full + 2;
-    uint64_t* pv_done = s_full + 4;
-    // Ancestor bitset of this row's node.
-    uint32_t* arow = sAnc + (t * kBM + r) * C::kAncWords;
+    // Ancestor bitset of this row's node (built by the half-0 thread of the row).
+    uint32_t* arow = sAnc + r * C::kAncWords;
+    if (hk == 0) {
 #pragma unroll
-    for (int w = 0; w < C::kAncWords; ++w) arow[w] = 0u;
+      for (int w = 0; w < C::kAncWords; ++w) arow[w] = 0u;
+    }
     if (anc != nullptr) {
-      if (valid) {
+      if (valid && hk == 0) {
         const uint4* src = reinterpret_cast<const uint4*>(anc + (size_t)(off + (row0 + r) / G) * TSV_ANC_WORDS);
         const uint4 a0 = __ldg(src), a1 = __ldg(src + 1);
         arow[0] = a0.x; arow[1] = a0.y; arow[2] = a0.z; arow[3] = a0.w;
@@ -271,226 +296,247 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       const bool bad = named_bar_or(kBarTcSoftmax, kTcSoftmaxThreads, tid < n && (p < -1 || p >= tid));
       if (local == 0 && tid == 0) status[b] = bad ? TSV_ERR_BAD_TREE : TSV_OK;
-      if (valid && !bad)
+      if (valid && hk == 0 && !bad)
         for (int a = (row0 + r) / G; a >= 0; a = sPar[a]) arow[a >> 5] |= 1u << (a & 31);
     }
     tc_fence_before();
     named_bar(kBarTcSetup, kTcSoftmaxThreads + 32);
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    const uint32_t tcol = tmem + lane_base + t * C::kTileCols;
+    const uint32_t trow = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    const uint32_t o_mine = trow + C::kColO + (uint32_t)(hk * D);  // O_h of this row
+    uint64_t* p_mine = p_full + 2 * hk;
+    uint64_t* pv_mine = pv_done + 2 * hk;
     const float sl2 = plan.scale_log2;
-    const int my_nblk = tile_on ? nblk : 0;
     float m_ref = -INFINITY, l = 0.f;
+    // No barrier inside the loop: a timed-out wait ends this warp's loop
+    // (every wait is bounded and sets the CTA's abort flag, so the other
+    // warps' waits end quickly too); the CTA agrees after the loop.
     bool ok = true;
-    for (int j = 0; j < my_nblk; ++j) {
-      ok = __all_sync(0xffffffffu, mbar_wait(&s_full[j & 1], (j >> 1) & 1, abort_v));
-      if (!ok) break;
-      tc_fence_after();
-      const uint32_t sbuf = tcol + (uint32_t)((j & 1) * kBN);
-      float s[kBN];
-      {
-        float t0[32], t1[32];
-        tmem_ld32(sbuf, t0);
-        tmem_ld32(sbuf + 32, t1);
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          s[e] = t0[e];
-          s[32 + e] = t1[e];
-        }
+    for (int j = 0; j < nblk; ++j) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&s_full[j & 1], (j >> 1) & 1, abort_v))) {
+        ok = false;
+        break;
       }
-      const int key0 = k_begin + j * kBN;
-      if (key0 + kBN > P) {  // uniform: the block reaches the tree keys (or past the request)
+      tc_fence_after();
+      const uint32_t sbuf = trow + (uint32_t)((j & 1) * kBN + hk * kHalfKeys);
+      float s[kHalfKeys];
+      tmem_ld32(sbuf, *reinterpret_cast<float(*)[32]>(&s[0]));
+      tmem_ld32(sbuf + 32, *reinterpret_cast<float(*)[32]>(&s[32]));
+      const int key0 = k_begin + j * kBN + hk * kHalfKeys;  // this half's first key
+      if (key0 + kHalfKeys > P) {  // uniform per warp: the half reaches the tree keys
         const uint64_t vis = valid ? block_visibility(arow, key0 - P) : 0ull;
 #pragma unroll
-        for (int e = 0; e < kBN; ++e) s[e] = ((vis >> e) & 1ull) ? s[e] : -INFINITY;
+        for (int e = 0; e < kHalfKeys; ++e) s[e] = ((vis >> e) & 1ull) ? s[e] : -INFINITY;
       } else if (!valid) {
 #pragma unroll
-        for (int e = 0; e < kBN; ++e) s[e] = -INFINITY;
+        for (int e = 0; e < kHalfKeys; ++e) s[e] = -INFINITY;
       }
-      // Raw maximum (the scale is positive, so it commutes with the max).
       float mx[4] = {s[0], s[1], s[2], s[3]};
 #pragma unroll
-      for (int e = 4; e < kBN; ++e) mx[e & 3] = fmaxf(mx[e & 3], s[e]);
-      const float bmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl2;
-      // Move the reference maximum only when the block's max exceeds it by
-      // more than the threshold (always on the first visible block).
+      for (int e = 4; e < kHalfKeys; ++e) mx[e & 3] = fmaxf(mx[e & 3], s[e]);
+      // Raw maximum times the (positive) scale = maximum of the scaled scores.
+      const float hmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl2;
+      // Move the reference only when a score exceeds it by more than the
+      // threshold (always on the first visible block).
       float alpha = 1.f;
-      bool resc = false;
-      if (bmax > m_ref + kRescaleThreshold) {
-        alpha = fast_exp2(m_ref - bmax);  // 0 when m_ref = -inf
-        m_ref = bmax;
-        resc = true;
+      if (hmax > m_ref + kRescaleThreshold) {
+        alpha = fast_exp2(m_ref - hmax);  // 0 when m_ref = -inf
+        m_ref = hmax;
       }
-      const float neg_ref = m_ref == -INFINITY ? 0.f : -m_ref;
-      uint32_t pk[kBN / 2];
-      float ps[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int e = 0; e < kBN; e += 2) {
-        const float p0 = fast_exp2(fmaf(s[e], sl2, neg_ref));
-        const float p1 = fast_exp2(fmaf(s[e + 1], sl2, neg_ref));
-        ps[(e >> 1) & 3] += p0 + p1;
-        pk[e >> 1] = pack_bf16x2(p0, p1);
-      }
-      l = l * alpha + ((ps[0] + ps[1]) + (ps[2] + ps[3]));
-      // O must hold PV(j-1) before it is rescaled.
-      if (j >= 1 && __any_sync(0xffffffffu, resc)) {
-        ok = __all_sync(0xffffffffu, mbar_wait(&pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort_v));
-        if (!ok) break;
+      l *= alpha;
+      if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
+        // O_h must hold PV_h(j-1) before it is rescaled (lanes with alpha = 1
+        // rewrite their row unchanged: TMEM loads and stores are warp-wide).
+        if (!__all_sync(0xffffffffu, mbar_wait(&pv_mine[(j - 1) & 1], ((j - 1) >> 1) & 1, abort_v))) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
 #pragma unroll 1
         for (int cc = 0; cc < D; cc += 32) {
           float o[32];
-          tmem_ld32(tcol + (uint32_t)(2 * kBN + cc), o);
+          tmem_ld32(o_mine + cc, o);
 #pragma unroll
           for (int e = 0; e < 32; ++e) o[e] *= alpha;
-          tmem_st32(tcol + (uint32_t)(2 * kBN + cc), o);
+          tmem_st32(o_mine + cc, o);
         }
       }
-      // P (bf16, two per column) over the first 32 columns of S(j), whose
-      // values are all in registers now.
-      {
-        uint32_t h0[16], h1[16];
+      const float neg_ref = m_ref == -INFINITY ? 0.f : -m_ref;
+      uint32_t h0[16], h1[16];
+      float ps[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          h0[e] = pk[e];
-          h1[e] = pk[16 + e];
-        }
-        tmem_st16u(sbuf, h0);
-        tmem_st16u(sbuf + 16, h1);
+      for (int e = 0; e < kHalfKeys; e += 2) {
+        const float p0 = fast_exp2(fmaf(s[e], sl2, neg_ref));
+        const float p1 = fast_exp2(fmaf(s[e + 1], sl2, neg_ref));
+        ps[(e >> 1) & 3] += p0 + p1;
+        if (e < 32) h0[e >> 1] = pack_bf16x2(p0, p1);
+        else h1[(e - 32) >> 1] = pack_bf16x2(p0, p1);
       }
-      // Rows of the last block past the request's keys may hold anything
-      // (even NaN): zero them in V so that 0 * garbage never reaches O.  Tile
-      // 0's warpgroup does it; PV of tile 1 is issued after PV of tile 0.
-      const int vrows = k_end - key0;
-      if (t == 0 && vrows < kBN) {
-        uint8_t* vt = sV + (j % S) * C::kTileBytes;
-        const int pieces = (kBN - vrows) * C::kHalves * 8;
-        for (int q = r; q < pieces; q += kBM) {
-          const int row = vrows + q / (C::kHalves * 8);
-          const int rem = q % (C::kHalves * 8);
-          *reinterpret_cast<uint4*>(vt + (rem >> 3) * (kBN * 128) + row * 128 + ((rem & 7) << 4)) =
-              make_uint4(0u, 0u, 0u, 0u);
+      l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
+      // P (bf16, two per column) over the first 32 of this thread's 64 S columns.
+      tmem_st16u(sbuf, h0);
+      tmem_st16u(sbuf + 16, h1);
+      // V rows of the last block past the request's keys may hold anything
+      // (even NaN): once the block has landed, each half zeroes the rows its
+      // own PV reads, so that 0 * garbage never reaches O.
+      const int vrows = k_end - (k_begin + j * kBN);
+      if (vrows < kBN) {
+        const int first = max(vrows, hk * kHalfKeys), last = (hk + 1) * kHalfKeys;
+        if (first < last) {
+          if (!__all_sync(0xffffffffu, mbar_wait(&v_full[j % SV], (j / SV) & 1, abort_v))) {
+            ok = false;
+            break;
+          }
+          uint8_t* vt = sV + (j % SV) * C::kTileBytes;
+          const int pieces = (last - first) * C::kHalves * 8;
+          for (int q = r; q < pieces; q += kBM) {
+            const int row = first + q / (C::kHalves * 8);
+            const int rem = q % (C::kHalves * 8);
+            *reinterpret_cast<uint4*>(vt + (rem >> 3) * (kBN * 128) + row * 128 + ((rem & 7) << 4)) =
+                make_uint4(0u, 0u, 0u, 0u);
+          }
+          fence_proxy_async_smem();
         }
-        fence_proxy_async_smem();
       }
       tc_fence_before();
-      mbar_arrive(&p_full[j & 1]);
+      mbar_arrive(&p_mine[j & 1]);
     }
-    if (ok && my_nblk > 0)
-      ok = __all_sync(0xffffffffu,
-                      mbar_wait(&pv_done[(my_nblk - 1) & 1], ((my_nblk - 1) >> 1) & 1, abort_v));
-    // Agree on success CTA-wide: the merge below has named barriers that all
-    // 256 softmax threads must reach.
+    // Both halves' last PV must be complete before the epilogue reads O0 and O1.
+    if (ok && nblk > 0) {
+      const int jl = nblk - 1;
+      ok = __all_sync(0xffffffffu, mbar_wait(&pv_done[jl & 1], (jl >> 1) & 1, abort_v) &&
+                                       mbar_wait(&pv_done[2 + (jl & 1)], (jl >> 1) & 1, abort_v));
+    }
+    // Agree on success CTA-wide: the epilogue has barriers that all 256
+    // softmax threads must reach.
     ok = !named_bar_or(kBarTcSoftmax, kTcSoftmaxThreads, !ok);
     if (ok && nblk > 0) {
-      if (tile_on) tc_fence_after();
+      tc_fence_after();
+      // Combine the halves of each row: weights 2^(m_h - M), sum L (the same
+      // order in both threads of a row).
+      sX[hk * kBM + r] = m_ref;
+      sX[(2 + hk) * kBM + r] = l;
+      named_bar(kBarTcSoftmax, kTcSoftmaxThreads);
+      const float m0 = sX[r], m1 = sX[kBM + r];
+      const float M = fmaxf(m0, m1);
+      const float w0 = m0 == -INFINITY ? 0.f : fast_exp2(m0 - M);
+      const float w1 = m1 == -INFINITY ? 0.f : fast_exp2(m1 - M);
+      const float L = w0 * sX[2 * kBM + r] + w1 * sX[3 * kBM + r];
+      const float inv_l = L > 0.f ? 1.f / L : 0.f;
+      const float c0 = w0 * inv_l, c1 = w1 * inv_l;
       const int gr = row0 + r;
       const int node = gr / G;
       const int h = g * G + (gr - node * G);
-      const float inv_l = l > 0.f ? 1.f / l : 0.f;
+      constexpr int kOHalf = D / 2;  // output columns this thread writes
+      const uint32_t oc0 = trow + C::kColO + (uint32_t)(hk * kOHalf);
       if (nch == 1) {
-        if (tile_on) {
-          __nv_bfloat16* dst = out + ((size_t)(off + node) * plan.Hq + h) * D;
+        __nv_bfloat16* dst = out + ((size_t)(off + node) * plan.Hq + h) * D + hk * kOHalf;
 #pragma unroll 1
-          for (int cc = 0; cc < D; cc += 32) {
-            float o[32];
-            tmem_ld32(tcol + (uint32_t)(2 * kBN + cc), o);
-            if (valid) {
-              uint4* d4 = reinterpret_cast<uint4*>(dst + cc);
+        for (int cc = 0; cc < kOHalf; cc += 32) {
+          float o[32], o1[32];
+          tmem_ld32(oc0 + cc, o);
+          tmem_ld32(oc0 + D + cc, o1);
+          if (valid) {
+            uint4* d4 = reinterpret_cast<uint4*>(dst + cc);
 #pragma unroll
-              for (int e = 0; e < 4; ++e)
-                d4[e] = make_uint4(pack_bf16x2(o[8 * e] * inv_l, o[8 * e + 1] * inv_l),
-                                   pack_bf16x2(o[8 * e + 2] * inv_l, o[8 * e + 3] * inv_l),
-                                   pack_bf16x2(o[8 * e + 4] * inv_l, o[8 * e + 5] * inv_l),
-                                   pack_bf16x2(o[8 * e + 6] * inv_l, o[8 * e + 7] * inv_l));
+            for (int e = 0; e < 4; ++e) {
+              float v[8];
+#pragma unroll
+              for (int x = 0; x < 8; ++x) v[x] = c0 * o[8 * e + x] + c1 * o1[8 * e + x];
+              d4[e] = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
+                                 pack_bf16x2(v[6], v[7]));
             }
           }
         }
       } else {
         // Partial of this chunk, then the group's last CTA merges all chunks.
         const int64_t base0 = plan.part_row[b] + (int64_t)g * nch * R;
-        if (tile_on) {
-          const int64_t prow_i = base0 + (int64_t)c * R + gr;
-          float* dst = part_o + prow_i * D;
+        const int64_t prow_i = base0 + (int64_t)c * R + gr;
+        float* dst = part_o + prow_i * D + hk * kOHalf;
 #pragma unroll 1
-          for (int cc = 0; cc < D; cc += 32) {
-            float o[32];
-            tmem_ld32(tcol + (uint32_t)(2 * kBN + cc), o);
-            if (valid) {
-              float4* d4 = reinterpret_cast<float4*>(dst + cc);
+        for (int cc = 0; cc < kOHalf; cc += 32) {
+          float o[32], o1[32];
+          tmem_ld32(oc0 + cc, o);
+          tmem_ld32(oc0 + D + cc, o1);
+          if (valid) {
+            float4* d4 = reinterpret_cast<float4*>(dst + cc);
 #pragma unroll
-              for (int e = 0; e < 8; ++e)
-                d4[e] = make_float4(o[4 * e] * inv_l, o[4 * e + 1] * inv_l, o[4 * e + 2] * inv_l,
-                                    o[4 * e + 3] * inv_l);
-            }
+            for (int e = 0; e < 8; ++e)
+              d4[e] = make_float4(c0 * o[4 * e] + c1 * o1[4 * e], c0 * o[4 * e + 1] + c1 * o1[4 * e + 1],
+                                  c0 * o[4 * e + 2] + c1 * o1[4 * e + 2], c0 * o[4 * e + 3] + c1 * o1[4 * e + 3]);
           }
-          if (valid) part_lse[prow_i] = l > 0.f ? m_ref + log2f(l) : -INFINITY;
         }
+        if (valid && hk == 0) part_lse[prow_i] = L > 0.f ? M + log2f(L) : -INFINITY;
         __threadfence();
         named_bar(kBarTcSoftmax, kTcSoftmaxThreads);
-        int32_t* ctr = counters + plan.ctr_base[b] + g * npairs + pr;
+        int32_t* ctr = counters + plan.ctr_base[b] + g * mtiles + mt;
         if (tid == 0) *last_cta = atomicAdd(ctr, 1) == nch - 1;
         named_bar(kBarTcSoftmax, kTcSoftmaxThreads);
         if (*last_cta) {
           __threadfence();
-          // Warp w merges rows w, w+8, ... of the pair.  Lane c holds the
-          // log2-sum-exp of chunks c and c + 32 (at most 64 chunks); the
-          // weights meet by shuffles, then each lane owns D/32 columns and
-          // keeps eight chunks' loads in flight.
-          constexpr int E = D / 32;
-          const int prow0 = 2 * pr * kBM;
-          const int rows_pair = min(2 * kBM, R - prow0);
-          for (int rr = warp; rr < rows_pair; rr += kTcSoftmaxThreads / 32) {
-            const int grr = prow0 + rr;
-            const float l0 = lane < nch ? __ldcg(part_lse + base0 + (int64_t)lane * R + grr) : -INFINITY;
-            const float l1 = lane + 32 < nch ? __ldcg(part_lse + base0 + (int64_t)(lane + 32) * R + grr) : -INFINITY;
-            float M = fmaxf(l0, l1);
-#pragma unroll
-            for (int o2 = 16; o2 > 0; o2 >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o2));
-            const float w0 = (l0 == -INFINITY) ? 0.f : fast_exp2(l0 - M);
-            const float w1 = (l1 == -INFINITY) ? 0.f : fast_exp2(l1 - M);
-            float wsum = w0 + w1;
-#pragma unroll
-            for (int o2 = 16; o2 > 0; o2 >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o2);
-            const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-            float acc[E];
-#pragma unroll
-            for (int e = 0; e < E; ++e) acc[e] = 0.f;
-            const float* src0 = part_o + (base0 + grr) * D + lane * E;
-            for (int c0 = 0; c0 < nch; c0 += 8) {
-              float v[8][E];
-#pragma unroll
-              for (int u = 0; u < 8; ++u) {
-                if (c0 + u < nch) {
-                  const float* src = src0 + (int64_t)(c0 + u) * R * D;
-                  if constexpr (E == 4) {
-                    const float4 x = __ldcg(reinterpret_cast<const float4*>(src));
-                    v[u][0] = x.x; v[u][1] = x.y; v[u][2] = x.z; v[u][3] = x.w;
-                  } else {
-                    const float2 x = __ldcg(reinterpret_cast<const float2*>(src));
-                    v[u][0] = x.x; v[u][1] = x.y;
-                  }
-                }
-              }
-#pragma unroll
-              for (int u = 0; u < 8; ++u) {
-                const int cc = c0 + u;
-                const float w = __shfl_sync(0xffffffffu, cc < 32 ? w0 : w1, cc & 31);
-                if (cc < nch && w > 0.f) {
-#pragma unroll
-                  for (int e = 0; e < E; ++e) acc[e] += w * v[u][e];
-                }
-              }
+          // Merge: first the chunk weights of every row (the idle K ring holds
+          // them: [chunk][row] weights, then [row] inverse sums), then rows x
+          // 4-column groups, four groups x four chunks of loads in flight.
+          float* sW = reinterpret_cast<float*>(sK);
+          if (tid < rows_valid) {
+            const float* lse = part_lse + base0 + row0 + tid;
+            float M2 = -INFINITY;
+#pragma unroll 8
+            for (int cc = 0; cc < nch; ++cc) M2 = fmaxf(M2, __ldcg(lse + (int64_t)cc * R));
+            float wsum = 0.f;
+#pragma unroll 8
+            for (int cc = 0; cc < nch; ++cc) {
+              const float x = __ldcg(lse + (int64_t)cc * R);
+              const float w = x == -INFINITY ? 0.f : fast_exp2(x - M2);
+              sW[cc * kBM + tid] = w;
+              wsum += w;
             }
-            const int nd = grr / G, hh = g * G + (grr - nd * G);
-            __nv_bfloat16* o = out + ((size_t)(off + nd) * plan.Hq + hh) * D + lane * E;
-            if constexpr (E == 4) {
-              *reinterpret_cast<uint2*>(o) =
-                  make_uint2(pack_bf16x2(acc[0] * inv, acc[1] * inv), pack_bf16x2(acc[2] * inv, acc[3] * inv));
-            } else {
-              *reinterpret_cast<uint32_t*>(o) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+            sW[64 * kBM + tid] = wsum > 0.f ? 1.f / wsum : 0.f;
+          }
+          named_bar(kBarTcSoftmax, kTcSoftmaxThreads);
+          constexpr int D4 = D / 4;
+          const int items = rows_valid * D4;
+          const int64_t cstride = (int64_t)R * D;  // floats between chunks of a row
+          for (int i0 = tid; i0 < items; i0 += 4 * kTcSoftmaxThreads) {
+            float4 acc[4];
+            int rr[4];
+            const float* src[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int i = min(i0 + u * kTcSoftmaxThreads, items - 1);  // clamped: duplicates are harmless
+              rr[u] = i / D4;
+              src[u] = part_o + (base0 + row0 + rr[u]) * D + (i - rr[u] * D4) * 4;
+              acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+            for (int c0 = 0; c0 < nch; c0 += 4) {
+              float4 v[4][4];
+#pragma unroll
+              for (int k2 = 0; k2 < 4; ++k2)
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                  if (c0 + k2 < nch) v[k2][u] = __ldcg(reinterpret_cast<const float4*>(src[u] + (c0 + k2) * cstride));
+#pragma unroll
+              for (int k2 = 0; k2 < 4; ++k2)
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                  if (c0 + k2 < nch) {
+                    const float w = sW[(c0 + k2) * kBM + rr[u]];
+                    acc[u].x += w * v[k2][u].x;
+                    acc[u].y += w * v[k2][u].y;
+                    acc[u].z += w * v[k2][u].z;
+                    acc[u].w += w * v[k2][u].w;
+                  }
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int i = i0 + u * kTcSoftmaxThreads;
+              if (i >= items) break;
+              const float inv = sW[64 * kBM + rr[u]];
+              const int grr = row0 + rr[u], nd = grr / G, hh = g * G + (grr - nd * G);
+              __nv_bfloat16* o = out + ((size_t)(off + nd) * plan.Hq + hh) * D + (i - rr[u] * D4) * 4;
+              *reinterpret_cast<uint2*>(o) = make_uint2(pack_bf16x2(acc[u].x * inv, acc[u].y * inv),
+                                                        pack_bf16x2(acc[u].z * inv, acc[u].w * inv));
             }
           }
           if (tid == 0) *ctr = 0;  // leave the counter zeroed for the next call

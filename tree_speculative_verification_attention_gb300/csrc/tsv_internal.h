@@ -12,7 +12,7 @@
 namespace tsv {
 
 constexpr int kBM = 128;  // query rows (node x head-in-group) per attention CTA = TMEM lanes
-constexpr int kBN = 64;   // keys per pipeline block
+constexpr int kBN = 128;  // keys per pipeline block
 
 // How one tsv_tree_attention call is cut into CTAs.  Passed by value as a
 // kernel parameter (no host-to-device copy, so a launch can be captured).
