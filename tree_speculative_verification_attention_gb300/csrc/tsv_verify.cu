@@ -137,49 +137,83 @@ __device__ void fail_request(int32_t* path, int n, int32_t* accept_len, int32_t*
   }
 }
 
+// Shared scratch of one greedy walk: the request's parents, tokens and
+// per-node results, and its (row, slice) argmax partials when they fit.
+constexpr int kWalkPartials = 1024;
+struct WalkSmem {
+  int32_t par[TSV_MAX_NODES];
+  int32_t tok[TSV_MAX_NODES];
+  int32_t am[TSV_MAX_NODES];
+  int32_t nxt[TSV_MAX_NODES];
+  ArgMax part[kWalkPartials];
+  int bad, len;
+};
+
 // The greedy walk of request b from its per-slice argmax partials: every
 // child c whose token equals argmax(parent(c)) proposes itself to its parent
 // with atomicMin (lowest index wins), then the chain is followed from the root.
-// Run by one whole CTA of up to 256 threads.
+// Parents, tokens and partials are loaded in one parallel step.  Run by one
+// whole CTA of up to 256 threads.
 __device__ void greedy_walk_request(int b, int off, int n, const float* part_val,
                                     const int32_t* part_idx, int splits, const int32_t* tokens,
                                     const int32_t* parent, int32_t* path, int32_t* accept_len,
-                                    int32_t* bonus, int32_t* status, int* sh_bad, int32_t* am,
-                                    int32_t* nxt, int* len_s) {
-  const int code = validate_verify_tree(parent + off, n, sh_bad);
-  if (code) {
-    fail_request(path + off, n, accept_len + b, bonus + b, nullptr, status + b, code);
+                                    int32_t* bonus, int32_t* status, WalkSmem& w) {
+  const int T = blockDim.x;
+  if (threadIdx.x == 0) w.bad = (n < 1) ? TSV_ERR_BAD_TREE : (n > TSV_MAX_NODES ? TSV_ERR_UNSUPPORTED : 0);
+  __syncthreads();
+  const int items = n * splits;  // rows of a request are consecutive, so its partials are too
+  const bool staged = items <= kWalkPartials;
+  if (w.bad == 0) {
+    for (int i = threadIdx.x; i < n; i += T) {
+      w.par[i] = parent[off + i];
+      w.tok[i] = tokens[off + i];
+    }
+    if (staged)
+      for (int i = threadIdx.x; i < items; i += T)
+        w.part[i] = ArgMax{__ldcg(part_val + (size_t)off * splits + i), __ldcg(part_idx + (size_t)off * splits + i)};
+  }
+  __syncthreads();
+  if (w.bad == 0) {
+    for (int i = threadIdx.x; i < n; i += T) {
+      const int p = w.par[i];
+      const bool ok = (i == 0) ? (p == -1) : (p >= 0 && p < i);
+      if (!ok) atomicMax(&w.bad, TSV_ERR_BAD_TREE);
+    }
+  }
+  __syncthreads();
+  if (w.bad) {
+    fail_request(path + off, n, accept_len + b, bonus + b, nullptr, status + b, w.bad);
     return;
   }
-  for (int u = threadIdx.x; u < n; u += blockDim.x) {
+  for (int u = threadIdx.x; u < n; u += T) {
     ArgMax best{-INFINITY, INT32_MAX};
     for (int s = 0; s < splits; ++s) {
       const size_t k = (size_t)(off + u) * splits + s;
-      best = better(best, ArgMax{__ldcg(part_val + k), __ldcg(part_idx + k)});
+      best = better(best, staged ? w.part[u * splits + s] : ArgMax{__ldcg(part_val + k), __ldcg(part_idx + k)});
     }
-    am[u] = best.i;
-    nxt[u] = INT32_MAX;
+    w.am[u] = best.i;
+    w.nxt[u] = INT32_MAX;
   }
   __syncthreads();
-  for (int c = 1 + threadIdx.x; c < n; c += blockDim.x) {
-    const int p = parent[off + c];
-    if (tokens[off + c] == am[p]) atomicMin(&nxt[p], c);
+  for (int c = 1 + threadIdx.x; c < n; c += T) {
+    const int p = w.par[c];
+    if (w.tok[c] == w.am[p]) atomicMin(&w.nxt[p], c);
   }
   __syncthreads();
   if (threadIdx.x == 0) {
     int u = 0, len = 0;
     path[off + len++] = 0;
-    while (nxt[u] != INT32_MAX) {
-      u = nxt[u];
+    while (w.nxt[u] != INT32_MAX) {
+      u = w.nxt[u];
       path[off + len++] = u;
     }
     accept_len[b] = len - 1;
-    bonus[b] = am[u];
+    bonus[b] = w.am[u];
     status[b] = TSV_OK;
-    *len_s = len;
+    w.len = len;
   }
   __syncthreads();
-  for (int i = *len_s + threadIdx.x; i < n; i += blockDim.x) path[off + i] = -1;
+  for (int i = w.len + threadIdx.x; i < n; i += T) path[off + i] = -1;
 }
 
 // Walk-only kernel: one CTA per request (used when N == 0, where no argmax CTA exists).
@@ -189,13 +223,11 @@ __global__ void __launch_bounds__(TSV_MAX_NODES)
                        const int32_t* __restrict__ parent, const int32_t* __restrict__ node_offsets,
                        int32_t* __restrict__ path, int32_t* __restrict__ accept_len,
                        int32_t* __restrict__ bonus, int32_t* __restrict__ status) {
-  __shared__ int32_t am[TSV_MAX_NODES];
-  __shared__ int32_t nxt[TSV_MAX_NODES];
-  __shared__ int bad, len_s;
+  __shared__ WalkSmem w;
   const int b = blockIdx.x;
   const int off = node_offsets[b];
   greedy_walk_request(b, off, node_offsets[b + 1] - off, part_val, part_idx, splits, tokens, parent,
-                      path, accept_len, bonus, status, &bad, am, nxt, &len_s);
+                      path, accept_len, bonus, status, w);
 }
 
 // Fused greedy verification: grid (splits, N).  Each CTA reduces one vocab
@@ -211,10 +243,9 @@ __global__ void __launch_bounds__(kArgmaxThreads)
                          int32_t* __restrict__ accept_len, int32_t* __restrict__ bonus,
                          int32_t* __restrict__ status) {
   __shared__ int32_t offs[TSV_MAX_BATCH + 1];
-  __shared__ int32_t am[TSV_MAX_NODES];
-  __shared__ int32_t nxt[TSV_MAX_NODES];
+  __shared__ WalkSmem w;
   __shared__ ArgMax red[kArgmaxThreads / 32];
-  __shared__ int bad, len_s, last;
+  __shared__ int last;
   const int row = blockIdx.y, s = blockIdx.x;
   for (int i = threadIdx.x; i <= B; i += blockDim.x) offs[i] = node_offsets[i];
   const ArgMax best = slice_argmax(logits, V, splits, row, s, red);
@@ -246,7 +277,7 @@ __global__ void __launch_bounds__(kArgmaxThreads)
   if (!last) return;
   __threadfence();
   greedy_walk_request(b, off, n, part_val, part_idx, splits, tokens, parent, path, accept_len, bonus,
-                      status, &bad, am, nxt, &len_s);
+                      status, w);
   if (threadIdx.x == 0) counters[b] = 0;
 }
 
@@ -300,47 +331,87 @@ __device__ __forceinline__ float exp_diff(float a, float m) {
   return expf(d) * (1.0f + err);
 }
 
-__device__ __forceinline__ double warp_sum_d(double v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
+// Sums are carried as unevaluated pairs of floats, hi + lo with |lo| at most
+// half an ulp of hi (about 44 significant bits), built from the error-free
+// TwoSum and FMA-based product transformations.  This GPU's fp64 rate is a
+// small fraction of its fp32 rate, so the walk keeps fp64 out of its loops.
+struct F2 {
+  float hi, lo;
+};
+
+__device__ __forceinline__ F2 two_sum(float a, float b) {
+  const float s = __fadd_rn(a, b);
+  const float bb = __fsub_rn(s, a);
+  const float e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+  return {s, e};
 }
 
-// Block-wide sums of three fp64 values (every thread gets them); red holds 3 x 32 doubles.
-__device__ void block_sum3(double& a, double& b, double& c, double* red) {
+__device__ __forceinline__ F2 f2_add(F2 a, F2 b) {
+  const F2 s = two_sum(a.hi, b.hi);
+  return two_sum(s.hi, __fadd_rn(s.lo, __fadd_rn(a.lo, b.lo)));
+}
+
+__device__ __forceinline__ F2 f2_scale(F2 a, float f) {  // a * f
+  const float p = __fmul_rn(a.hi, f);
+  const float e = fmaf(a.hi, f, -p);  // exact: a.hi * f = p + e
+  return two_sum(p, fmaf(a.lo, f, e));
+}
+
+__device__ __forceinline__ bool f2_lt(F2 a, F2 b) {
+  return a.hi < b.hi || (a.hi == b.hi && a.lo < b.lo);
+}
+
+// 1 / (hi + lo), to about one ulp.
+__device__ __forceinline__ float f2_inv(F2 a) {
+  const float r = 1.0f / a.hi;
+  return fmaf(-__fmul_rn(r, a.lo), r, r);
+}
+
+__device__ __forceinline__ F2 comp_value(const CompSum& c) { return two_sum(c.s, c.c); }
+
+__device__ __forceinline__ F2 shfl_xor_f2(F2 v, int o) {
+  return {__shfl_xor_sync(0xffffffffu, v.hi, o), __shfl_xor_sync(0xffffffffu, v.lo, o)};
+}
+
+// Block-wide sum of a pair sum and two plain floats (every thread gets them;
+// the floats are sums of one nonzero value and zeros, so exact).
+// `red` holds 4 x 32 floats.
+__device__ void block_sum(F2& a, float& b, float& c, float* red) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  a = warp_sum_d(a);
-  b = warp_sum_d(b);
-  c = warp_sum_d(c);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    a = f2_add(a, shfl_xor_f2(a, o));
+    b += __shfl_xor_sync(0xffffffffu, b, o);
+    c += __shfl_xor_sync(0xffffffffu, c, o);
+  }
   __syncthreads();  // red is free
   if (lane == 0) {
-    red[warp] = a;
-    red[32 + warp] = b;
-    red[64 + warp] = c;
+    red[warp] = a.hi;
+    red[32 + warp] = a.lo;
+    red[64 + warp] = b;
+    red[96 + warp] = c;
   }
   __syncthreads();
-  a = warp_sum_d(lane < kMssWarps ? red[lane] : 0.0);
-  b = warp_sum_d(lane < kMssWarps ? red[32 + lane] : 0.0);
-  c = warp_sum_d(lane < kMssWarps ? red[64 + lane] : 0.0);
+  // Every warp adds the per-warp values in warp order: the same result everywhere.
+  a = F2{0.f, 0.f};
+  b = 0.f;
+  c = 0.f;
+  for (int w = 0; w < kMssWarps; ++w) {
+    a = f2_add(a, F2{red[w], red[32 + w]});
+    b += red[64 + w];
+    c += red[96 + w];
+  }
 }
 
-__device__ float block_max(float v, double* red) {
+__device__ float block_max(float v, float* red) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  float* r = reinterpret_cast<float*>(red);
   __syncthreads();
-  if (lane == 0) r[warp] = v;
+  if (lane == 0) red[warp] = v;
   __syncthreads();
-  v = lane < kMssWarps ? r[lane] : -INFINITY;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  return v;
-}
-
-__device__ __forceinline__ double ld_dsmem_f64(uint32_t addr) {
-  double v;
-  asm volatile("ld.shared::cluster.f64 %0, [%1];" : "=d"(v) : "r"(addr) : "memory");
+  v = -INFINITY;
+  for (int w = 0; w < kMssWarps; ++w) v = fmaxf(v, red[w]);
   return v;
 }
 
@@ -358,23 +429,25 @@ __device__ __forceinline__ float at(const float4& v, int e) {
   return e == 0 ? v.x : e == 1 ? v.y : e == 2 ? v.z : v.w;
 }
 
-// The CTA's vocabulary slice is visited in 4-float groups: thread t takes
-// groups t, t + T, t + 2T, ... (T threads), kMssGroups groups per round so that
-// their loads are in flight together.  body(y, four floats ...) sees full
-// groups; a ragged end (hi - lo not a multiple of 4) goes element by element.
-struct Slice {
-  int64_t lo, hi;
-};
+// u * q < p exactly, for floats u, q >= 0 and p (the product is formed
+// without rounding as p0 + e).
+__device__ __forceinline__ bool accept_test(float u, float q, float p) {
+  const float p0 = __fmul_rn(u, q);
+  const float e = fmaf(u, q, -p0);
+  return p0 < p || (p0 == p && e < 0.f);
+}
 
 }  // namespace
 
 // Multi-step speculative sampling: one cluster of `ncl` CTAs per request, CTA
 // rank r owning vocab slice r.  All walk decisions are taken identically by
-// every CTA from values every CTA holds: the children and tokens, the row
-// statistics and residual sums (combined in rank order through distributed
-// shared memory), and p at the next child's token, which the residual pass of
-// the CTA owning that token publishes with the sums.  A CTA therefore reads
-// and writes only its own slice of the logits, proposals and residual rows.
+// every CTA from values every CTA holds: the children, their tokens, accept
+// uniforms, proposal probabilities q_c(x_c) and parent logits l(x_c) (read
+// once, in parallel, at the start), the row statistics and residual sums
+// (combined in rank order through distributed shared memory), and p at the
+// next child's token, which the residual pass of the CTA owning that token
+// publishes with the sums.  A CTA streams only its own slice of the logits,
+// proposals and residual rows.
 __global__ void __launch_bounds__(kMssThreads, 2)
     mss_verify_kernel(const float* __restrict__ llm_logits, const float* __restrict__ ssm_probs,
                       int64_t V, const int32_t* __restrict__ tokens,
@@ -385,9 +458,11 @@ __global__ void __launch_bounds__(kMssThreads, 2)
                       int32_t* __restrict__ n_tried, int32_t* __restrict__ status) {
   __shared__ int32_t first_child[TSV_MAX_NODES];
   __shared__ int32_t next_sib[TSV_MAX_NODES];
-  __shared__ double red[96];
-  __shared__ double scan_s[kMssWarps];
-  __shared__ __align__(16) double pub[2][4];  // exchange slots, alternating
+  __shared__ int32_t tok_s[TSV_MAX_NODES];
+  __shared__ float ua_s[TSV_MAX_NODES], qx_s[TSV_MAX_NODES], lx_s[TSV_MAX_NODES];
+  __shared__ float red[128];
+  __shared__ F2 scan_s[kMssWarps];
+  __shared__ __align__(16) float pub[2][4];  // exchange slots, alternating
   __shared__ int bad;
   __shared__ int pick_s, last_s;
   const int b = blockIdx.x / ncl;
@@ -408,10 +483,18 @@ __global__ void __launch_bounds__(kMssThreads, 2)
     return;  // uniform over the cluster: every CTA sees the same tree
   }
   const int32_t* par = parent + off;
-  // Tokens index the vocabulary rows: reject out-of-range ones before any access.
+  // Per child c: its token (rejected before any access when out of range),
+  // accept uniform, q_c(x_c) and the parent row's logit at x_c.
   for (int c = 1 + tid; c < n; c += T) {
     const int x = tokens[off + c];
-    if (x < 0 || (int64_t)x >= V) atomicMax(&bad, TSV_ERR_INVALID_ARG);
+    tok_s[c] = x;
+    if (x < 0 || (int64_t)x >= V) {
+      atomicMax(&bad, TSV_ERR_INVALID_ARG);
+    } else {
+      ua_s[c] = __ldg(u_acc + off + c);
+      qx_s[c] = __ldg(ssm_probs + (size_t)(off + c) * (size_t)V + x);
+      lx_s[c] = __ldg(llm_logits + (size_t)(off + par[c]) * (size_t)V + x);
+    }
   }
   __syncthreads();
   if (bad) {
@@ -443,18 +526,18 @@ __global__ void __launch_bounds__(kMssThreads, 2)
   const int64_t n4 = (hi - lo) >> 2;  // full groups
   float* resid[2] = {resid_all + (size_t)b * 2 * (size_t)V, resid_all + ((size_t)b * 2 + 1) * (size_t)V};
   int xk = 0;  // exchanges so far (the same count in every CTA)
-  // Publishes three values, waits for the cluster, returns the rank-ordered
-  // sums of slots 0..2 over the cluster (slot 0 may instead be max-combined).
-  auto exchange = [&](double v0, double v1, double v2) {
+  // Publishes four floats, then waits for the whole cluster.
+  auto exchange = [&](float v0, float v1, float v2, float v3) {
     if (tid == 0) {
       pub[xk & 1][0] = v0;
       pub[xk & 1][1] = v1;
       pub[xk & 1][2] = v2;
+      pub[xk & 1][3] = v3;
     }
     cluster_sync_all();
   };
   auto peer = [&](int slot, int r) {
-    return ld_dsmem_f64(mapa_shared(smem_u32(&pub[xk & 1][slot]), (uint32_t)r));
+    return ld_dsmem_f32(mapa_shared(smem_u32(&pub[xk & 1][slot]), (uint32_t)r));
   };
   const int lane = tid & 31;
 
@@ -493,30 +576,32 @@ __global__ void __launch_bounds__(kMssThreads, 2)
           for (int e = 0; e < 4; ++e) acc.add(exp_diff(at(v[k], e) * inv_t, m));
     }
     for (int64_t y = lo + 4 * n4 + tid; y < hi; y += T) acc.add(exp_diff(lrow[y] * inv_t, m));
-    double s = acc.value(), z1 = 0.0, z2 = 0.0;
-    block_sum3(s, z1, z2, red);
-    exchange((double)m, s, 0.0);
+    F2 s = comp_value(acc);
+    float z1 = 0.f, z2 = 0.f;
+    block_sum(s, z1, z2, red);
+    exchange(m, s.hi, s.lo, 0.f);
     // Combine in rank order (identical in every CTA): M = max m_r, S = sum s_r e^(m_r - M).
-    const double mine_m = lane < ncl ? peer(0, lane) : -INFINITY;
-    const double mine_s = lane < ncl ? peer(1, lane) : 0.0;
+    const float mr = lane < ncl ? peer(0, lane) : -INFINITY;
+    const float sh = lane < ncl ? peer(1, lane) : 0.f;
+    const float sl = lane < ncl ? peer(2, lane) : 0.f;
     float M = -INFINITY;
-    for (int r = 0; r < ncl; ++r) M = fmaxf(M, (float)__shfl_sync(0xffffffffu, mine_m, r));
-    double S = 0.0;
+    for (int r = 0; r < ncl; ++r) M = fmaxf(M, __shfl_sync(0xffffffffu, mr, r));
+    F2 S{0.f, 0.f};
     for (int r = 0; r < ncl; ++r) {
-      const float mr = (float)__shfl_sync(0xffffffffu, mine_m, r);
-      const double sr = __shfl_sync(0xffffffffu, mine_s, r);
-      if (mr != -INFINITY) S += sr * (double)exp_diff(mr, M);
+      const float m_r = __shfl_sync(0xffffffffu, mr, r);
+      const F2 s_r{__shfl_sync(0xffffffffu, sh, r), __shfl_sync(0xffffffffu, sl, r)};
+      if (m_r != -INFINITY) S = f2_add(S, f2_scale(s_r, exp_diff(m_r, M)));
     }
     ++xk;
     m_u = M;
-    inv_s = (float)(1.0 / S);
+    inv_s = f2_inv(S);
   };
 
   int u = 0, len = 1, cur = 0, tried = 0;
   bool from_resid = false;  // false: p = softmax(row u); true: p = resid[cur] / Z
   bool px_known = false;    // p at the current child's token came with the last exchange
   float px_next = 0.f;
-  double Z = 0.0;
+  F2 Z{0.f, 0.f};
   if (rank == 0 && tid == 0) path[off] = 0;
   row_stats(0);
   while (true) {
@@ -525,25 +610,24 @@ __global__ void __launch_bounds__(kMssThreads, 2)
     if (c == INT32_MAX) c = -1;
     const float* lrow = llm_logits + (size_t)(off + u) * (size_t)V;
     while (c >= 0) {
-      const int x = tokens[off + c];
       const float* q = ssm_probs + (size_t)(off + c) * (size_t)V;
-      // p(x) of the current distribution (fp32, ~2 ulp), compared in fp64.
-      const float px = px_known ? px_next : exp_diff(__ldg(lrow + x) * inv_t, m_u) * inv_s;
+      // p(x) of the current distribution (fp32, ~2 ulp); the test is exact.
+      const float px = px_known ? px_next : exp_diff(lx_s[c] * inv_t, m_u) * inv_s;
       ++tried;
-      if ((double)__ldg(u_acc + off + c) * (double)__ldg(q + x) < (double)px) {
+      if (accept_test(ua_s[c], qx_s[c], px)) {
         accepted = c;
         break;
       }
       // Rejected: residual pass over the slice, r = max(0, p - q).  The owner
       // of the next child's token records r and p there for the exchange.
       const int cn = next_sib[c];
-      const int64_t xn = cn >= 0 ? (int64_t)tokens[off + cn] : -1;
+      const int64_t xn = cn >= 0 ? (int64_t)tok_s[cn] : -1;
       const int nxt = cur ^ 1;
-      const float inv_z = (float)(1.0 / Z);
+      const float inv_z = f2_inv(Z);
       const float* rin = resid[cur];
       float* rout = resid[nxt];
       CompSum acc;
-      double r_x = 0.0, p_x = 0.0;
+      float r_x = 0.f, p_x = 0.f;
       for (int64_t g0 = tid; g0 < n4; g0 += (int64_t)T * kMssGroups) {
         float4 a[kMssGroups], qq[kMssGroups];
 #pragma unroll
@@ -589,26 +673,28 @@ __global__ void __launch_bounds__(kMssThreads, 2)
           p_x = py;
         }
       }
-      double zs = acc.value();
-      block_sum3(zs, r_x, p_x, red);
-      exchange(zs, r_x, p_x);
-      double zr = lane < ncl ? peer(0, lane) : 0.0;
-      double rr = lane < ncl ? peer(1, lane) : 0.0;
-      double pr = lane < ncl ? peer(2, lane) : 0.0;
-      double Znew = 0.0, rxn = 0.0, pxn = 0.0;
+      F2 zs = comp_value(acc);
+      block_sum(zs, r_x, p_x, red);
+      exchange(zs.hi, zs.lo, r_x, p_x);
+      const float zh = lane < ncl ? peer(0, lane) : 0.f;
+      const float zl = lane < ncl ? peer(1, lane) : 0.f;
+      const float rr = lane < ncl ? peer(2, lane) : 0.f;
+      const float pr = lane < ncl ? peer(3, lane) : 0.f;
+      F2 Znew{0.f, 0.f};
+      float rxn = 0.f, pxn = 0.f;
       for (int r = 0; r < ncl; ++r) {
-        Znew += __shfl_sync(0xffffffffu, zr, r);
+        Znew = f2_add(Znew, F2{__shfl_sync(0xffffffffu, zh, r), __shfl_sync(0xffffffffu, zl, r)});
         rxn += __shfl_sync(0xffffffffu, rr, r);  // one owner, the rest add zeros
         pxn += __shfl_sync(0xffffffffu, pr, r);
       }
       ++xk;
-      if (Znew > 0.0) {  // else p = q up to rounding: keep p
+      if (Znew.hi > 0.f) {  // else p = q up to rounding: keep p
         cur = nxt;
         Z = Znew;
         from_resid = true;
-        px_next = (float)rxn * (float)(1.0 / Znew);
+        px_next = rxn * f2_inv(Znew);
       } else {
-        px_next = (float)pxn;
+        px_next = pxn;
       }
       px_known = true;
       c = cn;
@@ -650,44 +736,48 @@ __global__ void __launch_bounds__(kMssThreads, 2)
         if (w > 0.0f) last_pos = y;
       }
     }
-    const double mine = acc.value();
-    // Exclusive prefix over the CTA's threads (fp64): warp scan, then across warps.
+    const F2 mine = comp_value(acc);
+    // Exclusive prefix over the CTA's threads: warp scan, then across warps.
     const int warp = tid >> 5;
-    double incl = mine;
+    F2 incl = mine;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const double t = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += t;
+      const F2 t{__shfl_up_sync(0xffffffffu, incl.hi, o), __shfl_up_sync(0xffffffffu, incl.lo, o)};
+      if (lane >= o) incl = f2_add(t, incl);
     }
+    F2 wexcl{__shfl_up_sync(0xffffffffu, incl.hi, 1), __shfl_up_sync(0xffffffffu, incl.lo, 1)};
+    if (lane == 0) wexcl = F2{0.f, 0.f};
     if (lane == 31) scan_s[warp] = incl;
     if (last_pos >= 0) atomicMax(&last_s, (int)last_pos);
     __syncthreads();
-    double wbase = 0.0, cta_total = 0.0;
+    F2 wbase{0.f, 0.f}, cta_total{0.f, 0.f};
     for (int w = 0; w < kMssWarps; ++w) {
-      if (w < warp) wbase += scan_s[w];
-      cta_total += scan_s[w];
+      if (w < warp) wbase = f2_add(wbase, scan_s[w]);
+      cta_total = f2_add(cta_total, scan_s[w]);
     }
-    exchange(cta_total, (double)last_s, 0.0);
-    const double tr = lane < ncl ? peer(0, lane) : 0.0;
-    const double lr = lane < ncl ? peer(1, lane) : -1.0;
-    double base = 0.0, total = 0.0, last_all = -1.0;
+    exchange(cta_total.hi, cta_total.lo, __int_as_float(last_s), 0.f);
+    const float th = lane < ncl ? peer(0, lane) : 0.f;
+    const float tl = lane < ncl ? peer(1, lane) : 0.f;
+    const int lr = lane < ncl ? __float_as_int(peer(2, lane)) : -1;
+    F2 base{0.f, 0.f}, total{0.f, 0.f};
+    int last_all = -1;
     for (int r = 0; r < ncl; ++r) {
-      const double t = __shfl_sync(0xffffffffu, tr, r);
-      if (r < rank) base += t;
-      total += t;
-      last_all = fmax(last_all, __shfl_sync(0xffffffffu, lr, r));
+      const F2 t{__shfl_sync(0xffffffffu, th, r), __shfl_sync(0xffffffffu, tl, r)};
+      if (r < rank) base = f2_add(base, t);
+      total = f2_add(total, t);
+      last_all = max(last_all, __shfl_sync(0xffffffffu, lr, r));
     }
     ++xk;
-    const double excl = base + wbase + incl - mine;
-    const double target = (double)__ldg(u_smp + off + u) * total;
-    if (mine > 0.0 && excl <= target && target < excl + mine) {
+    const F2 excl = f2_add(f2_add(base, wbase), wexcl);
+    const F2 target = f2_scale(total, __ldg(u_smp + off + u));
+    if (mine.hi > 0.f && !f2_lt(target, excl) && f2_lt(target, f2_add(excl, mine))) {
       // This run holds the crossing; walk it in order.
       int64_t pick = -1;
       CompSum run;
       for (int64_t y = tlo; y < thi; ++y) {
         const float w = weight(from_resid ? rin[y] : lrow[y]);
         run.add(w);
-        if (excl + run.value() > target) {
+        if (f2_lt(target, f2_add(excl, comp_value(run)))) {
           pick = y;
           break;
         }
@@ -696,12 +786,12 @@ __global__ void __launch_bounds__(kMssThreads, 2)
       atomicMin(&pick_s, (int)pick);
     }
     __syncthreads();
-    exchange((double)pick_s, 0.0, 0.0);
+    exchange(__int_as_float(pick_s), 0.f, 0.f, 0.f);
     if (rank == 0 && tid == 0) {
       int pick = INT32_MAX;
-      for (int r = 0; r < ncl; ++r) pick = min(pick, (int)peer(0, r));
+      for (int r = 0; r < ncl; ++r) pick = min(pick, __float_as_int(peer(0, r)));
       // No crossing (rounding left the target at the total): last positive entry.
-      bonus[b] = pick != INT32_MAX ? pick : (int)last_all;
+      bonus[b] = pick != INT32_MAX ? pick : last_all;
       accept_len[b] = len - 1;
       if (n_tried) n_tried[b] = tried;
       status[b] = TSV_OK;
