@@ -92,6 +92,19 @@ def attention_bytes(spec, trees):
     return 2 * keys * spec.Hkv * spec.D * esz + 2 * N * spec.Hq * spec.D * esz
 
 
+def attention_flops(spec, trees):
+    """Algorithmic FLOPs of one tree-attention launch: per query row and per
+    key it sees (the prefix, then the node and its ancestors), one D-long dot
+    product for the score and one for the value update, 2 FLOPs per MAC."""
+    import workloads as W
+    offs = trees.node_offsets
+    keys_seen = 0.0
+    for b in range(len(offs) - 1):
+        depth = W.tree_depths(np.asarray(trees.parent[offs[b]:offs[b + 1]]))
+        keys_seen += float(len(depth) * int(trees.prefix_len[b]) + (depth.astype(np.int64) + 1).sum())
+    return 4.0 * spec.D * spec.Hq * keys_seen
+
+
 def verify_bytes(spec, trees, n_rejected_rows=0):
     """Greedy: every logits row once.  Stochastic: every LLM row once plus the
     full proposal row of each rejected child (count from the oracle)."""
@@ -166,12 +179,13 @@ class ClockSampler:
 
 
 def measured_peaks():
+    """(HBM GB/s, dense bf16 TFLOP/s for a kernel timed alone, which)."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
         with open(path) as f:
             j = json.load(f)
-        return float(j["hbm_gbs"]), "measured"
-    return 6800.0, "fallback"
+        return float(j["hbm_gbs"]), float(j["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, "fallback"
 
 
 def kernel_source_hash():
@@ -434,18 +448,27 @@ def run_ours(args, spec):
     e2e = measure_e2e(args, spec, trees, att, gi, si, h, tsv, dev, stream, ws_attn, ws_g, ws_s)
 
     # ---------------------------------------------------------------- roofline
-    peak, peak_kind = measured_peaks()
+    peak, peak_tf, peak_kind = measured_peaks()
     abytes = attention_bytes(spec, trees)
+    aflops = attention_flops(spec, trees)
     achieved = abytes / (attn_ms * 1e-3) / 1e9
     traffic = recorded_traffic(spec.name)
     keys_kernel = all(int(n) * (spec.Hq // spec.Hkv) <= 64 for n in np.diff(trees.node_offsets)) and \
         64 % (spec.Hq // spec.Hkv) == 0
     kernel_name = ("tree_attn_simt_kernel" if spec.dtype != "bf16" else
                    "tree_attn_keys_kernel" if keys_kernel else "tree_attn_tc_kernel")
-    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                "frac": achieved / peak, "traffic": traffic,
-                "kernel": kernel_name,
-                "launch_ms": attn_ms, "algorithmic_bytes": abytes, "peak_kind": peak_kind + " hbm_gbs"}
+    # The bound is whichever of bytes / bandwidth and FLOPs / tensor peak takes longer.
+    tensor_bound = spec.dtype == "bf16" and aflops / (peak_tf * 1e12) > abytes / (peak * 1e9)
+    if tensor_bound:
+        tf = aflops / (attn_ms * 1e-3) / 1e12
+        roofline = {"bound": "tensor", "achieved": tf, "peak": peak_tf, "unit": "TFLOP/s",
+                    "frac": tf / peak_tf, "peak_kind": peak_kind + " bf16_tflops (burst)"}
+    else:
+        roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                    "frac": achieved / peak, "peak_kind": peak_kind + " hbm_gbs"}
+    roofline.update({"traffic": traffic, "kernel": kernel_name, "launch_ms": attn_ms,
+                     "algorithmic_bytes": abytes, "algorithmic_flops": aflops,
+                     "hbm_gbs": achieved, "hbm_frac": achieved / peak})
     step_bytes = abytes + verify_bytes(spec, trees)
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
