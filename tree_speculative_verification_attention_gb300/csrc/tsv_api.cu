@@ -45,6 +45,15 @@ tsv_status check_batch(int32_t B, const int32_t* prefix_len, const int32_t* node
   return TSV_OK;
 }
 
+// Slot order of the requests: longest key range (prefix + nodes) first, ties
+// by request index.
+void order_slots(AttnPlan& p) {
+  for (int s = 0; s < p.B; ++s) p.slot_req[s] = s;
+  std::stable_sort(p.slot_req, p.slot_req + p.B, [&](int32_t a, int32_t b) {
+    return (int64_t)p.prefix[a] + p.nodes[a] > (int64_t)p.prefix[b] + p.nodes[b];
+  });
+}
+
 // Splits every request's keys into chunks of one common length (a multiple of
 // the 64-key block) so that the CTAs fill whole waves of SMs: the estimated
 // makespan is waves * (chunk + per-CTA overhead), minimised over the chunk
@@ -82,11 +91,13 @@ void build_plan(AttnPlan& p, int num_sms, int32_t B, const int32_t* prefix_len,
     if (chunk == kBN) break;
   }
   p.chunk_keys = (int32_t)best_chunk;
+  order_slots(p);
   int64_t units = 0, rows = 0, ctrs = 0;
-  for (int b = 0; b < B; ++b) {
+  for (int s = 0; s < B; ++s) {
+    const int b = p.slot_req[s];
     const int64_t L = (int64_t)p.prefix[b] + p.nodes[b];
     p.n_chunks[b] = p.mtiles[b] > 0 ? (int32_t)cdiv(L, best_chunk) : 0;
-    p.unit_start[b] = (int32_t)units;
+    p.unit_start[s] = (int32_t)units;
     units += (int64_t)Hkv * p.mtiles[b] * p.n_chunks[b];
     p.ctr_base[b] = (int32_t)ctrs;
     ctrs += (int64_t)Hkv * p.mtiles[b];
@@ -147,12 +158,14 @@ void build_plan_keys(AttnPlan& p, int num_sms, int32_t B, const int32_t* prefix_
     }
   }
   p.cluster = best_k;
+  order_slots(p);
   int64_t units = 0;
-  for (int b = 0; b < B; ++b) {
+  for (int s = 0; s < B; ++s) {
+    const int b = p.slot_req[s];
     const int64_t L = (int64_t)p.prefix[b] + p.nodes[b];
     p.chunk_len[b] = (int32_t)(cdiv(cdiv(L, best_k), kKeysBlockKeys) * kKeysBlockKeys);
     p.n_chunks[b] = p.mtiles[b] > 0 ? best_k : 0;
-    p.unit_start[b] = (int32_t)units;
+    p.unit_start[s] = (int32_t)units;
     units += (int64_t)Hkv * p.mtiles[b] * p.n_chunks[b];
     p.part_row[b] = -1;
   }

@@ -139,8 +139,8 @@ __global__ void __launch_bounds__(kKeysThreads, 1)
     mbar_fence_init();
   }
   __syncthreads();
-  const int b = *req_slot;
-  const int local = unit - plan.unit_start[b];
+  const int b = plan.slot_req[*req_slot];
+  const int local = unit - plan.unit_start[*req_slot];
   const int nch = plan.n_chunks[b];  // == cluster size
   const int mtiles = plan.mtiles[b];
   const int c = local % nch;

@@ -122,8 +122,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int mid = (lo + hi) >> 1;
     if (plan.unit_start[mid] <= unit) lo = mid; else hi = mid;
   }
-  const int b = lo;
-  const int local = unit - plan.unit_start[b];
+  const int b = plan.slot_req[lo];
+  const int local = unit - plan.unit_start[lo];
   const int mtiles = plan.mtiles[b], nch = plan.n_chunks[b];
   const int mt = local % mtiles;
   const int cg = local / mtiles;

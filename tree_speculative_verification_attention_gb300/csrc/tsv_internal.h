@@ -18,13 +18,17 @@ constexpr int kBN = 128;  // keys per pipeline block
 // kernel parameter (no host-to-device copy, so a launch can be captured).
 // A unit (CTA) is (request b, KV head g, chunk c, M-tile mt); inside request b
 // the unit index is ((g * n_chunks + c) * mtiles + mt), so the M-tiles of one
-// KV chunk run next to each other and share its rows through L2.
+// KV chunk run next to each other and share its rows through L2.  Requests
+// take consecutive unit ranges in slot order: slot s holds request
+// slot_req[s], longest key range first, so that the block scheduler starts
+// the longest CTAs first (longest-processing-time list scheduling).
 struct AttnPlan {
   int32_t B, Hq, Hkv, G, D;
   int32_t n_units;
   int32_t chunk_keys;  // keys per chunk (multiple of kBN), same for every request
   float scale_log2;    // softmax scale * log2(e)
-  int32_t unit_start[TSV_MAX_BATCH + 1];
+  int32_t unit_start[TSV_MAX_BATCH + 1];  // per slot
+  int32_t slot_req[TSV_MAX_BATCH];
   int32_t n_chunks[TSV_MAX_BATCH];
   int32_t mtiles[TSV_MAX_BATCH];
   int32_t prefix[TSV_MAX_BATCH];
