@@ -10,6 +10,8 @@ Two layers:
     ordinary attention), greedy verification and multi-step speculative
     sampling.  Wrapped by :func:`tree_attention`, :func:`verify_greedy`,
     :func:`verify_stochastic`, :func:`tree_ancestors`.
+  * :func:`kv_commit` (numpy, a copy): moves the accepted path's cache rows
+    behind the prefix, in path order.
   * :func:`tree_attention_dense_mask` (formulation beta, numpy fp64): builds the
     full topology-aware mask as a boolean matrix from the transitive closure of
     the parent relation and runs masked attention over every cache row.  It is
@@ -32,7 +34,7 @@ import numpy as np
 
 from .build import build_oracle
 
-OK, BAD_TREE, NONFINITE = 0, 2, 6
+OK, INVALID_ARG, BAD_TREE, NONFINITE = 0, 1, 2, 6
 NEAR_TIE_EPS = 1e-6
 
 _LIB = None
@@ -213,3 +215,46 @@ def verify_stochastic(llm_logits, ssm_probs, tokens, parent, node_offsets, u_acc
         _p(out["status"], _i32p))
     out["path"] = path
     return out
+
+
+def kv_commit(k_cache, v_cache, prefix_len, node_offsets, path, accept_len):
+    """Commit the accepted path to the KV cache.
+
+    SpecInfer §4 (Token Tree Verifier) keeps one cache for the verified
+    sequence and the speculated tree; once a path is accepted, its tokens
+    become the next part of the verified sequence.  Tree node i of request b
+    sits at cache row prefix_len[b] + i (the root, node 0, is the last verified
+    token), so committing the path path[0] = 0, path[1], ..., path[L] means:
+    row prefix_len[b] + k of the result holds row prefix_len[b] + path[k] of
+    the input, for k = 1 .. L; every other row is unchanged.
+
+    A path is accepted for commit when 0 <= L < n_b, path[0] == 0 and
+    path[1..L] rise strictly below n_b; otherwise that request's rows are left
+    as they are and its status is INVALID_ARG.  Returns (k, v, new_len,
+    status) with new_len[b] = prefix_len[b] + 1 + L (-1 when rejected).
+    k_cache, v_cache: [B, Lcap, Hkv, D] arrays of any dtype (values are copied).
+    """
+    k_in = np.asarray(k_cache)
+    v_in = np.asarray(v_cache)
+    k_out = k_in.copy()
+    v_out = v_in.copy()
+    B = len(node_offsets) - 1
+    new_len = np.full(B, -1, dtype=np.int64)
+    status = np.zeros(B, dtype=np.int64)
+    for b in range(B):
+        off = int(node_offsets[b])
+        n = int(node_offsets[b + 1]) - off
+        L = int(accept_len[b])
+        P = int(prefix_len[b])
+        ok = 0 <= L < n
+        if ok:
+            pth = [int(x) for x in path[off:off + L + 1]]
+            ok = pth[0] == 0 and all(pth[k - 1] < pth[k] < n for k in range(1, L + 1))
+        if not ok:
+            status[b] = INVALID_ARG
+            continue
+        for k in range(1, L + 1):
+            k_out[b, P + k] = k_in[b, P + pth[k]]
+            v_out[b, P + k] = v_in[b, P + pth[k]]
+        new_len[b] = P + 1 + L
+    return k_out, v_out, new_len, status
