@@ -49,6 +49,9 @@ def parse_args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true", help="profiling runs: skip e2e, baselines, JSON line")
     p.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU oracle sample budget")
+    p.add_argument("--row", choices=["step", "kv_commit"], default="step",
+                   help="step: the hot path (attention + verification); kv_commit: the commit of the "
+                        "accepted path that follows verification, timed alone")
     return p.parse_args()
 
 
@@ -577,13 +580,102 @@ def measure_e2e(args, spec, trees, att, gi, si, h, tsv, dev, stream, ws_attn, ws
             "ms_per_step": ms, "steps": steps, "api": "C ABI via the ctypes binding, pinned host buffers"}
 
 
+def run_kv_commit(args, spec):
+    """KV commit of the accepted path, timed alone on the workload's shapes: one
+    accepted chain per request (the root-to-node chain of a seeded random node).
+    Only the rows from prefix_len on are touched, so each of R rotating copies
+    holds those rows (prefix 0 on a view of them); R copies exceed 4 x L2."""
+    import torch
+    import oracle
+    import tree_speculative_verification_attention_gb300 as tsv
+    import workloads as W
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    trees = W.make_trees(spec)
+    att = W.make_attention_inputs(spec, trees)
+    rng = np.random.default_rng(1234)
+    offs = trees.node_offsets
+    B = len(offs) - 1
+    path = np.full(int(offs[-1]), -1, np.int32)
+    lens = np.zeros(B, np.int32)
+    for b in range(B):
+        off, n = int(offs[b]), int(offs[b + 1] - offs[b])
+        node, chain = int(rng.integers(0, n)), []
+        while node >= 0:
+            chain.append(node)
+            node = int(trees.parent[off + node])
+        path[off:off + len(chain)] = chain[::-1]
+        lens[b] = len(chain) - 1
+    nmax = int(np.diff(offs).max())
+    rows_k = torch.stack([att.k_cache[b, int(trees.prefix_len[b]):int(trees.prefix_len[b]) + nmax]
+                          for b in range(B)])
+    rows_v = torch.stack([att.v_cache[b, int(trees.prefix_len[b]):int(trees.prefix_len[b]) + nmax]
+                          for b in range(B)])
+    esz = rows_k.element_size()
+    per_copy = 2 * rows_k.numel() * esz
+    R = max(4, int(math.ceil(4 * 129e6 / per_copy)))
+    ks = [rows_k.to(dev) for _ in range(R)]
+    vs = [rows_v.to(dev) for _ in range(R)]
+    zero = torch.zeros(B, dtype=torch.int32, device=dev)
+    d_offs, d_path, d_lens = (torch.as_tensor(x).to(dev) for x in (offs, path, lens))
+    out = dict(new_len=torch.empty(B, dtype=torch.int32, device=dev),
+               status=torch.empty(B, dtype=torch.int32, device=dev))
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        for i in range(max(3, args.warmup)):
+            tsv.kv_commit(ks[i % R], vs[i % R], zero, d_offs, d_path, d_lens, stream=stream, out=out)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(R):
+                tsv.kv_commit(ks[i], vs[i], zero, d_offs, d_path, d_lens, stream=stream, out=out)
+    torch.cuda.synchronize()
+    reps = max(1, args.steps // R)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / (reps * R)
+    assert out["status"].cpu().eq(0).all()
+    moved = 2 * 2 * int(lens.sum()) * spec.Hkv * spec.D * esz  # K and V, read + write
+    peak, _, peak_kind = measured_peaks()
+    gbs = moved / (ms * 1e-3) / 1e9
+    # The oracle on the host, same rows.
+    kc, vc = rows_k.float().numpy(), rows_v.float().numpy()
+    t0 = time.perf_counter()
+    n_cpu = 0
+    while time.perf_counter() - t0 < min(args.cpu_seconds, 2.0) or n_cpu == 0:
+        oracle.kv_commit(kc, vc, np.zeros(B, np.int32), offs, path, lens)
+        n_cpu += 1
+    cpu_s = (time.perf_counter() - t0) / n_cpu
+    print(json.dumps({
+        "row": "kv_commit", "metric": "committed KV bytes/s (read + write)", "value": gbs, "unit": "GB/s",
+        "n_gpus": 1, "steps": reps * R, "warmup": max(3, args.warmup), "ms_per_launch": ms,
+        "higher_is_better": True, "dtype": spec.dtype, "data": "synthetic",
+        "config": {"workload": spec.name, "B": B, "Hkv": spec.Hkv, "D": spec.D,
+                   "accepted_rows": int(lens.sum()), "l2": "rotating %d copies of the touched rows" % R},
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
+                     "traffic": None, "kernel": "kv_commit_kernel", "peak_kind": peak_kind + " hbm_gbs",
+                     "algorithmic_bytes": moved},
+        "gpu_launches": reps * R,
+        "cpu_baseline": {"value": moved / cpu_s / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": "%d full commits of the same rows (numpy, one core)" % n_cpu},
+    }), flush=True)
+
+
 def main():
     args = parse_args()
     import workloads as W
     if args.workload not in W.SPECS:
         raise SystemExit("unknown workload %s (known: %s)" % (args.workload, ", ".join(W.SPECS)))
     spec = W.SPECS[args.workload]
-    if args.impl == "reference":
+    if args.row == "kv_commit":
+        run_kv_commit(args, spec)
+    elif args.impl == "reference":
         run_reference(args, spec)
     else:
         run_ours(args, spec)

@@ -9,6 +9,7 @@
  *                               plus its own ancestors (topology-aware mask)
  *   tsv_tree_verify_greedy      greedy acceptance walk over the tree
  *   tsv_tree_verify_stochastic  multi-step speculative sampling over the tree
+ *   tsv_kv_commit               move the accepted path's K/V rows behind the prefix
  *
  * Sources: "SpecInfer: Accelerating Generative Large Language Model Serving
  * with Tree-based Speculative Inference and Verification" — §2 Overview (tree
@@ -234,6 +235,37 @@ tsv_status tsv_tree_verify_stochastic(tsv_handle h, const float* llm_logits_d,
                                       int32_t N, int32_t* path_d, int32_t* accept_len_d,
                                       int32_t* bonus_d, int32_t* n_tried_d, void* workspace_d,
                                       size_t workspace_bytes, int32_t* status_d, void* stream);
+
+/*
+ * tsv_kv_commit — commits the accepted path to the KV cache (SpecInfer §4,
+ * Token Tree Verifier: the verified and speculated tokens share one cache,
+ * and the accepted tokens become the next part of the verified sequence).
+ * Tree node i of request b sits at cache row prefix_len[b] + i; node 0 (the
+ * root) is the last verified token.  For the path returned by verification,
+ * path[0] = 0, path[1], ..., path[L] (L = accept_len[b]), row
+ * prefix_len[b] + k receives the K and V rows of node path[k], k = 1 .. L, in
+ * place; no other row changes.
+ *   dtype, k_cache_d, v_cache_d, kv_stride_*, Hkv, D   as in tsv_tree_attention
+ *                   (the caches are written); rows, strides and pointers must
+ *                   be 16-byte aligned
+ *   prefix_len_d    int32 [B]   device copy of the prefix lengths
+ *   node_offsets_d  int32 [B+1]
+ *   path_d          int32 [N]   per request as written by the verify calls
+ *   accept_len_d    int32 [B]
+ *   new_len_d (out) int32 [B]: prefix_len[b] + 1 + L, the verified length
+ *                   (-1 when the request's path is rejected); may be NULL
+ *   status_d (out)  int32 [B]: TSV_OK, or TSV_ERR_INVALID_ARG when the path
+ *                   does not start at node 0, does not rise strictly or leaves
+ *                   the request's nodes (that request's rows are not touched)
+ * Needs no workspace.  Rows of rejected branches past prefix_len + L keep
+ * whatever they held.
+ */
+tsv_status tsv_kv_commit(tsv_handle h, tsv_dtype dtype, void* k_cache_d, void* v_cache_d,
+                         int64_t kv_stride_b, int64_t kv_stride_l, int64_t kv_stride_h, int32_t B,
+                         int32_t Hkv, int32_t D, const int32_t* prefix_len_d,
+                         const int32_t* node_offsets_d, const int32_t* path_d,
+                         const int32_t* accept_len_d, int32_t* new_len_d, int32_t* status_d,
+                         void* stream);
 
 /*
  * tsv_tree_verify_greedy_noalloc — the same greedy verification as

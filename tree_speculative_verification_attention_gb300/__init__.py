@@ -36,7 +36,7 @@ EXPORTED = (
     "tsv_tree_attention_workspace_size", "tsv_tree_attention",
     "tsv_tree_verify_greedy_workspace_size", "tsv_tree_verify_greedy",
     "tsv_tree_verify_stochastic_workspace_size", "tsv_tree_verify_stochastic",
-    "tsv_tree_verify_greedy_noalloc",
+    "tsv_tree_verify_greedy_noalloc", "tsv_kv_commit",
 )
 
 
@@ -72,6 +72,8 @@ def _load():
             ctypes.c_int, [vp, vp, i64, vp, vp, vp, i32, i32, vp, vp, vp, vp, sz, vp, vp]),
         "tsv_tree_verify_greedy_noalloc": (
             ctypes.c_int, [vp, vp, i64, vp, vp, vp, i32, i32, vp, vp, vp, vp, vp]),
+        "tsv_kv_commit": (
+            ctypes.c_int, [vp, ctypes.c_int, vp, vp, i64, i64, i64, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp]),
         "tsv_tree_verify_stochastic_workspace_size": (ctypes.c_int, [vp, i32, i32, i64, szp]),
         "tsv_tree_verify_stochastic": (
             ctypes.c_int, [vp, vp, vp, i64, vp, vp, vp, vp, vp, f32, i32, i32, vp, vp, vp, vp, vp, sz,
@@ -197,6 +199,14 @@ def tsv_tree_verify_greedy_noalloc(h, logits, V, tree_tokens, parent, node_offse
         "tsv_tree_verify_greedy_noalloc")
 
 
+def tsv_kv_commit(h, dtype_code, k_cache, v_cache, sb, sl, sh, B, Hkv, D, prefix_len, node_offsets, path,
+                  accept_len, new_len, status, stream=None):
+    _check(_lib.tsv_kv_commit(h, int(dtype_code), _ptr(k_cache), _ptr(v_cache), int(sb), int(sl), int(sh),
+                              int(B), int(Hkv), int(D), _ptr(prefix_len), _ptr(node_offsets), _ptr(path),
+                              _ptr(accept_len), _ptr(new_len), _ptr(status), _stream(stream)),
+           "tsv_kv_commit")
+
+
 def tsv_tree_verify_stochastic_workspace_size(h, B, N, V) -> int:
     out = ctypes.c_size_t()
     _check(_lib.tsv_tree_verify_stochastic_workspace_size(h, int(B), int(N), int(V), ctypes.byref(out)),
@@ -305,4 +315,20 @@ def tree_verify_stochastic(llm_logits, ssm_probs, tree_tokens, parent, node_offs
     tsv_tree_verify_stochastic(h, llm_logits, ssm_probs, V, tree_tokens, parent, node_offsets, u_accept,
                                u_sample, temperature, B, N, o["path"], o["accept_len"], o["bonus"],
                                o["n_tried"], workspace, workspace.numel(), o["status"], stream)
+    return o
+
+
+def kv_commit(k_cache, v_cache, prefix_len, node_offsets, path, accept_len, stream=None, out=None):
+    """Moves the accepted path's K/V rows behind the prefix, in place: row
+    prefix_len[b] + k takes node path[k]'s row.  k_cache / v_cache [B, Lcap,
+    Hkv, D] (or views with d contiguous); the other arguments are device int32
+    tensors as the verify calls write them.  Returns dict(new_len, status)."""
+    B, _, Hkv, D = k_cache.shape
+    assert k_cache.stride() == v_cache.stride() and k_cache.stride(3) == 1
+    dev = k_cache.device
+    o = out or dict(new_len=torch.empty(B, dtype=torch.int32, device=dev),
+                    status=torch.empty(B, dtype=torch.int32, device=dev))
+    tsv_kv_commit(handle(dev.index), _dtype_code(k_cache.dtype), k_cache, v_cache, k_cache.stride(0),
+                  k_cache.stride(1), k_cache.stride(2), B, Hkv, D, prefix_len, node_offsets, path, accept_len,
+                  o["new_len"], o["status"], stream)
     return o

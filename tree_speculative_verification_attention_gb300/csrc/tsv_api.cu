@@ -483,4 +483,30 @@ tsv_status tsv_tree_verify_stochastic(tsv_handle h, const float* llm_logits_d,
                                        status_d, static_cast<cudaStream_t>(stream)));
 }
 
+tsv_status tsv_kv_commit(tsv_handle h, tsv_dtype dtype, void* k_cache_d, void* v_cache_d,
+                         int64_t kv_stride_b, int64_t kv_stride_l, int64_t kv_stride_h, int32_t B,
+                         int32_t Hkv, int32_t D, const int32_t* prefix_len_d,
+                         const int32_t* node_offsets_d, const int32_t* path_d,
+                         const int32_t* accept_len_d, int32_t* new_len_d, int32_t* status_d,
+                         void* stream) {
+  if (!h || !k_cache_d || !v_cache_d || !prefix_len_d || !node_offsets_d || !path_d ||
+      !accept_len_d || !status_d)
+    return TSV_ERR_INVALID_ARG;
+  if (dtype != TSV_F32 && dtype != TSV_BF16) return TSV_ERR_INVALID_ARG;
+  if (B < 1 || B > TSV_MAX_BATCH || Hkv < 1 || D < 1) return TSV_ERR_INVALID_ARG;
+  const int64_t esz = dtype == TSV_BF16 ? 2 : 4;
+  // Whole 16-byte chunks: pointers, strides and the row of one head aligned.
+  if ((reinterpret_cast<uintptr_t>(k_cache_d) | reinterpret_cast<uintptr_t>(v_cache_d)) & 15)
+    return TSV_ERR_INVALID_ARG;
+  if (((int64_t)D * esz) % 16 || (kv_stride_b * esz) % 16 || (kv_stride_l * esz) % 16 ||
+      (kv_stride_h * esz) % 16 || kv_stride_b < 0 || kv_stride_l < 0 || kv_stride_h < 0)
+    return TSV_ERR_INVALID_ARG;
+  if ((int64_t)Hkv * D * esz / 16 > INT32_MAX) return TSV_ERR_UNSUPPORTED;
+  return cuda_status(launch_kv_commit(static_cast<uint8_t*>(k_cache_d), static_cast<uint8_t*>(v_cache_d),
+                                      kv_stride_b * esz, kv_stride_l * esz, kv_stride_h * esz, B, Hkv,
+                                      (int32_t)(D * esz / 16), prefix_len_d, node_offsets_d, path_d,
+                                      accept_len_d, new_len_d, status_d,
+                                      static_cast<cudaStream_t>(stream)));
+}
+
 }  // extern "C"

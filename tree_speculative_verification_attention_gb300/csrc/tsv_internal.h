@@ -113,4 +113,12 @@ cudaError_t launch_mss_verify(const float* llm_logits, const float* ssm_probs, i
                               int32_t* accept_len, int32_t* bonus, int32_t* n_tried,
                               int32_t* status, cudaStream_t st);
 
+// KV commit of the accepted path: rows hold row_chunks 16-byte chunks per
+// cache row (Hkv x D x element size / 16); strides in bytes.
+cudaError_t launch_kv_commit(uint8_t* k, uint8_t* v, int64_t sb, int64_t sl, int64_t sh, int32_t B,
+                             int32_t Hkv, int32_t d_chunks, const int32_t* prefix_len,
+                             const int32_t* node_offsets, const int32_t* path,
+                             const int32_t* accept_len, int32_t* new_len, int32_t* status,
+                             cudaStream_t st);
+
 }  // namespace tsv
