@@ -191,25 +191,35 @@ def measured_peaks():
     return 6800.0, 1900.0, "fallback"
 
 
-def kernel_source_hash():
+KERNEL_SOURCES = {
+    # What decides one attention launch's DRAM traffic: the kernel, the device
+    # headers it includes and the host planner that cuts the work.
+    "tree_attn_keys_kernel": ["tsv_attention_keys.cu"],
+    "tree_attn_tc_kernel": ["tsv_attention_tc.cu"],
+    "tree_attn_simt_kernel": ["tsv_attention_simt.cu"],
+}
+KERNEL_COMMON = ["tsv_attention_common.cuh", "tsv_device.cuh", "tsv_internal.h", "tsv_api.cu"]
+
+
+def kernel_source_hash(kernel):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "tree_speculative_verification_attention_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in KERNEL_SOURCES[kernel] + KERNEL_COMMON:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload):
+def recorded_traffic(workload, kernel):
     """DRAM bytes per attention launch from the committed ncu summary, if it
-    was taken on the current kernel sources; else None."""
+    was taken on the current sources of that kernel; else None."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         j = json.load(f)
     e = j.get(workload)
-    if not e or e.get("source_hash") != kernel_source_hash():
+    if not e or e.get("kernel") != kernel or e.get("source_hash") != kernel_source_hash(kernel):
         return None
     return float(e["dram_bytes_per_launch"])
 
@@ -387,9 +397,10 @@ def run_ours(args, spec):
             attention(c, st)
     torch.cuda.synchronize()
     # Kernels per step: one attention launch (masks built inside, splits merged
-    # inside), one for greedy verification, one for stochastic verification;
-    # checked against the captured graph when torch exposes it.
-    attn_kernels = 1
+    # inside; the fp32 CUDA-core path first prepares the ancestor bitsets in a
+    # launch of its own), one for greedy verification, one for stochastic
+    # verification; checked against the captured graph when torch exposes it.
+    attn_kernels = 1 if spec.dtype == "bf16" else 2
     kernels_per_step = attn_kernels + (1 if gi is not None else 0) + (1 if si is not None else 0)
     counted = graph_kernel_count(g_one[0])
     if counted is not None:
@@ -455,11 +466,11 @@ def run_ours(args, spec):
     abytes = attention_bytes(spec, trees)
     aflops = attention_flops(spec, trees)
     achieved = abytes / (attn_ms * 1e-3) / 1e9
-    traffic = recorded_traffic(spec.name)
     keys_kernel = all(int(n) * (spec.Hq // spec.Hkv) <= 64 for n in np.diff(trees.node_offsets)) and \
         64 % (spec.Hq // spec.Hkv) == 0
     kernel_name = ("tree_attn_simt_kernel" if spec.dtype != "bf16" else
                    "tree_attn_keys_kernel" if keys_kernel else "tree_attn_tc_kernel")
+    traffic = recorded_traffic(spec.name, kernel_name)
     # The bound is whichever of bytes / bandwidth and FLOPs / tensor peak takes longer.
     tensor_bound = spec.dtype == "bf16" and aflops / (peak_tf * 1e12) > abytes / (peak * 1e9)
     if tensor_bound:
