@@ -49,9 +49,10 @@ def parse_args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true", help="profiling runs: skip e2e, baselines, JSON line")
     p.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU oracle sample budget")
-    p.add_argument("--row", choices=["step", "kv_commit"], default="step",
+    p.add_argument("--row", choices=["step", "kv_commit", "sequence_baseline"], default="step",
                    help="step: the hot path (attention + verification); kv_commit: the commit of the "
-                        "accepted path that follows verification, timed alone")
+                        "accepted path that follows verification, timed alone; sequence_baseline: tree "
+                        "attention against the same work done per root-to-leaf sequence")
     return p.parse_args()
 
 
@@ -678,6 +679,101 @@ def run_kv_commit(args, spec):
     }), flush=True)
 
 
+def _attention_parts(q, k, v, trees, max_batch=128):
+    """Splits a batch into slices of at most max_batch requests (one launch each)."""
+    import workloads as W
+    offs = trees.node_offsets
+    parts = []
+    for b0 in range(0, len(offs) - 1, max_batch):
+        b1 = min(len(offs) - 1, b0 + max_batch)
+        r0, r1 = int(offs[b0]), int(offs[b1])
+        sub = W.Trees(trees.prefix_len[b0:b1], (offs[b0:b1 + 1] - offs[b0]).astype(np.int32),
+                      trees.parent[r0:r1], trees.Lcap)
+        parts.append((q[r0:r1], k[b0:b1], v[b0:b1], sub))
+    return parts
+
+
+def _time_attention(tsv, q, k, v, trees, dev, stream, reps):
+    """Milliseconds per tree attention over the whole batch (one launch per
+    slice of at most 128 requests, all replayed from one CUDA graph)."""
+    import torch
+    h = tsv.handle(dev.index)
+    code = 1 if q.dtype == torch.bfloat16 else 0
+    calls, outs, stats = [], [], []
+    for qp, kp, vp, tp in _attention_parts(q, k, v, trees):
+        plen, offs, parent = (torch.as_tensor(x).to(dev) for x in (tp.prefix_len, tp.node_offsets, tp.parent))
+        need = tsv.tsv_tree_attention_workspace_size(h, code, len(tp.prefix_len), tp.prefix_len, tp.node_offsets,
+                                                     qp.shape[1], kp.shape[2], qp.shape[2], 0, 0)
+        ws = torch.zeros(max(16, need), dtype=torch.uint8, device=dev)
+        out = torch.empty_like(qp)
+        st = torch.empty(len(tp.prefix_len), dtype=torch.int32, device=dev)
+        outs.append(out)
+        stats.append(st)
+        calls.append((qp, kp, vp, tp, plen, offs, parent, ws, out, st))
+
+    def run_all():
+        for qp, kp, vp, tp, plen, offs, parent, ws, out, st in calls:
+            tsv.tree_attention(qp, kp, vp, tp.prefix_len, tp.node_offsets, plen, offs, parent=parent, out=out,
+                               workspace=ws, status=st, stream=stream)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            run_all()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(reps):
+                run_all()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        g.replay()
+        e0.record(stream)
+        for _ in range(3):
+            g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    assert all(st.cpu().eq(0).all() for st in stats)
+    return e0.elapsed_time(e1) / (3 * reps), torch.cat(outs), len(calls)
+
+
+def run_sequence_baseline(args, spec):
+    """Tree attention against a sequence-based verifier doing the same work at
+    the kernel level: every root-to-leaf path as its own request (tree width
+    1) with its own copy of the prefix, through the same attention entry
+    point.  Both caches exceed 4 x L2 or are timed over launches that each
+    stream the whole cache."""
+    import torch
+    import tree_speculative_verification_attention_gb300 as tsv
+    import workloads as W
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    trees = W.make_trees(spec)
+    att = W.make_attention_inputs(spec, trees)
+    att_d = W.AttentionInputs(att.q.to(dev), att.k_cache.to(dev), att.v_cache.to(dev))
+    seq = W.sequence_decomposition(trees, att_d)
+    stream = torch.cuda.Stream()
+    reps = max(1, min(50, args.steps))
+    t_tree, out_tree, n_tree = _time_attention(tsv, att_d.q, att_d.k_cache, att_d.v_cache, trees, dev, stream,
+                                               reps)
+    t_seq, out_seq, n_seq = _time_attention(tsv, seq.inputs.q, seq.inputs.k_cache, seq.inputs.v_cache, seq.trees,
+                                            dev, stream, reps)
+    diff = (out_seq.float() - out_tree[torch.as_tensor(seq.tree_row, device=dev)].float()).abs().max().item()
+    b_tree, b_seq = attention_bytes(spec, trees), attention_bytes(spec, seq.trees)
+    peak, _, peak_kind = measured_peaks()
+    print(json.dumps({
+        "row": "sequence_baseline", "metric": "attention speed-up of the tree over per-sequence attention",
+        "value": t_seq / t_tree, "unit": "x", "higher_is_better": True, "n_gpus": 1, "dtype": spec.dtype,
+        "data": "synthetic",
+        "config": {"workload": spec.name, "tree_nodes": int(trees.node_offsets[-1]),
+                   "sequences": int(len(seq.trees.prefix_len)), "sequence_tokens": int(seq.trees.node_offsets[-1])},
+        "tree": {"ms": t_tree, "launches": n_tree, "algorithmic_bytes": b_tree,
+                 "hbm_gbs": b_tree / (t_tree * 1e-3) / 1e9},
+        "sequences": {"ms": t_seq, "launches": n_seq, "algorithmic_bytes": b_seq,
+                      "hbm_gbs": b_seq / (t_seq * 1e-3) / 1e9},
+        "peak_hbm_gbs": peak, "peak_kind": peak_kind, "max_abs_diff_sequence_vs_tree": diff,
+    }), flush=True)
+
+
 def main():
     args = parse_args()
     import workloads as W
@@ -686,6 +782,8 @@ def main():
     spec = W.SPECS[args.workload]
     if args.row == "kv_commit":
         run_kv_commit(args, spec)
+    elif args.row == "sequence_baseline":
+        run_sequence_baseline(args, spec)
     elif args.impl == "reference":
         run_reference(args, spec)
     else:

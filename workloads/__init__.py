@@ -322,3 +322,55 @@ def fuzz_spec(seed: int, dtype: str = "bf16", max_nodes: int = 40) -> Spec:
     return Spec(f"fuzz{seed}", 1000 + seed, dtype, B, Hkv * G, Hkv, D, int(r.integers(2, 3000)),
                 (lo, lo + int(r.integers(0, 300))), int(r.integers(1, max_nodes + 1)), "random",
                 max_depth=int(r.integers(1, 9)), stochastic=True)
+
+
+# --------------------------------------------------------------------------- sequence baseline
+
+
+@dataclass
+class SequenceBatch:
+    """A tree batch decomposed into its root-to-leaf sequences: one request per
+    leaf, a chain tree whose cache holds its own copy of the prefix followed by
+    the rows of the leaf's path (the layout a sequence-based verifier uses)."""
+    trees: Trees
+    inputs: AttentionInputs
+    tree_row: np.ndarray  # int64 [N_seq]: global tree node each sequence token stands for
+
+
+def sequence_decomposition(trees: Trees, att: AttentionInputs) -> SequenceBatch:
+    offs = trees.node_offsets
+    chains, reqs = [], []
+    for b in range(len(offs) - 1):
+        off, n = int(offs[b]), int(offs[b + 1] - offs[b])
+        par = trees.parent[off:off + n]
+        has_child = np.zeros(n, dtype=bool)
+        has_child[par[par >= 0]] = True
+        for leaf in np.nonzero(~has_child)[0]:
+            chain, node = [], int(leaf)
+            while node >= 0:
+                chain.append(node)
+                node = int(par[node])
+            chains.append(chain[::-1])
+            reqs.append(b)
+    S = len(chains)
+    sizes = np.array([len(c) for c in chains], dtype=np.int32)
+    prefix = np.array([int(trees.prefix_len[b]) for b in reqs], dtype=np.int32)
+    Lcap = int((prefix + sizes).max())
+    B, _, Hkv, D = att.k_cache.shape
+    dev = att.k_cache.device  # gathers run where the cache lives (the copies can be large)
+    k = torch.zeros((S, Lcap, Hkv, D), dtype=att.k_cache.dtype, device=dev)
+    v = torch.zeros_like(k)
+    q_rows, tree_row = [], []
+    for s, (b, chain) in enumerate(zip(reqs, chains)):
+        P = int(trees.prefix_len[b])
+        k[s, :P] = att.k_cache[b, :P]
+        v[s, :P] = att.v_cache[b, :P]
+        rows = torch.as_tensor([P + c for c in chain], device=dev)
+        k[s, P:P + len(chain)] = att.k_cache[b, rows]
+        v[s, P:P + len(chain)] = att.v_cache[b, rows]
+        tree_row.extend(int(offs[b]) + c for c in chain)
+    tree_row = np.array(tree_row, dtype=np.int64)
+    q = att.q[torch.as_tensor(tree_row, device=att.q.device)]
+    offsets = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    parent = np.concatenate([np.arange(-1, len(c) - 1, dtype=np.int32) for c in chains])
+    return SequenceBatch(Trees(prefix, offsets, parent, Lcap), AttentionInputs(q, k, v), tree_row)
