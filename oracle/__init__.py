@@ -57,7 +57,8 @@ def _bind(path):
         _i32p, _i32p, _i32p, _i32p]
     lib.oracle_verify_stochastic.argtypes = [
         _f32p, _f32p, ctypes.c_int64, _i32p, _i32p, _i32p, _f32p, _f32p,
-        ctypes.c_int32, ctypes.c_double, _i32p, _i32p, _i32p, _i32p, _i32p, _i32p, _i32p]
+        ctypes.c_int32, ctypes.c_double, ctypes.c_int32, ctypes.c_double,
+        _i32p, _i32p, _i32p, _i32p, _i32p, _i32p, _i32p]
     lib.oracle_num_threads.argtypes = []
     for f in (lib.oracle_tree_ancestors, lib.oracle_tree_attention,
               lib.oracle_verify_greedy, lib.oracle_verify_stochastic, lib.oracle_num_threads):
@@ -189,8 +190,10 @@ def verify_greedy(logits, tokens, parent, node_offsets):
 
 
 def verify_stochastic(llm_logits, ssm_probs, tokens, parent, node_offsets, u_accept, u_sample,
-                      temperature=1.0):
-    """Multi-step speculative sampling.
+                      temperature=1.0, top_k=0, top_p=1.0):
+    """Multi-step speculative sampling against the LLM distribution
+    softmax(logits / temperature), warped by top-k (top_k > 0) and then top-p
+    (top_p < 1) when asked (see warp_row in oracle.c for the exact rule).
 
     Returns dict(path, accept_len, bonus, n_tried, n_near_tie, tie_path_len, status).
     """
@@ -210,7 +213,7 @@ def verify_stochastic(llm_logits, ssm_probs, tokens, parent, node_offsets, u_acc
     _lib().oracle_verify_stochastic(
         _p(llm_logits, _f32p), _p(ssm_probs, _f32p), V, _p(tokens, _i32p), _p(parent, _i32p),
         _p(node_offsets, _i32p), _p(u_accept, _f32p), _p(u_sample, _f32p), B, float(temperature),
-        _p(path, _i32p), _p(out["accept_len"], _i32p), _p(out["bonus"], _i32p),
+        int(top_k), float(top_p), _p(path, _i32p), _p(out["accept_len"], _i32p), _p(out["bonus"], _i32p),
         _p(out["n_tried"], _i32p), _p(out["n_near_tie"], _i32p), _p(out["tie_path_len"], _i32p),
         _p(out["status"], _i32p))
     out["path"] = path

@@ -307,10 +307,66 @@ static void softmax_row(const float* x, int64_t V, double T, double* p) {
  * tie_path_len[b] = len(path) at the first such decision (-1 if none).  Two
  * implementations that round differently may part ways only from that point.
  */
+/*
+ * Warping of the LLM distribution before verification: top-k, then top-p
+ * (nucleus), as samplers apply them (SpecInfer's evaluation samples with
+ * top-k; the task asks for top-k/top-p).  Reading: tokens are ranked by their
+ * logit, larger first, equal logits by lower token index (p is an increasing
+ * function of the logit, so this is the ranking by probability with a fixed
+ * tie rule).  top_k > 0 keeps the first top_k tokens of the ranking (all when
+ * top_k <= 0 or >= V); 0 < top_p < 1 then keeps the shortest prefix of that
+ * ranking whose share of the kept mass reaches top_p.  p is set to zero
+ * elsewhere and renormalised.  A top-p cut whose cumulative share is within
+ * NEAR_TIE_EPS of top_p is reported through *near_tie.
+ */
+static const float* g_rank_logits;
+static int rank_cmp(const void* a, const void* b) {
+  const int64_t i = *(const int64_t*)a, j = *(const int64_t*)b;
+  const float li = g_rank_logits[i], lj = g_rank_logits[j];
+  if (li > lj) return -1;
+  if (li < lj) return 1;
+  return (i > j) - (i < j);
+}
+
+static void warp_row(const float* logits, int64_t V, int32_t top_k, double top_p, double* p,
+                     int* near_tie) {
+  const int use_k = top_k > 0 && (int64_t)top_k < V;
+  const int use_p = top_p < 1.0;
+  if (!use_k && !use_p) return;
+  int64_t* order = (int64_t*)malloc(sizeof(int64_t) * (size_t)V);
+  for (int64_t t = 0; t < V; ++t) order[t] = t;
+  g_rank_logits = logits;
+  qsort(order, (size_t)V, sizeof(int64_t), rank_cmp);
+  const int64_t K = use_k ? (int64_t)top_k : V;
+  double mass_k = 0.0;
+  for (int64_t j = 0; j < K; ++j) mass_k += p[order[j]];
+  int64_t keep = K;
+  if (use_p) {
+    double cum = 0.0, prev = 0.0;
+    for (int64_t j = 0; j < K; ++j) {
+      prev = cum;
+      cum += p[order[j]];
+      if (cum >= top_p * mass_k) {
+        keep = j + 1;
+        break;
+      }
+    }
+    if (fabs(cum - top_p * mass_k) < NEAR_TIE_EPS * mass_k ||
+        fabs(prev - top_p * mass_k) < NEAR_TIE_EPS * mass_k)
+      *near_tie = 1;
+  }
+  double mass = 0.0;
+  for (int64_t j = 0; j < keep; ++j) mass += p[order[j]];
+  for (int64_t j = keep; j < V; ++j) p[order[j]] = 0.0;
+  for (int64_t j = 0; j < keep; ++j) p[order[j]] /= mass;
+  free(order);
+}
+
 int oracle_verify_stochastic(const float* llm_logits, const float* ssm_probs, int64_t V,
                              const int32_t* tokens, const int32_t* parent,
                              const int32_t* node_offsets, const float* u_acc,
-                             const float* u_smp, int32_t B, double temperature, int32_t* path,
+                             const float* u_smp, int32_t B, double temperature, int32_t top_k,
+                             double top_p, int32_t* path,
                              int32_t* accept_len, int32_t* bonus, int32_t* n_tried,
                              int32_t* n_near_tie, int32_t* tie_path_len, int32_t* status) {
   int rc = ORACLE_OK;
@@ -333,7 +389,13 @@ int oracle_verify_stochastic(const float* llm_logits, const float* ssm_probs, in
     }
     int32_t u = 0, len = 0;
     pth[len++] = 0;
+    int warp_tie = 0;
     softmax_row(llm_logits + (size_t)(off + u) * V, V, temperature, p);
+    warp_row(llm_logits + (size_t)(off + u) * V, V, top_k, top_p, p, &warp_tie);
+    if (warp_tie) {
+      if (n_near_tie[b] == 0) tie_path_len[b] = len;
+      n_near_tie[b] += 1;
+    }
     for (;;) {
       int32_t next = -1;
       for (int32_t c = u + 1; c < n && next < 0; ++c) {
@@ -372,6 +434,12 @@ int oracle_verify_stochastic(const float* llm_logits, const float* ssm_probs, in
       u = next;
       pth[len++] = u;
       softmax_row(llm_logits + (size_t)(off + u) * V, V, temperature, p);
+      warp_tie = 0;
+      warp_row(llm_logits + (size_t)(off + u) * V, V, top_k, top_p, p, &warp_tie);
+      if (warp_tie) {
+        if (n_near_tie[b] == 0) tie_path_len[b] = len;
+        n_near_tie[b] += 1;
+      }
     }
     accept_len[b] = len - 1;
 

@@ -180,8 +180,10 @@ def _softmax(z):
     return e / e.sum(-1, keepdims=True)
 
 
-def _run_mss_markov(lib_verify, trials, seed, V=4, n=8, max_depth=3, n_ssm=3, emit=3):
-    """Iterate tree verification on a Markov toy LLM until every trial emitted `emit` tokens."""
+def _run_mss_markov(lib_verify, trials, seed, V=4, n=8, max_depth=3, n_ssm=3, emit=3, law=None):
+    """Iterate tree verification on a Markov toy LLM until every trial emitted `emit` tokens.
+    `law(A)` gives the next-token law the emitted tokens must follow (default:
+    softmax of the LLM's logits)."""
     rng = np.random.default_rng(seed)
     A = rng.standard_normal((V, V)).astype(np.float32)  # LLM logits given the previous token
     Q = np.stack([_softmax(rng.standard_normal((V, V)) * 1.5) for _ in range(n_ssm)]).astype(np.float32)
@@ -227,7 +229,7 @@ def _run_mss_markov(lib_verify, trials, seed, V=4, n=8, max_depth=3, n_ssm=3, em
             if len(seqs[t]) < emit:
                 still.append(t)
         active = np.array(still, dtype=np.int64)
-    P1 = _softmax(A)  # next-token law of the LLM
+    P1 = _softmax(A) if law is None else law(A)  # next-token law of the LLM
     expected = np.zeros([V] * emit)
     for idx in np.ndindex(*([V] * emit)):
         pr, prev = 1.0, t0
