@@ -49,6 +49,8 @@ def parse_args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true", help="profiling runs: skip e2e, baselines, JSON line")
     p.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU oracle sample budget")
+    p.add_argument("--top-k", type=int, default=0, help="stochastic verification against the top-k warped LLM law")
+    p.add_argument("--top-p", type=float, default=1.0, help="... and top-p (needs --top-k)")
     p.add_argument("--row", choices=["step", "kv_commit", "sequence_baseline"], default="step",
                    help="step: the hot path (attention + verification); kv_commit: the commit of the "
                         "accepted path that follows verification, timed alone; sequence_baseline: tree "
@@ -75,12 +77,17 @@ def workload_inputs(spec):
     return trees, att, gi, si
 
 
+WARP = {}  # top_k / top_p of the stochastic verification, when warped
+
+
 def config_of(spec, extra=None):
     cfg = {"workload": spec.name, "B": spec.B, "Hq": spec.Hq, "Hkv": spec.Hkv, "D": spec.D,
            "prefix": list(spec.prefix) if isinstance(spec.prefix, tuple) else spec.prefix,
            "nodes_per_request": spec.nodes, "vocab": spec.V,
            "verify": "+".join(v for v, on in (("greedy", spec.greedy), ("stochastic", spec.stochastic)) if on),
            "tree": spec.tree}
+    if WARP:
+        cfg["warp"] = dict(WARP)
     if extra:
         cfg.update(extra)
     return cfg
@@ -249,7 +256,7 @@ def oracle_step_time(spec, trees, att, gi, si, budget_s, heads_sample=None):
             oracle.verify_greedy(gi.logits, gi.tokens, trees.parent, trees.node_offsets)
         if si is not None:
             oracle.verify_stochastic(si.llm_logits, si.ssm_probs, si.tokens, trees.parent,
-                                     trees.node_offsets, si.u_accept, si.u_sample)
+                                     trees.node_offsets, si.u_accept, si.u_sample, **WARP)
         t2 = time.perf_counter()
         t_att += t1 - t0
         t_ver += t2 - t1
@@ -372,7 +379,7 @@ def run_ours(args, spec):
                                    out=st["g"])
         if si is not None:
             tsv.tree_verify_stochastic(c["llm"], c["ssm"], c["stok"], c["parent"], c["offs"], c["ua"],
-                                       c["us"], workspace=st["ws_s"], out=st["s"])
+                                       c["us"], workspace=st["ws_s"], out=st["s"], **WARP)
 
     states = [make_state(c) for c in copies]
     # Eager run once (also checks statuses), then capture one graph per input copy.
@@ -568,7 +575,7 @@ def measure_e2e(args, spec, trees, att, gi, si, h, tsv, dev, stream, ws_attn, ws
                 res_h[k].copy_(res[k], non_blocking=True)
         if si is not None:
             tsv.tree_verify_stochastic(d["llm"], d["ssm"], d["stok"], d["parent"], d["offs"], d["ua"], d["us"],
-                                       workspace=wss, out=res2)
+                                       workspace=wss, out=res2, **WARP)
             for k in ("path", "accept_len", "bonus"):
                 res_h[k].copy_(res2[k], non_blocking=True)
 
@@ -780,6 +787,8 @@ def main():
     if args.workload not in W.SPECS:
         raise SystemExit("unknown workload %s (known: %s)" % (args.workload, ", ".join(W.SPECS)))
     spec = W.SPECS[args.workload]
+    if args.top_k or args.top_p < 1.0:
+        WARP.update(top_k=args.top_k, top_p=args.top_p)
     if args.row == "kv_commit":
         run_kv_commit(args, spec)
     elif args.row == "sequence_baseline":

@@ -9,6 +9,7 @@
  *                               plus its own ancestors (topology-aware mask)
  *   tsv_tree_verify_greedy      greedy acceptance walk over the tree
  *   tsv_tree_verify_stochastic  multi-step speculative sampling over the tree
+ *   tsv_tree_verify_stochastic_warped  the same against a top-k / top-p warped LLM distribution
  *   tsv_kv_commit               move the accepted path's K/V rows behind the prefix
  *
  * Sources: "SpecInfer: Accelerating Generative Large Language Model Serving
@@ -235,6 +236,33 @@ tsv_status tsv_tree_verify_stochastic(tsv_handle h, const float* llm_logits_d,
                                       int32_t N, int32_t* path_d, int32_t* accept_len_d,
                                       int32_t* bonus_d, int32_t* n_tried_d, void* workspace_d,
                                       size_t workspace_bytes, int32_t* status_d, void* stream);
+
+/*
+ * tsv_tree_verify_stochastic_warped — tsv_tree_verify_stochastic against the
+ * warped LLM distribution that top-k / top-p sampling draws from (the pages'
+ * evaluation samples with top-k): p = softmax(llm_logits[u] / temperature),
+ * then
+ *   top_k > 0    keep the top_k tokens of the ranking (larger logit first,
+ *                equal logits by lower token index), all when top_k >= V;
+ *   top_p < 1    then keep the shortest prefix of that ranking whose share of
+ *                the kept mass reaches top_p;
+ * and renormalise over the kept tokens, zero elsewhere.  Acceptance, residual
+ * and bonus follow the same rules on this p, so the emitted tokens follow it.
+ * ssm_probs rows are used as given: they are the proposal distributions the
+ * proposer actually sampled from (warped or not).
+ *   top_k   0 (off) or 1 .. 1024; top_p in (0, 1] (1 = off); top_p < 1 needs
+ *           top_k >= 1 (TSV_ERR_UNSUPPORTED otherwise, as for top_k > 1024)
+ *   other arguments, workspace and outputs as in tsv_tree_verify_stochastic.
+ * A top-p cut within about 1e-6 of top_p may go either way relative to an
+ * exact computation.
+ */
+tsv_status tsv_tree_verify_stochastic_warped(
+    tsv_handle h, const float* llm_logits_d, const float* ssm_probs_d, int64_t V,
+    const int32_t* tree_tokens_d, const int32_t* parent_d, const int32_t* node_offsets_d,
+    const float* u_accept_d, const float* u_sample_d, float temperature, int32_t top_k, float top_p,
+    int32_t B, int32_t N, int32_t* path_d, int32_t* accept_len_d, int32_t* bonus_d,
+    int32_t* n_tried_d, void* workspace_d, size_t workspace_bytes, int32_t* status_d,
+    void* stream);
 
 /*
  * tsv_kv_commit — commits the accepted path to the KV cache (SpecInfer §4,

@@ -36,7 +36,7 @@ EXPORTED = (
     "tsv_tree_attention_workspace_size", "tsv_tree_attention",
     "tsv_tree_verify_greedy_workspace_size", "tsv_tree_verify_greedy",
     "tsv_tree_verify_stochastic_workspace_size", "tsv_tree_verify_stochastic",
-    "tsv_tree_verify_greedy_noalloc", "tsv_kv_commit",
+    "tsv_tree_verify_greedy_noalloc", "tsv_kv_commit", "tsv_tree_verify_stochastic_warped",
 )
 
 
@@ -72,6 +72,9 @@ def _load():
             ctypes.c_int, [vp, vp, i64, vp, vp, vp, i32, i32, vp, vp, vp, vp, sz, vp, vp]),
         "tsv_tree_verify_greedy_noalloc": (
             ctypes.c_int, [vp, vp, i64, vp, vp, vp, i32, i32, vp, vp, vp, vp, vp]),
+        "tsv_tree_verify_stochastic_warped": (
+            ctypes.c_int, [vp, vp, vp, i64, vp, vp, vp, vp, vp, f32, i32, f32, i32, i32, vp, vp, vp, vp, vp, sz,
+                           vp, vp]),
         "tsv_kv_commit": (
             ctypes.c_int, [vp, ctypes.c_int, vp, vp, i64, i64, i64, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp]),
         "tsv_tree_verify_stochastic_workspace_size": (ctypes.c_int, [vp, i32, i32, i64, szp]),
@@ -199,6 +202,16 @@ def tsv_tree_verify_greedy_noalloc(h, logits, V, tree_tokens, parent, node_offse
         "tsv_tree_verify_greedy_noalloc")
 
 
+def tsv_tree_verify_stochastic_warped(h, llm_logits, ssm_probs, V, tree_tokens, parent, node_offsets, u_accept,
+                                      u_sample, temperature, top_k, top_p, B, N, path, accept_len, bonus,
+                                      n_tried, workspace, workspace_bytes, status, stream=None):
+    _check(_lib.tsv_tree_verify_stochastic_warped(
+        h, _ptr(llm_logits), _ptr(ssm_probs), int(V), _ptr(tree_tokens), _ptr(parent), _ptr(node_offsets),
+        _ptr(u_accept), _ptr(u_sample), float(temperature), int(top_k), float(top_p), int(B), int(N), _ptr(path),
+        _ptr(accept_len), _ptr(bonus), _ptr(n_tried), _ptr(workspace), int(workspace_bytes), _ptr(status),
+        _stream(stream)), "tsv_tree_verify_stochastic_warped")
+
+
 def tsv_kv_commit(h, dtype_code, k_cache, v_cache, sb, sl, sh, B, Hkv, D, prefix_len, node_offsets, path,
                   accept_len, new_len, status, stream=None):
     _check(_lib.tsv_kv_commit(h, int(dtype_code), _ptr(k_cache), _ptr(v_cache), int(sb), int(sl), int(sh),
@@ -299,8 +312,10 @@ def tree_verify_greedy(logits, tree_tokens, parent, node_offsets, workspace=None
 
 
 def tree_verify_stochastic(llm_logits, ssm_probs, tree_tokens, parent, node_offsets, u_accept, u_sample,
-                           temperature=1.0, workspace=None, stream=None, out=None):
-    """Multi-step speculative sampling; returns dict(path, accept_len, bonus, n_tried, status)."""
+                           temperature=1.0, workspace=None, stream=None, out=None, top_k=0, top_p=1.0):
+    """Multi-step speculative sampling, against the top-k / top-p warped LLM
+    distribution when top_k > 0 or top_p < 1; returns dict(path, accept_len,
+    bonus, n_tried, status)."""
     N, V = llm_logits.shape
     B = node_offsets.shape[0] - 1
     dev = llm_logits.device
@@ -312,9 +327,15 @@ def tree_verify_stochastic(llm_logits, ssm_probs, tree_tokens, parent, node_offs
                     status=torch.empty(B, dtype=torch.int32, device=dev))
     if workspace is None:
         workspace = _workspace(tsv_tree_verify_stochastic_workspace_size(h, B, N, V), dev)
-    tsv_tree_verify_stochastic(h, llm_logits, ssm_probs, V, tree_tokens, parent, node_offsets, u_accept,
-                               u_sample, temperature, B, N, o["path"], o["accept_len"], o["bonus"],
-                               o["n_tried"], workspace, workspace.numel(), o["status"], stream)
+    if top_k or top_p < 1.0:
+        tsv_tree_verify_stochastic_warped(h, llm_logits, ssm_probs, V, tree_tokens, parent, node_offsets,
+                                          u_accept, u_sample, temperature, top_k, top_p, B, N, o["path"],
+                                          o["accept_len"], o["bonus"], o["n_tried"], workspace, workspace.numel(),
+                                          o["status"], stream)
+    else:
+        tsv_tree_verify_stochastic(h, llm_logits, ssm_probs, V, tree_tokens, parent, node_offsets, u_accept,
+                                   u_sample, temperature, B, N, o["path"], o["accept_len"], o["bonus"],
+                                   o["n_tried"], workspace, workspace.numel(), o["status"], stream)
     return o
 
 

@@ -459,6 +459,32 @@ tsv_status tsv_tree_verify_stochastic_workspace_size(tsv_handle h, int32_t B, in
   return TSV_OK;
 }
 
+static tsv_status verify_stochastic(tsv_handle h, const float* llm_logits_d, const float* ssm_probs_d,
+                                    int64_t V, const int32_t* tree_tokens_d, const int32_t* parent_d,
+                                    const int32_t* node_offsets_d, const float* u_accept_d,
+                                    const float* u_sample_d, float temperature, int32_t top_k,
+                                    float top_p, int32_t B, int32_t N, int32_t* path_d,
+                                    int32_t* accept_len_d, int32_t* bonus_d, int32_t* n_tried_d,
+                                    void* workspace_d, size_t workspace_bytes, int32_t* status_d,
+                                    void* stream) {
+  if (!h || !tree_tokens_d || !parent_d || !node_offsets_d || !accept_len_d || !bonus_d ||
+      !status_d)
+    return TSV_ERR_INVALID_ARG;
+  if (B < 1 || B > TSV_MAX_BATCH || N < 0 || V < 1 || V > INT32_MAX) return TSV_ERR_INVALID_ARG;
+  if (!(temperature > 0.f) || isinf(temperature)) return TSV_ERR_INVALID_ARG;
+  if (top_k < 0 || !(top_p > 0.f) || top_p > 1.f) return TSV_ERR_INVALID_ARG;
+  if (top_k > kMssMaxTopK || (top_p < 1.f && top_k == 0)) return TSV_ERR_UNSUPPORTED;
+  if (N > 0 && (!llm_logits_d || !ssm_probs_d || !u_accept_d || !u_sample_d || !path_d))
+    return TSV_ERR_INVALID_ARG;
+  const size_t need = round256((size_t)B * 2 * (size_t)V * 4);
+  if (!workspace_d || workspace_bytes < need) return TSV_ERR_INVALID_ARG;
+  float* resid = static_cast<float*>(workspace_d);
+  return cuda_status(launch_mss_verify(llm_logits_d, ssm_probs_d, V, tree_tokens_d, parent_d,
+                                       node_offsets_d, u_accept_d, u_sample_d, 1.0f / temperature,
+                                       top_k, top_p, B, resid, path_d, accept_len_d, bonus_d,
+                                       n_tried_d, status_d, static_cast<cudaStream_t>(stream)));
+}
+
 tsv_status tsv_tree_verify_stochastic(tsv_handle h, const float* llm_logits_d,
                                       const float* ssm_probs_d, int64_t V,
                                       const int32_t* tree_tokens_d, const int32_t* parent_d,
@@ -467,20 +493,23 @@ tsv_status tsv_tree_verify_stochastic(tsv_handle h, const float* llm_logits_d,
                                       int32_t N, int32_t* path_d, int32_t* accept_len_d,
                                       int32_t* bonus_d, int32_t* n_tried_d, void* workspace_d,
                                       size_t workspace_bytes, int32_t* status_d, void* stream) {
-  if (!h || !tree_tokens_d || !parent_d || !node_offsets_d || !accept_len_d || !bonus_d ||
-      !status_d)
-    return TSV_ERR_INVALID_ARG;
-  if (B < 1 || B > TSV_MAX_BATCH || N < 0 || V < 1 || V > INT32_MAX) return TSV_ERR_INVALID_ARG;
-  if (!(temperature > 0.f) || isinf(temperature)) return TSV_ERR_INVALID_ARG;
-  if (N > 0 && (!llm_logits_d || !ssm_probs_d || !u_accept_d || !u_sample_d || !path_d))
-    return TSV_ERR_INVALID_ARG;
-  const size_t need = round256((size_t)B * 2 * (size_t)V * 4);
-  if (!workspace_d || workspace_bytes < need) return TSV_ERR_INVALID_ARG;
-  float* resid = static_cast<float*>(workspace_d);
-  return cuda_status(launch_mss_verify(llm_logits_d, ssm_probs_d, V, tree_tokens_d, parent_d,
-                                       node_offsets_d, u_accept_d, u_sample_d, 1.0f / temperature,
-                                       B, resid, path_d, accept_len_d, bonus_d, n_tried_d,
-                                       status_d, static_cast<cudaStream_t>(stream)));
+  return verify_stochastic(h, llm_logits_d, ssm_probs_d, V, tree_tokens_d, parent_d, node_offsets_d,
+                           u_accept_d, u_sample_d, temperature, 0, 1.0f, B, N, path_d,
+                           accept_len_d, bonus_d, n_tried_d, workspace_d, workspace_bytes,
+                           status_d, stream);
+}
+
+tsv_status tsv_tree_verify_stochastic_warped(
+    tsv_handle h, const float* llm_logits_d, const float* ssm_probs_d, int64_t V,
+    const int32_t* tree_tokens_d, const int32_t* parent_d, const int32_t* node_offsets_d,
+    const float* u_accept_d, const float* u_sample_d, float temperature, int32_t top_k, float top_p,
+    int32_t B, int32_t N, int32_t* path_d, int32_t* accept_len_d, int32_t* bonus_d,
+    int32_t* n_tried_d, void* workspace_d, size_t workspace_bytes, int32_t* status_d,
+    void* stream) {
+  return verify_stochastic(h, llm_logits_d, ssm_probs_d, V, tree_tokens_d, parent_d, node_offsets_d,
+                           u_accept_d, u_sample_d, temperature, top_k, top_p, B, N, path_d,
+                           accept_len_d, bonus_d, n_tried_d, workspace_d, workspace_bytes,
+                           status_d, stream);
 }
 
 tsv_status tsv_kv_commit(tsv_handle h, tsv_dtype dtype, void* k_cache_d, void* v_cache_d,

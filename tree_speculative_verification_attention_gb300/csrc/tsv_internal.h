@@ -109,9 +109,10 @@ int mss_cluster_size(int64_t V);
 cudaError_t launch_mss_verify(const float* llm_logits, const float* ssm_probs, int64_t V,
                               const int32_t* tokens, const int32_t* parent,
                               const int32_t* node_offsets, const float* u_acc, const float* u_smp,
-                              float inv_t, int32_t B, float* resid, int32_t* path,
-                              int32_t* accept_len, int32_t* bonus, int32_t* n_tried,
+                              float inv_t, int32_t top_k, float top_p, int32_t B, float* resid,
+                              int32_t* path, int32_t* accept_len, int32_t* bonus, int32_t* n_tried,
                               int32_t* status, cudaStream_t st);
+constexpr int kMssMaxTopK = 1024;  // largest top_k of the warped stochastic verification
 
 // KV commit of the accepted path: rows hold row_chunks 16-byte chunks per
 // cache row (Hkv x D x element size / 16); strides in bytes.

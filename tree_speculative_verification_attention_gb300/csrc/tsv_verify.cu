@@ -320,6 +320,7 @@ constexpr int kMssWarps = kMssThreads / 32;
 constexpr int kMssMaxCluster = 8;
 constexpr int64_t kMssMinSlice = 4096;  // vocab entries per CTA at least
 constexpr int kMssGroups = 4;           // 4-float groups in flight per thread
+constexpr int kMaxTopK = kMssMaxTopK;   // largest top-k the warped support handles
 
 // exp(a - m) with the subtraction's rounding error folded back in (TwoSum:
 // a - m = d + err exactly), so the result is as accurate as expf itself even
@@ -437,6 +438,257 @@ __device__ __forceinline__ bool accept_test(float u, float q, float p) {
   return p0 < p || (p0 == p && e < 0.f);
 }
 
+// Order-preserving 32-bit key of a float (-0 counts as +0): larger logit,
+// larger key.
+__device__ __forceinline__ uint32_t order_key(float l) {
+  const uint32_t u = __float_as_uint(l + 0.0f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ float key_value(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+__device__ __forceinline__ int ld_dsmem_s32(uint32_t addr) {
+  int v;
+  asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+// Token y of the row is kept by the warp iff its logit l ranks before the
+// boundary: l > tau, or l == tau and y <= ycut (ranking: larger logit first,
+// equal logits by lower index).
+__device__ __forceinline__ bool kept(float l, int64_t y, float tau, int ycut) {
+  return l > tau || (l == tau && y <= ycut);
+}
+
+// Shared scratch of the warped support.
+static_assert(kMssThreads == 256, "one histogram bin per thread");
+struct SelSmem {
+  int hist[2][256];  // per-CTA digit histograms, alternating with the exchanges
+  int wsum[kMssThreads / 32];
+  int ints[8];
+  float cand_v[kMaxTopK];
+  int cand_i[kMaxTopK];
+  float srt_v[kMaxTopK];
+  int srt_i[kMaxTopK];
+  F2 tsum[kMssWarps];
+  F2 s_cut;
+};
+
+struct Support {
+  float tau;
+  int ycut;
+  F2 S;
+};
+
+// The warped support of one LLM row (top-k, then top-p, as the oracle defines
+// them), found by the whole cluster: its boundary (tau, ycut) in the ranking
+// and the kept mass S = sum exp(l / T - M) over kept tokens.  Radix selection
+// of the k-th key (four 8-bit digits, histograms summed over the cluster),
+// then, for equal logits at the boundary, the cut by token index; the kept
+// tokens (at most kMaxTopK) are gathered into every CTA and sorted there, the
+// same way in every CTA, for the top-p cut and the mass.  Every CTA of the
+// cluster runs it in lockstep; `xk` counts the exchanges.
+__device__ __noinline__ Support warped_support(const float* __restrict__ lrow, int64_t V, int64_t lo,
+                                               int64_t hi, float inv_t, float M, int top_k, float top_p,
+                                               int ncl, int rank, int& xk, float (*pub)[4], SelSmem& w) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int Kt = (int64_t)top_k < V ? top_k : (int)V;
+  uint32_t prefix = 0;
+  float tau = -INFINITY;
+  int ycut = INT32_MAX;
+  if (Kt < V) {
+    int r = Kt, ties_total = 0;
+    for (int pass = 0; pass < 4; ++pass) {
+      const int shift = 24 - 8 * pass;
+      int* h = w.hist[xk & 1];
+      h[tid] = 0;  // kMssThreads == 256 bins
+      __syncthreads();
+      for (int64_t y = lo + tid; y < hi; y += kMssThreads) {
+        const uint32_t k = order_key(__ldg(lrow + y));
+        if (pass == 0 || (k >> (shift + 8)) == prefix) atomicAdd(&h[(k >> shift) & 255], 1);
+      }
+      __syncthreads();
+      cluster_sync_all();
+      int cnt = 0;
+      for (int rr = 0; rr < ncl; ++rr) cnt += ld_dsmem_s32(mapa_shared(smem_u32(&h[tid]), (uint32_t)rr));
+      ++xk;
+      // Suffix sums over the digits (larger digit = larger logit).
+      int sfx = cnt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_down_sync(0xffffffffu, sfx, o);
+        if (lane + o < 32) sfx += t;
+      }
+      if (lane == 0) w.wsum[warp] = sfx;
+      __syncthreads();
+      for (int ww = warp + 1; ww < kMssWarps; ++ww) sfx += w.wsum[ww];
+      if (sfx >= r && sfx - cnt < r) {
+        w.ints[0] = tid;
+        w.ints[1] = sfx - cnt;
+        w.ints[2] = cnt;
+      }
+      __syncthreads();
+      r -= w.ints[1];
+      ties_total = w.ints[2];
+      prefix = (prefix << 8) | (uint32_t)w.ints[0];
+      __syncthreads();
+    }
+    tau = key_value(prefix);
+    if (r < ties_total) {
+      // Keep the r lowest-index tokens among those equal to tau.
+      if (tid == 0) w.ints[3] = 0;
+      __syncthreads();
+      int c = 0;
+      for (int64_t y = lo + tid; y < hi; y += kMssThreads) c += order_key(__ldg(lrow + y)) == prefix;
+      atomicAdd(&w.ints[3], c);
+      __syncthreads();
+      if (tid == 0) pub[xk & 1][0] = __int_as_float(w.ints[3]);
+      cluster_sync_all();
+      int before = 0, mine = 0;
+      for (int rr = 0; rr < ncl; ++rr) {
+        const int t = __float_as_int(ld_dsmem_f32(mapa_shared(smem_u32(&pub[xk & 1][0]), (uint32_t)rr)));
+        if (rr < rank) before += t;
+        if (rr == rank) mine = t;
+      }
+      ++xk;
+      int found = -1;
+      if (warp == 0 && before < r && r <= before + mine) {
+        int need = r - before;
+        for (int64_t base = lo; base < hi; base += 32) {
+          const int64_t y = base + lane;
+          const bool tie = y < hi && order_key(__ldg(lrow + y)) == prefix;
+          const uint32_t bal = __ballot_sync(0xffffffffu, tie);
+          const int n = __popc(bal);
+          if (need <= n) {
+            uint32_t b2 = bal;
+            for (int q = 1; q < need; ++q) b2 &= b2 - 1;
+            found = (int)(base + __ffs(b2) - 1);
+            break;
+          }
+          need -= n;
+        }
+      }
+      if (tid == 0) pub[xk & 1][0] = __int_as_float(found);
+      cluster_sync_all();
+      ycut = -1;
+      for (int rr = 0; rr < ncl; ++rr)
+        ycut = max(ycut, __float_as_int(ld_dsmem_f32(mapa_shared(smem_u32(&pub[xk & 1][0]), (uint32_t)rr))));
+      ++xk;
+    }
+  }
+  // Gather the kept tokens of every CTA, then sort them (larger logit first,
+  // equal logits by lower index) identically in every CTA.
+  if (tid == 0) w.ints[4] = 0;
+  __syncthreads();
+  for (int64_t y = lo + tid; y < hi; y += kMssThreads) {
+    const float l = __ldg(lrow + y);
+    if (kept(l, y, tau, ycut)) {
+      const int j = atomicAdd(&w.ints[4], 1);
+      if (j < kMaxTopK) {  // at most min(top_k, V) <= kMaxTopK tokens are kept
+        w.cand_v[j] = l;
+        w.cand_i[j] = (int)y;
+      }
+    }
+  }
+  __syncthreads();
+  if (tid == 0) pub[xk & 1][0] = __int_as_float(w.ints[4]);
+  cluster_sync_all();
+  int cnt_r[kMssMaxCluster], K = 0;
+  for (int rr = 0; rr < ncl; ++rr) {
+    cnt_r[rr] = __float_as_int(ld_dsmem_f32(mapa_shared(smem_u32(&pub[xk & 1][0]), (uint32_t)rr)));
+    K += cnt_r[rr];
+  }
+  ++xk;
+  int P2 = 1;
+  while (P2 < K) P2 <<= 1;
+  for (int j = tid; j < P2; j += kMssThreads) {
+    float v = -INFINITY;
+    int id = INT32_MAX;
+    if (j < K) {
+      int rr = 0, jl = j;
+      while (jl >= cnt_r[rr]) jl -= cnt_r[rr++];
+      v = ld_dsmem_f32(mapa_shared(smem_u32(&w.cand_v[jl]), (uint32_t)rr));
+      id = ld_dsmem_s32(mapa_shared(smem_u32(&w.cand_i[jl]), (uint32_t)rr));
+    }
+    w.srt_v[j] = v;
+    w.srt_i[j] = id;
+  }
+  __syncthreads();
+  for (int k = 2; k <= P2; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = tid; i < P2; i += kMssThreads) {
+        const int ixj = i ^ j;
+        if (ixj > i) {
+          const float a = w.srt_v[i], bv = w.srt_v[ixj];
+          const int ai = w.srt_i[i], bi = w.srt_i[ixj];
+          const bool a_first = a > bv || (a == bv && ai < bi);
+          if (((i & k) == 0) != a_first) {
+            w.srt_v[i] = bv;
+            w.srt_v[ixj] = a;
+            w.srt_i[i] = bi;
+            w.srt_i[ixj] = ai;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+  // Cumulative mass in ranking order: thread t owns a run of consecutive entries.
+  const int per = (K + kMssThreads - 1) / kMssThreads;
+  const int j0 = min(K, tid * per), j1 = min(K, j0 + per);
+  F2 run{0.f, 0.f};
+  for (int j = j0; j < j1; ++j) run = f2_add(run, F2{exp_diff(w.srt_v[j] * inv_t, M), 0.f});
+  F2 incl = run;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const F2 t{__shfl_up_sync(0xffffffffu, incl.hi, o), __shfl_up_sync(0xffffffffu, incl.lo, o)};
+    if (lane >= o) incl = f2_add(t, incl);
+  }
+  if (lane == 31) w.tsum[warp] = incl;
+  if (tid == 0) w.ints[5] = INT32_MAX;
+  __syncthreads();
+  F2 base{0.f, 0.f}, total{0.f, 0.f};
+  for (int ww = 0; ww < kMssWarps; ++ww) {
+    if (ww < warp) base = f2_add(base, w.tsum[ww]);
+    total = f2_add(total, w.tsum[ww]);
+  }
+  // Exclusive prefix of this thread's run (all threads shuffle, then branch).
+  const F2 up{__shfl_up_sync(0xffffffffu, incl.hi, 1), __shfl_up_sync(0xffffffffu, incl.lo, 1)};
+  const F2 excl = lane == 0 ? base : f2_add(base, up);
+  int J = K;
+  F2 S = total;
+  if (top_p < 1.0f) {
+    // Shortest prefix whose share of the kept mass reaches top_p.
+    const F2 target = f2_scale(total, top_p);
+    F2 cum = excl;
+    for (int j = j0; j < j1; ++j) {
+      cum = f2_add(cum, F2{exp_diff(w.srt_v[j] * inv_t, M), 0.f});
+      if (!f2_lt(cum, target)) {
+        atomicMin(&w.ints[5], j);
+        break;
+      }
+    }
+    __syncthreads();
+    J = min(K, w.ints[5] + 1);
+    // The mass up to the cut, from the thread that owns entry J-1.
+    if (J - 1 >= j0 && J - 1 < j1) {
+      F2 c2 = excl;
+      for (int j = j0; j < J; ++j) c2 = f2_add(c2, F2{exp_diff(w.srt_v[j] * inv_t, M), 0.f});
+      w.s_cut = c2;
+    }
+    __syncthreads();
+    S = w.s_cut;
+  }
+  Support out;
+  out.tau = w.srt_v[J - 1];
+  out.ycut = w.srt_i[J - 1];
+  out.S = S;
+  __syncthreads();  // the scratch may be rewritten by the next call
+  return out;
+}
+
 }  // namespace
 
 // Multi-step speculative sampling: one cluster of `ncl` CTAs per request, CTA
@@ -453,7 +705,8 @@ __global__ void __launch_bounds__(kMssThreads, 2)
                       int64_t V, const int32_t* __restrict__ tokens,
                       const int32_t* __restrict__ parent, const int32_t* __restrict__ node_offsets,
                       const float* __restrict__ u_acc, const float* __restrict__ u_smp, float inv_t,
-                      int ncl, int vec, float* __restrict__ resid_all, int32_t* __restrict__ path,
+                      int top_k, float top_p, int ncl, int vec, float* __restrict__ resid_all,
+                      int32_t* __restrict__ path,
                       int32_t* __restrict__ accept_len, int32_t* __restrict__ bonus,
                       int32_t* __restrict__ n_tried, int32_t* __restrict__ status) {
   __shared__ int32_t first_child[TSV_MAX_NODES];
@@ -465,6 +718,8 @@ __global__ void __launch_bounds__(kMssThreads, 2)
   __shared__ __align__(16) float pub[2][4];  // exchange slots, alternating
   __shared__ int bad;
   __shared__ int pick_s, last_s;
+  __shared__ SelSmem sel;
+  const bool warped = top_k > 0 || top_p < 1.0f;
   const int b = blockIdx.x / ncl;
   const int rank = blockIdx.x - b * ncl;  // == %cluster_ctarank for 1-D clusters of ncl
   const int tid = threadIdx.x;
@@ -541,8 +796,11 @@ __global__ void __launch_bounds__(kMssThreads, 2)
   };
   const int lane = tid & 31;
 
-  // Row statistics of node u's logits: m = max(l / T), s = sum exp(l / T - m).
-  float m_u = 0.f, inv_s = 0.f;
+  // Row statistics of node u's logits: m = max(l / T), s = sum exp(l / T - m)
+  // over the kept tokens (all tokens unless warped), and the boundary
+  // (tau, ycut) of the kept set.
+  float m_u = 0.f, inv_s = 0.f, tau = -INFINITY;
+  int ycut = INT32_MAX;
   auto row_stats = [&](int u) {
     const float* lrow = llm_logits + (size_t)(off + u) * (size_t)V;
     float m = -INFINITY;
@@ -561,6 +819,19 @@ __global__ void __launch_bounds__(kMssThreads, 2)
     }
     for (int64_t y = lo + 4 * n4 + tid; y < hi; y += T) m = fmaxf(m, lrow[y] * inv_t);
     m = block_max(m, red);
+    if (warped) {
+      exchange(m, 0.f, 0.f, 0.f);
+      const float mr = lane < ncl ? peer(0, lane) : -INFINITY;
+      float M = -INFINITY;
+      for (int r = 0; r < ncl; ++r) M = fmaxf(M, __shfl_sync(0xffffffffu, mr, r));
+      ++xk;
+      const Support sp = warped_support(lrow, V, lo, hi, inv_t, M, top_k, top_p, ncl, rank, xk, pub, sel);
+      m_u = M;
+      inv_s = f2_inv(sp.S);
+      tau = sp.tau;
+      ycut = sp.ycut;
+      return;
+    }
     CompSum acc;
     for (int64_t g0 = tid; g0 < n4; g0 += (int64_t)T * kMssGroups) {
       float4 v[kMssGroups];
@@ -595,6 +866,8 @@ __global__ void __launch_bounds__(kMssThreads, 2)
     ++xk;
     m_u = M;
     inv_s = f2_inv(S);
+    tau = -INFINITY;
+    ycut = INT32_MAX;
   };
 
   int u = 0, len = 1, cur = 0, tried = 0;
@@ -612,7 +885,8 @@ __global__ void __launch_bounds__(kMssThreads, 2)
     while (c >= 0) {
       const float* q = ssm_probs + (size_t)(off + c) * (size_t)V;
       // p(x) of the current distribution (fp32, ~2 ulp); the test is exact.
-      const float px = px_known ? px_next : exp_diff(lx_s[c] * inv_t, m_u) * inv_s;
+      const float px = px_known ? px_next
+                                : (kept(lx_s[c], tok_s[c], tau, ycut) ? exp_diff(lx_s[c] * inv_t, m_u) * inv_s : 0.f);
       ++tried;
       if (accept_test(ua_s[c], qx_s[c], px)) {
         accepted = c;
@@ -646,7 +920,9 @@ __global__ void __launch_bounds__(kMssThreads, 2)
             float r[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const float py = from_resid ? at(a[k], e) * inv_z : exp_diff(at(a[k], e) * inv_t, m_u) * inv_s;
+              const float py = from_resid ? at(a[k], e) * inv_z
+                                          : (kept(at(a[k], e), y + e, tau, ycut)
+                                                 ? exp_diff(at(a[k], e) * inv_t, m_u) * inv_s : 0.f);
               r[e] = fmaxf(py - at(qq[k], e), 0.0f);
               acc.add(r[e]);
               if (y + e == xn) {
@@ -664,7 +940,9 @@ __global__ void __launch_bounds__(kMssThreads, 2)
         }
       }
       for (int64_t y = lo + 4 * n4 + tid; y < hi; y += T) {
-        const float py = from_resid ? rin[y] * inv_z : exp_diff(__ldg(lrow + y) * inv_t, m_u) * inv_s;
+        const float ly = from_resid ? 0.f : __ldg(lrow + y);
+        const float py = from_resid ? rin[y] * inv_z
+                                    : (kept(ly, y, tau, ycut) ? exp_diff(ly * inv_t, m_u) * inv_s : 0.f);
         const float r = fmaxf(py - __ldcs(q + y), 0.0f);
         rout[y] = r;
         acc.add(r);
@@ -716,7 +994,9 @@ __global__ void __launch_bounds__(kMssThreads, 2)
     const float* rin = resid[cur];
     const int64_t per_t = ((((hi - lo) + T - 1) / T) + 3) & ~int64_t(3);
     const int64_t tlo = min(hi, lo + (int64_t)tid * per_t), thi = min(hi, tlo + per_t);
-    auto weight = [&](float a) { return from_resid ? a : exp_diff(a * inv_t, m_u); };
+    auto weight = [&](float a, int64_t y) {
+      return from_resid ? a : (kept(a, y, tau, ycut) ? exp_diff(a * inv_t, m_u) : 0.f);
+    };
     CompSum acc;
     int64_t last_pos = -1;
     {
@@ -725,13 +1005,13 @@ __global__ void __launch_bounds__(kMssThreads, 2)
         const float4 a = from_resid ? load4<2>(rin, y, vec) : load4<0>(lrow, y, vec);
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const float w = weight(at(a, e));
+          const float w = weight(at(a, e), y + e);
           acc.add(w);
           if (w > 0.0f) last_pos = y + e;
         }
       }
       for (; y < thi; ++y) {
-        const float w = weight(from_resid ? rin[y] : lrow[y]);
+        const float w = weight(from_resid ? rin[y] : lrow[y], y);
         acc.add(w);
         if (w > 0.0f) last_pos = y;
       }
@@ -775,7 +1055,7 @@ __global__ void __launch_bounds__(kMssThreads, 2)
       int64_t pick = -1;
       CompSum run;
       for (int64_t y = tlo; y < thi; ++y) {
-        const float w = weight(from_resid ? rin[y] : lrow[y]);
+        const float w = weight(from_resid ? rin[y] : lrow[y], y);
         run.add(w);
         if (f2_lt(target, f2_add(excl, comp_value(run)))) {
           pick = y;
@@ -810,8 +1090,8 @@ int mss_cluster_size(int64_t V) {
 cudaError_t launch_mss_verify(const float* llm_logits, const float* ssm_probs, int64_t V,
                               const int32_t* tokens, const int32_t* parent,
                               const int32_t* node_offsets, const float* u_acc, const float* u_smp,
-                              float inv_t, int32_t B, float* resid, int32_t* path,
-                              int32_t* accept_len, int32_t* bonus, int32_t* n_tried,
+                              float inv_t, int32_t top_k, float top_p, int32_t B, float* resid,
+                              int32_t* path, int32_t* accept_len, int32_t* bonus, int32_t* n_tried,
                               int32_t* status, cudaStream_t st) {
   const int ncl = mss_cluster_size(V);
   const int vec = (V % 4 == 0) && ((reinterpret_cast<uintptr_t>(llm_logits) |
@@ -829,8 +1109,8 @@ cudaError_t launch_mss_verify(const float* llm_logits, const float* ssm_probs, i
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, mss_verify_kernel, llm_logits, ssm_probs, V, tokens, parent,
-                            node_offsets, u_acc, u_smp, inv_t, ncl, vec, resid, path, accept_len,
-                            bonus, n_tried, status);
+                            node_offsets, u_acc, u_smp, inv_t, top_k, top_p, ncl, vec, resid, path,
+                            accept_len, bonus, n_tried, status);
 }
 
 }  // namespace tsv
