@@ -261,3 +261,47 @@ def kv_commit(k_cache, v_cache, prefix_len, node_offsets, path, accept_len):
             v_out[b, P + k] = v_in[b, P + pth[k]]
         new_len[b] = P + 1 + L
     return k_out, v_out, new_len, status
+
+
+def tree_expand(ssm_logits, k):
+    """Expansion step of token-tree construction (SpecInfer §3, expansion-based
+    token tree construction: each node of the frontier gets the SSM's top-k
+    tokens as children).
+
+    ssm_logits: [F, V] logits of the F frontier nodes.  Returns tokens [F, k]:
+    row f lists the k tokens of largest logit, larger first, equal logits by
+    lower token index (k <= V).
+    """
+    z = np.asarray(ssm_logits, dtype=np.float32)
+    F, V = z.shape
+    out = np.zeros((F, k), dtype=np.int32)
+    for f in range(F):
+        ranked = sorted(range(V), key=lambda t: (-float(z[f, t]), t))
+        out[f] = ranked[:k]
+    return out
+
+
+def tree_merge(parents, tokens):
+    """Merge-based token-tree construction (SpecInfer §3: the trees of several
+    speculators are merged into one token tree).  Every input tree shares the
+    root (node 0, the last verified token); a node is identified by the token
+    path from the root, so equal paths become one node.
+
+    parents / tokens: lists of int arrays, one pair per input tree (parent[0]
+    = -1, parent[i] < i).  Returns (parent, token, source) of the union in
+    creation order: input trees in order, nodes in order, a node created the
+    first time its path is seen; source[j] = (tree, node) that created it.
+    """
+    key_to_id = {(): 0}
+    par_out, tok_out, src = [-1], [int(tokens[0][0])], [(0, 0)]
+    for t, (par, tok) in enumerate(zip(parents, tokens)):
+        path_of = {0: ()}
+        for i in range(1, len(par)):
+            path = path_of[int(par[i])] + (int(tok[i]),)
+            path_of[i] = path
+            if path not in key_to_id:
+                key_to_id[path] = len(par_out)
+                par_out.append(key_to_id[path[:-1]])
+                tok_out.append(int(tok[i]))
+                src.append((t, i))
+    return (np.array(par_out, dtype=np.int32), np.array(tok_out, dtype=np.int32), src)
