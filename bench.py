@@ -51,10 +51,11 @@ def parse_args():
     p.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU oracle sample budget")
     p.add_argument("--top-k", type=int, default=0, help="stochastic verification against the top-k warped LLM law")
     p.add_argument("--top-p", type=float, default=1.0, help="... and top-p (needs --top-k)")
-    p.add_argument("--row", choices=["step", "kv_commit", "sequence_baseline"], default="step",
+    p.add_argument("--row", choices=["step", "kv_commit", "sequence_baseline", "tree_build"], default="step",
                    help="step: the hot path (attention + verification); kv_commit: the commit of the "
                         "accepted path that follows verification, timed alone; sequence_baseline: tree "
-                        "attention against the same work done per root-to-leaf sequence")
+                        "attention against the same work done per root-to-leaf sequence; tree_build: "
+                        "expansion (top-k children) and merge of token trees on the GPU")
     return p.parse_args()
 
 
@@ -781,6 +782,91 @@ def run_sequence_baseline(args, spec):
     }), flush=True)
 
 
+def _graph_ms(fn, stream, reps):
+    import torch
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            fn()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(reps):
+                fn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        g.replay()
+        e0.record(stream)
+        for _ in range(5):
+            g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / (5 * reps)
+
+
+def run_tree_build(args, spec):
+    """Token-tree construction: one expansion step (k = 4 children for 8
+    frontier nodes per request, the workload's vocabulary) and the merge of
+    three speculator trees per request (random-branching, 21 nodes each, as in
+    the merge workload), each timed alone from a CUDA graph, the oracle beside."""
+    import torch
+    import oracle
+    import tree_speculative_verification_attention_gb300 as tsv
+    import workloads as W
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream()
+    B, V, k = spec.B, spec.V, 4
+    F = 8 * B
+    z = W.normal_f32(spec.wid, 20, (F, V), 2.0)
+    zd = torch.as_tensor(z).to(dev)
+    tok = torch.empty((F, k), dtype=torch.int32, device=dev)
+    ms_expand = _graph_ms(lambda: tsv.tree_expand(zd, k, stream=stream, out=tok), stream, 20)
+    assert np.array_equal(tok.cpu().numpy(), oracle.tree_expand(z, k))
+    rng = W._rng(spec.wid, 21)
+    trees = []
+    for b in range(B):
+        for _ in range(3):
+            par = W.random_tree(rng, 21, 8)
+            t = rng.integers(0, 6, 21).astype(np.int32)  # small token range: paths repeat across speculators
+            t[0] = 1
+            trees.append((par.astype(np.int32), t))
+    parent = torch.as_tensor(np.concatenate([t[0] for t in trees])).to(dev)
+    tokens = torch.as_tensor(np.concatenate([t[1] for t in trees])).to(dev)
+    toffs = torch.as_tensor(np.arange(0, 21 * 3 * B + 1, 21, dtype=np.int32)).to(dev)
+    rtrees = torch.as_tensor(np.arange(0, 3 * B + 1, 3, dtype=np.int32)).to(dev)
+    res = {}
+
+    def merge():
+        res.update(tsv.tree_merge(parent, tokens, toffs, rtrees, stream=stream))
+    ms_merge = _graph_ms(merge, stream, 20)
+    union = [oracle.tree_merge([t[0] for t in trees[3 * b:3 * b + 3]], [t[1] for t in trees[3 * b:3 * b + 3]])
+             for b in range(B)]
+    assert res["count"].cpu().tolist() == [len(u[0]) for u in union]
+    t0 = time.perf_counter()
+    oracle.tree_expand(z[:min(F, 8)], k)
+    cpu_expand_ms = (time.perf_counter() - t0) * 1e3 * F / min(F, 8)
+    t0 = time.perf_counter()
+    for b in range(B):
+        oracle.tree_merge([t[0] for t in trees[3 * b:3 * b + 3]], [t[1] for t in trees[3 * b:3 * b + 3]])
+    cpu_merge_ms = (time.perf_counter() - t0) * 1e3
+    peak, _, peak_kind = measured_peaks()
+    gbs = F * V * 4 / (ms_expand * 1e-3) / 1e9
+    print(json.dumps({
+        "row": "tree_build", "metric": "expansion: frontier logits read per second", "value": gbs, "unit": "GB/s",
+        "n_gpus": 1, "data": "synthetic",
+        "config": {"workload": spec.name, "frontier_rows": F, "vocab": V, "k": k, "merge_requests": B,
+                   "merge_trees_per_request": 3, "merge_nodes_per_tree": 21,
+                   "union_nodes_mean": float(np.mean([len(u[0]) for u in union]))},
+        "expand": {"ms": ms_expand, "bytes": F * V * 4,
+                   "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
+                                "kernel": "tree_expand_kernel", "peak_kind": peak_kind + " hbm_gbs"}},
+        "merge": {"ms": ms_merge, "bound": "latency (one CTA walks each request's input nodes in order)"},
+        "cpu_baseline": {"expand_ms": cpu_expand_ms, "merge_ms": cpu_merge_ms, "cores": 1, "kind": "oracle",
+                         "sample": "expansion of %d rows scaled to %d; merge of all %d requests" % (min(F, 8), F, B)},
+    }), flush=True)
+
+
 def main():
     args = parse_args()
     import workloads as W
@@ -793,6 +879,8 @@ def main():
         run_kv_commit(args, spec)
     elif args.row == "sequence_baseline":
         run_sequence_baseline(args, spec)
+    elif args.row == "tree_build":
+        run_tree_build(args, spec)
     elif args.impl == "reference":
         run_reference(args, spec)
     else:

@@ -10,6 +10,7 @@
  *   tsv_tree_verify_greedy      greedy acceptance walk over the tree
  *   tsv_tree_verify_stochastic  multi-step speculative sampling over the tree
  *   tsv_tree_verify_stochastic_warped  the same against a top-k / top-p warped LLM distribution
+ *   tsv_tree_expand, tsv_tree_merge  token-tree construction on the GPU
  *   tsv_kv_commit               move the accepted path's K/V rows behind the prefix
  *
  * Sources: "SpecInfer: Accelerating Generative Large Language Model Serving
@@ -263,6 +264,50 @@ tsv_status tsv_tree_verify_stochastic_warped(
     int32_t B, int32_t N, int32_t* path_d, int32_t* accept_len_d, int32_t* bonus_d,
     int32_t* n_tried_d, void* workspace_d, size_t workspace_bytes, int32_t* status_d,
     void* stream);
+
+/*
+ * tsv_tree_expand — one expansion step of token-tree construction (SpecInfer
+ * §3, expansion-based token trees: every node of the current frontier gets
+ * the small model's top-k tokens as children).
+ *   ssm_logits_d  float32 [F, V]: the small model's logits at the F frontier nodes
+ *   k             1 .. min(V, 1024)
+ *   tokens_d (out) int32 [F, k]: row f lists the k tokens of largest logit,
+ *                 larger first, equal logits by lower token index; child j of
+ *                 frontier node f carries tokens[f][j] (the caller appends the
+ *                 children, F*k nodes, after the current tree)
+ * Needs no workspace.
+ */
+tsv_status tsv_tree_expand(tsv_handle h, const float* ssm_logits_d, int64_t V, int32_t F, int32_t k,
+                           int32_t* tokens_d, void* stream);
+
+/*
+ * tsv_tree_merge — merge-based token-tree construction (SpecInfer §3: the
+ * trees of several speculators are merged into one token tree to verify).
+ * All input trees of a request share its root (node 0 of each, the last
+ * verified token; the first tree's root token is kept).  A node is identified
+ * by its token path from the root, so nodes with equal paths become one.
+ *   parent_d, tokens_d  int32 [M]: the input trees one after another, parent
+ *                       indices local to each tree (parent[0] = -1, parent[i] < i)
+ *   tree_offsets_d      int32 [T+1]: node range of input tree t
+ *   request_trees_d     int32 [B+1]: input trees request_trees[b] .. [b+1]-1
+ *                       belong to request b (at least one each)
+ *   out_parent_d, out_tokens_d (out) int32 [M]: request b's union at rows
+ *                       tree_offsets[request_trees[b]] .. + out_count[b] - 1,
+ *                       in creation order (trees in order, nodes in order; a
+ *                       node appears where its path is first seen, so parents
+ *                       come first); the rest of the request's rows are -1
+ *   out_source_d (out)  int32 [M]: the input node (row of parent_d) that
+ *                       created each union node; may be NULL
+ *   out_count_d (out)   int32 [B]
+ *   status_d (out)      int32 [B]: TSV_OK, TSV_ERR_BAD_TREE (an input breaks
+ *                       the tree rules), TSV_ERR_UNSUPPORTED (more than 1024
+ *                       input nodes, or a union of more than TSV_MAX_NODES)
+ * Needs no workspace.
+ */
+tsv_status tsv_tree_merge(tsv_handle h, const int32_t* parent_d, const int32_t* tokens_d,
+                          const int32_t* tree_offsets_d, const int32_t* request_trees_d, int32_t B,
+                          int32_t* out_parent_d, int32_t* out_tokens_d, int32_t* out_source_d,
+                          int32_t* out_count_d, int32_t* status_d, void* stream);
 
 /*
  * tsv_kv_commit — commits the accepted path to the KV cache (SpecInfer §4,

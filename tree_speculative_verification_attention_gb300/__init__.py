@@ -37,6 +37,7 @@ EXPORTED = (
     "tsv_tree_verify_greedy_workspace_size", "tsv_tree_verify_greedy",
     "tsv_tree_verify_stochastic_workspace_size", "tsv_tree_verify_stochastic",
     "tsv_tree_verify_greedy_noalloc", "tsv_kv_commit", "tsv_tree_verify_stochastic_warped",
+    "tsv_tree_expand", "tsv_tree_merge",
 )
 
 
@@ -75,6 +76,8 @@ def _load():
         "tsv_tree_verify_stochastic_warped": (
             ctypes.c_int, [vp, vp, vp, i64, vp, vp, vp, vp, vp, f32, i32, f32, i32, i32, vp, vp, vp, vp, vp, sz,
                            vp, vp]),
+        "tsv_tree_expand": (ctypes.c_int, [vp, vp, i64, i32, i32, vp, vp]),
+        "tsv_tree_merge": (ctypes.c_int, [vp, vp, vp, vp, vp, i32, vp, vp, vp, vp, vp, vp]),
         "tsv_kv_commit": (
             ctypes.c_int, [vp, ctypes.c_int, vp, vp, i64, i64, i64, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp]),
         "tsv_tree_verify_stochastic_workspace_size": (ctypes.c_int, [vp, i32, i32, i64, szp]),
@@ -210,6 +213,18 @@ def tsv_tree_verify_stochastic_warped(h, llm_logits, ssm_probs, V, tree_tokens, 
         _ptr(u_accept), _ptr(u_sample), float(temperature), int(top_k), float(top_p), int(B), int(N), _ptr(path),
         _ptr(accept_len), _ptr(bonus), _ptr(n_tried), _ptr(workspace), int(workspace_bytes), _ptr(status),
         _stream(stream)), "tsv_tree_verify_stochastic_warped")
+
+
+def tsv_tree_expand(h, ssm_logits, V, F, k, tokens, stream=None):
+    _check(_lib.tsv_tree_expand(h, _ptr(ssm_logits), int(V), int(F), int(k), _ptr(tokens), _stream(stream)),
+           "tsv_tree_expand")
+
+
+def tsv_tree_merge(h, parent, tokens, tree_offsets, request_trees, B, out_parent, out_tokens, out_source,
+                   out_count, status, stream=None):
+    _check(_lib.tsv_tree_merge(h, _ptr(parent), _ptr(tokens), _ptr(tree_offsets), _ptr(request_trees), int(B),
+                               _ptr(out_parent), _ptr(out_tokens), _ptr(out_source), _ptr(out_count),
+                               _ptr(status), _stream(stream)), "tsv_tree_merge")
 
 
 def tsv_kv_commit(h, dtype_code, k_cache, v_cache, sb, sl, sh, B, Hkv, D, prefix_len, node_offsets, path,
@@ -352,4 +367,27 @@ def kv_commit(k_cache, v_cache, prefix_len, node_offsets, path, accept_len, stre
     tsv_kv_commit(handle(dev.index), _dtype_code(k_cache.dtype), k_cache, v_cache, k_cache.stride(0),
                   k_cache.stride(1), k_cache.stride(2), B, Hkv, D, prefix_len, node_offsets, path, accept_len,
                   o["new_len"], o["status"], stream)
+    return o
+
+
+def tree_expand(ssm_logits, k, stream=None, out=None):
+    """Top-k children of every frontier row: int32 [F, k] tokens (larger logit
+    first, equal logits by lower token index)."""
+    F, V = ssm_logits.shape
+    out = out if out is not None else torch.empty((F, k), dtype=torch.int32, device=ssm_logits.device)
+    tsv_tree_expand(handle(ssm_logits.device.index), ssm_logits, V, F, k, out, stream)
+    return out
+
+
+def tree_merge(parent, tokens, tree_offsets, request_trees, stream=None):
+    """Union of each request's input trees by token path; returns dict(parent,
+    tokens, source, count, status) laid out as tsv_tree_merge describes."""
+    dev = parent.device
+    M = parent.shape[0]
+    B = request_trees.shape[0] - 1
+    o = dict(parent=torch.empty(M, dtype=torch.int32, device=dev), tokens=torch.empty(M, dtype=torch.int32, device=dev),
+             source=torch.empty(M, dtype=torch.int32, device=dev), count=torch.empty(B, dtype=torch.int32, device=dev),
+             status=torch.empty(B, dtype=torch.int32, device=dev))
+    tsv_tree_merge(handle(dev.index), parent, tokens, tree_offsets, request_trees, B, o["parent"], o["tokens"],
+                   o["source"], o["count"], o["status"], stream)
     return o

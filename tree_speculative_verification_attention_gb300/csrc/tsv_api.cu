@@ -538,4 +538,25 @@ tsv_status tsv_kv_commit(tsv_handle h, tsv_dtype dtype, void* k_cache_d, void* v
                                       static_cast<cudaStream_t>(stream)));
 }
 
+tsv_status tsv_tree_expand(tsv_handle h, const float* ssm_logits_d, int64_t V, int32_t F, int32_t k,
+                           int32_t* tokens_d, void* stream) {
+  if (!h || F < 0 || V < 1 || V > INT32_MAX || k < 1 || (int64_t)k > V) return TSV_ERR_INVALID_ARG;
+  if (k > kMssMaxTopK) return TSV_ERR_UNSUPPORTED;
+  if (F > 0 && (!ssm_logits_d || !tokens_d)) return TSV_ERR_INVALID_ARG;
+  return cuda_status(launch_tree_expand(ssm_logits_d, V, F, k, tokens_d, static_cast<cudaStream_t>(stream)));
+}
+
+tsv_status tsv_tree_merge(tsv_handle h, const int32_t* parent_d, const int32_t* tokens_d,
+                          const int32_t* tree_offsets_d, const int32_t* request_trees_d, int32_t B,
+                          int32_t* out_parent_d, int32_t* out_tokens_d, int32_t* out_source_d,
+                          int32_t* out_count_d, int32_t* status_d, void* stream) {
+  if (!h || !parent_d || !tokens_d || !tree_offsets_d || !request_trees_d || !out_parent_d ||
+      !out_tokens_d || !out_count_d || !status_d)
+    return TSV_ERR_INVALID_ARG;
+  if (B < 1 || B > TSV_MAX_BATCH) return TSV_ERR_INVALID_ARG;
+  return cuda_status(launch_tree_merge(parent_d, tokens_d, tree_offsets_d, request_trees_d, B, out_parent_d,
+                                       out_tokens_d, out_source_d, out_count_d, status_d,
+                                       static_cast<cudaStream_t>(stream)));
+}
+
 }  // extern "C"

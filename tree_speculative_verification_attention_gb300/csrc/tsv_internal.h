@@ -114,6 +114,16 @@ cudaError_t launch_mss_verify(const float* llm_logits, const float* ssm_probs, i
                               int32_t* status, cudaStream_t st);
 constexpr int kMssMaxTopK = 1024;  // largest top_k of the warped stochastic verification
 
+// Token-tree construction: expansion (top-k children per frontier row) and
+// merge of several trees per request.
+constexpr int kTreeMergeMaxInput = 1024;  // input nodes of one request's merge
+cudaError_t launch_tree_expand(const float* logits, int64_t V, int32_t F, int32_t k, int32_t* tokens,
+                               cudaStream_t st);
+cudaError_t launch_tree_merge(const int32_t* parent, const int32_t* tokens, const int32_t* tree_offsets,
+                              const int32_t* request_trees, int32_t B, int32_t* out_parent,
+                              int32_t* out_tokens, int32_t* out_source, int32_t* out_count,
+                              int32_t* status, cudaStream_t st);
+
 // KV commit of the accepted path: rows hold row_chunks 16-byte chunks per
 // cache row (Hkv x D x element size / 16); strides in bytes.
 cudaError_t launch_kv_commit(uint8_t* k, uint8_t* v, int64_t sb, int64_t sl, int64_t sh, int32_t B,

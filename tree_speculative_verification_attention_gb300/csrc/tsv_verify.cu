@@ -1082,6 +1082,247 @@ __global__ void __launch_bounds__(kMssThreads, 2)
     for (int i = len + tid; i < n; i += T) path[off + i] = -1;
 }
 
+// ------------------------------------------------------------------ tree construction
+
+// Expansion step (SpecInfer §3, expansion-based token trees): row f of the
+// frontier's SSM logits gets its k largest-logit tokens as children, larger
+// first, equal logits by lower token index.  One CTA per row: for k <= 8 one
+// pass with per-thread top-k lists; wider expansions use the same selection
+// as the warped support (a CTA launched without a cluster is a cluster of one).
+constexpr int kExpandSmallK = 8;  // widest expansion done in one pass over the row
+
+__device__ __forceinline__ bool ranks_before(float a, int ia, float b, int ib) {
+  return a > b || (a == b && ia < ib);
+}
+
+// Top-k of one row for k <= KP <= kExpandSmallK, in one pass: every thread
+// keeps its KP best (value, index) sorted in registers; then k rounds pick
+// the best head among the 256 lists (a block-wide argmax in ranking order).
+template <int KP>
+__device__ void expand_small(const float* __restrict__ row, int64_t V, int k, int32_t* __restrict__ out,
+                             float* lv, int* li, float* rv, int* ri) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  float bv[KP];
+  int bi[KP];
+#pragma unroll
+  for (int i = 0; i < KP; ++i) {
+    bv[i] = -INFINITY;
+    bi[i] = INT32_MAX;
+  }
+  auto offer = [&](float v, int y) {
+    if (ranks_before(v, y, bv[KP - 1], bi[KP - 1])) {
+      bv[KP - 1] = v;
+      bi[KP - 1] = y;
+#pragma unroll
+      for (int i = KP - 1; i > 0; --i) {
+        if (ranks_before(bv[i], bi[i], bv[i - 1], bi[i - 1])) {
+          const float tv = bv[i];
+          bv[i] = bv[i - 1];
+          bv[i - 1] = tv;
+          const int ti = bi[i];
+          bi[i] = bi[i - 1];
+          bi[i - 1] = ti;
+        }
+      }
+    }
+  };
+  // 16-byte loads, eight in flight per thread, when the row is aligned.
+  constexpr int kInFlight = 8;
+  const bool vec = (V % 4 == 0) && ((reinterpret_cast<uintptr_t>(row) & 15) == 0);
+  const int64_t n4 = vec ? V / 4 : 0;
+  const float4* r4 = reinterpret_cast<const float4*>(row);
+  for (int64_t g0 = tid; g0 < n4; g0 += kInFlight * kMssThreads) {
+    float4 a[kInFlight];
+#pragma unroll
+    for (int u = 0; u < kInFlight; ++u)
+      if (g0 + u * kMssThreads < n4) a[u] = __ldg(r4 + g0 + u * kMssThreads);
+#pragma unroll
+    for (int u = 0; u < kInFlight; ++u) {
+      const int64_t g = g0 + u * kMssThreads;
+      if (g < n4) {
+        offer(a[u].x, (int)(4 * g));
+        offer(a[u].y, (int)(4 * g + 1));
+        offer(a[u].z, (int)(4 * g + 2));
+        offer(a[u].w, (int)(4 * g + 3));
+      }
+    }
+  }
+  for (int64_t y = 4 * n4 + tid; y < V; y += kMssThreads) offer(__ldg(row + y), (int)y);
+#pragma unroll
+  for (int i = 0; i < KP; ++i) {
+    lv[tid * KP + i] = bv[i];
+    li[tid * KP + i] = bi[i];
+  }
+  __syncthreads();
+  int pos = 0;
+  for (int j = 0; j < k; ++j) {
+    float v = pos < KP ? lv[tid * KP + pos] : -INFINITY;
+    int id = pos < KP ? li[tid * KP + pos] : INT32_MAX;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, v, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, id, o);
+      if (ranks_before(ov, oi, v, id)) {
+        v = ov;
+        id = oi;
+      }
+    }
+    if (lane == 0) {
+      rv[warp] = v;
+      ri[warp] = id;
+    }
+    __syncthreads();
+    float bvv = rv[0];
+    int bid = ri[0];
+    for (int ww = 1; ww < kMssWarps; ++ww)
+      if (ranks_before(rv[ww], ri[ww], bvv, bid)) {
+        bvv = rv[ww];
+        bid = ri[ww];
+      }
+    if (tid == 0) out[j] = bid;
+    if (pos < KP && li[tid * KP + pos] == bid) ++pos;  // indices are unique: one list advances
+    __syncthreads();
+  }
+}
+
+__global__ void __launch_bounds__(kMssThreads)
+    tree_expand_kernel(const float* __restrict__ logits, int64_t V, int k, int32_t* __restrict__ tokens) {
+  __shared__ __align__(16) float pub[2][4];
+  __shared__ SelSmem sel;
+  __shared__ float red[128];
+  __shared__ float lv[kMssThreads * kExpandSmallK];
+  __shared__ int li[kMssThreads * kExpandSmallK];
+  __shared__ float rv[kMssWarps];
+  __shared__ int ri[kMssWarps];
+  const float* row = logits + (size_t)blockIdx.x * (size_t)V;
+  int32_t* out = tokens + (size_t)blockIdx.x * k;
+  if (k <= 1) return expand_small<1>(row, V, k, out, lv, li, rv, ri);
+  if (k <= 2) return expand_small<2>(row, V, k, out, lv, li, rv, ri);
+  if (k <= 4) return expand_small<4>(row, V, k, out, lv, li, rv, ri);
+  if (k <= 8) return expand_small<8>(row, V, k, out, lv, li, rv, ri);
+  float m = -INFINITY;
+  for (int64_t y = threadIdx.x; y < V; y += kMssThreads) m = fmaxf(m, __ldg(row + y));
+  m = block_max(m, red);
+  int xk = 0;
+  warped_support(row, V, 0, V, 1.0f, m, k, 1.0f, 1, 0, xk, pub, sel);
+  for (int j = threadIdx.x; j < k; j += kMssThreads) tokens[(size_t)blockIdx.x * k + j] = sel.srt_i[j];
+}
+
+// Merge (SpecInfer §3, merge-based token trees): the input trees of request b
+// share its root; a node is identified by its token path, so an input node
+// maps to the union child of its parent's image that carries its token, or
+// becomes a new union node.  Inputs are taken tree by tree, node by node, so
+// the union is in creation order (parents first).  Warp 0 walks the nodes;
+// a lookup compares 32 union nodes per ballot.
+constexpr int kMergeMaxInput = kTreeMergeMaxInput;
+
+__global__ void __launch_bounds__(256)
+    tree_merge_kernel(const int32_t* __restrict__ parent, const int32_t* __restrict__ tokens,
+                      const int32_t* __restrict__ tree_offsets, const int32_t* __restrict__ request_trees,
+                      int32_t* __restrict__ out_parent, int32_t* __restrict__ out_tokens,
+                      int32_t* __restrict__ out_source, int32_t* __restrict__ out_count,
+                      int32_t* __restrict__ status) {
+  __shared__ int32_t up[TSV_MAX_NODES], ut[TSV_MAX_NODES], usrc[TSV_MAX_NODES];
+  __shared__ int32_t ipar[kMergeMaxInput], itok[kMergeMaxInput], imap[kMergeMaxInput];
+  __shared__ int bad, ucount_s;
+  const int b = blockIdx.x, tid = threadIdx.x;
+  const int t0 = request_trees[b], t1 = request_trees[b + 1];
+  const int n0 = tree_offsets[t0], total = tree_offsets[t1] - n0;
+  if (tid == 0) bad = (t1 <= t0) ? TSV_ERR_BAD_TREE : (total > kMergeMaxInput ? TSV_ERR_UNSUPPORTED : 0);
+  __syncthreads();
+  if (!bad) {
+    for (int i = tid; i < total; i += blockDim.x) {
+      ipar[i] = parent[n0 + i];
+      itok[i] = tokens[n0 + i];
+    }
+    for (int t = t0 + tid; t < t1; t += blockDim.x)
+      if (tree_offsets[t + 1] <= tree_offsets[t]) atomicMax(&bad, TSV_ERR_BAD_TREE);
+  }
+  __syncthreads();
+  if (!bad) {
+    // Each input tree: a root at its first node, every other parent earlier.
+    for (int t = t0; t < t1; ++t) {
+      const int s = tree_offsets[t] - n0, e = tree_offsets[t + 1] - n0;
+      for (int i = s + tid; i < e; i += blockDim.x) {
+        const int p = ipar[i];
+        if (!((i == s) ? (p == -1) : (p >= 0 && p < i - s))) atomicMax(&bad, TSV_ERR_BAD_TREE);
+      }
+    }
+  }
+  __syncthreads();
+  if (!bad && tid < 32) {
+    const int lane = tid;
+    int ucount = 1;
+    if (lane == 0) {
+      up[0] = -1;
+      ut[0] = itok[0];
+      usrc[0] = n0;
+    }
+    for (int t = t0; t < t1 && ucount >= 0; ++t) {
+      const int s = tree_offsets[t] - n0, e = tree_offsets[t + 1] - n0;
+      if (lane == 0) imap[s] = 0;
+      __syncwarp();
+      for (int i = s + 1; i < e; ++i) {
+        const int mp = imap[s + ipar[i]], tk = itok[i];
+        int found = -1;
+        for (int j0 = mp + 1; j0 < ucount; j0 += 32) {
+          const int j = j0 + lane;
+          const uint32_t hit = __ballot_sync(0xffffffffu, j < ucount && up[j] == mp && ut[j] == tk);
+          if (hit) {
+            found = j0 + __ffs(hit) - 1;
+            break;
+          }
+        }
+        if (found < 0) {
+          if (ucount >= TSV_MAX_NODES) {
+            ucount = -1;  // the union outgrows a verifiable tree
+            break;
+          }
+          if (lane == 0) {
+            up[ucount] = mp;
+            ut[ucount] = tk;
+            usrc[ucount] = n0 + i;
+          }
+          found = ucount++;
+        }
+        if (lane == 0) imap[i] = found;
+        __syncwarp();
+      }
+    }
+    if (lane == 0) {
+      ucount_s = ucount;
+      if (ucount < 0) bad = TSV_ERR_UNSUPPORTED;
+    }
+  }
+  __syncthreads();
+  const int cnt = bad ? 0 : ucount_s;
+  for (int j = tid; j < total; j += blockDim.x) {
+    out_parent[n0 + j] = j < cnt ? up[j] : -1;
+    out_tokens[n0 + j] = j < cnt ? ut[j] : -1;
+    if (out_source) out_source[n0 + j] = j < cnt ? usrc[j] : -1;
+  }
+  if (tid == 0) {
+    out_count[b] = cnt;
+    status[b] = bad ? bad : TSV_OK;
+  }
+}
+
+cudaError_t launch_tree_expand(const float* logits, int64_t V, int32_t F, int32_t k, int32_t* tokens,
+                               cudaStream_t st) {
+  if (F == 0) return cudaSuccess;
+  tree_expand_kernel<<<F, kMssThreads, 0, st>>>(logits, V, k, tokens);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_tree_merge(const int32_t* parent, const int32_t* tokens, const int32_t* tree_offsets,
+                              const int32_t* request_trees, int32_t B, int32_t* out_parent,
+                              int32_t* out_tokens, int32_t* out_source, int32_t* out_count,
+                              int32_t* status, cudaStream_t st) {
+  tree_merge_kernel<<<B, 256, 0, st>>>(parent, tokens, tree_offsets, request_trees, out_parent, out_tokens,
+                                       out_source, out_count, status);
+  return cudaGetLastError();
+}
+
 int mss_cluster_size(int64_t V) {
   const int64_t c = (V + kMssMinSlice - 1) / kMssMinSlice;
   return (int)(c < 1 ? 1 : (c > kMssMaxCluster ? kMssMaxCluster : c));
