@@ -384,7 +384,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-// Neumaier-compensated running sum in fp32.
+// Neumaier-compensated running sum in fp32: the sum is s + c (read both).
 struct CompSum {
   float s = 0.f, c = 0.f;
   __device__ __forceinline__ void add(float x) {
@@ -392,7 +392,6 @@ struct CompSum {
     c += (fabsf(s) >= fabsf(x)) ? ((s - t) + x) : ((x - t) + s);
     s = t;
   }
-  __device__ __forceinline__ double value() const { return (double)s + (double)c; }
 };
 
 }  // namespace tsv
