@@ -139,6 +139,7 @@ __global__ void __launch_bounds__(kKeysThreads, 1)
     mbar_fence_init();
   }
   __syncthreads();
+  pdl_wait();  // the previous kernel's results are visible from here on
   const int b = plan.slot_req[*req_slot];
   const int local = unit - plan.unit_start[*req_slot];
   const int nch = plan.n_chunks[b];  // == cluster size
@@ -441,6 +442,7 @@ __global__ void __launch_bounds__(kKeysThreads, 1)
     if (ok && nblk > 0 &&
         !__all_sync(0xffffffffu, mbar_wait(&pv_done[(nblk - 1) & 1], ((nblk - 1) >> 1) & 1, abort_v)))
       ok = false;
+    pdl_trigger();  // the main loop is done: let the next kernel be scheduled
     // Epilogue: lane kl holds O^T[d = kl][rows] and L^T[.][rows] (the same on
     // every lane); this thread takes its 8 of every 16 rows.
     if (ok && nblk > 0) tc_fence_after();
@@ -564,24 +566,13 @@ cudaError_t launch_attention_keys(const CUtensorMap& tmap_q, const CUtensorMap& 
                                   const int32_t* parent, const uint32_t* anc, void* out,
                                   int32_t* status, cudaStream_t st) {
   if (plan.n_units == 0) return cudaSuccess;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(plan.n_units);
-  cfg.blockDim = dim3(kKeysThreads);
-  cfg.dynamicSmemBytes = attention_keys_smem_bytes(plan.D);
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = plan.cluster;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
   __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(out);
+  const size_t smem = attention_keys_smem_bytes(plan.D);
   if (plan.D == 64)
-    return cudaLaunchKernelEx(&cfg, tree_attn_keys_kernel<64>, tmap_q, tmap_k, tmap_v, plan, parent, anc,
-                              ob, status);
-  return cudaLaunchKernelEx(&cfg, tree_attn_keys_kernel<128>, tmap_q, tmap_k, tmap_v, plan, parent, anc,
-                            ob, status);
+    return launch_pdl(tree_attn_keys_kernel<64>, dim3(plan.n_units), dim3(kKeysThreads), smem, st,
+                      (unsigned)plan.cluster, tmap_q, tmap_k, tmap_v, plan, parent, anc, ob, status);
+  return launch_pdl(tree_attn_keys_kernel<128>, dim3(plan.n_units), dim3(kKeysThreads), smem, st,
+                    (unsigned)plan.cluster, tmap_q, tmap_k, tmap_v, plan, parent, anc, ob, status);
 }
 
 }  // namespace tsv

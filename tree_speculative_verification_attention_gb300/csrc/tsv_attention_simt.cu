@@ -51,6 +51,8 @@ __global__ void __launch_bounds__(kSimtWarps * 32)
                           const int32_t* __restrict__ node_offsets,
                           const uint32_t* __restrict__ anc, int32_t B, int32_t Hq, int32_t Hkv,
                           float scale_log2) {
+  pdl_trigger();
+  pdl_wait();  // the previous kernel's results are visible from here on
   constexpr int E = D / 32;
   const int h = blockIdx.x;
   const int gi = blockIdx.y;
@@ -142,25 +144,24 @@ cudaError_t launch_attention_simt(bool bf16, const void* q, const void* k, const
   if (bf16) {
     using T = __nv_bfloat16;
     if (D == 64)
-      tree_attn_simt_kernel<T, 64><<<grid, block, 0, st>>>(
-          (const T*)q, (const T*)k, (const T*)v, sb, sl, sh, (T*)out, prefix_len, node_offsets,
-          anc, B, Hq, Hkv, scale_log2);
+      return launch_pdl(tree_attn_simt_kernel<T, 64>, grid, block, 0, st, 0u,
+          (const T*)q, (const T*)k, (const T*)v, sb, sl, sh, (T*)out, prefix_len,
+          node_offsets, anc, B, Hq, Hkv, scale_log2);
     else
-      tree_attn_simt_kernel<T, 128><<<grid, block, 0, st>>>(
-          (const T*)q, (const T*)k, (const T*)v, sb, sl, sh, (T*)out, prefix_len, node_offsets,
-          anc, B, Hq, Hkv, scale_log2);
+      return launch_pdl(tree_attn_simt_kernel<T, 128>, grid, block, 0, st, 0u,
+          (const T*)q, (const T*)k, (const T*)v, sb, sl, sh, (T*)out, prefix_len,
+          node_offsets, anc, B, Hq, Hkv, scale_log2);
   } else {
     using T = float;
     if (D == 64)
-      tree_attn_simt_kernel<T, 64><<<grid, block, 0, st>>>(
-          (const T*)q, (const T*)k, (const T*)v, sb, sl, sh, (T*)out, prefix_len, node_offsets,
-          anc, B, Hq, Hkv, scale_log2);
+      return launch_pdl(tree_attn_simt_kernel<T, 64>, grid, block, 0, st, 0u,
+          (const T*)q, (const T*)k, (const T*)v, sb, sl, sh, (T*)out, prefix_len,
+          node_offsets, anc, B, Hq, Hkv, scale_log2);
     else
-      tree_attn_simt_kernel<T, 128><<<grid, block, 0, st>>>(
-          (const T*)q, (const T*)k, (const T*)v, sb, sl, sh, (T*)out, prefix_len, node_offsets,
-          anc, B, Hq, Hkv, scale_log2);
+      return launch_pdl(tree_attn_simt_kernel<T, 128>, grid, block, 0, st, 0u,
+          (const T*)q, (const T*)k, (const T*)v, sb, sl, sh, (T*)out, prefix_len,
+          node_offsets, anc, B, Hq, Hkv, scale_log2);
   }
-  return cudaGetLastError();
 }
 
 }  // namespace tsv

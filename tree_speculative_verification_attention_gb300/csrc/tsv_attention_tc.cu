@@ -158,6 +158,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     mbar_fence_init();
   }
   __syncthreads();
+  pdl_wait();  // the previous kernel's results are visible from here on
 
   if (warp == kTcProducerWarp) {
     // ------------------------------------------------------------ producer
@@ -402,6 +403,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tc_fence_before();
       mbar_arrive(&p_mine[j & 1]);
     }
+    pdl_trigger();  // the main loop is done: let the next kernel be scheduled
     // Both halves' last PV must be complete before the epilogue reads O0 and O1.
     if (ok && nblk > 0) {
       const int jl = nblk - 1;
@@ -574,12 +576,10 @@ cudaError_t launch_attention_tc(const CUtensorMap& tmap_q, const CUtensorMap& tm
   if (plan.n_units == 0) return cudaSuccess;
   __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(out);
   if (plan.D == 64)
-    tree_attn_tc_kernel<64><<<plan.n_units, kTcThreads, TcCfg<64>::kSmemBytes, st>>>(
-        tmap_q, tmap_k, tmap_v, plan, parent, anc, ob, part_o, part_lse, counters, status);
-  else
-    tree_attn_tc_kernel<128><<<plan.n_units, kTcThreads, TcCfg<128>::kSmemBytes, st>>>(
-        tmap_q, tmap_k, tmap_v, plan, parent, anc, ob, part_o, part_lse, counters, status);
-  return cudaGetLastError();
+    return launch_pdl(tree_attn_tc_kernel<64>, dim3(plan.n_units), dim3(kTcThreads), TcCfg<64>::kSmemBytes, st, 0u,
+                      tmap_q, tmap_k, tmap_v, plan, parent, anc, ob, part_o, part_lse, counters, status);
+  return launch_pdl(tree_attn_tc_kernel<128>, dim3(plan.n_units), dim3(kTcThreads), TcCfg<128>::kSmemBytes, st, 0u,
+                    tmap_q, tmap_k, tmap_v, plan, parent, anc, ob, part_o, part_lse, counters, status);
 }
 
 }  // namespace tsv

@@ -13,6 +13,7 @@
 // before any of them is stored, for memory-level parallelism.
 #include <cuda_runtime.h>
 
+#include "tsv_device.cuh"
 #include "tsv_internal.h"
 
 namespace tsv {
@@ -28,6 +29,8 @@ __global__ void __launch_bounds__(kCommitThreads)
                      const int32_t* __restrict__ node_offsets, const int32_t* __restrict__ path,
                      const int32_t* __restrict__ accept_len, int32_t* __restrict__ new_len,
                      int32_t* __restrict__ status) {
+  pdl_trigger();
+  pdl_wait();  // the previous kernel's results are visible from here on
   __shared__ int32_t spath[TSV_MAX_NODES];
   __shared__ int bad;
   const int b = blockIdx.x;
@@ -92,9 +95,8 @@ cudaError_t launch_kv_commit(uint8_t* k, uint8_t* v, int64_t sb, int64_t sl, int
                              cudaStream_t st) {
   const int chunks = Hkv * d_chunks;
   dim3 grid(B, (chunks + kCommitThreads - 1) / kCommitThreads);
-  kv_commit_kernel<<<grid, kCommitThreads, 0, st>>>(k, v, sb, sl, sh, Hkv, d_chunks, prefix_len,
-                                                    node_offsets, path, accept_len, new_len, status);
-  return cudaGetLastError();
+  return launch_pdl(kv_commit_kernel, grid, dim3(kCommitThreads), 0, st, 0u, k, v, sb, sl, sh, Hkv, d_chunks,
+                    prefix_len, node_offsets, path, accept_len, new_len, status);
 }
 
 }  // namespace tsv

@@ -74,6 +74,18 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
+// ----------------------------------------------------------------- launch order
+// Programmatic dependent launch: a kernel launched with the programmatic
+// stream serialization attribute may start while the previous kernel in the
+// stream is still running.  pdl_wait() blocks until that kernel has completed
+// and its memory operations are visible, so every kernel calls it before its
+// first global-memory access: results are those of plain serialised launches,
+// only launch latency overlaps.  pdl_trigger() lets the next kernel be
+// scheduled (once every CTA of this one has called it or exited).  Both are
+// no-ops for a kernel launched without the attribute.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ----------------------------------------------------------------- TMA
 
 __device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {

@@ -7,6 +7,7 @@
 // words per node.  One CTA per request computes the reflexive-transitive
 // closure of the parent relation by pointer jumping: after round k every node
 // knows its ancestors within distance 2^k, so 8 rounds cover 256 nodes.
+#include "tsv_device.cuh"
 #include "tsv_internal.h"
 
 namespace tsv {
@@ -15,6 +16,8 @@ __global__ void __launch_bounds__(TSV_MAX_NODES)
     tree_prepare_kernel(const int32_t* __restrict__ parent, const int32_t* __restrict__ node_offsets,
                         uint32_t* __restrict__ anc, int32_t* __restrict__ depth,
                         int32_t* __restrict__ status) {
+  pdl_trigger();
+  pdl_wait();  // the previous kernel's results are visible from here on
   __shared__ uint32_t A[2][TSV_MAX_NODES][TSV_ANC_WORDS];
   __shared__ int32_t J[2][TSV_MAX_NODES];
   __shared__ int bad;
@@ -73,8 +76,8 @@ __global__ void __launch_bounds__(TSV_MAX_NODES)
 
 cudaError_t launch_tree_prepare(const int32_t* parent, const int32_t* node_offsets, int32_t B,
                                 uint32_t* anc, int32_t* depth, int32_t* status, cudaStream_t st) {
-  tree_prepare_kernel<<<B, TSV_MAX_NODES, 0, st>>>(parent, node_offsets, anc, depth, status);
-  return cudaGetLastError();
+  return launch_pdl(tree_prepare_kernel, dim3(B), dim3(TSV_MAX_NODES), 0, st, 0u, parent, node_offsets, anc, depth,
+                    status);
 }
 
 }  // namespace tsv

@@ -223,6 +223,8 @@ __global__ void __launch_bounds__(TSV_MAX_NODES)
                        const int32_t* __restrict__ parent, const int32_t* __restrict__ node_offsets,
                        int32_t* __restrict__ path, int32_t* __restrict__ accept_len,
                        int32_t* __restrict__ bonus, int32_t* __restrict__ status) {
+  pdl_trigger();
+  pdl_wait();  // the previous kernel's results are visible from here on
   __shared__ WalkSmem w;
   const int b = blockIdx.x;
   const int off = node_offsets[b];
@@ -242,6 +244,7 @@ __global__ void __launch_bounds__(kArgmaxThreads)
                          int32_t* __restrict__ counters, int32_t* __restrict__ path,
                          int32_t* __restrict__ accept_len, int32_t* __restrict__ bonus,
                          int32_t* __restrict__ status) {
+  pdl_wait();  // the previous kernel's results are visible from here on
   __shared__ int32_t offs[TSV_MAX_BATCH + 1];
   __shared__ WalkSmem w;
   __shared__ ArgMax red[kArgmaxThreads / 32];
@@ -249,6 +252,7 @@ __global__ void __launch_bounds__(kArgmaxThreads)
   const int row = blockIdx.y, s = blockIdx.x;
   for (int i = threadIdx.x; i <= B; i += blockDim.x) offs[i] = node_offsets[i];
   const ArgMax best = slice_argmax(logits, V, splits, row, s, red);
+  pdl_trigger();  // this CTA's share of the logits is read: let the next kernel be scheduled
   if (threadIdx.x == 0) {
     part_val[(size_t)row * splits + s] = best.v;
     part_idx[(size_t)row * splits + s] = best.i;
@@ -295,10 +299,8 @@ cudaError_t launch_greedy_verify(const float* logits, int64_t V, int32_t N, int 
                                  int32_t* accept_len, int32_t* bonus, int32_t* status,
                                  cudaStream_t st) {
   dim3 grid(splits, N);
-  greedy_verify_kernel<<<grid, kArgmaxThreads, 0, st>>>(logits, V, splits, tokens, parent,
-                                                        node_offsets, B, part_val, part_idx,
-                                                        counters, path, accept_len, bonus, status);
-  return cudaGetLastError();
+  return launch_pdl(greedy_verify_kernel, grid, dim3(kArgmaxThreads), 0, st, 0u, logits, V, splits, tokens, parent,
+                    node_offsets, B, part_val, part_idx, counters, path, accept_len, bonus, status);
 }
 
 cudaError_t launch_greedy_walk(const float* part_val, const int32_t* part_idx, int splits,
@@ -306,9 +308,8 @@ cudaError_t launch_greedy_walk(const float* part_val, const int32_t* part_idx, i
                                const int32_t* node_offsets, int32_t B, int32_t* path,
                                int32_t* accept_len, int32_t* bonus, int32_t* status,
                                cudaStream_t st) {
-  greedy_walk_kernel<<<B, TSV_MAX_NODES, 0, st>>>(part_val, part_idx, splits, tokens, parent,
-                                                  node_offsets, path, accept_len, bonus, status);
-  return cudaGetLastError();
+  return launch_pdl(greedy_walk_kernel, dim3(B), dim3(TSV_MAX_NODES), 0, st, 0u, part_val, part_idx, splits, tokens,
+                    parent, node_offsets, path, accept_len, bonus, status);
 }
 
 // ------------------------------------------------------------------ stochastic
@@ -709,6 +710,7 @@ __global__ void __launch_bounds__(kMssThreads, 2)
                       int32_t* __restrict__ path,
                       int32_t* __restrict__ accept_len, int32_t* __restrict__ bonus,
                       int32_t* __restrict__ n_tried, int32_t* __restrict__ status) {
+  pdl_wait();  // the previous kernel's results are visible from here on
   __shared__ int32_t first_child[TSV_MAX_NODES];
   __shared__ int32_t next_sib[TSV_MAX_NODES];
   __shared__ int32_t tok_s[TSV_MAX_NODES];
@@ -986,6 +988,7 @@ __global__ void __launch_bounds__(kMssThreads, 2)
     row_stats(u);
   }
 
+  pdl_trigger();  // the walk is done: let the next kernel be scheduled
   // Bonus token: smallest y with cumsum(w)[y] > u_smp[u] * sum(w), w = the
   // unnormalised current distribution.  Each thread owns a contiguous run of
   // its CTA's slice; runs and slices are in vocabulary order.
@@ -1187,6 +1190,8 @@ __device__ void expand_small(const float* __restrict__ row, int64_t V, int k, in
 
 __global__ void __launch_bounds__(kMssThreads)
     tree_expand_kernel(const float* __restrict__ logits, int64_t V, int k, int32_t* __restrict__ tokens) {
+  pdl_trigger();
+  pdl_wait();  // the previous kernel's results are visible from here on
   __shared__ __align__(16) float pub[2][4];
   __shared__ SelSmem sel;
   __shared__ float red[128];
@@ -1222,6 +1227,8 @@ __global__ void __launch_bounds__(256)
                       int32_t* __restrict__ out_parent, int32_t* __restrict__ out_tokens,
                       int32_t* __restrict__ out_source, int32_t* __restrict__ out_count,
                       int32_t* __restrict__ status) {
+  pdl_trigger();
+  pdl_wait();  // the previous kernel's results are visible from here on
   __shared__ int32_t up[TSV_MAX_NODES], ut[TSV_MAX_NODES], usrc[TSV_MAX_NODES];
   __shared__ int32_t ipar[kMergeMaxInput], itok[kMergeMaxInput], imap[kMergeMaxInput];
   __shared__ int bad, ucount_s;
@@ -1310,17 +1317,15 @@ __global__ void __launch_bounds__(256)
 cudaError_t launch_tree_expand(const float* logits, int64_t V, int32_t F, int32_t k, int32_t* tokens,
                                cudaStream_t st) {
   if (F == 0) return cudaSuccess;
-  tree_expand_kernel<<<F, kMssThreads, 0, st>>>(logits, V, k, tokens);
-  return cudaGetLastError();
+  return launch_pdl(tree_expand_kernel, dim3(F), dim3(kMssThreads), 0, st, 0u, logits, V, k, tokens);
 }
 
 cudaError_t launch_tree_merge(const int32_t* parent, const int32_t* tokens, const int32_t* tree_offsets,
                               const int32_t* request_trees, int32_t B, int32_t* out_parent,
                               int32_t* out_tokens, int32_t* out_source, int32_t* out_count,
                               int32_t* status, cudaStream_t st) {
-  tree_merge_kernel<<<B, 256, 0, st>>>(parent, tokens, tree_offsets, request_trees, out_parent, out_tokens,
-                                       out_source, out_count, status);
-  return cudaGetLastError();
+  return launch_pdl(tree_merge_kernel, dim3(B), dim3(256), 0, st, 0u, parent, tokens, tree_offsets, request_trees,
+                    out_parent, out_tokens, out_source, out_count, status);
 }
 
 int mss_cluster_size(int64_t V) {
@@ -1338,20 +1343,9 @@ cudaError_t launch_mss_verify(const float* llm_logits, const float* ssm_probs, i
   const int vec = (V % 4 == 0) && ((reinterpret_cast<uintptr_t>(llm_logits) |
                                     reinterpret_cast<uintptr_t>(ssm_probs) |
                                     reinterpret_cast<uintptr_t>(resid)) & 15) == 0;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(B * ncl));
-  cfg.blockDim = dim3(kMssThreads);
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = (unsigned)ncl;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, mss_verify_kernel, llm_logits, ssm_probs, V, tokens, parent,
-                            node_offsets, u_acc, u_smp, inv_t, top_k, top_p, ncl, vec, resid, path,
-                            accept_len, bonus, n_tried, status);
+  return launch_pdl(mss_verify_kernel, dim3((unsigned)(B * ncl)), dim3(kMssThreads), 0, st, (unsigned)ncl,
+                    llm_logits, ssm_probs, V, tokens, parent, node_offsets, u_acc, u_smp, inv_t, top_k, top_p,
+                    ncl, vec, resid, path, accept_len, bonus, n_tried, status);
 }
 
 }  // namespace tsv
