@@ -121,6 +121,24 @@ def test_stochastic_fuzz(tsv, seed):
     compare_stochastic(r, ref, trees)
 
 
+@pytest.mark.parametrize("V,like_llm", [(160000, False), (160000, True), (137984, True), (138000, True)])
+def test_stochastic_slices_staged_or_streamed(tsv, V, like_llm):
+    """Vocabularies around the largest whose three slices per CTA fit in shared
+    memory (137984 at eight CTAs per request): above it the slices are read
+    from global memory, below it they are staged; both walks must agree with
+    the oracle, through rejections (residual passes) and acceptances."""
+    spec = W.spec_variant(W.fuzz_spec(310, max_nodes=24), V=V, B=2)
+    trees = W.make_trees(spec)
+    si = W.make_stochastic_inputs(spec, trees)
+    if like_llm:  # proposals close to the LLM law at each parent: long accepted paths
+        from test_gpu_verify_warped import _propose_like_llm
+        _propose_like_llm(si, trees, seed=V)
+    r = _stochastic(tsv, trees, si)
+    ref = oracle.verify_stochastic(si.llm_logits, si.ssm_probs, si.tokens, trees.parent,
+                                   trees.node_offsets, si.u_accept, si.u_sample)
+    compare_stochastic(r, ref, trees)
+
+
 def test_stochastic_temperature(tsv):
     spec = W.spec_variant(W.fuzz_spec(300), V=2000)
     trees = W.make_trees(spec)

@@ -24,6 +24,8 @@ struct tsv_handle_s {
   EncodeTiledFn encode;
   bool tc_attr_set[2];    // rows-on-lanes kernel, D = 64, 128
   bool keys_attr_set[2];  // keys-on-lanes kernel, D = 64, 128
+  bool mss_attr_set;      // MSS kernel's shared-memory limit
+  size_t mss_staged_limit;
 };
 
 namespace {
@@ -287,6 +289,8 @@ tsv_status tsv_create(tsv_handle* out, int device) {
   h->encode = reinterpret_cast<EncodeTiledFn>(fn);
   h->tc_attr_set[0] = h->tc_attr_set[1] = false;
   h->keys_attr_set[0] = h->keys_attr_set[1] = false;
+  h->mss_attr_set = false;
+  h->mss_staged_limit = 0;
   *out = h;
   return TSV_OK;
 }
@@ -479,10 +483,15 @@ static tsv_status verify_stochastic(tsv_handle h, const float* llm_logits_d, con
   const size_t need = round256((size_t)B * 2 * (size_t)V * 4);
   if (!workspace_d || workspace_bytes < need) return TSV_ERR_INVALID_ARG;
   float* resid = static_cast<float*>(workspace_d);
+  if (!h->mss_attr_set) {
+    if (mss_set_attributes(h->device, &h->mss_staged_limit) != cudaSuccess) return TSV_ERR_CUDA;
+    h->mss_attr_set = true;
+  }
   return cuda_status(launch_mss_verify(llm_logits_d, ssm_probs_d, V, tree_tokens_d, parent_d,
                                        node_offsets_d, u_accept_d, u_sample_d, 1.0f / temperature,
                                        top_k, top_p, B, resid, path_d, accept_len_d, bonus_d,
-                                       n_tried_d, status_d, static_cast<cudaStream_t>(stream)));
+                                       n_tried_d, status_d, h->mss_staged_limit,
+                                       static_cast<cudaStream_t>(stream)));
 }
 
 tsv_status tsv_tree_verify_stochastic(tsv_handle h, const float* llm_logits_d,

@@ -140,7 +140,11 @@ cudaError_t launch_mss_verify(const float* llm_logits, const float* ssm_probs, i
                               const int32_t* node_offsets, const float* u_acc, const float* u_smp,
                               float inv_t, int32_t top_k, float top_p, int32_t B, float* resid,
                               int32_t* path, int32_t* accept_len, int32_t* bonus, int32_t* n_tried,
-                              int32_t* status, cudaStream_t st);
+                              int32_t* status, size_t staged_limit, cudaStream_t st);
+// Sets the MSS kernel's dynamic shared-memory limit on `device` to all that is
+// left beside its static shared memory, and returns that limit (the largest
+// staged slice set a launch may use).
+cudaError_t mss_set_attributes(int device, size_t* staged_limit);
 constexpr int kMssMaxTopK = 1024;  // largest top_k of the warped stochastic verification
 
 // Token-tree construction: expansion (top-k children per frontier row) and

@@ -30,6 +30,7 @@ namespace tsv {
 namespace {
 
 constexpr int kArgmaxThreads = 256;
+constexpr int kArgmaxInFlight = 8;
 constexpr int kMinSlice = 4096;  // vocab entries per CTA at least
 
 struct ArgMax {
@@ -73,13 +74,13 @@ __device__ __forceinline__ ArgMax slice_argmax(const float* __restrict__ logits,
     const float4* x4 = reinterpret_cast<const float4*>(x);
     const int64_t lo4 = lo >> 2, hi4 = hi >> 2;
     int64_t k = lo4 + threadIdx.x;
-    // Four independent 16-byte loads in flight per thread.
-    for (; k + 3 * kArgmaxThreads < hi4; k += 4 * kArgmaxThreads) {
-      float4 a[4];
+    // Eight independent 16-byte loads in flight per thread (32 KB per CTA).
+    for (; k + (kArgmaxInFlight - 1) * kArgmaxThreads < hi4; k += kArgmaxInFlight * kArgmaxThreads) {
+      float4 a[kArgmaxInFlight];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) a[u] = __ldcs(x4 + k + u * kArgmaxThreads);
+      for (int u = 0; u < kArgmaxInFlight; ++u) a[u] = __ldcs(x4 + k + u * kArgmaxThreads);
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+      for (int u = 0; u < kArgmaxInFlight; ++u) {
         const int32_t base = (int32_t)((k + u * kArgmaxThreads) << 2);
         best = better(best, ArgMax{a[u].x, base});
         best = better(best, ArgMax{a[u].y, base + 1});
@@ -108,22 +109,6 @@ __device__ __forceinline__ ArgMax slice_argmax(const float* __restrict__ logits,
     best = warp_argmax(best);
   }
   return best;
-}
-
-// Validates one request's tree for verification: a single root at node 0,
-// every other parent earlier in the order.  Returns a TSV status.
-__device__ int validate_verify_tree(const int32_t* par_g, int n, int* bad_flag) {
-  if (threadIdx.x == 0) *bad_flag = (n < 1) ? TSV_ERR_BAD_TREE : (n > TSV_MAX_NODES ? TSV_ERR_UNSUPPORTED : 0);
-  __syncthreads();
-  if (*bad_flag == 0) {
-    for (int i = threadIdx.x; i < n; i += blockDim.x) {
-      const int p = par_g[i];
-      const bool ok = (i == 0) ? (p == -1) : (p >= 0 && p < i);
-      if (!ok) atomicMax(bad_flag, TSV_ERR_BAD_TREE);
-    }
-  }
-  __syncthreads();
-  return *bad_flag;
 }
 
 __device__ void fail_request(int32_t* path, int n, int32_t* accept_len, int32_t* bonus,
@@ -164,13 +149,34 @@ __device__ void greedy_walk_request(int b, int off, int n, const float* part_val
   const int items = n * splits;  // rows of a request are consecutive, so its partials are too
   const bool staged = items <= kWalkPartials;
   if (w.bad == 0) {
-    for (int i = threadIdx.x; i < n; i += T) {
-      w.par[i] = parent[off + i];
-      w.tok[i] = tokens[off + i];
+    // Every load is issued before the first shared-memory store, so they all
+    // travel together (n <= T; items <= kWalkPartials = 4 T).
+    static_assert(kWalkPartials <= 4 * kArgmaxThreads && TSV_MAX_NODES <= kArgmaxThreads, "one pass");
+    const int i = threadIdx.x;
+    int pv = 0, tv = 0;
+    if (i < n) {
+      pv = parent[off + i];
+      tv = tokens[off + i];
     }
-    if (staged)
-      for (int i = threadIdx.x; i < items; i += T)
-        w.part[i] = ArgMax{__ldcg(part_val + (size_t)off * splits + i), __ldcg(part_idx + (size_t)off * splits + i)};
+    float pval[4];
+    int32_t pidx[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int e = i + k * T;
+      if (staged && e < items) {
+        pval[k] = __ldcg(part_val + (size_t)off * splits + e);
+        pidx[k] = __ldcg(part_idx + (size_t)off * splits + e);
+      }
+    }
+    if (i < n) {
+      w.par[i] = pv;
+      w.tok[i] = tv;
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int e = i + k * T;
+      if (staged && e < items) w.part[e] = ArgMax{pval[k], pidx[k]};
+    }
   }
   __syncthreads();
   if (w.bad == 0) {
@@ -236,7 +242,9 @@ __global__ void __launch_bounds__(TSV_MAX_NODES)
 // slice of one row; the last CTA to finish among a request's rows x slices
 // (atomic counter, no waiting) walks that request's tree.  CTA (0, 0) also
 // reports requests that own no rows.  Counters start at zero and are reset.
-__global__ void __launch_bounds__(kArgmaxThreads)
+// Thread 0 writes the CTA's partial and counts it with one acquire-release
+// atomic, so the last CTA sees every partial without a separate fence.
+__global__ void __launch_bounds__(kArgmaxThreads, 4)  // <= 64 registers: the loads stay in flight
     greedy_verify_kernel(const float* __restrict__ logits, int64_t V, int splits,
                          const int32_t* __restrict__ tokens, const int32_t* __restrict__ parent,
                          const int32_t* __restrict__ node_offsets, int B,
@@ -250,14 +258,13 @@ __global__ void __launch_bounds__(kArgmaxThreads)
   __shared__ ArgMax red[kArgmaxThreads / 32];
   __shared__ int last;
   const int row = blockIdx.y, s = blockIdx.x;
-  for (int i = threadIdx.x; i <= B; i += blockDim.x) offs[i] = node_offsets[i];
+  // The offsets travel with the first logits loads: stored after the slice.
+  static_assert(TSV_MAX_BATCH < kArgmaxThreads, "one offset per thread");
+  const int my_off = threadIdx.x <= B ? node_offsets[threadIdx.x] : 0;
   const ArgMax best = slice_argmax(logits, V, splits, row, s, red);
   pdl_trigger();  // this CTA's share of the logits is read: let the next kernel be scheduled
-  if (threadIdx.x == 0) {
-    part_val[(size_t)row * splits + s] = best.v;
-    part_idx[(size_t)row * splits + s] = best.i;
-  }
-  __syncthreads();  // offs loaded
+  if (threadIdx.x <= B) offs[threadIdx.x] = my_off;
+  __syncthreads();
   int lo = 0, hi = B;
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
@@ -274,12 +281,13 @@ __global__ void __launch_bounds__(kArgmaxThreads)
         status[e] = TSV_ERR_BAD_TREE;
       }
   }
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) last = atomicAdd(counters + b, 1) == n * splits - 1;
+  if (threadIdx.x == 0) {
+    part_val[(size_t)row * splits + s] = best.v;
+    part_idx[(size_t)row * splits + s] = best.i;
+    last = atom_add_acq_rel_gpu(counters + b, 1) == n * splits - 1;
+  }
   __syncthreads();
   if (!last) return;
-  __threadfence();
   greedy_walk_request(b, off, n, part_val, part_idx, splits, tokens, parent, path, accept_len, bonus,
                       status, w);
   if (threadIdx.x == 0) counters[b] = 0;
@@ -321,6 +329,7 @@ constexpr int kMssWarps = kMssThreads / 32;
 constexpr int kMssMaxCluster = 8;
 constexpr int64_t kMssMinSlice = 4096;  // vocab entries per CTA at least
 constexpr int kMssGroups = 4;           // 4-float groups in flight per thread
+constexpr uint32_t kBulkChunk = 32768;  // bytes per bulk copy instruction
 constexpr int kMaxTopK = kMssMaxTopK;   // largest top-k the warped support handles
 
 // exp(a - m) with the subtraction's rounding error folded back in (TwoSum:
@@ -427,6 +436,21 @@ __device__ __forceinline__ float4 load4(const float* p, int64_t y, bool vec) {
   return make_float4(p[y], p[y + 1], p[y + 2], p[y + 3]);
 }
 
+// A CTA's view of one vocabulary row restricted to its slice: element y of
+// the row is p[y - off].  p points either into global memory (off = 0, the
+// whole row) or at the slice staged in shared memory (off = the slice's first
+// index); loads are generic, so both work.
+struct Slice {
+  const float* p;
+  int64_t off;
+  __device__ __forceinline__ float operator[](int64_t y) const { return p[y - off]; }
+  __device__ __forceinline__ float4 ld4(int64_t y, bool vec) const {
+    const float* q = p + (y - off);
+    if (vec) return *reinterpret_cast<const float4*>(q);
+    return make_float4(q[0], q[1], q[2], q[3]);
+  }
+};
+
 __device__ __forceinline__ float at(const float4& v, int e) {
   return e == 0 ? v.x : e == 1 ? v.y : e == 2 ? v.z : v.w;
 }
@@ -491,7 +515,7 @@ struct Support {
 // tokens (at most kMaxTopK) are gathered into every CTA and sorted there, the
 // same way in every CTA, for the top-p cut and the mass.  Every CTA of the
 // cluster runs it in lockstep; `xk` counts the exchanges.
-__device__ __noinline__ Support warped_support(const float* __restrict__ lrow, int64_t V, int64_t lo,
+__device__ __noinline__ Support warped_support(const Slice lrow, int64_t V, int64_t lo,
                                                int64_t hi, float inv_t, float M, int top_k, float top_p,
                                                int ncl, int rank, int& xk, float (*pub)[4], SelSmem& w) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -507,7 +531,7 @@ __device__ __noinline__ Support warped_support(const float* __restrict__ lrow, i
       h[tid] = 0;  // kMssThreads == 256 bins
       __syncthreads();
       for (int64_t y = lo + tid; y < hi; y += kMssThreads) {
-        const uint32_t k = order_key(__ldg(lrow + y));
+        const uint32_t k = order_key(lrow[y]);
         if (pass == 0 || (k >> (shift + 8)) == prefix) atomicAdd(&h[(k >> shift) & 255], 1);
       }
       __syncthreads();
@@ -542,7 +566,7 @@ __device__ __noinline__ Support warped_support(const float* __restrict__ lrow, i
       if (tid == 0) w.ints[3] = 0;
       __syncthreads();
       int c = 0;
-      for (int64_t y = lo + tid; y < hi; y += kMssThreads) c += order_key(__ldg(lrow + y)) == prefix;
+      for (int64_t y = lo + tid; y < hi; y += kMssThreads) c += order_key(lrow[y]) == prefix;
       atomicAdd(&w.ints[3], c);
       __syncthreads();
       if (tid == 0) pub[xk & 1][0] = __int_as_float(w.ints[3]);
@@ -559,7 +583,7 @@ __device__ __noinline__ Support warped_support(const float* __restrict__ lrow, i
         int need = r - before;
         for (int64_t base = lo; base < hi; base += 32) {
           const int64_t y = base + lane;
-          const bool tie = y < hi && order_key(__ldg(lrow + y)) == prefix;
+          const bool tie = y < hi && order_key(lrow[y]) == prefix;
           const uint32_t bal = __ballot_sync(0xffffffffu, tie);
           const int n = __popc(bal);
           if (need <= n) {
@@ -584,7 +608,7 @@ __device__ __noinline__ Support warped_support(const float* __restrict__ lrow, i
   if (tid == 0) w.ints[4] = 0;
   __syncthreads();
   for (int64_t y = lo + tid; y < hi; y += kMssThreads) {
-    const float l = __ldg(lrow + y);
+    const float l = lrow[y];
     if (kept(l, y, tau, ycut)) {
       const int j = atomicAdd(&w.ints[4], 1);
       if (j < kMaxTopK) {  // at most min(top_k, V) <= kMaxTopK tokens are kept
@@ -699,76 +723,173 @@ __device__ __noinline__ Support warped_support(const float* __restrict__ lrow, i
 // once, in parallel, at the start), the row statistics and residual sums
 // (combined in rank order through distributed shared memory), and p at the
 // next child's token, which the residual pass of the CTA owning that token
-// publishes with the sums.  A CTA streams only its own slice of the logits,
+// publishes with the sums.  A CTA reads only its own slice of the logits,
 // proposals and residual rows.
+//
+// Staged (`staged`, when the slices fit): each CTA holds three slice buffers
+// in shared memory.  One holds the row the current distribution comes from
+// (the logits of the node being expanded, or the last residual); the others
+// hold the proposals of the child being tested and of its next sibling,
+// fetched ahead.  A rejection writes the residual max(0, p - q) over the
+// tested child's proposals, which are not needed again, and that buffer
+// becomes the distribution's row; the old row's buffer is free.  Slices move
+// by bulk asynchronous copies counted on one mbarrier per buffer.  Otherwise
+// the slices are read from global memory and the residual rows live in the
+// workspace.
 __global__ void __launch_bounds__(kMssThreads, 2)
     mss_verify_kernel(const float* __restrict__ llm_logits, const float* __restrict__ ssm_probs,
                       int64_t V, const int32_t* __restrict__ tokens,
                       const int32_t* __restrict__ parent, const int32_t* __restrict__ node_offsets,
                       const float* __restrict__ u_acc, const float* __restrict__ u_smp, float inv_t,
-                      int top_k, float top_p, int ncl, int vec, float* __restrict__ resid_all,
-                      int32_t* __restrict__ path,
+                      int top_k, float top_p, int ncl, int vec, int staged,
+                      float* __restrict__ resid_all, int32_t* __restrict__ path,
                       int32_t* __restrict__ accept_len, int32_t* __restrict__ bonus,
                       int32_t* __restrict__ n_tried, int32_t* __restrict__ status) {
   pdl_wait();  // the previous kernel's results are visible from here on
   __shared__ int32_t first_child[TSV_MAX_NODES];
   __shared__ int32_t next_sib[TSV_MAX_NODES];
-  __shared__ int32_t tok_s[TSV_MAX_NODES];
+  __shared__ int32_t tok_s[TSV_MAX_NODES], par_s[TSV_MAX_NODES];
   __shared__ float ua_s[TSV_MAX_NODES], qx_s[TSV_MAX_NODES], lx_s[TSV_MAX_NODES];
   __shared__ float red[128];
   __shared__ F2 scan_s[kMssWarps];
   __shared__ __align__(16) float pub[2][4];  // exchange slots, alternating
-  __shared__ int bad;
+  __shared__ int bad, bad_tok;
   __shared__ int pick_s, last_s;
+  __shared__ __align__(8) uint64_t cbar[3];  // staged copies: one barrier per slice buffer
   __shared__ SelSmem sel;
+  extern __shared__ __align__(128) float mss_dyn[];
   const bool warped = top_k > 0 || top_p < 1.0f;
   const int b = blockIdx.x / ncl;
   const int rank = blockIdx.x - b * ncl;  // == %cluster_ctarank for 1-D clusters of ncl
   const int tid = threadIdx.x;
   const int T = blockDim.x;
+  const int lane = tid & 31;
   if (tid == 0) {
     pick_s = INT32_MAX;
     last_s = -1;
+    if (staged) {
+      for (int i = 0; i < 3; ++i) mbar_init(&cbar[i], 1);
+      mbar_fence_init();
+    }
   }
   const int off = node_offsets[b];
   const int n = node_offsets[b + 1] - off;
-  const int code = validate_verify_tree(parent + off, n, &bad);
+
+  // This CTA's slice (a multiple of 4 long, so 16-byte aligned rows stay aligned).
+  const int64_t per = (((V + ncl - 1) / ncl) + 3) & ~int64_t(3);
+  const int64_t lo = min(V, (int64_t)rank * per), hi = min(V, lo + per);
+  const int64_t n4 = (hi - lo) >> 2;  // full groups
+  const int64_t per_al = (per + 31) & ~int64_t(31);
+  const uint32_t slice_bytes = (uint32_t)((hi - lo) * 4);  // a multiple of 16 when staged
+  // Staged buffers (bookkeeping identical in every thread): buffer pb holds
+  // the distribution's row; node_of[j] is the child whose proposals buffer j
+  // holds or receives (-1: none); pend[j]: a copy into j not yet waited for;
+  // par[j]: parity of the next phase of j's barrier.
+  auto buf = [&](int j) { return mss_dyn + (size_t)j * (size_t)per_al; };
+  int pb = 0;
+  int node_of[3] = {-1, -1, -1};
+  bool pend[3] = {false, false, false};
+  uint32_t par_bar[3] = {0u, 0u, 0u};
+  bool tmo = false;
+  auto ready = [&](int j) {  // the copy into buffer j (if any) has landed
+    if (pend[j]) {
+      if (!mbar_wait(&cbar[j], par_bar[j], nullptr)) tmo = true;
+      par_bar[j] ^= 1u;
+      pend[j] = false;
+    }
+  };
+  // Thread 0 copies this CTA's slice of a global row into buffer j.  Every
+  // thread is done reading j (a barrier since) and has fenced its writes.
+  auto issue_copy = [&](int j, const float* row) {
+    if (pend[j]) {  // a copy still in flight into j lands first ...
+      ready(j);
+      // ... and every thread has seen that phase complete before the next
+      // one can (a waiter that slept through both would wait for a third).
+      __syncthreads();
+    }
+    if (tid == 0) {
+      fence_proxy_async_smem();
+      mbar_arrive_expect_tx(&cbar[j], slice_bytes);
+      for (uint32_t o = 0; o < slice_bytes; o += kBulkChunk)
+        bulk_copy_g2s(buf(j) + o / 4, row + lo + o / 4, min(kBulkChunk, slice_bytes - o), &cbar[j]);
+    }
+    pend[j] = true;
+  };
+  auto q_buffer_of = [&](int c) {
+    for (int j = 0; j < 3; ++j)
+      if (j != pb && node_of[j] == c) return j;
+    return -1;
+  };
+  // A buffer other than pb and `not_j`, preferring one with no copy in flight.
+  auto free_buffer = [&](int not_j) {
+    int pick = -1;
+    for (int j = 0; j < 3; ++j)
+      if (j != pb && j != not_j && (pick < 0 || (pend[pick] && !pend[j]))) pick = j;
+    return pick;
+  };
+  auto q_issue = [&](int j, int c) {
+    issue_copy(j, ssm_probs + (size_t)(off + c) * (size_t)V);
+    node_of[j] = c;
+  };
+  // Row of node u into buffer pb, and the proposals of its first child c.
+  auto stage_row = [&](int u, int c) {
+    issue_copy(pb, llm_logits + (size_t)(off + u) * (size_t)V);
+    node_of[pb] = -1;
+    if (c >= 0 && q_buffer_of(c) < 0) q_issue(free_buffer(-1), c);
+  };
+  auto drain = [&]() {  // no copy may be in flight when the CTA leaves
+    if (!staged) return;
+    for (int j = 0; j < 3; ++j) ready(j);
+  };
+  __syncthreads();  // barriers initialised
+  // Node 0 is the root and node 1 (if any) its first child in every valid
+  // tree: their slices travel while the tree is read and checked.
+  if (staged && n >= 1) stage_row(0, n >= 2 ? 1 : -1);
+
+  // One parallel step reads every node's parent, token and accept uniform,
+  // and checks them: a single root at node 0, every other parent earlier in
+  // the order (else TSV_ERR_BAD_TREE), tokens in [0, V) (else
+  // TSV_ERR_INVALID_ARG; tree errors take precedence).
+  if (tid == 0) {
+    bad = (n < 1) ? TSV_ERR_BAD_TREE : (n > TSV_MAX_NODES ? TSV_ERR_UNSUPPORTED : 0);
+    bad_tok = 0;
+  }
+  __syncthreads();
+  if (bad == 0) {
+    for (int i = tid; i < n; i += T) {
+      const int p = parent[off + i];
+      const int x = i > 0 ? tokens[off + i] : 0;
+      const float ua = i > 0 ? u_acc[off + i] : 0.f;
+      par_s[i] = p;
+      if (!((i == 0) ? (p == -1) : (p >= 0 && p < i))) atomicMax(&bad, TSV_ERR_BAD_TREE);
+      if (i > 0) {
+        tok_s[i] = x;
+        ua_s[i] = ua;
+        if (x < 0 || (int64_t)x >= V) bad_tok = TSV_ERR_INVALID_ARG;
+      }
+    }
+  }
+  __syncthreads();
+  const int code = bad ? bad : bad_tok;
   if (code) {
+    drain();
     if (rank == 0)
       fail_request(path + off, n, accept_len + b, bonus + b, n_tried ? n_tried + b : nullptr,
                    status + b, code);
     return;  // uniform over the cluster: every CTA sees the same tree
   }
-  const int32_t* par = parent + off;
-  // Per child c: its token (rejected before any access when out of range),
-  // accept uniform, q_c(x_c) and the parent row's logit at x_c.
-  for (int c = 1 + tid; c < n; c += T) {
-    const int x = tokens[off + c];
-    tok_s[c] = x;
-    if (x < 0 || (int64_t)x >= V) {
-      atomicMax(&bad, TSV_ERR_INVALID_ARG);
-    } else {
-      ua_s[c] = __ldg(u_acc + off + c);
-      qx_s[c] = __ldg(ssm_probs + (size_t)(off + c) * (size_t)V + x);
-      lx_s[c] = __ldg(llm_logits + (size_t)(off + par[c]) * (size_t)V + x);
-    }
-  }
-  __syncthreads();
-  if (bad) {
-    if (rank == 0)
-      fail_request(path + off, n, accept_len + b, bonus + b, n_tried ? n_tried + b : nullptr,
-                   status + b, bad);
-    return;
-  }
-  // Sibling lists in increasing index order.
+  // Per child c: q_c(x_c) and the parent row's logit at x_c (one parallel
+  // step), and the sibling lists in increasing index order.
   for (int c = tid; c < n; c += T) first_child[c] = INT32_MAX;
   __syncthreads();
   for (int c = 1 + tid; c < n; c += T) {
-    const int p = par[c];
+    const int x = tok_s[c], p = par_s[c];
+    qx_s[c] = __ldg(ssm_probs + (size_t)(off + c) * (size_t)V + x);
+    lx_s[c] = __ldg(llm_logits + (size_t)(off + p) * (size_t)V + x);
     atomicMin(&first_child[p], c);
     int nx = -1;
     for (int c2 = c + 1; c2 < n; ++c2) {
-      if (par[c2] == p) {
+      if (par_s[c2] == p) {
         nx = c2;
         break;
       }
@@ -777,10 +898,6 @@ __global__ void __launch_bounds__(kMssThreads, 2)
   }
   __syncthreads();
 
-  // This CTA's slice (a multiple of 4 long, so 16-byte aligned rows stay aligned).
-  const int64_t per = (((V + ncl - 1) / ncl) + 3) & ~int64_t(3);
-  const int64_t lo = min(V, (int64_t)rank * per), hi = min(V, lo + per);
-  const int64_t n4 = (hi - lo) >> 2;  // full groups
   float* resid[2] = {resid_all + (size_t)b * 2 * (size_t)V, resid_all + ((size_t)b * 2 + 1) * (size_t)V};
   int xk = 0;  // exchanges so far (the same count in every CTA)
   // Publishes four floats, then waits for the whole cluster.
@@ -796,22 +913,28 @@ __global__ void __launch_bounds__(kMssThreads, 2)
   auto peer = [&](int slot, int r) {
     return ld_dsmem_f32(mapa_shared(smem_u32(&pub[xk & 1][slot]), (uint32_t)r));
   };
-  const int lane = tid & 31;
+  // Node u's logits, this CTA's slice.
+  auto logits_of = [&](int u) {
+    return staged ? Slice{buf(pb), lo} : Slice{llm_logits + (size_t)(off + u) * (size_t)V, 0};
+  };
 
   // Row statistics of node u's logits: m = max(l / T), s = sum exp(l / T - m)
   // over the kept tokens (all tokens unless warped), and the boundary
-  // (tau, ycut) of the kept set.
-  float m_u = 0.f, inv_s = 0.f, tau = -INFINITY;
+  // (tau, ycut) of the kept set.  Staged, the row's slice is left holding
+  // weights w(y) with p(y) = w(y) * wscale: exp(l / T - m_local) (0 for tokens
+  // the warp drops), so later passes multiply instead of exponentiating.
+  float m_u = 0.f, inv_s = 0.f, tau = -INFINITY, wscale = 0.f;
   int ycut = INT32_MAX;
   auto row_stats = [&](int u) {
-    const float* lrow = llm_logits + (size_t)(off + u) * (size_t)V;
+    if (staged) ready(pb);
+    const Slice lrow = logits_of(u);
     float m = -INFINITY;
     for (int64_t g0 = tid; g0 < n4; g0 += (int64_t)T * kMssGroups) {
       float4 v[kMssGroups];
 #pragma unroll
       for (int k = 0; k < kMssGroups; ++k) {
         const int64_t g = g0 + (int64_t)k * T;
-        if (g < n4) v[k] = load4<0>(lrow, lo + 4 * g, vec);
+        if (g < n4) v[k] = lrow.ld4(lo + 4 * g, vec);
       }
 #pragma unroll
       for (int k = 0; k < kMssGroups; ++k)
@@ -832,6 +955,16 @@ __global__ void __launch_bounds__(kMssThreads, 2)
       inv_s = f2_inv(sp.S);
       tau = sp.tau;
       ycut = sp.ycut;
+      if (staged) {  // weights relative to the row maximum M
+        float* w = buf(pb);
+        for (int64_t y = lo + tid; y < hi; y += T) {
+          const float l = w[y - lo];
+          w[y - lo] = kept(l, y, tau, ycut) ? exp_diff(l * inv_t, M) : 0.f;
+        }
+        wscale = inv_s;
+        fence_proxy_async_smem();  // the slice may be overwritten by a later copy
+        __syncthreads();
+      }
       return;
     }
     CompSum acc;
@@ -840,15 +973,31 @@ __global__ void __launch_bounds__(kMssThreads, 2)
 #pragma unroll
       for (int k = 0; k < kMssGroups; ++k) {
         const int64_t g = g0 + (int64_t)k * T;
-        if (g < n4) v[k] = load4<0>(lrow, lo + 4 * g, vec);
+        if (g < n4) v[k] = lrow.ld4(lo + 4 * g, vec);
       }
 #pragma unroll
-      for (int k = 0; k < kMssGroups; ++k)
-        if (g0 + (int64_t)k * T < n4)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) acc.add(exp_diff(at(v[k], e) * inv_t, m));
+      for (int k = 0; k < kMssGroups; ++k) {
+        const int64_t g = g0 + (int64_t)k * T;
+        if (g < n4) {
+          float4 w;
+          w.x = exp_diff(v[k].x * inv_t, m);
+          w.y = exp_diff(v[k].y * inv_t, m);
+          w.z = exp_diff(v[k].z * inv_t, m);
+          w.w = exp_diff(v[k].w * inv_t, m);
+          acc.add(w.x);
+          acc.add(w.y);
+          acc.add(w.z);
+          acc.add(w.w);
+          if (staged) *reinterpret_cast<float4*>(buf(pb) + 4 * g) = w;
+        }
+      }
     }
-    for (int64_t y = lo + 4 * n4 + tid; y < hi; y += T) acc.add(exp_diff(lrow[y] * inv_t, m));
+    for (int64_t y = lo + 4 * n4 + tid; y < hi; y += T) {
+      const float w = exp_diff(lrow[y] * inv_t, m);
+      acc.add(w);
+      if (staged) buf(pb)[y - lo] = w;
+    }
+    if (staged) fence_proxy_async_smem();  // the slice may be overwritten by a later copy
     F2 s = comp_value(acc);
     float z1 = 0.f, z2 = 0.f;
     block_sum(s, z1, z2, red);
@@ -860,20 +1009,24 @@ __global__ void __launch_bounds__(kMssThreads, 2)
     float M = -INFINITY;
     for (int r = 0; r < ncl; ++r) M = fmaxf(M, __shfl_sync(0xffffffffu, mr, r));
     F2 S{0.f, 0.f};
+    float own = 0.f;  // e^(m - M) of this CTA
     for (int r = 0; r < ncl; ++r) {
       const float m_r = __shfl_sync(0xffffffffu, mr, r);
       const F2 s_r{__shfl_sync(0xffffffffu, sh, r), __shfl_sync(0xffffffffu, sl, r)};
-      if (m_r != -INFINITY) S = f2_add(S, f2_scale(s_r, exp_diff(m_r, M)));
+      const float f = m_r != -INFINITY ? exp_diff(m_r, M) : 0.f;
+      if (m_r != -INFINITY) S = f2_add(S, f2_scale(s_r, f));
+      if (r == rank) own = f;
     }
     ++xk;
     m_u = M;
     inv_s = f2_inv(S);
+    wscale = own * inv_s;
     tau = -INFINITY;
     ycut = INT32_MAX;
   };
 
   int u = 0, len = 1, cur = 0, tried = 0;
-  bool from_resid = false;  // false: p = softmax(row u); true: p = resid[cur] / Z
+  bool from_resid = false;  // false: p = softmax(row u); true: p = residual / Z
   bool px_known = false;    // p at the current child's token came with the last exchange
   float px_next = 0.f;
   F2 Z{0.f, 0.f};
@@ -883,9 +1036,7 @@ __global__ void __launch_bounds__(kMssThreads, 2)
     int accepted = -1;
     int c = first_child[u];
     if (c == INT32_MAX) c = -1;
-    const float* lrow = llm_logits + (size_t)(off + u) * (size_t)V;
     while (c >= 0) {
-      const float* q = ssm_probs + (size_t)(off + c) * (size_t)V;
       // p(x) of the current distribution (fp32, ~2 ulp); the test is exact.
       const float px = px_known ? px_next
                                 : (kept(lx_s[c], tok_s[c], tau, ycut) ? exp_diff(lx_s[c] * inv_t, m_u) * inv_s : 0.f);
@@ -899,9 +1050,31 @@ __global__ void __launch_bounds__(kMssThreads, 2)
       const int cn = next_sib[c];
       const int64_t xn = cn >= 0 ? (int64_t)tok_s[cn] : -1;
       const int nxt = cur ^ 1;
-      const float inv_z = f2_inv(Z);
-      const float* rin = resid[cur];
-      float* rout = resid[nxt];
+      // p(y) = source(y) * pscale, except on a logits row read from global
+      // memory, where it is exponentiated here.
+      const float pscale = from_resid ? f2_inv(Z) : wscale;
+      Slice src, q;
+      float* rout;
+      int64_t rout_off;
+      int qj = -1;  // staged: the buffer of c's proposals, then of the residual
+      if (staged) {
+        qj = q_buffer_of(c);
+        if (qj < 0) {  // not fetched ahead
+          qj = free_buffer(-1);
+          q_issue(qj, c);
+        }
+        if (cn >= 0 && q_buffer_of(cn) < 0) q_issue(free_buffer(qj), cn);  // the next sibling's, ahead
+        ready(qj);
+        src = Slice{buf(pb), lo};
+        q = Slice{buf(qj), lo};
+        rout = buf(qj);  // over q: every element is read, then written, by one thread
+        rout_off = lo;
+      } else {
+        src = from_resid ? Slice{resid[cur], 0} : logits_of(u);
+        q = Slice{ssm_probs + (size_t)(off + c) * (size_t)V, 0};
+        rout = resid[nxt];
+        rout_off = 0;
+      }
       CompSum acc;
       float r_x = 0.f, p_x = 0.f;
       for (int64_t g0 = tid; g0 < n4; g0 += (int64_t)T * kMssGroups) {
@@ -910,8 +1083,8 @@ __global__ void __launch_bounds__(kMssThreads, 2)
         for (int k = 0; k < kMssGroups; ++k) {
           const int64_t g = g0 + (int64_t)k * T;
           if (g < n4) {
-            a[k] = from_resid ? load4<2>(rin, lo + 4 * g, vec) : load4<0>(lrow, lo + 4 * g, vec);
-            qq[k] = load4<1>(q, lo + 4 * g, vec);
+            a[k] = src.ld4(lo + 4 * g, vec);
+            qq[k] = q.ld4(lo + 4 * g, vec);
           }
         }
 #pragma unroll
@@ -922,9 +1095,10 @@ __global__ void __launch_bounds__(kMssThreads, 2)
             float r[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const float py = from_resid ? at(a[k], e) * inv_z
-                                          : (kept(at(a[k], e), y + e, tau, ycut)
-                                                 ? exp_diff(at(a[k], e) * inv_t, m_u) * inv_s : 0.f);
+              const float py = staged || from_resid
+                                   ? at(a[k], e) * pscale
+                                   : (kept(at(a[k], e), y + e, tau, ycut)
+                                          ? exp_diff(at(a[k], e) * inv_t, m_u) * inv_s : 0.f);
               r[e] = fmaxf(py - at(qq[k], e), 0.0f);
               acc.add(r[e]);
               if (y + e == xn) {
@@ -932,27 +1106,30 @@ __global__ void __launch_bounds__(kMssThreads, 2)
                 p_x = py;
               }
             }
+            float* o = rout + (y - rout_off);
             if (vec) {
-              *reinterpret_cast<float4*>(rout + y) = make_float4(r[0], r[1], r[2], r[3]);
+              *reinterpret_cast<float4*>(o) = make_float4(r[0], r[1], r[2], r[3]);
             } else {
 #pragma unroll
-              for (int e = 0; e < 4; ++e) rout[y + e] = r[e];
+              for (int e = 0; e < 4; ++e) o[e] = r[e];
             }
           }
         }
       }
       for (int64_t y = lo + 4 * n4 + tid; y < hi; y += T) {
-        const float ly = from_resid ? 0.f : __ldg(lrow + y);
-        const float py = from_resid ? rin[y] * inv_z
-                                    : (kept(ly, y, tau, ycut) ? exp_diff(ly * inv_t, m_u) * inv_s : 0.f);
-        const float r = fmaxf(py - __ldcs(q + y), 0.0f);
-        rout[y] = r;
+        const float a = src[y];
+        const float py = staged || from_resid
+                             ? a * pscale
+                             : (kept(a, y, tau, ycut) ? exp_diff(a * inv_t, m_u) * inv_s : 0.f);
+        const float r = fmaxf(py - q[y], 0.0f);
+        rout[y - rout_off] = r;
         acc.add(r);
         if (y == xn) {
           r_x = r;
           p_x = py;
         }
       }
+      if (staged) fence_proxy_async_smem();  // the residual may be overwritten by a later copy
       F2 zs = comp_value(acc);
       block_sum(zs, r_x, p_x, red);
       exchange(zs.hi, zs.lo, r_x, p_x);
@@ -968,8 +1145,10 @@ __global__ void __launch_bounds__(kMssThreads, 2)
         pxn += __shfl_sync(0xffffffffu, pr, r);
       }
       ++xk;
+      if (staged) node_of[qj] = -1;  // c's proposals are spent
       if (Znew.hi > 0.f) {  // else p = q up to rounding: keep p
         cur = nxt;
+        if (staged) pb = qj;  // the residual is the distribution's row now
         Z = Znew;
         from_resid = true;
         px_next = rxn * f2_inv(Znew);
@@ -985,6 +1164,10 @@ __global__ void __launch_bounds__(kMssThreads, 2)
     ++len;
     from_resid = false;
     px_known = false;
+    if (staged) {
+      const int fc = first_child[u];
+      stage_row(u, fc == INT32_MAX ? -1 : fc);
+    }
     row_stats(u);
   }
 
@@ -993,11 +1176,12 @@ __global__ void __launch_bounds__(kMssThreads, 2)
   // unnormalised current distribution.  Each thread owns a contiguous run of
   // its CTA's slice; runs and slices are in vocabulary order.
   {
-    const float* lrow = llm_logits + (size_t)(off + u) * (size_t)V;
-    const float* rin = resid[cur];
+    const Slice wsrc = staged ? Slice{buf(pb), lo} : (from_resid ? Slice{resid[cur], 0} : logits_of(u));
     const int64_t per_t = ((((hi - lo) + T - 1) / T) + 3) & ~int64_t(3);
     const int64_t tlo = min(hi, lo + (int64_t)tid * per_t), thi = min(hi, tlo + per_t);
+    const float bscale = from_resid ? 1.f : wscale;  // staged weights to one common scale
     auto weight = [&](float a, int64_t y) {
+      if (staged) return a * bscale;
       return from_resid ? a : (kept(a, y, tau, ycut) ? exp_diff(a * inv_t, m_u) : 0.f);
     };
     CompSum acc;
@@ -1005,7 +1189,7 @@ __global__ void __launch_bounds__(kMssThreads, 2)
     {
       int64_t y = tlo;
       for (; y + 4 <= thi; y += 4) {
-        const float4 a = from_resid ? load4<2>(rin, y, vec) : load4<0>(lrow, y, vec);
+        const float4 a = wsrc.ld4(y, vec);
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const float w = weight(at(a, e), y + e);
@@ -1014,7 +1198,7 @@ __global__ void __launch_bounds__(kMssThreads, 2)
         }
       }
       for (; y < thi; ++y) {
-        const float w = weight(from_resid ? rin[y] : lrow[y], y);
+        const float w = weight(wsrc[y], y);
         acc.add(w);
         if (w > 0.0f) last_pos = y;
       }
@@ -1058,7 +1242,7 @@ __global__ void __launch_bounds__(kMssThreads, 2)
       int64_t pick = -1;
       CompSum run;
       for (int64_t y = tlo; y < thi; ++y) {
-        const float w = weight(from_resid ? rin[y] : lrow[y], y);
+        const float w = weight(wsrc[y], y);
         run.add(w);
         if (f2_lt(target, f2_add(excl, comp_value(run)))) {
           pick = y;
@@ -1068,16 +1252,21 @@ __global__ void __launch_bounds__(kMssThreads, 2)
       if (pick < 0) pick = last_pos;  // rounding inside the run
       atomicMin(&pick_s, (int)pick);
     }
+    drain();
     __syncthreads();
-    exchange(__int_as_float(pick_s), 0.f, 0.f, 0.f);
+    exchange(__int_as_float(pick_s), tmo ? 1.f : 0.f, 0.f, 0.f);
     if (rank == 0 && tid == 0) {
       int pick = INT32_MAX;
-      for (int r = 0; r < ncl; ++r) pick = min(pick, __float_as_int(peer(0, r)));
+      bool timed_out = false;
+      for (int r = 0; r < ncl; ++r) {
+        pick = min(pick, __float_as_int(peer(0, r)));
+        timed_out = timed_out || peer(1, r) != 0.f;
+      }
       // No crossing (rounding left the target at the total): last positive entry.
       bonus[b] = pick != INT32_MAX ? pick : last_all;
       accept_len[b] = len - 1;
       if (n_tried) n_tried[b] = tried;
-      status[b] = TSV_OK;
+      status[b] = timed_out ? TSV_ERR_TIMEOUT : TSV_OK;
     }
     cluster_sync_all();  // peers keep their exchange slots until rank 0 has read them
   }
@@ -1209,7 +1398,7 @@ __global__ void __launch_bounds__(kMssThreads)
   for (int64_t y = threadIdx.x; y < V; y += kMssThreads) m = fmaxf(m, __ldg(row + y));
   m = block_max(m, red);
   int xk = 0;
-  warped_support(row, V, 0, V, 1.0f, m, k, 1.0f, 1, 0, xk, pub, sel);
+  warped_support(Slice{row, 0}, V, 0, V, 1.0f, m, k, 1.0f, 1, 0, xk, pub, sel);
   for (int j = threadIdx.x; j < k; j += kMssThreads) tokens[(size_t)blockIdx.x * k + j] = sel.srt_i[j];
 }
 
@@ -1333,19 +1522,44 @@ int mss_cluster_size(int64_t V) {
   return (int)(c < 1 ? 1 : (c > kMssMaxCluster ? kMssMaxCluster : c));
 }
 
+cudaError_t mss_set_attributes(int device, size_t* staged_limit) {
+  cudaFuncAttributes fa;
+  cudaError_t e = cudaFuncGetAttributes(&fa, mss_verify_kernel);
+  if (e != cudaSuccess) return e;
+  int optin = 0;
+  e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
+  if (e != cudaSuccess) return e;
+  const size_t limit = (size_t)optin > fa.sharedSizeBytes ? (size_t)optin - fa.sharedSizeBytes : 0;
+  e = cudaFuncSetAttribute(mss_verify_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)limit);
+  if (e != cudaSuccess) return e;
+  *staged_limit = limit;
+  return cudaSuccess;
+}
+
+size_t mss_staged_bytes(int64_t V) {
+  const int ncl = mss_cluster_size(V);
+  const int64_t per = (((V + ncl - 1) / ncl) + 3) & ~int64_t(3);
+  const int64_t per_al = (per + 31) & ~int64_t(31);
+  return (size_t)(3 * per_al * 4);
+}
+
 cudaError_t launch_mss_verify(const float* llm_logits, const float* ssm_probs, int64_t V,
                               const int32_t* tokens, const int32_t* parent,
                               const int32_t* node_offsets, const float* u_acc, const float* u_smp,
                               float inv_t, int32_t top_k, float top_p, int32_t B, float* resid,
                               int32_t* path, int32_t* accept_len, int32_t* bonus, int32_t* n_tried,
-                              int32_t* status, cudaStream_t st) {
+                              int32_t* status, size_t staged_limit, cudaStream_t st) {
   const int ncl = mss_cluster_size(V);
   const int vec = (V % 4 == 0) && ((reinterpret_cast<uintptr_t>(llm_logits) |
                                     reinterpret_cast<uintptr_t>(ssm_probs) |
                                     reinterpret_cast<uintptr_t>(resid)) & 15) == 0;
-  return launch_pdl(mss_verify_kernel, dim3((unsigned)(B * ncl)), dim3(kMssThreads), 0, st, (unsigned)ncl,
-                    llm_logits, ssm_probs, V, tokens, parent, node_offsets, u_acc, u_smp, inv_t, top_k, top_p,
-                    ncl, vec, resid, path, accept_len, bonus, n_tried, status);
+  // Slices staged in shared memory when three of them fit (bulk copies want
+  // the 16-byte alignment `vec` stands for).
+  const size_t dyn = mss_staged_bytes(V);
+  const int staged = vec && dyn <= staged_limit;
+  return launch_pdl(mss_verify_kernel, dim3((unsigned)(B * ncl)), dim3(kMssThreads), staged ? dyn : 0, st,
+                    (unsigned)ncl, llm_logits, ssm_probs, V, tokens, parent, node_offsets, u_acc, u_smp, inv_t,
+                    top_k, top_p, ncl, vec, staged, resid, path, accept_len, bonus, n_tried, status);
 }
 
 }  // namespace tsv
