@@ -31,7 +31,7 @@ namespace {
 
 constexpr int kArgmaxThreads = 256;
 constexpr int kArgmaxInFlight = 8;
-constexpr int kMinSlice = 4096;  // vocab entries per CTA at least
+constexpr int kMinSlice = 2048;  // vocab entries per CTA at least
 
 struct ArgMax {
   float v;
@@ -384,34 +384,12 @@ __device__ __forceinline__ F2 shfl_xor_f2(F2 v, int o) {
   return {__shfl_xor_sync(0xffffffffu, v.hi, o), __shfl_xor_sync(0xffffffffu, v.lo, o)};
 }
 
-// Block-wide sum of a pair sum and two plain floats (every thread gets them;
-// the floats are sums of one nonzero value and zeros, so exact).
-// `red` holds 4 x 32 floats.
-__device__ void block_sum(F2& a, float& b, float& c, float* red) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+// Sum over the warp's lanes, the same in every lane (butterfly; f2_add is
+// commutative, so partners compute identical sums).
+__device__ __forceinline__ F2 warp_sum_f2(F2 a) {
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    a = f2_add(a, shfl_xor_f2(a, o));
-    b += __shfl_xor_sync(0xffffffffu, b, o);
-    c += __shfl_xor_sync(0xffffffffu, c, o);
-  }
-  __syncthreads();  // red is free
-  if (lane == 0) {
-    red[warp] = a.hi;
-    red[32 + warp] = a.lo;
-    red[64 + warp] = b;
-    red[96 + warp] = c;
-  }
-  __syncthreads();
-  // Every warp adds the per-warp values in warp order: the same result everywhere.
-  a = F2{0.f, 0.f};
-  b = 0.f;
-  c = 0.f;
-  for (int w = 0; w < kMssWarps; ++w) {
-    a = f2_add(a, F2{red[w], red[32 + w]});
-    b += red[64 + w];
-    c += red[96 + w];
-  }
+  for (int o = 16; o > 0; o >>= 1) a = f2_add(a, shfl_xor_f2(a, o));
+  return a;
 }
 
 __device__ float block_max(float v, float* red) {
@@ -721,10 +699,17 @@ __device__ __noinline__ Support warped_support(const Slice lrow, int64_t V, int6
 // every CTA from values every CTA holds: the children, their tokens, accept
 // uniforms, proposal probabilities q_c(x_c) and parent logits l(x_c) (read
 // once, in parallel, at the start), the row statistics and residual sums
-// (combined in rank order through distributed shared memory), and p at the
-// next child's token, which the residual pass of the CTA owning that token
-// publishes with the sums.  A CTA reads only its own slice of the logits,
-// proposals and residual rows.
+// (combined in a fixed order from partials every CTA pushes into every
+// other's shared memory), and p at the next child's token, which the residual
+// pass of the CTA owning that token publishes with the sums.  A CTA reads only
+// its own slice of the logits, proposals and residual rows.
+//
+// Exchanges: each CTA (or each warp of each CTA) stores its 16-byte partial
+// into a slot of every CTA of the cluster with st.async, which completes the
+// receiver's mbarrier transaction count; a CTA waits on its own mbarrier and
+// reads the slots locally.  Two slot sets alternate: a CTA pushes exchange
+// k + 2 only after exchange k + 1 completed, that is after every CTA pushed
+// k + 1, which each does only after its threads have read exchange k.
 //
 // Staged (`staged`, when the slices fit): each CTA holds three slice buffers
 // in shared memory.  One holds the row the current distribution comes from
@@ -756,6 +741,8 @@ __global__ void __launch_bounds__(kMssThreads, 2)
   __shared__ int bad, bad_tok;
   __shared__ int pick_s, last_s;
   __shared__ __align__(8) uint64_t cbar[3];  // staged copies: one barrier per slice buffer
+  __shared__ __align__(8) uint64_t xbar[2];  // exchanges, alternating
+  __shared__ __align__(16) float4 xslot[2][kMssMaxCluster * kMssWarps];
   __shared__ SelSmem sel;
   extern __shared__ __align__(128) float mss_dyn[];
   const bool warped = top_k > 0 || top_p < 1.0f;
@@ -767,10 +754,11 @@ __global__ void __launch_bounds__(kMssThreads, 2)
   if (tid == 0) {
     pick_s = INT32_MAX;
     last_s = -1;
-    if (staged) {
+    if (staged)
       for (int i = 0; i < 3; ++i) mbar_init(&cbar[i], 1);
-      mbar_fence_init();
-    }
+    mbar_init(&xbar[0], 1);
+    mbar_init(&xbar[1], 1);
+    mbar_fence_init();
   }
   const int off = node_offsets[b];
   const int n = node_offsets[b + 1] - off;
@@ -841,7 +829,8 @@ __global__ void __launch_bounds__(kMssThreads, 2)
     if (!staged) return;
     for (int j = 0; j < 3; ++j) ready(j);
   };
-  __syncthreads();  // barriers initialised
+  __syncthreads();  // barriers initialised ...
+  cluster_sync_all();  // ... in every CTA of the cluster, before anyone pushes
   // Node 0 is the root and node 1 (if any) its first child in every valid
   // tree: their slices travel while the tree is read and checked.
   if (staged && n >= 1) stage_row(0, n >= 2 ? 1 : -1);
@@ -899,19 +888,27 @@ __global__ void __launch_bounds__(kMssThreads, 2)
   __syncthreads();
 
   float* resid[2] = {resid_all + (size_t)b * 2 * (size_t)V, resid_all + ((size_t)b * 2 + 1) * (size_t)V};
-  int xk = 0;  // exchanges so far (the same count in every CTA)
-  // Publishes four floats, then waits for the whole cluster.
-  auto exchange = [&](float v0, float v1, float v2, float v3) {
-    if (tid == 0) {
-      pub[xk & 1][0] = v0;
-      pub[xk & 1][1] = v1;
-      pub[xk & 1][2] = v2;
-      pub[xk & 1][3] = v3;
+  int xk = 0;  // exchanges of the warped support so far (the same count in every CTA)
+  int xp = 0;  // pushed exchanges so far (the same count in every CTA)
+  uint32_t xpar = 0u;  // bit s: parity of the next phase of xbar[s]
+  // Pushed exchange: `per_warp` false, one float4 per CTA (slot = rank);
+  // true, one per warp of every CTA (slot = rank * kMssWarps + warp).
+  // Returns the slots once all have landed.
+  auto push = [&](float4 v, bool per_warp) -> const float4* {
+    const int s = xp & 1;
+    const int slots = per_warp ? ncl * kMssWarps : ncl;
+    if (tid == 0) mbar_arrive_expect_tx(&xbar[s], (uint32_t)slots * 16u);
+    const int w = tid >> 5;
+    if (per_warp ? lane < ncl : tid < ncl) {
+      const int dst = per_warp ? lane : tid;
+      const int slot = per_warp ? rank * kMssWarps + w : rank;
+      st_async_v4(mapa_shared(smem_u32(&xslot[s][slot]), (uint32_t)dst), v,
+                  mapa_shared(smem_u32(&xbar[s]), (uint32_t)dst));
     }
-    cluster_sync_all();
-  };
-  auto peer = [&](int slot, int r) {
-    return ld_dsmem_f32(mapa_shared(smem_u32(&pub[xk & 1][slot]), (uint32_t)r));
+    if (!mbar_wait(&xbar[s], (xpar >> s) & 1u, nullptr)) tmo = true;
+    xpar ^= 1u << s;
+    ++xp;
+    return xslot[s];
   };
   // Node u's logits, this CTA's slice.
   auto logits_of = [&](int u) {
@@ -945,11 +942,9 @@ __global__ void __launch_bounds__(kMssThreads, 2)
     for (int64_t y = lo + 4 * n4 + tid; y < hi; y += T) m = fmaxf(m, lrow[y] * inv_t);
     m = block_max(m, red);
     if (warped) {
-      exchange(m, 0.f, 0.f, 0.f);
-      const float mr = lane < ncl ? peer(0, lane) : -INFINITY;
+      const float4* e = push(make_float4(m, 0.f, 0.f, 0.f), false);
       float M = -INFINITY;
-      for (int r = 0; r < ncl; ++r) M = fmaxf(M, __shfl_sync(0xffffffffu, mr, r));
-      ++xk;
+      for (int r = 0; r < ncl; ++r) M = fmaxf(M, e[r].x);
       const Support sp = warped_support(lrow, V, lo, hi, inv_t, M, top_k, top_p, ncl, rank, xk, pub, sel);
       m_u = M;
       inv_s = f2_inv(sp.S);
@@ -998,26 +993,21 @@ __global__ void __launch_bounds__(kMssThreads, 2)
       if (staged) buf(pb)[y - lo] = w;
     }
     if (staged) fence_proxy_async_smem();  // the slice may be overwritten by a later copy
-    F2 s = comp_value(acc);
-    float z1 = 0.f, z2 = 0.f;
-    block_sum(s, z1, z2, red);
-    exchange(m, s.hi, s.lo, 0.f);
-    // Combine in rank order (identical in every CTA): M = max m_r, S = sum s_r e^(m_r - M).
-    const float mr = lane < ncl ? peer(0, lane) : -INFINITY;
-    const float sh = lane < ncl ? peer(1, lane) : 0.f;
-    const float sl = lane < ncl ? peer(2, lane) : 0.f;
-    float M = -INFINITY;
-    for (int r = 0; r < ncl; ++r) M = fmaxf(M, __shfl_sync(0xffffffffu, mr, r));
+    F2 s = warp_sum_f2(comp_value(acc));
+    // Combine the warp partials (identical in every CTA):
+    // M = max m_i, S = sum s_i e^(m_i - M).
+    const float4* e = push(make_float4(m, s.hi, s.lo, 0.f), true);
+    const int cnt = ncl * kMssWarps;
+    const float4 e0 = lane < cnt ? e[lane] : make_float4(-INFINITY, 0.f, 0.f, 0.f);
+    const float4 e1 = lane + 32 < cnt ? e[lane + 32] : make_float4(-INFINITY, 0.f, 0.f, 0.f);
+    float M = fmaxf(e0.x, e1.x);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
     F2 S{0.f, 0.f};
-    float own = 0.f;  // e^(m - M) of this CTA
-    for (int r = 0; r < ncl; ++r) {
-      const float m_r = __shfl_sync(0xffffffffu, mr, r);
-      const F2 s_r{__shfl_sync(0xffffffffu, sh, r), __shfl_sync(0xffffffffu, sl, r)};
-      const float f = m_r != -INFINITY ? exp_diff(m_r, M) : 0.f;
-      if (m_r != -INFINITY) S = f2_add(S, f2_scale(s_r, f));
-      if (r == rank) own = f;
-    }
-    ++xk;
+    if (e0.x != -INFINITY) S = f2_scale(F2{e0.y, e0.z}, exp_diff(e0.x, M));
+    if (e1.x != -INFINITY) S = f2_add(S, f2_scale(F2{e1.y, e1.z}, exp_diff(e1.x, M)));
+    S = warp_sum_f2(S);
+    const float own = m != -INFINITY ? exp_diff(m, M) : 0.f;  // e^(m - M) of this CTA
     m_u = M;
     inv_s = f2_inv(S);
     wscale = own * inv_s;
@@ -1130,21 +1120,25 @@ __global__ void __launch_bounds__(kMssThreads, 2)
         }
       }
       if (staged) fence_proxy_async_smem();  // the residual may be overwritten by a later copy
-      F2 zs = comp_value(acc);
-      block_sum(zs, r_x, p_x, red);
-      exchange(zs.hi, zs.lo, r_x, p_x);
-      const float zh = lane < ncl ? peer(0, lane) : 0.f;
-      const float zl = lane < ncl ? peer(1, lane) : 0.f;
-      const float rr = lane < ncl ? peer(2, lane) : 0.f;
-      const float pr = lane < ncl ? peer(3, lane) : 0.f;
-      F2 Znew{0.f, 0.f};
-      float rxn = 0.f, pxn = 0.f;
-      for (int r = 0; r < ncl; ++r) {
-        Znew = f2_add(Znew, F2{__shfl_sync(0xffffffffu, zh, r), __shfl_sync(0xffffffffu, zl, r)});
-        rxn += __shfl_sync(0xffffffffu, rr, r);  // one owner, the rest add zeros
-        pxn += __shfl_sync(0xffffffffu, pr, r);
+      // Warp partials, then every warp of every CTA combines them in the
+      // same order (r and p at xn: one owner, the rest add zeros).
+      const F2 zs = warp_sum_f2(comp_value(acc));
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        r_x += __shfl_xor_sync(0xffffffffu, r_x, o);
+        p_x += __shfl_xor_sync(0xffffffffu, p_x, o);
       }
-      ++xk;
+      const float4* e = push(make_float4(zs.hi, zs.lo, r_x, p_x), true);
+      const int cnt = ncl * kMssWarps;
+      const float4 e0 = lane < cnt ? e[lane] : make_float4(0.f, 0.f, 0.f, 0.f);
+      const float4 e1 = lane + 32 < cnt ? e[lane + 32] : make_float4(0.f, 0.f, 0.f, 0.f);
+      F2 Znew = warp_sum_f2(f2_add(F2{e0.x, e0.y}, F2{e1.x, e1.y}));
+      float rxn = e0.z + e1.z, pxn = e0.w + e1.w;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        rxn += __shfl_xor_sync(0xffffffffu, rxn, o);
+        pxn += __shfl_xor_sync(0xffffffffu, pxn, o);
+      }
       if (staged) node_of[qj] = -1;  // c's proposals are spent
       if (Znew.hi > 0.f) {  // else p = q up to rounding: keep p
         cur = nxt;
@@ -1222,19 +1216,15 @@ __global__ void __launch_bounds__(kMssThreads, 2)
       if (w < warp) wbase = f2_add(wbase, scan_s[w]);
       cta_total = f2_add(cta_total, scan_s[w]);
     }
-    exchange(cta_total.hi, cta_total.lo, __int_as_float(last_s), 0.f);
-    const float th = lane < ncl ? peer(0, lane) : 0.f;
-    const float tl = lane < ncl ? peer(1, lane) : 0.f;
-    const int lr = lane < ncl ? __float_as_int(peer(2, lane)) : -1;
+    const float4* e = push(make_float4(cta_total.hi, cta_total.lo, __int_as_float(last_s), 0.f), false);
     F2 base{0.f, 0.f}, total{0.f, 0.f};
     int last_all = -1;
-    for (int r = 0; r < ncl; ++r) {
-      const F2 t{__shfl_sync(0xffffffffu, th, r), __shfl_sync(0xffffffffu, tl, r)};
+    for (int r = 0; r < ncl; ++r) {  // in rank order, identical in every CTA
+      const F2 t{e[r].x, e[r].y};
       if (r < rank) base = f2_add(base, t);
       total = f2_add(total, t);
-      last_all = max(last_all, __shfl_sync(0xffffffffu, lr, r));
+      last_all = max(last_all, __float_as_int(e[r].z));
     }
-    ++xk;
     const F2 excl = f2_add(f2_add(base, wbase), wexcl);
     const F2 target = f2_scale(total, __ldg(u_smp + off + u));
     if (mine.hi > 0.f && !f2_lt(target, excl) && f2_lt(target, f2_add(excl, mine))) {
@@ -1254,13 +1244,13 @@ __global__ void __launch_bounds__(kMssThreads, 2)
     }
     drain();
     __syncthreads();
-    exchange(__int_as_float(pick_s), tmo ? 1.f : 0.f, 0.f, 0.f);
+    const float4* e2 = push(make_float4(__int_as_float(pick_s), tmo ? 1.f : 0.f, 0.f, 0.f), false);
     if (rank == 0 && tid == 0) {
       int pick = INT32_MAX;
-      bool timed_out = false;
+      bool timed_out = tmo;
       for (int r = 0; r < ncl; ++r) {
-        pick = min(pick, __float_as_int(peer(0, r)));
-        timed_out = timed_out || peer(1, r) != 0.f;
+        pick = min(pick, __float_as_int(e2[r].x));
+        timed_out = timed_out || e2[r].y != 0.f;
       }
       // No crossing (rounding left the target at the total): last positive entry.
       bonus[b] = pick != INT32_MAX ? pick : last_all;
@@ -1268,7 +1258,8 @@ __global__ void __launch_bounds__(kMssThreads, 2)
       if (n_tried) n_tried[b] = tried;
       status[b] = timed_out ? TSV_ERR_TIMEOUT : TSV_OK;
     }
-    cluster_sync_all();  // peers keep their exchange slots until rank 0 has read them
+    // Every push into this CTA has landed (the last wait counted them all) and
+    // it reads no other CTA's memory from here on: it may leave.
   }
   if (rank == 0)
     for (int i = len + tid; i < n; i += T) path[off + i] = -1;
