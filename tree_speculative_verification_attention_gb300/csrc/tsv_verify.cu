@@ -731,8 +731,6 @@ __global__ void __launch_bounds__(kMssThreads, 2)
                       int32_t* __restrict__ accept_len, int32_t* __restrict__ bonus,
                       int32_t* __restrict__ n_tried, int32_t* __restrict__ status) {
   pdl_wait();  // the previous kernel's results are visible from here on
-  __shared__ int32_t first_child[TSV_MAX_NODES];
-  __shared__ int32_t next_sib[TSV_MAX_NODES];
   __shared__ int32_t tok_s[TSV_MAX_NODES], par_s[TSV_MAX_NODES];
   __shared__ float ua_s[TSV_MAX_NODES], qx_s[TSV_MAX_NODES], lx_s[TSV_MAX_NODES];
   __shared__ float red[128];
@@ -867,25 +865,26 @@ __global__ void __launch_bounds__(kMssThreads, 2)
                    status + b, code);
     return;  // uniform over the cluster: every CTA sees the same tree
   }
-  // Per child c: q_c(x_c) and the parent row's logit at x_c (one parallel
-  // step), and the sibling lists in increasing index order.
-  for (int c = tid; c < n; c += T) first_child[c] = INT32_MAX;
-  __syncthreads();
-  for (int c = 1 + tid; c < n; c += T) {
-    const int x = tok_s[c], p = par_s[c];
-    qx_s[c] = __ldg(ssm_probs + (size_t)(off + c) * (size_t)V + x);
-    lx_s[c] = __ldg(llm_logits + (size_t)(off + p) * (size_t)V + x);
-    atomicMin(&first_child[p], c);
-    int nx = -1;
-    for (int c2 = c + 1; c2 < n; ++c2) {
-      if (par_s[c2] == p) {
-        nx = c2;
-        break;
-      }
-    }
-    next_sib[c] = nx;
+  // Per child c: q_c(x_c) and the parent row's logit at x_c, loaded now and
+  // stored once the root's row statistics are done (the loads travel
+  // meanwhile; the first accept test is the first use).
+  static_assert(kMssThreads >= TSV_MAX_NODES, "one child per thread");
+  float my_qx = 0.f, my_lx = 0.f;
+  if (tid >= 1 && tid < n) {
+    my_qx = __ldg(ssm_probs + (size_t)(off + tid) * (size_t)V + tok_s[tid]);
+    my_lx = __ldg(llm_logits + (size_t)(off + par_s[tid]) * (size_t)V + tok_s[tid]);
   }
-  __syncthreads();
+  // The lowest-index child of p after node `from` (children follow their
+  // parent in the order), or -1: a ballot scan by the calling warp; every
+  // warp finds the same node.
+  auto next_child = [&](int p, int from) {
+    for (int base = from + 1; base < n; base += 32) {
+      const int c = base + lane;
+      const uint32_t bal = __ballot_sync(0xffffffffu, c < n && par_s[c] == p);
+      if (bal) return base + __ffs(bal) - 1;
+    }
+    return -1;
+  };
 
   float* resid[2] = {resid_all + (size_t)b * 2 * (size_t)V, resid_all + ((size_t)b * 2 + 1) * (size_t)V};
   int xk = 0;  // exchanges of the warped support so far (the same count in every CTA)
@@ -1022,10 +1021,14 @@ __global__ void __launch_bounds__(kMssThreads, 2)
   F2 Z{0.f, 0.f};
   if (rank == 0 && tid == 0) path[off] = 0;
   row_stats(0);
+  if (tid >= 1 && tid < n) {
+    qx_s[tid] = my_qx;
+    lx_s[tid] = my_lx;
+  }
+  __syncthreads();
   while (true) {
     int accepted = -1;
-    int c = first_child[u];
-    if (c == INT32_MAX) c = -1;
+    int c = next_child(u, u);
     while (c >= 0) {
       // p(x) of the current distribution (fp32, ~2 ulp); the test is exact.
       const float px = px_known ? px_next
@@ -1037,7 +1040,7 @@ __global__ void __launch_bounds__(kMssThreads, 2)
       }
       // Rejected: residual pass over the slice, r = max(0, p - q).  The owner
       // of the next child's token records r and p there for the exchange.
-      const int cn = next_sib[c];
+      const int cn = next_child(u, c);
       const int64_t xn = cn >= 0 ? (int64_t)tok_s[cn] : -1;
       const int nxt = cur ^ 1;
       // p(y) = source(y) * pscale, except on a logits row read from global
@@ -1158,10 +1161,7 @@ __global__ void __launch_bounds__(kMssThreads, 2)
     ++len;
     from_resid = false;
     px_known = false;
-    if (staged) {
-      const int fc = first_child[u];
-      stage_row(u, fc == INT32_MAX ? -1 : fc);
-    }
+    if (staged) stage_row(u, next_child(u, u));
     row_stats(u);
   }
 
