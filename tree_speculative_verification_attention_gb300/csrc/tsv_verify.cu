@@ -131,95 +131,91 @@ struct WalkSmem {
   int32_t am[TSV_MAX_NODES];
   int32_t nxt[TSV_MAX_NODES];
   ArgMax part[kWalkPartials];
-  int bad, len;
 };
 
 // The greedy walk of request b from its per-slice argmax partials: every
 // child c whose token equals argmax(parent(c)) proposes itself to its parent
-// with atomicMin (lowest index wins), then the chain is followed from the root.
-// Parents, tokens and partials are loaded in one parallel step.  Run by one
-// whole CTA of up to 256 threads.
+// with atomicMin (lowest index wins), then the chain is followed from the
+// root.  Run by one whole CTA of kArgmaxThreads threads: one load step
+// (parents, tokens, partials), then three barriers — partials staged; every
+// node's argmax known and the tree checked; proposals made — and warp 0
+// follows the chain and writes the path.
 __device__ void greedy_walk_request(int b, int off, int n, const float* part_val,
                                     const int32_t* part_idx, int splits, const int32_t* tokens,
                                     const int32_t* parent, int32_t* path, int32_t* accept_len,
                                     int32_t* bonus, int32_t* status, WalkSmem& w) {
   const int T = blockDim.x;
-  if (threadIdx.x == 0) w.bad = (n < 1) ? TSV_ERR_BAD_TREE : (n > TSV_MAX_NODES ? TSV_ERR_UNSUPPORTED : 0);
-  __syncthreads();
-  const int items = n * splits;  // rows of a request are consecutive, so its partials are too
-  const bool staged = items <= kWalkPartials;
-  if (w.bad == 0) {
-    // Every load is issued before the first shared-memory store, so they all
-    // travel together (n <= T; items <= kWalkPartials = 4 T).
-    static_assert(kWalkPartials <= 4 * kArgmaxThreads && TSV_MAX_NODES <= kArgmaxThreads, "one pass");
-    const int i = threadIdx.x;
-    int pv = 0, tv = 0;
-    if (i < n) {
-      pv = parent[off + i];
-      tv = tokens[off + i];
-    }
-    float pval[4];
-    int32_t pidx[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int e = i + k * T;
-      if (staged && e < items) {
-        pval[k] = __ldcg(part_val + (size_t)off * splits + e);
-        pidx[k] = __ldcg(part_idx + (size_t)off * splits + e);
-      }
-    }
-    if (i < n) {
-      w.par[i] = pv;
-      w.tok[i] = tv;
-    }
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int e = i + k * T;
-      if (staged && e < items) w.part[e] = ArgMax{pval[k], pidx[k]};
-    }
-  }
-  __syncthreads();
-  if (w.bad == 0) {
-    for (int i = threadIdx.x; i < n; i += T) {
-      const int p = w.par[i];
-      const bool ok = (i == 0) ? (p == -1) : (p >= 0 && p < i);
-      if (!ok) atomicMax(&w.bad, TSV_ERR_BAD_TREE);
-    }
-  }
-  __syncthreads();
-  if (w.bad) {
-    fail_request(path + off, n, accept_len + b, bonus + b, nullptr, status + b, w.bad);
+  const int i = threadIdx.x;
+  static_assert(kWalkPartials <= 4 * kArgmaxThreads && TSV_MAX_NODES <= kArgmaxThreads, "one pass");
+  const int size_code = (n < 1) ? TSV_ERR_BAD_TREE : (n > TSV_MAX_NODES ? TSV_ERR_UNSUPPORTED : 0);
+  if (size_code) {  // uniform: n is the same for every thread
+    fail_request(path + off, n, accept_len + b, bonus + b, nullptr, status + b, size_code);
     return;
   }
-  for (int u = threadIdx.x; u < n; u += T) {
+  const int items = n * splits;  // rows of a request are consecutive, so its partials are too
+  const bool staged = items <= kWalkPartials;
+  // Every load is issued before the first shared-memory store, so they all
+  // travel together.
+  int pv = 0, tv = 0;
+  if (i < n) {
+    pv = parent[off + i];
+    tv = tokens[off + i];
+  }
+  float pval[4];
+  int32_t pidx[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int e = i + k * T;
+    if (staged && e < items) {
+      pval[k] = __ldcg(part_val + (size_t)off * splits + e);
+      pidx[k] = __ldcg(part_idx + (size_t)off * splits + e);
+    }
+  }
+  if (i < n) {
+    w.par[i] = pv;
+    w.tok[i] = tv;
+    w.nxt[i] = INT32_MAX;
+  }
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int e = i + k * T;
+    if (staged && e < items) w.part[e] = ArgMax{pval[k], pidx[k]};
+  }
+  __syncthreads();
+  // Node i: its parent is checked (a single root at 0, every other parent
+  // earlier) and its row's slices merged into its argmax.
+  bool bad = false;
+  if (i < n) {
+    bad = !((i == 0) ? (pv == -1) : (pv >= 0 && pv < i));
     ArgMax best{-INFINITY, INT32_MAX};
-    for (int s = 0; s < splits; ++s) {
-      const size_t k = (size_t)(off + u) * splits + s;
-      best = better(best, staged ? w.part[u * splits + s] : ArgMax{__ldcg(part_val + k), __ldcg(part_idx + k)});
+    for (int sl = 0; sl < splits; ++sl) {
+      const size_t k = (size_t)(off + i) * splits + sl;
+      best = better(best, staged ? w.part[i * splits + sl] : ArgMax{__ldcg(part_val + k), __ldcg(part_idx + k)});
     }
-    w.am[u] = best.i;
-    w.nxt[u] = INT32_MAX;
+    w.am[i] = best.i;
   }
-  __syncthreads();
-  for (int c = 1 + threadIdx.x; c < n; c += T) {
-    const int p = w.par[c];
-    if (w.tok[c] == w.am[p]) atomicMin(&w.nxt[p], c);
+  if (__syncthreads_or(bad)) {
+    fail_request(path + off, n, accept_len + b, bonus + b, nullptr, status + b, TSV_ERR_BAD_TREE);
+    return;
   }
+  if (i >= 1 && i < n && tv == w.am[pv]) atomicMin(&w.nxt[pv], i);
   __syncthreads();
-  if (threadIdx.x == 0) {
-    int u = 0, len = 0;
-    path[off + len++] = 0;
-    while (w.nxt[u] != INT32_MAX) {
-      u = w.nxt[u];
-      path[off + len++] = u;
+  if (i < 32) {  // warp 0: lane 0 follows the chain, the warp writes the rest
+    int len = 0;
+    if (i == 0) {
+      int u = 0;
+      path[off + len++] = 0;
+      while (w.nxt[u] != INT32_MAX) {
+        u = w.nxt[u];
+        path[off + len++] = u;
+      }
+      accept_len[b] = len - 1;
+      bonus[b] = w.am[u];
+      status[b] = TSV_OK;
     }
-    accept_len[b] = len - 1;
-    bonus[b] = w.am[u];
-    status[b] = TSV_OK;
-    w.len = len;
+    len = __shfl_sync(0xffffffffu, len, 0);
+    for (int k = len + i; k < n; k += 32) path[off + k] = -1;
   }
-  __syncthreads();
-  for (int i = w.len + threadIdx.x; i < n; i += T) path[off + i] = -1;
 }
 
 // Walk-only kernel: one CTA per request (used when N == 0, where no argmax CTA exists).
