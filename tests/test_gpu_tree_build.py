@@ -13,7 +13,10 @@ pytestmark = pytest.mark.gpu
 
 @pytest.mark.parametrize("F,V,k,grid", [(7, 5, 1, 0.0), (7, 5, 5, 0.5), (33, 1000, 4, 0.0), (33, 1000, 16, 0.5),
                                         (64, 32000, 4, 0.0), (8, 32000, 1024, 0.25), (5, 128256, 8, 0.0),
-                                        (300, 3000, 3, 1.0)])
+                                        (300, 3000, 3, 1.0),
+                                        # few long rows: each row split over a cluster of CTAs
+                                        (1, 128256, 1, 0.0), (2, 50001, 7, 0.5), (3, 40000, 9, 1.0),
+                                        (1, 16384, 8, 0.0), (4, 128256, 64, 0.25)])
 def test_expand_matches_oracle(tsv, F, V, k, grid):
     rng = np.random.default_rng(F * 7 + k)
     z = (rng.standard_normal((F, V)) * 2).astype(np.float32)

@@ -552,7 +552,8 @@ tsv_status tsv_tree_expand(tsv_handle h, const float* ssm_logits_d, int64_t V, i
   if (!h || F < 0 || V < 1 || V > INT32_MAX || k < 1 || (int64_t)k > V) return TSV_ERR_INVALID_ARG;
   if (k > kMssMaxTopK) return TSV_ERR_UNSUPPORTED;
   if (F > 0 && (!ssm_logits_d || !tokens_d)) return TSV_ERR_INVALID_ARG;
-  return cuda_status(launch_tree_expand(ssm_logits_d, V, F, k, tokens_d, static_cast<cudaStream_t>(stream)));
+  return cuda_status(
+      launch_tree_expand(ssm_logits_d, V, F, k, tokens_d, h->num_sms, static_cast<cudaStream_t>(stream)));
 }
 
 tsv_status tsv_tree_merge(tsv_handle h, const int32_t* parent_d, const int32_t* tokens_d,

@@ -151,7 +151,7 @@ constexpr int kMssMaxTopK = 1024;  // largest top_k of the warped stochastic ver
 // merge of several trees per request.
 constexpr int kTreeMergeMaxInput = 1024;  // input nodes of one request's merge
 cudaError_t launch_tree_expand(const float* logits, int64_t V, int32_t F, int32_t k, int32_t* tokens,
-                               cudaStream_t st);
+                               int num_sms, cudaStream_t st);
 cudaError_t launch_tree_merge(const int32_t* parent, const int32_t* tokens, const int32_t* tree_offsets,
                               const int32_t* request_trees, int32_t B, int32_t* out_parent,
                               int32_t* out_tokens, int32_t* out_source, int32_t* out_count,

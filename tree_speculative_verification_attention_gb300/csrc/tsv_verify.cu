@@ -1265,21 +1265,26 @@ __global__ void __launch_bounds__(kMssThreads, 2)
 
 // Expansion step (SpecInfer §3, expansion-based token trees): row f of the
 // frontier's SSM logits gets its k largest-logit tokens as children, larger
-// first, equal logits by lower token index.  One CTA per row: for k <= 8 one
-// pass with per-thread top-k lists; wider expansions use the same selection
-// as the warped support (a CTA launched without a cluster is a cluster of one).
+// first, equal logits by lower token index.  A row is split over a cluster
+// of CTAs when the frontier is small: for k <= 8 each CTA makes one pass over
+// its slice with per-thread top-k lists and rank 0 merges the CTAs' lists;
+// wider expansions use the same selection as the warped support (a CTA
+// launched without a cluster is a cluster of one).
 constexpr int kExpandSmallK = 8;  // widest expansion done in one pass over the row
 
 __device__ __forceinline__ bool ranks_before(float a, int ia, float b, int ib) {
   return a > b || (a == b && ia < ib);
 }
 
-// Top-k of one row for k <= KP <= kExpandSmallK, in one pass: every thread
-// keeps its KP best (value, index) sorted in registers; then k rounds pick
-// the best head among the 256 lists (a block-wide argmax in ranking order).
+// Top-k of entries [lo, hi) of one row for k <= KP <= kExpandSmallK, in one
+// pass: every thread keeps its KP best (value, index) sorted in registers;
+// then k rounds pick the best head among the 256 lists (a block-wide argmax in
+// ranking order).  Entry j of the result goes to (out_v[j], out_i[j]) (thread
+// 0 writes; -inf / INT32_MAX when the slice holds fewer than k entries).
 template <int KP>
-__device__ void expand_small(const float* __restrict__ row, int64_t V, int k, int32_t* __restrict__ out,
-                             float* lv, int* li, float* rv, int* ri) {
+__device__ void expand_small(const float* __restrict__ row, int64_t lo, int64_t hi, int k,
+                             float* __restrict__ out_v, int32_t* __restrict__ out_i, float* lv, int* li,
+                             float* rv, int* ri) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   float bv[KP];
   int bi[KP];
@@ -1305,11 +1310,12 @@ __device__ void expand_small(const float* __restrict__ row, int64_t V, int k, in
       }
     }
   };
-  // 16-byte loads, eight in flight per thread, when the row is aligned.
+  // 16-byte loads, eight in flight per thread, when the slice is aligned
+  // (lo is a multiple of 4).
   constexpr int kInFlight = 8;
-  const bool vec = (V % 4 == 0) && ((reinterpret_cast<uintptr_t>(row) & 15) == 0);
-  const int64_t n4 = vec ? V / 4 : 0;
-  const float4* r4 = reinterpret_cast<const float4*>(row);
+  const bool vec = ((lo & 3) == 0) && ((reinterpret_cast<uintptr_t>(row) & 15) == 0);
+  const int64_t n4 = vec ? (hi - lo) / 4 : 0;
+  const float4* r4 = reinterpret_cast<const float4*>(row + lo);
   for (int64_t g0 = tid; g0 < n4; g0 += kInFlight * kMssThreads) {
     float4 a[kInFlight];
 #pragma unroll
@@ -1319,14 +1325,15 @@ __device__ void expand_small(const float* __restrict__ row, int64_t V, int k, in
     for (int u = 0; u < kInFlight; ++u) {
       const int64_t g = g0 + u * kMssThreads;
       if (g < n4) {
-        offer(a[u].x, (int)(4 * g));
-        offer(a[u].y, (int)(4 * g + 1));
-        offer(a[u].z, (int)(4 * g + 2));
-        offer(a[u].w, (int)(4 * g + 3));
+        const int y = (int)(lo + 4 * g);
+        offer(a[u].x, y);
+        offer(a[u].y, y + 1);
+        offer(a[u].z, y + 2);
+        offer(a[u].w, y + 3);
       }
     }
   }
-  for (int64_t y = 4 * n4 + tid; y < V; y += kMssThreads) offer(__ldg(row + y), (int)y);
+  for (int64_t y = lo + 4 * n4 + tid; y < hi; y += kMssThreads) offer(__ldg(row + y), (int)y);
 #pragma unroll
   for (int i = 0; i < KP; ++i) {
     lv[tid * KP + i] = bv[i];
@@ -1358,14 +1365,22 @@ __device__ void expand_small(const float* __restrict__ row, int64_t V, int k, in
         bvv = rv[ww];
         bid = ri[ww];
       }
-    if (tid == 0) out[j] = bid;
+    if (tid == 0) {
+      out_v[j] = bvv;
+      out_i[j] = bid;
+    }
     if (pos < KP && li[tid * KP + pos] == bid) ++pos;  // indices are unique: one list advances
     __syncthreads();
   }
 }
 
+// One frontier row per cluster of `ncl` CTAs (ncl = 1: one CTA), CTA rank r
+// taking vocabulary slice r.  k <= 8: every CTA finds its slice's top-k, rank
+// 0 merges the ncl lists through distributed shared memory.  Wider: the
+// cluster runs the warped support's selection (maximum first, exchanged).
 __global__ void __launch_bounds__(kMssThreads)
-    tree_expand_kernel(const float* __restrict__ logits, int64_t V, int k, int32_t* __restrict__ tokens) {
+    tree_expand_kernel(const float* __restrict__ logits, int64_t V, int k, int ncl,
+                       int32_t* __restrict__ tokens) {
   pdl_trigger();
   pdl_wait();  // the previous kernel's results are visible from here on
   __shared__ __align__(16) float pub[2][4];
@@ -1375,18 +1390,79 @@ __global__ void __launch_bounds__(kMssThreads)
   __shared__ int li[kMssThreads * kExpandSmallK];
   __shared__ float rv[kMssWarps];
   __shared__ int ri[kMssWarps];
-  const float* row = logits + (size_t)blockIdx.x * (size_t)V;
-  int32_t* out = tokens + (size_t)blockIdx.x * k;
-  if (k <= 1) return expand_small<1>(row, V, k, out, lv, li, rv, ri);
-  if (k <= 2) return expand_small<2>(row, V, k, out, lv, li, rv, ri);
-  if (k <= 4) return expand_small<4>(row, V, k, out, lv, li, rv, ri);
-  if (k <= 8) return expand_small<8>(row, V, k, out, lv, li, rv, ri);
+  __shared__ float top_v[kExpandSmallK];
+  __shared__ int32_t top_i[kExpandSmallK];
+  const int f = blockIdx.x / ncl;
+  const int rank = blockIdx.x - f * ncl;  // == %cluster_ctarank for 1-D clusters of ncl
+  const float* row = logits + (size_t)f * (size_t)V;
+  int32_t* out = tokens + (size_t)f * k;
+  const int64_t per = (((V + ncl - 1) / ncl) + 3) & ~int64_t(3);
+  const int64_t lo = min(V, (int64_t)rank * per), hi = min(V, lo + per);
+  if (k <= kExpandSmallK) {
+    if (k <= 1) expand_small<1>(row, lo, hi, k, top_v, top_i, lv, li, rv, ri);
+    else if (k <= 2) expand_small<2>(row, lo, hi, k, top_v, top_i, lv, li, rv, ri);
+    else if (k <= 4) expand_small<4>(row, lo, hi, k, top_v, top_i, lv, li, rv, ri);
+    else expand_small<8>(row, lo, hi, k, top_v, top_i, lv, li, rv, ri);
+    if (ncl == 1) {
+      if (threadIdx.x < k) out[threadIdx.x] = top_i[threadIdx.x];
+      return;
+    }
+    __syncthreads();
+    cluster_sync_all();  // every CTA's list is in its shared memory
+    if (rank == 0 && threadIdx.x < 32) {
+      // The ncl lists (k entries each, at most 64 in all): lane l holds
+      // entries l and l + 32; k rounds of a warp argmax in ranking order.
+      const int lane = threadIdx.x, total = ncl * k;
+      float v0 = -INFINITY, v1 = -INFINITY;
+      int i0 = INT32_MAX, i1 = INT32_MAX;
+      if (lane < total) {
+        v0 = ld_dsmem_f32(mapa_shared(smem_u32(&top_v[lane % k]), (uint32_t)(lane / k)));
+        i0 = ld_dsmem_s32(mapa_shared(smem_u32(&top_i[lane % k]), (uint32_t)(lane / k)));
+      }
+      if (lane + 32 < total) {
+        v1 = ld_dsmem_f32(mapa_shared(smem_u32(&top_v[(lane + 32) % k]), (uint32_t)((lane + 32) / k)));
+        i1 = ld_dsmem_s32(mapa_shared(smem_u32(&top_i[(lane + 32) % k]), (uint32_t)((lane + 32) / k)));
+      }
+      for (int j = 0; j < k; ++j) {
+        const bool first = ranks_before(v0, i0, v1, i1) || i1 == INT32_MAX;
+        float v = first ? v0 : v1;
+        int id = first ? i0 : i1;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          const float ov = __shfl_xor_sync(0xffffffffu, v, o);
+          const int oi = __shfl_xor_sync(0xffffffffu, id, o);
+          if (ranks_before(ov, oi, v, id)) {
+            v = ov;
+            id = oi;
+          }
+        }
+        if (lane == 0) out[j] = id;
+        if (i0 == id) {  // indices are unique: exactly one entry leaves
+          v0 = -INFINITY;
+          i0 = INT32_MAX;
+        } else if (i1 == id) {
+          v1 = -INFINITY;
+          i1 = INT32_MAX;
+        }
+      }
+    }
+    cluster_sync_all();  // every CTA keeps its list until rank 0 has read it
+    return;
+  }
   float m = -INFINITY;
-  for (int64_t y = threadIdx.x; y < V; y += kMssThreads) m = fmaxf(m, __ldg(row + y));
+  for (int64_t y = lo + threadIdx.x; y < hi; y += kMssThreads) m = fmaxf(m, __ldg(row + y));
   m = block_max(m, red);
   int xk = 0;
-  warped_support(Slice{row, 0}, V, 0, V, 1.0f, m, k, 1.0f, 1, 0, xk, pub, sel);
-  for (int j = threadIdx.x; j < k; j += kMssThreads) tokens[(size_t)blockIdx.x * k + j] = sel.srt_i[j];
+  if (ncl > 1) {  // the row maximum over the cluster
+    if (threadIdx.x == 0) pub[0][0] = m;
+    cluster_sync_all();
+    for (int r = 0; r < ncl; ++r) m = fmaxf(m, ld_dsmem_f32(mapa_shared(smem_u32(&pub[0][0]), (uint32_t)r)));
+    ++xk;
+  }
+  warped_support(Slice{row, 0}, V, lo, hi, 1.0f, m, k, 1.0f, ncl, rank, xk, pub, sel);
+  if (rank == 0)
+    for (int j = threadIdx.x; j < k; j += kMssThreads) out[j] = sel.srt_i[j];
+  if (ncl > 1) cluster_sync_all();  // peers' candidate lists were read in the selection
 }
 
 // Merge (SpecInfer §3, merge-based token trees): the input trees of request b
@@ -1490,10 +1566,22 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// CTAs per frontier row: enough to fill the SMs when the frontier is small,
+// at most 8 (one portable cluster) and slices of at least kMssMinSlice.
+int expand_cluster_size(int64_t V, int32_t F, int num_sms) {
+  int64_t c = num_sms / (F > 0 ? F : 1);
+  const int64_t cap = (V + kMssMinSlice - 1) / kMssMinSlice;
+  c = c < cap ? c : cap;
+  c = c < kMssMaxCluster ? c : kMssMaxCluster;
+  return (int)(c < 1 ? 1 : c);
+}
+
 cudaError_t launch_tree_expand(const float* logits, int64_t V, int32_t F, int32_t k, int32_t* tokens,
-                               cudaStream_t st) {
+                               int num_sms, cudaStream_t st) {
   if (F == 0) return cudaSuccess;
-  return launch_pdl(tree_expand_kernel, dim3(F), dim3(kMssThreads), 0, st, 0u, logits, V, k, tokens);
+  const int ncl = expand_cluster_size(V, F, num_sms);
+  return launch_pdl(tree_expand_kernel, dim3((unsigned)(F * ncl)), dim3(kMssThreads), 0, st,
+                    ncl > 1 ? (unsigned)ncl : 0u, logits, V, k, ncl, tokens);
 }
 
 cudaError_t launch_tree_merge(const int32_t* parent, const int32_t* tokens, const int32_t* tree_offsets,
