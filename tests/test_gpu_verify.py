@@ -139,6 +139,30 @@ def test_stochastic_slices_staged_or_streamed(tsv, V, like_llm):
     compare_stochastic(r, ref, trees)
 
 
+@pytest.mark.parametrize("V,seed", [(32000, 32000), (160000, 160003)])  # seeds with no near tie
+def test_stochastic_vanishing_residual_keeps_p(tsv, V, seed):
+    """Proposal rows of all ones make every residual max(0, p - q) exactly zero,
+    so p must survive each rejection unchanged (the staged kernel writes the
+    residual over the spent proposals, never over p); a tiny accept uniform
+    then accepts a later child, and the bonus is drawn from the kept p."""
+    par = np.array([-1, 0, 0, 0, 0, 3, 3, 2], np.int32)
+    n = len(par)
+    trees = W.Trees(np.array([64], np.int32), np.array([0, n], np.int32), par, 64 + n)
+    rng = np.random.default_rng(seed)
+    llm = (rng.standard_normal((n, V)) * 2).astype(np.float32)
+    ssm = np.ones((n, V), np.float32)
+    tok = rng.integers(0, V, n).astype(np.int32)
+    ua = np.full(n, 0.5, np.float32)
+    ua[3] = 1e-12  # the third child of the root is accepted after two rejections;
+    # its two children are rejected too, and the bonus comes from its kept p
+    us = rng.random(n).astype(np.float32)
+    si = W.StochasticInputs(llm, ssm, tok, ua, us)
+    r = _stochastic(tsv, trees, si)
+    ref = oracle.verify_stochastic(llm, ssm, tok, par, trees.node_offsets, ua, us)
+    assert compare_stochastic(r, ref, trees) == 0
+    assert ref["path"][1] == 3 and ref["accept_len"][0] == 1 and ref["n_tried"][0] == 5
+
+
 def test_stochastic_temperature(tsv):
     spec = W.spec_variant(W.fuzz_spec(300), V=2000)
     trees = W.make_trees(spec)
