@@ -56,10 +56,13 @@ void order_slots(AttnPlan& p) {
   });
 }
 
+// CTAs of the rows-on-lanes kernel per (KV head, key chunk): each takes two
+// 128-row query tiles.
+inline int64_t tc_pairs(int32_t mtiles) { return (mtiles + 1) / 2; }
+
 // Splits every request's keys into chunks of one common length (a multiple of
-// the 64-key block) so that the CTAs fill whole waves of SMs: the estimated
-// makespan is waves * (chunk + per-CTA overhead), minimised over the chunk
-// counts that cut the longest request into 1 .. 64 pieces.
+// the 128-key block), over the chunk counts that cut the longest request into
+// 1 .. 64 pieces.
 void build_plan(AttnPlan& p, int num_sms, int32_t B, const int32_t* prefix_len,
                 const int32_t* node_offsets, int32_t Hq, int32_t Hkv, int32_t D, float scale) {
   memset(&p, 0, sizeof(p));
@@ -77,13 +80,17 @@ void build_plan(AttnPlan& p, int num_sms, int32_t B, const int32_t* prefix_len,
     p.mtiles[b] = (int32_t)cdiv((int64_t)p.nodes[b] * p.G, kBM);
     lmax = std::max<int64_t>(lmax, (int64_t)p.prefix[b] + p.nodes[b]);
   }
+  // Fewest chunks whose CTAs fill at least 3/4 of the SMs in one wave: every
+  // extra chunk adds partial rows to write and to merge, and the merge of a
+  // group runs in its last CTA.  Failing that, the least estimated makespan.
   const int64_t overhead = 2 * kBN;
-  int64_t best_cost = INT64_MAX, best_chunk = cdiv(lmax, kBN) * kBN;
+  int64_t best_cost = INT64_MAX, best_chunk = cdiv(lmax, kBN) * kBN, one_wave_chunk = 0;
   for (int pieces = 1; pieces <= 64; ++pieces) {
     const int64_t chunk = cdiv(cdiv(lmax, pieces), kBN) * kBN;
     int64_t units = 0;
     for (int b = 0; b < B; ++b)
-      units += (int64_t)Hkv * p.mtiles[b] * cdiv((int64_t)p.prefix[b] + p.nodes[b], chunk);
+      units += (int64_t)Hkv * tc_pairs(p.mtiles[b]) * cdiv((int64_t)p.prefix[b] + p.nodes[b], chunk);
+    if (one_wave_chunk == 0 && units <= num_sms && 4 * units >= 3 * (int64_t)num_sms) one_wave_chunk = chunk;
     const int64_t waves = cdiv(units, num_sms);
     const int64_t cost = waves * (chunk + overhead);
     if (cost < best_cost || (cost == best_cost && chunk > best_chunk)) {
@@ -92,6 +99,7 @@ void build_plan(AttnPlan& p, int num_sms, int32_t B, const int32_t* prefix_len,
     }
     if (chunk == kBN) break;
   }
+  if (one_wave_chunk > 0) best_chunk = one_wave_chunk;
   p.chunk_keys = (int32_t)best_chunk;
   order_slots(p);
   int64_t units = 0, rows = 0, ctrs = 0;
@@ -100,7 +108,7 @@ void build_plan(AttnPlan& p, int num_sms, int32_t B, const int32_t* prefix_len,
     const int64_t L = (int64_t)p.prefix[b] + p.nodes[b];
     p.n_chunks[b] = p.mtiles[b] > 0 ? (int32_t)cdiv(L, best_chunk) : 0;
     p.unit_start[s] = (int32_t)units;
-    units += (int64_t)Hkv * p.mtiles[b] * p.n_chunks[b];
+    units += (int64_t)Hkv * tc_pairs(p.mtiles[b]) * p.n_chunks[b];
     p.ctr_base[b] = (int32_t)ctrs;
     ctrs += (int64_t)Hkv * p.mtiles[b];
     if (p.n_chunks[b] > 1) {

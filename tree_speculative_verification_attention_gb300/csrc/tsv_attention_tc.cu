@@ -46,7 +46,7 @@ namespace tsv {
 constexpr int kTcSoftmaxThreads = 256;
 constexpr int kTcThreads = kTcSoftmaxThreads + 64;
 constexpr int kTcProducerWarp = 8, kTcMmaWarp = 9;
-constexpr int kHalfKeys = kBN / 2;         // keys of a block per softmax thread
+constexpr int kTcTiles = 2;                // query tiles of 128 rows per CTA
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: P stays below 2^8 between rescales
 constexpr int kBarTcSetup = 1;             // softmax warps + MMA warp
 constexpr int kBarTcSoftmax = 2;           // softmax warps
@@ -54,31 +54,37 @@ constexpr int kBarTcSoftmax = 2;           // softmax warps
 template <int D>
 struct TcCfg {
   static constexpr int kHalves = D / 64;      // 128-byte column groups per row
-  static constexpr int kKStages = 3, kVStages = 2;
-  static constexpr int kQBytes = kBM * D * 2;
+  static constexpr int kKStages = 2, kVStages = 2;
+  static constexpr int kQTileBytes = kBM * D * 2;
+  static constexpr int kQBytes = kTcTiles * kQTileBytes;
   static constexpr int kTileBytes = kBN * D * 2;  // one K (or V) block
   static constexpr int kAncWords = TSV_ANC_WORDS + 2;  // two zero words past the end
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kOffQ + kQBytes;
   static constexpr int kOffV = kOffK + kKStages * kTileBytes;
   static constexpr int kOffAnc = kOffV + kVStages * kTileBytes;
-  static constexpr int kOffPar = kOffAnc + kBM * kAncWords * 4;
-  static constexpr int kOffX = kOffPar + TSV_MAX_NODES * 4;  // float [4][128]: per-half row values
-  static constexpr int kOffBar = kOffX + 4 * kBM * 4;
-  // q_full, k_full[3], k_empty[3], v_full[2], v_empty[2], s_full[2],
-  // p_full[half][2], pv_done[half][2], mma_done
-  static constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + 2 + 4 + 4 + 1;
+  static constexpr int kOffPar = kOffAnc + kTcTiles * kBM * kAncWords * 4;
+  static constexpr int kOffBar = kOffPar + TSV_MAX_NODES * 4;
+  // q_full, k_full[S], k_empty[S], v_full[S], v_empty[S], s_full[tile],
+  // p_full[tile], pv_done[tile], mma_done
+  static constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + 3 * kTcTiles + 1;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + slack to align the base to 1024
-  static constexpr uint32_t kColO = 2 * kBN;               // S0 | S1 | O0 | O1 (D columns each)
+  static constexpr uint32_t kColO = kTcTiles * kBN;        // S0 | S1 | O0 | O1
   static constexpr uint32_t kTmemCols = 512;
   static_assert(kOffK % 1024 == 0 && kOffV % 1024 == 0 && kTileBytes % 1024 == 0, "swizzle atoms");
+  static_assert(kQTileBytes % 1024 == 0, "swizzle atoms");
   static_assert(kOffBar % 8 == 0, "mbarrier alignment");
-  static_assert(kColO + 2 * D <= kTmemCols, "TMEM columns");
-  static_assert(kKStages * kTileBytes >= (64 + 1) * kBM * 4, "merge weights fit in the K ring");
+  static_assert(kColO + kTcTiles * D <= kTmemCols, "TMEM columns");
+  static_assert(kOffV == kOffK + kKStages * kTileBytes, "the K and V rings are contiguous");
+  static_assert((kKStages + kVStages) * kTileBytes >= (64 + 1) * kBM * 4, "merge weights fit in the K/V rings");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 };
 
+// One 128-row query tile's softmax pass over key block j for the row on this
+// thread's TMEM lane: masked scores, base-2 online softmax with a lazily moved
+// reference maximum, O rescaled in TMEM when the reference moves, P (bf16)
+// written back over the tile's first 64 S columns.
 template <int D>
 __global__ void __launch_bounds__(kTcThreads, 1)
     tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
@@ -97,17 +103,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint8_t* sV = smem + C::kOffV;
   uint32_t* sAnc = reinterpret_cast<uint32_t*>(smem + C::kOffAnc);
   int32_t* sPar = reinterpret_cast<int32_t*>(smem + C::kOffPar);
-  float* sX = reinterpret_cast<float*>(smem + C::kOffX);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
   uint64_t* q_full = bars;
   uint64_t* k_full = q_full + 1;
   uint64_t* k_empty = k_full + SK;
   uint64_t* v_full = k_empty + SK;
   uint64_t* v_empty = v_full + SV;
-  uint64_t* s_full = v_empty + SV;
-  uint64_t* p_full = s_full + 2;   // [half][2]
-  uint64_t* pv_done = p_full + 4;  // [half][2]
-  uint64_t* mma_done = pv_done + 4;
+  uint64_t* s_full = v_empty + SV;       // [tile]
+  uint64_t* p_full = s_full + kTcTiles;  // [tile]
+  uint64_t* pv_done = p_full + kTcTiles;  // [tile]
+  uint64_t* mma_done = pv_done + kTcTiles;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   int* abort_flag = reinterpret_cast<int*>(smem + C::kOffMisc + 4);
   int* last_cta = reinterpret_cast<int*>(smem + C::kOffMisc + 8);
@@ -116,6 +121,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   // ---------------------------------------------------------------- the unit
+  // (request b, KV head g, key chunk c, tile pair tp): query rows
+  // [256 tp, 256 tp + 256) of the request, tile t = rows 256 tp + 128 t ...
   const int unit = blockIdx.x;
   int lo = 0, hi = plan.B;
   while (hi - lo > 1) {
@@ -125,15 +132,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int b = plan.slot_req[lo];
   const int local = unit - plan.unit_start[lo];
   const int mtiles = plan.mtiles[b], nch = plan.n_chunks[b];
-  const int mt = local % mtiles;
-  const int cg = local / mtiles;
+  const int pairs = (mtiles + kTcTiles - 1) / kTcTiles;
+  const int tp = local % pairs;
+  const int cg = local / pairs;
   const int c = cg % nch;
   const int g = cg / nch;
   const int G = plan.G;
   const int P = plan.prefix[b], n = plan.nodes[b], off = plan.node_off[b];
   const int R = n * G;
-  const int row0 = mt * kBM;
-  const int rows_valid = min(kBM, R - row0);
+  const int row0 = tp * kTcTiles * kBM;
+  const int ntiles = min(kTcTiles, mtiles - tp * kTcTiles);  // 1 or 2
   const int k_begin = c * plan.chunk_keys;
   const int k_end = min(P + n, k_begin + plan.chunk_keys);
   const int nblk = (k_end - k_begin + kBN - 1) / kBN;
@@ -148,10 +156,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(&v_full[s], 1);
       mbar_init(&v_empty[s], 1);
     }
-    for (int x = 0; x < 2; ++x) mbar_init(&s_full[x], 1);
-    for (int x = 0; x < 4; ++x) {
-      mbar_init(&p_full[x], kTcSoftmaxThreads / 2);  // every thread of the key half
-      mbar_init(&pv_done[x], 1);
+    for (int t = 0; t < kTcTiles; ++t) {
+      mbar_init(&s_full[t], 1);
+      mbar_init(&p_full[t], kBM);  // every thread of the tile
+      mbar_init(&pv_done[t], 1);
     }
     mbar_init(mma_done, 1);
     *abort_flag = 0;
@@ -162,16 +170,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   if (warp == kTcProducerWarp) {
     // ------------------------------------------------------------ producer
-    const uint64_t pol = mtiles > 1 ? l2_policy_evict_last() : l2_policy_evict_first();
+    const uint64_t pol = mtiles > kTcTiles ? l2_policy_evict_last() : l2_policy_evict_first();
     if (lane == 0) {
       tma_prefetch_desc(&tmap_q);
       tma_prefetch_desc(&tmap_k);
-      // Q tile: box (64 d, G heads, 128/G nodes) lands as 128 rows r = node*G + head.
-      mbar_arrive_expect_tx(q_full, C::kQBytes);
+      // Q tile t: box (64 d, G heads, 128/G nodes) lands as 128 rows r = node*G + head.
+      mbar_arrive_expect_tx(q_full, ntiles * C::kQTileBytes);
+      for (int t = 0; t < ntiles; ++t)
 #pragma unroll
-      for (int hf = 0; hf < C::kHalves; ++hf)
-        tma_load_3d(sQ + hf * (kBM * 128), &tmap_q, q_full, hf * 64, g * G, off + row0 / G,
-                    l2_policy_evict_first());
+        for (int hf = 0; hf < C::kHalves; ++hf)
+          tma_load_3d(sQ + t * C::kQTileBytes + hf * (kBM * 128), &tmap_q, q_full, hf * 64, g * G,
+                      off + (row0 + t * kBM) / G, l2_policy_evict_first());
       int issued = 0;
       for (int j = 0; j < nblk; ++j) {
         const int st = j % SK;
@@ -221,68 +230,77 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const uint64_t dq = sdesc_sw128(smem_u32(sQ), 16, 1024);
       const uint64_t dk = sdesc_sw128(smem_u32(sK), 16, 1024);
       const uint64_t dv = sdesc_sw128(smem_u32(sV), kBN * 128, 1024);
-      auto issue_s = [&](int j) {
-        const uint32_t dst = tmem + (uint32_t)((j & 1) * kBN);
+      // S_t = Q_t K(j)^T into the tile's S columns.
+      auto issue_s = [&](int t, int j) {
+        const uint32_t dst = tmem + (uint32_t)(t * kBN);
+        const uint64_t da = dq + (uint64_t)((t * C::kQTileBytes) >> 4);
         const uint64_t db = dk + (uint64_t)(((j % SK) * C::kTileBytes) >> 4);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t ao = ((kk >> 2) * (kBM * 128) + (kk & 3) * 32) >> 4;
           const uint32_t bo = ((kk >> 2) * (kBN * 128) + (kk & 3) * 32) >> 4;
-          umma_bf16(dst, dq + ao, db + bo, idS, kk > 0 ? 1u : 0u);
+          umma_bf16(dst, da + ao, db + bo, idS, kk > 0 ? 1u : 0u);
         }
-        umma_commit(&s_full[j & 1]);
-        umma_commit(&k_empty[j % SK]);  // K(j) is free once S(j) has read it
+        umma_commit(&s_full[t]);
       };
-      auto issue_pv = [&](int h, int j) {
-        // P_h sits over the first 32 of key half h's 64 S columns; V_h is rows
-        // 64h .. 64h+63 of the V block.
-        const uint32_t pa = tmem + (uint32_t)((j & 1) * kBN + h * kHalfKeys);
-        const uint64_t db = dv + (uint64_t)(((j % SV) * C::kTileBytes + h * kHalfKeys * 128) >> 4);
+      // O_t += P_t V(j): P_t (128 keys, bf16, two per column) over the tile's
+      // first 64 S columns, read from TMEM.
+      auto issue_pv = [&](int t, int j) {
+        const uint32_t pa = tmem + (uint32_t)(t * kBN);
+        const uint64_t db = dv + (uint64_t)(((j % SV) * C::kTileBytes) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < kHalfKeys / 16; ++kk)
-          umma_bf16_ts(tmem + C::kColO + h * D, pa + kk * 8, db + (uint32_t)((kk * 16 * 128) >> 4), idPV,
+        for (int kk = 0; kk < kBN / 16; ++kk)
+          umma_bf16_ts(tmem + C::kColO + t * D, pa + kk * 8, db + (uint32_t)((kk * 16 * 128) >> 4), idPV,
                        (j > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(&pv_done[2 * h + (j & 1)]);
+        umma_commit(&pv_done[t]);
       };
+      // Order: S_0(0) S_1(0), then per block PV_0(j) S_0(j+1) PV_1(j) S_1(j+1):
+      // while one tile's softmax runs, the tensor pipe works for the other.
       bool ok = nblk > 0 && mbar_wait(q_full, 0, abort_v) && mbar_wait(&k_full[0], 0, abort_v);
       if (ok) {
         tc_fence_after();
-        issue_s(0);
+        for (int t = 0; t < ntiles; ++t) issue_s(t, 0);
+        umma_commit(&k_empty[0]);
       }
       for (int j = 0; ok && j < nblk; ++j) {
-        if (j + 1 < nblk) {
+        const bool more = j + 1 < nblk;
+        if (!mbar_wait(&v_full[j % SV], (j / SV) & 1, abort_v)) break;
+        if (!mbar_wait(&p_full[0], j & 1, abort_v)) break;
+        tc_fence_after();
+        issue_pv(0, j);
+        if (more) {
           if (!mbar_wait(&k_full[(j + 1) % SK], ((j + 1) / SK) & 1, abort_v)) break;
           tc_fence_after();
-          issue_s(j + 1);
+          issue_s(0, j + 1);
         }
-        if (!mbar_wait(&v_full[j % SV], (j / SV) & 1, abort_v)) break;
-        for (int h = 0; ok && h < 2; ++h) {
-          if (!mbar_wait(&p_full[2 * h + (j & 1)], (j >> 1) & 1, abort_v)) {
-            ok = false;
-            break;
-          }
+        if (ntiles > 1) {
+          if (!mbar_wait(&p_full[1], j & 1, abort_v)) break;
           tc_fence_after();
-          issue_pv(h, j);
+          issue_pv(1, j);
         }
-        if (ok) umma_commit(&v_empty[j % SV]);
+        umma_commit(&v_empty[j % SV]);
+        if (more) {
+          if (ntiles > 1) issue_s(1, j + 1);
+          umma_commit(&k_empty[(j + 1) % SK]);
+        }
       }
       umma_commit(mma_done);  // every MMA of this CTA has finished before TMEM is freed
       mbar_wait(mma_done, 0, nullptr);
     }
   } else {
     // ------------------------------------------------------------ softmax
-    const int hk = warp >> 2;       // key half of every block
-    const int r = tid & (kBM - 1);  // row = TMEM lane
+    const int t = warp >> 2;        // query tile
+    const int r = tid & (kBM - 1);  // row of the tile = TMEM lane
+    const int rows_valid = min(kBM, R - (row0 + t * kBM));  // <= 0 for a missing tile
     const bool valid = r < rows_valid;
-    // Ancestor bitset of this row's node (built by the half-0 thread of the row).
-    uint32_t* arow = sAnc + r * C::kAncWords;
-    if (hk == 0) {
+    const int grow = row0 + t * kBM + r;  // row of the request
+    // Ancestor bitset of this row's node.
+    uint32_t* arow = sAnc + (t * kBM + r) * C::kAncWords;
 #pragma unroll
-      for (int w = 0; w < C::kAncWords; ++w) arow[w] = 0u;
-    }
+    for (int w = 0; w < C::kAncWords; ++w) arow[w] = 0u;
     if (anc != nullptr) {
-      if (valid && hk == 0) {
-        const uint4* src = reinterpret_cast<const uint4*>(anc + (size_t)(off + (row0 + r) / G) * TSV_ANC_WORDS);
+      if (valid) {
+        const uint4* src = reinterpret_cast<const uint4*>(anc + (size_t)(off + grow / G) * TSV_ANC_WORDS);
         const uint4 a0 = __ldg(src), a1 = __ldg(src + 1);
         arow[0] = a0.x; arow[1] = a0.y; arow[2] = a0.z; arow[3] = a0.w;
         arow[4] = a1.x; arow[5] = a1.y; arow[6] = a1.z; arow[7] = a1.w;
@@ -297,45 +315,53 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       const bool bad = named_bar_or(kBarTcSoftmax, kTcSoftmaxThreads, tid < n && (p < -1 || p >= tid));
       if (local == 0 && tid == 0) status[b] = bad ? TSV_ERR_BAD_TREE : TSV_OK;
-      if (valid && hk == 0 && !bad)
-        for (int a = (row0 + r) / G; a >= 0; a = sPar[a]) arow[a >> 5] |= 1u << (a & 31);
+      if (valid && !bad)
+        for (int a = grow / G; a >= 0; a = sPar[a]) arow[a >> 5] |= 1u << (a & 31);
     }
     tc_fence_before();
     named_bar(kBarTcSetup, kTcSoftmaxThreads + 32);
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const uint32_t trow = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-    const uint32_t o_mine = trow + C::kColO + (uint32_t)(hk * D);  // O_h of this row
-    uint64_t* p_mine = p_full + 2 * hk;
-    uint64_t* pv_mine = pv_done + 2 * hk;
+    const uint32_t sbuf = trow + (uint32_t)(t * kBN);               // S_t / P_t of this row
+    const uint32_t o_mine = trow + C::kColO + (uint32_t)(t * D);    // O_t of this row
     const float sl2 = plan.scale_log2;
     float m_ref = -INFINITY, l = 0.f;
     // No barrier inside the loop: a timed-out wait ends this warp's loop
     // (every wait is bounded and sets the CTA's abort flag, so the other
     // warps' waits end quickly too); the CTA agrees after the loop.
     bool ok = true;
-    for (int j = 0; j < nblk; ++j) {
-      if (!__all_sync(0xffffffffu, mbar_wait(&s_full[j & 1], (j >> 1) & 1, abort_v))) {
+    const bool active = t < ntiles;
+    for (int j = 0; active && j < nblk; ++j) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&s_full[t], j & 1, abort_v))) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const uint32_t sbuf = trow + (uint32_t)((j & 1) * kBN + hk * kHalfKeys);
-      float s[kHalfKeys];
-      tmem_ld32(sbuf, *reinterpret_cast<float(*)[32]>(&s[0]));
-      tmem_ld32(sbuf + 32, *reinterpret_cast<float(*)[32]>(&s[32]));
-      const int key0 = k_begin + j * kBN + hk * kHalfKeys;  // this half's first key
-      if (key0 + kHalfKeys > P) {  // uniform per warp: the half reaches the tree keys
-        const uint64_t vis = valid ? block_visibility(arow, key0 - P) : 0ull;
+      float s[kBN];
 #pragma unroll
-        for (int e = 0; e < kHalfKeys; ++e) s[e] = ((vis >> e) & 1ull) ? s[e] : -INFINITY;
+      for (int q4 = 0; q4 < kBN / 32; ++q4) tmem_ld32(sbuf + 32 * q4, *reinterpret_cast<float(*)[32]>(&s[32 * q4]));
+      const int key0 = k_begin + j * kBN;  // this block's first key
+      if (key0 + kBN > P) {  // uniform: the block reaches the tree keys (or the end)
+        // Keys key0 + e are visible iff e < k_end - key0 and they are prefix
+        // keys or the row's node and its ancestors.
+        const int lim = k_end - key0;  // 1 .. 128
+        const uint64_t m0 = lim >= 64 ? ~0ull : ((1ull << lim) - 1ull);
+        const uint64_t m1 = lim >= 128 ? ~0ull : (lim > 64 ? ((1ull << (lim - 64)) - 1ull) : 0ull);
+        const uint64_t v0 = valid ? block_visibility(arow, key0 - P) & m0 : 0ull;
+        const uint64_t v1 = (valid && lim > 64) ? block_visibility(arow, key0 + 64 - P) & m1 : 0ull;
+#pragma unroll
+        for (int e = 0; e < 64; ++e) {
+          s[e] = ((v0 >> e) & 1ull) ? s[e] : -INFINITY;
+          s[64 + e] = ((v1 >> e) & 1ull) ? s[64 + e] : -INFINITY;
+        }
       } else if (!valid) {
 #pragma unroll
-        for (int e = 0; e < kHalfKeys; ++e) s[e] = -INFINITY;
+        for (int e = 0; e < kBN; ++e) s[e] = -INFINITY;
       }
       float mx[4] = {s[0], s[1], s[2], s[3]};
 #pragma unroll
-      for (int e = 4; e < kHalfKeys; ++e) mx[e & 3] = fmaxf(mx[e & 3], s[e]);
+      for (int e = 4; e < kBN; ++e) mx[e & 3] = fmaxf(mx[e & 3], s[e]);
       // Raw maximum times the (positive) scale = maximum of the scaled scores.
       const float hmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl2;
       // Move the reference only when a score exceeds it by more than the
@@ -347,9 +373,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       l *= alpha;
       if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
-        // O_h must hold PV_h(j-1) before it is rescaled (lanes with alpha = 1
+        // O_t must hold PV_t(j-1) before it is rescaled (lanes with alpha = 1
         // rewrite their row unchanged: TMEM loads and stores are warp-wide).
-        if (!__all_sync(0xffffffffu, mbar_wait(&pv_mine[(j - 1) & 1], ((j - 1) >> 1) & 1, abort_v))) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&pv_done[t], (j - 1) & 1, abort_v))) {
           ok = false;
           break;
         }
@@ -364,182 +390,170 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
       }
       const float neg_ref = m_ref == -INFINITY ? 0.f : -m_ref;
-      uint32_t h0[16], h1[16];
       float ps[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int e = 0; e < kHalfKeys; e += 2) {
-        const float p0 = fast_exp2(fmaf(s[e], sl2, neg_ref));
-        const float p1 = fast_exp2(fmaf(s[e + 1], sl2, neg_ref));
-        ps[(e >> 1) & 3] += p0 + p1;
-        if (e < 32) h0[e >> 1] = pack_bf16x2(p0, p1);
-        else h1[(e - 32) >> 1] = pack_bf16x2(p0, p1);
+      for (int hh = 0; hh < 4; ++hh) {  // 32 keys -> 16 P columns at a time
+        uint32_t h[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          const float p0 = fast_exp2(fmaf(s[32 * hh + e], sl2, neg_ref));
+          const float p1 = fast_exp2(fmaf(s[32 * hh + e + 1], sl2, neg_ref));
+          ps[(e >> 1) & 3] += p0 + p1;
+          h[e >> 1] = pack_bf16x2(p0, p1);
+        }
+        tmem_st16u(sbuf + 16 * hh, h);
       }
       l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
-      // P (bf16, two per column) over the first 32 of this thread's 64 S columns.
-      tmem_st16u(sbuf, h0);
-      tmem_st16u(sbuf + 16, h1);
       // V rows of the last block past the request's keys may hold anything
-      // (even NaN): once the block has landed, each half zeroes the rows its
-      // own PV reads, so that 0 * garbage never reaches O.
-      const int vrows = k_end - (k_begin + j * kBN);
-      if (vrows < kBN) {
-        const int first = max(vrows, hk * kHalfKeys), last = (hk + 1) * kHalfKeys;
-        if (first < last) {
-          if (!__all_sync(0xffffffffu, mbar_wait(&v_full[j % SV], (j / SV) & 1, abort_v))) {
-            ok = false;
-            break;
-          }
-          uint8_t* vt = sV + (j % SV) * C::kTileBytes;
-          const int pieces = (last - first) * C::kHalves * 8;
-          for (int q = r; q < pieces; q += kBM) {
-            const int row = first + q / (C::kHalves * 8);
-            const int rem = q % (C::kHalves * 8);
-            *reinterpret_cast<uint4*>(vt + (rem >> 3) * (kBN * 128) + row * 128 + ((rem & 7) << 4)) =
-                make_uint4(0u, 0u, 0u, 0u);
-          }
-          fence_proxy_async_smem();
+      // (even NaN): once the block has landed, tile 0 zeroes them before
+      // either tile's PV reads the block (PV_1 follows PV_0), so that
+      // 0 * garbage never reaches O.
+      const int vrows = k_end - key0;
+      if (t == 0 && vrows < kBN) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&v_full[j % SV], (j / SV) & 1, abort_v))) {
+          ok = false;
+          break;
         }
+        uint8_t* vt = sV + (j % SV) * C::kTileBytes;
+        const int pieces = (kBN - vrows) * C::kHalves * 8;
+        for (int q = r; q < pieces; q += kBM) {
+          const int row = vrows + q / (C::kHalves * 8);
+          const int rem = q % (C::kHalves * 8);
+          *reinterpret_cast<uint4*>(vt + (rem >> 3) * (kBN * 128) + row * 128 + ((rem & 7) << 4)) =
+              make_uint4(0u, 0u, 0u, 0u);
+        }
+        fence_proxy_async_smem();
       }
       tc_fence_before();
-      mbar_arrive(&p_mine[j & 1]);
+      mbar_arrive(&p_full[t]);
     }
     pdl_trigger();  // the main loop is done: let the next kernel be scheduled
-    // Both halves' last PV must be complete before the epilogue reads O0 and O1.
-    if (ok && nblk > 0) {
-      const int jl = nblk - 1;
-      ok = __all_sync(0xffffffffu, mbar_wait(&pv_done[jl & 1], (jl >> 1) & 1, abort_v) &&
-                                       mbar_wait(&pv_done[2 + (jl & 1)], (jl >> 1) & 1, abort_v));
-    }
-    // Agree on success CTA-wide: the epilogue has barriers that all 256
+    // The tile's last PV must be complete before the epilogue reads O_t.
+    if (active && ok && nblk > 0)
+      ok = __all_sync(0xffffffffu, mbar_wait(&pv_done[t], (nblk - 1) & 1, abort_v));
+    // Agree on success CTA-wide: the merge below has barriers that all 256
     // softmax threads must reach.
-    ok = !named_bar_or(kBarTcSoftmax, kTcSoftmaxThreads, !ok);
+    ok = !named_bar_or(kBarTcSoftmax, kTcSoftmaxThreads, active && !ok);
     if (ok && nblk > 0) {
       tc_fence_after();
-      // Combine the halves of each row: weights 2^(m_h - M), sum L (the same
-      // order in both threads of a row).
-      sX[hk * kBM + r] = m_ref;
-      sX[(2 + hk) * kBM + r] = l;
-      named_bar(kBarTcSoftmax, kTcSoftmaxThreads);
-      const float m0 = sX[r], m1 = sX[kBM + r];
-      const float M = fmaxf(m0, m1);
-      const float w0 = m0 == -INFINITY ? 0.f : fast_exp2(m0 - M);
-      const float w1 = m1 == -INFINITY ? 0.f : fast_exp2(m1 - M);
-      const float L = w0 * sX[2 * kBM + r] + w1 * sX[3 * kBM + r];
-      const float inv_l = L > 0.f ? 1.f / L : 0.f;
-      const float c0 = w0 * inv_l, c1 = w1 * inv_l;
-      const int gr = row0 + r;
-      const int node = gr / G;
-      const int h = g * G + (gr - node * G);
-      constexpr int kOHalf = D / 2;  // output columns this thread writes
-      const uint32_t oc0 = trow + C::kColO + (uint32_t)(hk * kOHalf);
+      const float inv_l = l > 0.f ? 1.f / l : 0.f;
+      const int node = grow / G;
+      const int h = g * G + (grow - node * G);
       if (nch == 1) {
-        __nv_bfloat16* dst = out + ((size_t)(off + node) * plan.Hq + h) * D + hk * kOHalf;
+        if (active) {
+          __nv_bfloat16* dst = out + ((size_t)(off + node) * plan.Hq + h) * D;
 #pragma unroll 1
-        for (int cc = 0; cc < kOHalf; cc += 32) {
-          float o[32], o1[32];
-          tmem_ld32(oc0 + cc, o);
-          tmem_ld32(oc0 + D + cc, o1);
-          if (valid) {
-            uint4* d4 = reinterpret_cast<uint4*>(dst + cc);
+          for (int cc = 0; cc < D; cc += 32) {
+            float o[32];
+            tmem_ld32(o_mine + cc, o);
+            if (valid) {
+              uint4* d4 = reinterpret_cast<uint4*>(dst + cc);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              float v[8];
-#pragma unroll
-              for (int x = 0; x < 8; ++x) v[x] = c0 * o[8 * e + x] + c1 * o1[8 * e + x];
-              d4[e] = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
-                                 pack_bf16x2(v[6], v[7]));
+              for (int e = 0; e < 4; ++e)
+                d4[e] = make_uint4(pack_bf16x2(o[8 * e] * inv_l, o[8 * e + 1] * inv_l),
+                                   pack_bf16x2(o[8 * e + 2] * inv_l, o[8 * e + 3] * inv_l),
+                                   pack_bf16x2(o[8 * e + 4] * inv_l, o[8 * e + 5] * inv_l),
+                                   pack_bf16x2(o[8 * e + 6] * inv_l, o[8 * e + 7] * inv_l));
             }
           }
         }
       } else {
         // Partial of this chunk, then the group's last CTA merges all chunks.
         const int64_t base0 = plan.part_row[b] + (int64_t)g * nch * R;
-        const int64_t prow_i = base0 + (int64_t)c * R + gr;
-        float* dst = part_o + prow_i * D + hk * kOHalf;
+        if (active) {
+          const int64_t prow_i = base0 + (int64_t)c * R + grow;
+          float* dst = part_o + prow_i * D;
 #pragma unroll 1
-        for (int cc = 0; cc < kOHalf; cc += 32) {
-          float o[32], o1[32];
-          tmem_ld32(oc0 + cc, o);
-          tmem_ld32(oc0 + D + cc, o1);
-          if (valid) {
-            float4* d4 = reinterpret_cast<float4*>(dst + cc);
+          for (int cc = 0; cc < D; cc += 32) {
+            float o[32];
+            tmem_ld32(o_mine + cc, o);
+            if (valid) {
+              float4* d4 = reinterpret_cast<float4*>(dst + cc);
 #pragma unroll
-            for (int e = 0; e < 8; ++e)
-              d4[e] = make_float4(c0 * o[4 * e] + c1 * o1[4 * e], c0 * o[4 * e + 1] + c1 * o1[4 * e + 1],
-                                  c0 * o[4 * e + 2] + c1 * o1[4 * e + 2], c0 * o[4 * e + 3] + c1 * o1[4 * e + 3]);
+              for (int e = 0; e < 8; ++e)
+                d4[e] = make_float4(o[4 * e] * inv_l, o[4 * e + 1] * inv_l, o[4 * e + 2] * inv_l,
+                                    o[4 * e + 3] * inv_l);
+            }
           }
+          if (valid) part_lse[prow_i] = l > 0.f ? m_ref + log2f(l) : -INFINITY;
         }
-        if (valid && hk == 0) part_lse[prow_i] = L > 0.f ? M + log2f(L) : -INFINITY;
         __threadfence();
         named_bar(kBarTcSoftmax, kTcSoftmaxThreads);
-        int32_t* ctr = counters + plan.ctr_base[b] + g * mtiles + mt;
+        int32_t* ctr = counters + plan.ctr_base[b] + g * mtiles + tp;
         if (tid == 0) *last_cta = atomicAdd(ctr, 1) == nch - 1;
         named_bar(kBarTcSoftmax, kTcSoftmaxThreads);
         if (*last_cta) {
           __threadfence();
-          // Merge: first the chunk weights of every row (the idle K ring holds
-          // them: [chunk][row] weights, then [row] inverse sums), then rows x
-          // 4-column groups, four groups x four chunks of loads in flight.
+          // Merge, one tile at a time: first the chunk weights of every row
+          // (the idle K/V rings hold them: [chunk][row] weights, then [row]
+          // inverse sums), then rows x 4-column groups, four groups x four
+          // chunks of loads in flight.
           float* sW = reinterpret_cast<float*>(sK);
-          if (tid < rows_valid) {
-            const float* lse = part_lse + base0 + row0 + tid;
-            float M2 = -INFINITY;
+          for (int tt = 0; tt < ntiles; ++tt) {
+            const int trow0 = row0 + tt * kBM;
+            const int trows = min(kBM, R - trow0);
+            if (tid < trows) {
+              const float* lse = part_lse + base0 + trow0 + tid;
+              float M2 = -INFINITY;
 #pragma unroll 8
-            for (int cc = 0; cc < nch; ++cc) M2 = fmaxf(M2, __ldcg(lse + (int64_t)cc * R));
-            float wsum = 0.f;
+              for (int cc = 0; cc < nch; ++cc) M2 = fmaxf(M2, __ldcg(lse + (int64_t)cc * R));
+              float wsum = 0.f;
 #pragma unroll 8
-            for (int cc = 0; cc < nch; ++cc) {
-              const float x = __ldcg(lse + (int64_t)cc * R);
-              const float w = x == -INFINITY ? 0.f : fast_exp2(x - M2);
-              sW[cc * kBM + tid] = w;
-              wsum += w;
+              for (int cc = 0; cc < nch; ++cc) {
+                const float x = __ldcg(lse + (int64_t)cc * R);
+                const float w = x == -INFINITY ? 0.f : fast_exp2(x - M2);
+                sW[cc * kBM + tid] = w;
+                wsum += w;
+              }
+              sW[64 * kBM + tid] = wsum > 0.f ? 1.f / wsum : 0.f;
             }
-            sW[64 * kBM + tid] = wsum > 0.f ? 1.f / wsum : 0.f;
-          }
-          named_bar(kBarTcSoftmax, kTcSoftmaxThreads);
-          constexpr int D4 = D / 4;
-          const int items = rows_valid * D4;
-          const int64_t cstride = (int64_t)R * D;  // floats between chunks of a row
-          for (int i0 = tid; i0 < items; i0 += 4 * kTcSoftmaxThreads) {
-            float4 acc[4];
-            int rr[4];
-            const float* src[4];
+            named_bar(kBarTcSoftmax, kTcSoftmaxThreads);
+            constexpr int D4 = D / 4;
+            const int items = trows * D4;
+            const int64_t cstride = (int64_t)R * D;  // floats between chunks of a row
+            for (int i0 = tid; i0 < items; i0 += 4 * kTcSoftmaxThreads) {
+              float4 acc[4];
+              int rr[4];
+              const float* src[4];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const int i = min(i0 + u * kTcSoftmaxThreads, items - 1);  // clamped: duplicates are harmless
-              rr[u] = i / D4;
-              src[u] = part_o + (base0 + row0 + rr[u]) * D + (i - rr[u] * D4) * 4;
-              acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+              for (int u = 0; u < 4; ++u) {
+                const int i = min(i0 + u * kTcSoftmaxThreads, items - 1);  // clamped: duplicates are harmless
+                rr[u] = i / D4;
+                src[u] = part_o + (base0 + trow0 + rr[u]) * D + (i - rr[u] * D4) * 4;
+                acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+              }
+              for (int c0 = 0; c0 < nch; c0 += 4) {
+                float4 v[4][4];
+#pragma unroll
+                for (int k2 = 0; k2 < 4; ++k2)
+#pragma unroll
+                  for (int u = 0; u < 4; ++u)
+                    if (c0 + k2 < nch)
+                      v[k2][u] = __ldcg(reinterpret_cast<const float4*>(src[u] + (c0 + k2) * cstride));
+#pragma unroll
+                for (int k2 = 0; k2 < 4; ++k2)
+#pragma unroll
+                  for (int u = 0; u < 4; ++u)
+                    if (c0 + k2 < nch) {
+                      const float w = sW[(c0 + k2) * kBM + rr[u]];
+                      acc[u].x += w * v[k2][u].x;
+                      acc[u].y += w * v[k2][u].y;
+                      acc[u].z += w * v[k2][u].z;
+                      acc[u].w += w * v[k2][u].w;
+                    }
+              }
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const int i = i0 + u * kTcSoftmaxThreads;
+                if (i >= items) break;
+                const float inv = sW[64 * kBM + rr[u]];
+                const int grr = trow0 + rr[u], nd = grr / G, hh = g * G + (grr - nd * G);
+                __nv_bfloat16* o = out + ((size_t)(off + nd) * plan.Hq + hh) * D + (i - rr[u] * D4) * 4;
+                *reinterpret_cast<uint2*>(o) = make_uint2(pack_bf16x2(acc[u].x * inv, acc[u].y * inv),
+                                                          pack_bf16x2(acc[u].z * inv, acc[u].w * inv));
+              }
             }
-            for (int c0 = 0; c0 < nch; c0 += 4) {
-              float4 v[4][4];
-#pragma unroll
-              for (int k2 = 0; k2 < 4; ++k2)
-#pragma unroll
-                for (int u = 0; u < 4; ++u)
-                  if (c0 + k2 < nch) v[k2][u] = __ldcg(reinterpret_cast<const float4*>(src[u] + (c0 + k2) * cstride));
-#pragma unroll
-              for (int k2 = 0; k2 < 4; ++k2)
-#pragma unroll
-                for (int u = 0; u < 4; ++u)
-                  if (c0 + k2 < nch) {
-                    const float w = sW[(c0 + k2) * kBM + rr[u]];
-                    acc[u].x += w * v[k2][u].x;
-                    acc[u].y += w * v[k2][u].y;
-                    acc[u].z += w * v[k2][u].z;
-                    acc[u].w += w * v[k2][u].w;
-                  }
-            }
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const int i = i0 + u * kTcSoftmaxThreads;
-              if (i >= items) break;
-              const float inv = sW[64 * kBM + rr[u]];
-              const int grr = row0 + rr[u], nd = grr / G, hh = g * G + (grr - nd * G);
-              __nv_bfloat16* o = out + ((size_t)(off + nd) * plan.Hq + hh) * D + (i - rr[u] * D4) * 4;
-              *reinterpret_cast<uint2*>(o) = make_uint2(pack_bf16x2(acc[u].x * inv, acc[u].y * inv),
-                                                        pack_bf16x2(acc[u].z * inv, acc[u].w * inv));
-            }
+            named_bar(kBarTcSoftmax, kTcSoftmaxThreads);  // sW is rewritten for the next tile
           }
           if (tid == 0) *ctr = 0;  // leave the counter zeroed for the next call
         }
