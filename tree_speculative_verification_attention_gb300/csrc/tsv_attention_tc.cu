@@ -9,33 +9,32 @@
 // Implementation) becomes a split of each request's keys into chunks whose
 // partial results are merged by log-sum-exp.
 //
-// One CTA = one unit (request b, KV head g, key chunk c, M-tile mt).  Its 128
-// query rows are (node, head-in-group) pairs: all query heads that share KV
-// head g sit in the same tiles, so each streamed K/V row serves every tree
-// node and every grouped head at once.  Keys go in blocks of 128, so both
-// MMAs of a block have N >= 128 (smaller N runs the tensor pipe below its
-// rate).  Warp roles (320 threads):
-//   warp 8        TMA producer.  Lane 0: the Q tile, then K blocks into a
-//                 3-stage ring, each released as soon as S has read it; lane
-//                 1: V blocks into a 2-stage ring, released after PV.
-//   warp 9        tcgen05 issuer and TMEM owner (S0 | S1 | O0 | O1): S(j+1) =
-//                 Q K^T is issued before PV(j), so the next scores are ready
-//                 when the softmax of a block ends; O_h += P_h V_h reads P_h
-//                 from TMEM, one accumulator per key half.
-//   warps 0-7     softmax.  Warp w serves the rows on TMEM lanes 32(w%4).. and
-//                 key half h = w/4 (64 keys) of every block.  The two halves
-//                 of a row are independent online softmaxes (own reference
-//                 maximum, row sum and O accumulator), so no barrier is needed
-//                 inside the loop; they are combined once at the end.  Set-up:
-//                 the ancestor bitset of the row's node (prepared, or by
-//                 walking parent[] up to the root).  Loop: read S, mask the
-//                 tree part of the keys with the bitset, base-2 softmax with a
-//                 lazily moved reference maximum, P in bf16 written back over
-//                 the thread's own S columns, O_h rescaled in TMEM when the
-//                 reference moves.  End: combine the halves, normalise and
-//                 store; when a request's keys are split over several CTAs,
-//                 store a partial + log2-sum-exp and let the last CTA of the
-//                 group (atomic counter, no waiting) merge the partials.
+// One CTA = one unit (request b, KV head g, key chunk c, tile pair tp): two
+// query tiles of 128 rows, rows = (node, head-in-group) pairs, so all query
+// heads that share KV head g sit in the same tiles and each streamed K/V row
+// serves every tree node and every grouped head of both tiles at once.  Keys
+// go in blocks of 128, so both MMAs of a block have N >= 128 (smaller N runs
+// the tensor pipe below its rate).  Warp roles (320 threads):
+//   warp 8        TMA producer.  Lane 0: both Q tiles, then K blocks into a
+//                 2-stage ring, each released once both tiles' S have read
+//                 it; lane 1: V blocks into a 2-stage ring, released after
+//                 both tiles' PV.
+//   warp 9        tcgen05 issuer and TMEM owner (S_0 | S_1 | O_0 | O_1).
+//                 Per block j it issues PV_0(j), S_0(j+1), PV_1(j), S_1(j+1):
+//                 while one tile's softmax runs, the tensor pipe works for the
+//                 other.  O_t += P_t V reads P_t from TMEM.
+//   warps 0-7     softmax.  Warps 0-3 serve tile 0 and warps 4-7 tile 1; each
+//                 thread owns the row on its TMEM lane and all 128 keys of a
+//                 block.  Set-up: the ancestor bitset of the row's node
+//                 (prepared, or by walking parent[] up to the root).  Loop:
+//                 read S, mask the tree part of the keys with the bitset (and
+//                 keys past the chunk by count), base-2 online softmax with a
+//                 lazily moved reference maximum, O_t rescaled in TMEM when
+//                 the reference moves, P in bf16 written back over the tile's
+//                 S columns.  End: normalise and store; when a request's keys
+//                 are split over several CTAs, store a partial + log2-sum-exp
+//                 and let the last CTA of the group (atomic counter, no
+//                 waiting) merge the partials.
 #include <cuda_bf16.h>
 #include <math.h>
 
@@ -81,10 +80,6 @@ struct TcCfg {
   static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 };
 
-// One 128-row query tile's softmax pass over key block j for the row on this
-// thread's TMEM lane: masked scores, base-2 online softmax with a lazily moved
-// reference maximum, O rescaled in TMEM when the reference moves, P (bf16)
-// written back over the tile's first 64 S columns.
 template <int D>
 __global__ void __launch_bounds__(kTcThreads, 1)
     tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
