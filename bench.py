@@ -205,6 +205,7 @@ KERNEL_SOURCES = {
     # headers it includes and the host planner that cuts the work.
     "tree_attn_keys_kernel": ["tsv_attention_keys.cu"],
     "tree_attn_tc_kernel": ["tsv_attention_tc.cu"],
+    "tree_attn_tc1_kernel": ["tsv_attention_tc1.cu"],
     "tree_attn_simt_kernel": ["tsv_attention_simt.cu"],
 }
 KERNEL_COMMON = ["tsv_attention_common.cuh", "tsv_device.cuh", "tsv_internal.h", "tsv_api.cu"]
@@ -477,8 +478,11 @@ def run_ours(args, spec):
     achieved = abytes / (attn_ms * 1e-3) / 1e9
     keys_kernel = all(int(n) * (spec.Hq // spec.Hkv) <= 64 for n in np.diff(trees.node_offsets)) and \
         64 % (spec.Hq // spec.Hkv) == 0
+    G = spec.Hq // spec.Hkv
+    tile_pairs = any(int(n) * G > 128 for n in np.diff(trees.node_offsets))  # some request has 2+ row tiles
     kernel_name = ("tree_attn_simt_kernel" if spec.dtype != "bf16" else
-                   "tree_attn_keys_kernel" if keys_kernel else "tree_attn_tc_kernel")
+                   "tree_attn_keys_kernel" if keys_kernel else
+                   "tree_attn_tc_kernel" if tile_pairs else "tree_attn_tc1_kernel")
     traffic = recorded_traffic(spec.name, kernel_name)
     # The bound is whichever of bytes / bandwidth and FLOPs / tensor peak takes longer.
     tensor_bound = spec.dtype == "bf16" and aflops / (peak_tf * 1e12) > abytes / (peak * 1e9)

@@ -130,6 +130,10 @@ EDGE = {
     "head-dim-64-gqa": dict(B=2, Hq=8, Hkv=1, D=64, nodes=40, prefix=(500, 900), tree="random"),
     "many-requests": dict(B=128, Hq=2, Hkv=1, nodes=3, prefix=(0, 70), tree="random"),
     "long-prefix-one-head": dict(B=1, Hq=1, Hkv=1, nodes=9, prefix=20000, tree="random"),
+    # rows-on-lanes kernels: one 128-row tile per KV head (one-tile kernel), and
+    # three tiles (a full pair and a pair with one tile)
+    "one-row-tile-mha": dict(B=2, Hq=4, Hkv=4, nodes=100, prefix=(300, 900), tree="random", max_depth=9),
+    "three-row-tiles": dict(B=2, Hq=4, Hkv=2, nodes=150, prefix=(200, 700), tree="random", max_depth=9),
 }
 
 

@@ -22,7 +22,8 @@ struct tsv_handle_s {
   int device;
   int num_sms;
   EncodeTiledFn encode;
-  bool tc_attr_set[2];    // rows-on-lanes kernel, D = 64, 128
+  bool tc_attr_set[2];    // rows-on-lanes kernel (tile pairs), D = 64, 128
+  bool tc1_attr_set[2];   // rows-on-lanes kernel (one tile), D = 64, 128
   bool keys_attr_set[2];  // keys-on-lanes kernel, D = 64, 128
   bool mss_attr_set;      // MSS kernel's shared-memory limit
   size_t mss_staged_limit;
@@ -56,9 +57,11 @@ void order_slots(AttnPlan& p) {
   });
 }
 
-// CTAs of the rows-on-lanes kernel per (KV head, key chunk): each takes two
-// 128-row query tiles.
-inline int64_t tc_pairs(int32_t mtiles) { return (mtiles + 1) / 2; }
+// CTAs of the rows-on-lanes kernel per (KV head, key chunk): two 128-row
+// query tiles each when the plan pairs tiles, else one.
+inline int64_t tc_units(const AttnPlan& p, int32_t mtiles) {
+  return p.tc_tile_pairs ? (mtiles + 1) / 2 : mtiles;
+}
 
 // Splits every request's keys into chunks of one common length (a multiple of
 // the 128-key block), over the chunk counts that cut the longest request into
@@ -79,17 +82,19 @@ void build_plan(AttnPlan& p, int num_sms, int32_t B, const int32_t* prefix_len,
     p.nodes[b] = node_offsets[b + 1] - node_offsets[b];
     p.mtiles[b] = (int32_t)cdiv((int64_t)p.nodes[b] * p.G, kBM);
     lmax = std::max<int64_t>(lmax, (int64_t)p.prefix[b] + p.nodes[b]);
+    if (p.mtiles[b] >= 2) p.tc_tile_pairs = 1;  // some request has two tiles or more
   }
-  // Fewest chunks whose CTAs fill at least 3/4 of the SMs in one wave: every
-  // extra chunk adds partial rows to write and to merge, and the merge of a
-  // group runs in its last CTA.  Failing that, the least estimated makespan.
+  // Tile pairs: the fewest chunks whose CTAs fill at least 3/4 of the SMs in
+  // one wave (every extra chunk adds partial rows to write and to merge, and
+  // the merge of a group runs in its last CTA).  Otherwise, or failing that,
+  // the least estimated makespan waves * (chunk + per-CTA overhead).
   const int64_t overhead = 2 * kBN;
   int64_t best_cost = INT64_MAX, best_chunk = cdiv(lmax, kBN) * kBN, one_wave_chunk = 0;
   for (int pieces = 1; pieces <= 64; ++pieces) {
     const int64_t chunk = cdiv(cdiv(lmax, pieces), kBN) * kBN;
     int64_t units = 0;
     for (int b = 0; b < B; ++b)
-      units += (int64_t)Hkv * tc_pairs(p.mtiles[b]) * cdiv((int64_t)p.prefix[b] + p.nodes[b], chunk);
+      units += (int64_t)Hkv * tc_units(p, p.mtiles[b]) * cdiv((int64_t)p.prefix[b] + p.nodes[b], chunk);
     if (one_wave_chunk == 0 && units <= num_sms && 4 * units >= 3 * (int64_t)num_sms) one_wave_chunk = chunk;
     const int64_t waves = cdiv(units, num_sms);
     const int64_t cost = waves * (chunk + overhead);
@@ -99,7 +104,7 @@ void build_plan(AttnPlan& p, int num_sms, int32_t B, const int32_t* prefix_len,
     }
     if (chunk == kBN) break;
   }
-  if (one_wave_chunk > 0) best_chunk = one_wave_chunk;
+  if (p.tc_tile_pairs && one_wave_chunk > 0) best_chunk = one_wave_chunk;
   p.chunk_keys = (int32_t)best_chunk;
   order_slots(p);
   int64_t units = 0, rows = 0, ctrs = 0;
@@ -108,7 +113,7 @@ void build_plan(AttnPlan& p, int num_sms, int32_t B, const int32_t* prefix_len,
     const int64_t L = (int64_t)p.prefix[b] + p.nodes[b];
     p.n_chunks[b] = p.mtiles[b] > 0 ? (int32_t)cdiv(L, best_chunk) : 0;
     p.unit_start[s] = (int32_t)units;
-    units += (int64_t)Hkv * tc_pairs(p.mtiles[b]) * p.n_chunks[b];
+    units += (int64_t)Hkv * tc_units(p, p.mtiles[b]) * p.n_chunks[b];
     p.ctr_base[b] = (int32_t)ctrs;
     ctrs += (int64_t)Hkv * p.mtiles[b];
     if (p.n_chunks[b] > 1) {
@@ -296,6 +301,7 @@ tsv_status tsv_create(tsv_handle* out, int device) {
   h->num_sms = sms;
   h->encode = reinterpret_cast<EncodeTiledFn>(fn);
   h->tc_attr_set[0] = h->tc_attr_set[1] = false;
+  h->tc1_attr_set[0] = h->tc1_attr_set[1] = false;
   h->keys_attr_set[0] = h->keys_attr_set[1] = false;
   h->mss_attr_set = false;
   h->mss_staged_limit = 0;
@@ -415,13 +421,21 @@ tsv_status tsv_tree_attention(tsv_handle h, tsv_dtype dtype, const void* q_d, co
     }
     return cuda_status(launch_attention_keys(tmq, tmk, tmv, plan, parent_d, anc_d, out_d, status_d, cs));
   }
+  int32_t* counters = reinterpret_cast<int32_t*>(ws + lay.ctr_off);
+  float* part_o = reinterpret_cast<float*>(ws + lay.part_o_off);
+  float* part_lse = reinterpret_cast<float*>(ws + lay.part_lse_off);
+  if (!plan.tc_tile_pairs) {
+    if (!h->tc1_attr_set[di]) {
+      if (attention_tc1_set_attributes(D) != cudaSuccess) return TSV_ERR_CUDA;
+      h->tc1_attr_set[di] = true;
+    }
+    return cuda_status(launch_attention_tc1(tmq, tmk, tmv, plan, parent_d, anc_d, out_d, part_o,
+                                            part_lse, counters, status_d, cs));
+  }
   if (!h->tc_attr_set[di]) {
     if (attention_tc_set_attributes(D) != cudaSuccess) return TSV_ERR_CUDA;
     h->tc_attr_set[di] = true;
   }
-  int32_t* counters = reinterpret_cast<int32_t*>(ws + lay.ctr_off);
-  float* part_o = reinterpret_cast<float*>(ws + lay.part_o_off);
-  float* part_lse = reinterpret_cast<float*>(ws + lay.part_lse_off);
   return cuda_status(launch_attention_tc(tmq, tmk, tmv, plan, parent_d, anc_d, out_d, part_o,
                                          part_lse, counters, status_d, cs));
 }

@@ -44,6 +44,9 @@ struct AttnPlan {
   int32_t chunk_len[TSV_MAX_BATCH];
   int32_t cluster;
   int32_t keys_kernel;  // 1: keys-on-lanes kernel, 0: rows-on-lanes kernel
+  // Rows-on-lanes kernel: 1 = two 128-row query tiles per CTA (units are
+  // tile pairs), 0 = one tile per CTA (every request has mtiles <= 1).
+  int32_t tc_tile_pairs;
 };
 
 // Launches a kernel with programmatic stream serialization (it may be
@@ -98,6 +101,14 @@ cudaError_t launch_attention_tc(const CUtensorMap& tmap_q, const CUtensorMap& tm
                                 int32_t* status, cudaStream_t st);
 cudaError_t attention_tc_set_attributes(int D);
 size_t attention_tc_smem_bytes(int D);
+// The same with one query tile per CTA (plans with tc_tile_pairs == 0).
+cudaError_t launch_attention_tc1(const CUtensorMap& tmap_q, const CUtensorMap& tmap_k,
+                                 const CUtensorMap& tmap_v, const AttnPlan& plan,
+                                 const int32_t* parent, const uint32_t* anc, void* out,
+                                 float* part_o, float* part_lse, int32_t* counters,
+                                 int32_t* status, cudaStream_t st);
+cudaError_t attention_tc1_set_attributes(int D);
+size_t attention_tc1_smem_bytes(int D);
 
 constexpr int kKeysBlockKeys = 128;  // keys per block of the keys-on-lanes kernel
 constexpr int kKeysTileRows = 64;    // query rows per CTA of the keys-on-lanes kernel
