@@ -67,7 +67,7 @@ struct KeysCfg {
   static constexpr int kOffAlpha = kOffMref + kKeysRows * 4;    // float [64]
   static constexpr int kOffWmax = kOffAlpha + kKeysRows * 4;    // float [4][64]
   static constexpr int kOffLse = kOffWmax + 4 * kKeysRows * 4;  // float [64]
-  static constexpr int kOffWts = kOffLse + kKeysRows * 4;       // float [8][64]
+  static constexpr int kOffWts = kOffLse + kKeysRows * 4;       // float [8][64] (spare)
   static constexpr int kOffBar = kOffWts + 8 * kKeysRows * 4;
   // q_full, kv_full[S], kv_empty[S], s_full[2], p_full[2], pv_done[2], mma_done
   static constexpr int kNumBars = 1 + 2 * kStages + 7;
@@ -102,7 +102,6 @@ __global__ void __launch_bounds__(kKeysThreads, 1)
   float* sAlpha = reinterpret_cast<float*>(smem + C::kOffAlpha);
   float* sWmax = reinterpret_cast<float*>(smem + C::kOffWmax);
   float* sLse = reinterpret_cast<float*>(smem + C::kOffLse);
-  float* sWts = reinterpret_cast<float*>(smem + C::kOffWts);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
   uint64_t* q_full = bars;
   uint64_t* kv_full = bars + 1;
@@ -492,49 +491,46 @@ __global__ void __launch_bounds__(kKeysThreads, 1)
       const int t = tid;
       const int r_lo = (c * rows_valid) / nch, r_hi = ((c + 1) * rows_valid) / nch;
       const int nr = r_hi - r_lo;
-      // Weights of the chunks for every row.
-      for (int i = t; i < nch * nr; i += kKeysLaneThreads) {
-        const int cc = i / nr, r = r_lo + (i - cc * nr);
-        sWts[cc * kKeysRows + r] = ld_dsmem_f32(mapa_shared(smem_u32(sLse + r), cc));
-      }
-      named_bar(kBarKeys, kKeysLaneThreads);
-      if (t >= r_lo && t < r_hi) {
-        float M = -INFINITY;
-        for (int cc = 0; cc < nch; ++cc) M = fmaxf(M, sWts[cc * kKeysRows + t]);
-        float wsum = 0.f;
-        for (int cc = 0; cc < nch; ++cc) {
-          const float lse = sWts[cc * kKeysRows + t];
-          const float w = (M == -INFINITY || lse == -INFINITY) ? 0.f : fast_exp2(lse - M);
-          sWts[cc * kKeysRows + t] = w;
-          wsum += w;
-        }
-        const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-        for (int cc = 0; cc < nch; ++cc) sWts[cc * kKeysRows + t] *= inv;
-      }
-      named_bar(kBarKeys, kKeysLaneThreads);
-      // out[row][4 d] = sum over chunks of weight x partial, 16-byte remote loads.
+      // out[row][4 d] = sum over chunks of w_c x partial_c / sum of w_c with
+      // w_c = 2^(lse_c - max lse): each item loads its row's log-sum-exps and
+      // its 16 bytes of every partial in one round of remote loads, then
+      // weighs them itself (no barrier between weights and sums).
       constexpr int D4 = D / 4;
       const uint32_t part_s = smem_u32(sStage);
       for (int i = t; i < nr * D4; i += kKeysLaneThreads) {
         const int r = r_lo + i / D4, d4 = i % D4;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        float lse[8];
         float4 v[8];
 #pragma unroll
         for (int cc = 0; cc < 8; ++cc)
-          if (cc < nch) v[cc] = ld_dsmem_f32x4(mapa_shared(part_s + (uint32_t)(r * D + 4 * d4) * 4, cc));
+          if (cc < nch) {
+            lse[cc] = ld_dsmem_f32(mapa_shared(smem_u32(sLse + r), cc));
+            v[cc] = ld_dsmem_f32x4(mapa_shared(part_s + (uint32_t)(r * D + 4 * d4) * 4, cc));
+          }
+        float M = -INFINITY;
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc)
+          if (cc < nch) M = fmaxf(M, lse[cc]);
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        float wsum = 0.f;
 #pragma unroll
         for (int cc = 0; cc < 8; ++cc) {
           if (cc < nch) {
-            const float w = sWts[cc * kKeysRows + r];
-            acc.x += w * v[cc].x;
-            acc.y += w * v[cc].y;
-            acc.z += w * v[cc].z;
-            acc.w += w * v[cc].w;
+            const float w = (M == -INFINITY || lse[cc] == -INFINITY) ? 0.f : fast_exp2(lse[cc] - M);
+            if (w > 0.f) {  // a chunk of weight 0 may hold anything
+              acc.x += w * v[cc].x;
+              acc.y += w * v[cc].y;
+              acc.z += w * v[cc].z;
+              acc.w += w * v[cc].w;
+              wsum += w;
+            }
           }
         }
+        const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
         const int gr = row0 + r, node = gr / G;
         __nv_bfloat16* o = out + ((size_t)(off + node) * plan.Hq + g * G + (gr - node * G)) * D + 4 * d4;
-        *reinterpret_cast<uint2*>(o) = make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
+        *reinterpret_cast<uint2*>(o) =
+            make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
       }
     }
     cluster_sync_all();  // every CTA keeps its shared memory until its peers have read it
