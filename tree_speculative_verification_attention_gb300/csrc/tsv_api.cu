@@ -127,6 +127,17 @@ void build_plan(AttnPlan& p, int num_sms, int32_t B, const int32_t* prefix_len,
   p.n_units = (int32_t)units;
   p.part_rows_total = rows;
   p.n_counters = (int32_t)ctrs;
+  // Tile pairs with the same chunk count K (2 .. 8) in every request: the K
+  // chunk CTAs of a group form a cluster and merge through distributed shared
+  // memory instead of global partials and a last-CTA merge.
+  int K = 0;
+  bool uniform = true;
+  for (int b = 0; b < B; ++b) {
+    if (p.mtiles[b] == 0) continue;
+    if (K == 0) K = p.n_chunks[b];
+    else if (p.n_chunks[b] != K) uniform = false;
+  }
+  p.cluster = (p.tc_tile_pairs && uniform && K >= 2 && K <= 8) ? K : 0;
 }
 
 // Plan of the keys-on-lanes kernel (every request at most 64 query rows per

@@ -63,7 +63,8 @@ struct TcCfg {
   static constexpr int kOffV = kOffK + kKStages * kTileBytes;
   static constexpr int kOffAnc = kOffV + kVStages * kTileBytes;
   static constexpr int kOffPar = kOffAnc + kTcTiles * kBM * kAncWords * 4;
-  static constexpr int kOffBar = kOffPar + TSV_MAX_NODES * 4;
+  static constexpr int kOffLse = kOffPar + TSV_MAX_NODES * 4;  // float [256]: the pair's rows
+  static constexpr int kOffBar = kOffLse + kTcTiles * kBM * 4;
   // q_full, k_full[S], k_empty[S], v_full[S], v_empty[S], s_full[tile],
   // p_full[tile], pv_done[tile], mma_done
   static constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + 3 * kTcTiles + 1;
@@ -78,6 +79,7 @@ struct TcCfg {
   static_assert(kOffV == kOffK + kKStages * kTileBytes, "the K and V rings are contiguous");
   static_assert((kKStages + kVStages) * kTileBytes >= (64 + 1) * kBM * 4, "merge weights fit in the K/V rings");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory");
+  static_assert((kKStages + kVStages) * kTileBytes >= kTcTiles * kBM * D * 4, "cluster partials fit in the K/V rings");
 };
 
 template <int D>
@@ -98,6 +100,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint8_t* sV = smem + C::kOffV;
   uint32_t* sAnc = reinterpret_cast<uint32_t*>(smem + C::kOffAnc);
   int32_t* sPar = reinterpret_cast<int32_t*>(smem + C::kOffPar);
+  float* sLse = reinterpret_cast<float*>(smem + C::kOffLse);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
   uint64_t* q_full = bars;
   uint64_t* k_full = q_full + 1;
@@ -128,10 +131,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int local = unit - plan.unit_start[lo];
   const int mtiles = plan.mtiles[b], nch = plan.n_chunks[b];
   const int pairs = (mtiles + kTcTiles - 1) / kTcTiles;
-  const int tp = local % pairs;
-  const int cg = local / pairs;
-  const int c = cg % nch;
-  const int g = cg / nch;
+  // Clustered plans (plan.cluster == nch): the chunks of one (KV head, tile
+  // pair) are consecutive units and form one cluster, rank = chunk.
+  const bool clustered = plan.cluster > 1;
+  const int tp = clustered ? (local / nch) % pairs : local % pairs;
+  const int c = clustered ? local % nch : (local / pairs) % nch;
+  const int g = clustered ? local / nch / pairs : local / pairs / nch;
   const int G = plan.G;
   const int P = plan.prefix[b], n = plan.nodes[b], off = plan.node_off[b];
   const int R = n * G;
@@ -429,6 +434,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // Agree on success CTA-wide: the merge below has barriers that all 256
     // softmax threads must reach.
     ok = !named_bar_or(kBarTcSoftmax, kTcSoftmaxThreads, active && !ok);
+    if (clustered)  // a chunk of weight 0 (no keys, no success) is skipped by the merge
+      sLse[t * kBM + r] = (ok && nblk > 0 && active && l > 0.f) ? m_ref + log2f(l) : -INFINITY;
     if (ok && nblk > 0) {
       tc_fence_after();
       const float inv_l = l > 0.f ? 1.f / l : 0.f;
@@ -450,6 +457,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                    pack_bf16x2(o[8 * e + 4] * inv_l, o[8 * e + 5] * inv_l),
                                    pack_bf16x2(o[8 * e + 6] * inv_l, o[8 * e + 7] * inv_l));
             }
+          }
+        }
+      } else if (clustered) {
+        // Partial of this chunk, normalised, into this CTA's idle K/V rings:
+        // row t * 128 + r of the pair; the cluster merges after the loop.
+        if (active) {
+          float* dst = reinterpret_cast<float*>(sK) + (size_t)(t * kBM + r) * D;
+#pragma unroll 1
+          for (int cc = 0; cc < D; cc += 32) {
+            float o[32];
+            tmem_ld32(o_mine + cc, o);
+            float4* d4 = reinterpret_cast<float4*>(dst + cc);
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              d4[e] = make_float4(o[4 * e] * inv_l, o[4 * e + 1] * inv_l, o[4 * e + 2] * inv_l,
+                                  o[4 * e + 3] * inv_l);
           }
         }
       } else {
@@ -556,6 +579,58 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
   }
 
+  // ---------------------------------------------------------------- cluster merge
+  // Rank c merges rows [c * 256 / nch, (c + 1) * 256 / nch) of the pair: each
+  // output item loads its row's log-sum-exps and its 16 bytes of every
+  // chunk's partial from the cluster's shared memory in one round, then
+  // weighs them (w = 2^(lse - max lse); a chunk of weight 0 is skipped).
+  __syncwarp();
+  if (clustered) {
+    cluster_sync_all();  // every chunk's partial and log-sum-exps are in place
+    if (warp < kTcSoftmaxThreads / 32) {
+      const int npr = min(kTcTiles * kBM, R - row0);  // valid rows of the pair
+      const int r_lo = (c * npr) / nch, r_hi = ((c + 1) * npr) / nch;
+      constexpr int D4 = D / 4;
+      const uint32_t part_s = smem_u32(sK);
+      for (int i = tid; i < (r_hi - r_lo) * D4; i += kTcSoftmaxThreads) {
+        const int pr = r_lo + i / D4, d4 = i % D4;
+        float lse[8];
+        float4 v[8];
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc)
+          if (cc < nch) {
+            lse[cc] = ld_dsmem_f32(mapa_shared(smem_u32(sLse + pr), (uint32_t)cc));
+            v[cc] = ld_dsmem_f32x4(mapa_shared(part_s + (uint32_t)(pr * D + 4 * d4) * 4, (uint32_t)cc));
+          }
+        float M = -INFINITY;
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc)
+          if (cc < nch) M = fmaxf(M, lse[cc]);
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        float wsum = 0.f;
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc) {
+          if (cc < nch) {
+            const float w = (M == -INFINITY || lse[cc] == -INFINITY) ? 0.f : fast_exp2(lse[cc] - M);
+            if (w > 0.f) {
+              acc.x += w * v[cc].x;
+              acc.y += w * v[cc].y;
+              acc.z += w * v[cc].z;
+              acc.w += w * v[cc].w;
+              wsum += w;
+            }
+          }
+        }
+        const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+        const int grr = row0 + pr, nd = grr / G, hh = g * G + (grr - nd * G);
+        __nv_bfloat16* o = out + ((size_t)(off + nd) * plan.Hq + hh) * D + 4 * d4;
+        *reinterpret_cast<uint2*>(o) =
+            make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
+      }
+    }
+    cluster_sync_all();  // every CTA keeps its shared memory until its peers have read it
+  }
+
   tc_fence_before();
   __syncthreads();
   if (tid == 0 && *abort_v) status[b] = TSV_ERR_TIMEOUT;
@@ -585,9 +660,11 @@ cudaError_t launch_attention_tc(const CUtensorMap& tmap_q, const CUtensorMap& tm
   if (plan.n_units == 0) return cudaSuccess;
   __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(out);
   if (plan.D == 64)
-    return launch_pdl(tree_attn_tc_kernel<64>, dim3(plan.n_units), dim3(kTcThreads), TcCfg<64>::kSmemBytes, st, 0u,
+    return launch_pdl(tree_attn_tc_kernel<64>, dim3(plan.n_units), dim3(kTcThreads), TcCfg<64>::kSmemBytes, st,
+                      plan.cluster > 1 ? (unsigned)plan.cluster : 0u,
                       tmap_q, tmap_k, tmap_v, plan, parent, anc, ob, part_o, part_lse, counters, status);
-  return launch_pdl(tree_attn_tc_kernel<128>, dim3(plan.n_units), dim3(kTcThreads), TcCfg<128>::kSmemBytes, st, 0u,
+  return launch_pdl(tree_attn_tc_kernel<128>, dim3(plan.n_units), dim3(kTcThreads), TcCfg<128>::kSmemBytes, st,
+                    plan.cluster > 1 ? (unsigned)plan.cluster : 0u,
                     tmap_q, tmap_k, tmap_v, plan, parent, anc, ob, part_o, part_lse, counters, status);
 }
 
