@@ -41,6 +41,9 @@ struct AttnPlan {
   // Keys-on-lanes kernel: every request is cut into n_chunks[b] == cluster
   // chunks of chunk_len[b] keys (a multiple of 128); the chunks of one (KV
   // head, M-tile) group are consecutive units and form one cluster.
+  // Tile-pair rows kernel: cluster == n_chunks[b] (2 .. 8, the same for every
+  // request) when the chunks of a (KV head, tile pair) merge in a cluster,
+  // else 0.
   int32_t chunk_len[TSV_MAX_BATCH];
   int32_t cluster;
   int32_t keys_kernel;  // 1: keys-on-lanes kernel, 0: rows-on-lanes kernel
