@@ -138,7 +138,6 @@ __global__ void __launch_bounds__(kKeysThreads, 1)
     mbar_fence_init();
   }
   __syncthreads();
-  pdl_wait();  // the previous kernel's results are visible from here on
   const int b = plan.slot_req[*req_slot];
   const int local = unit - plan.unit_start[*req_slot];
   const int nch = plan.n_chunks[b];  // == cluster size
@@ -157,6 +156,20 @@ __global__ void __launch_bounds__(kKeysThreads, 1)
   const int k_begin = min(P + n, c * clen);
   const int k_end = min(P + n, k_begin + clen);
   const int nblk = (k_end - k_begin + kKeysBlock - 1) / kKeysBlock;
+  // The unit comes from the plan alone, so when all units run in the first
+  // wave the first ring's worth of K/V is pulled into L2 while the previous
+  // kernel finishes.
+  if (plan.prefetch_l2 && warp == kKeysProducerWarp && lane == 0) {
+    tma_prefetch_desc(&tmap_k);
+    tma_prefetch_desc(&tmap_v);
+    for (int j = 0; j < nblk && j < C::kStages; ++j)
+#pragma unroll
+      for (int hf = 0; hf < C::kHalves; ++hf) {
+        tma_prefetch_4d(&tmap_k, hf * 64, g, k_begin + j * kKeysBlock, b);
+        tma_prefetch_4d(&tmap_v, hf * 64, g, k_begin + j * kKeysBlock, b);
+      }
+  }
+  pdl_wait();  // the previous kernel's results are visible from here on
 
   if (warp == kKeysProducerWarp) {
     // ------------------------------------------------------------ producer

@@ -92,6 +92,16 @@ __device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
 }
 
+// Asks for a 4-D tile to be brought into L2 (no shared memory, no completion
+// to wait for).  It reads no value, so it may run before the previous
+// kernel's writes are visible: L2 stays coherent with them.
+__device__ __forceinline__ void tma_prefetch_4d(const void* tmap, int c0, int c1, int c2, int c3) {
+  asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
+                   reinterpret_cast<uint64_t>(tmap)),
+               "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+               : "memory");
+}
+
 // 4-D tiled tensor load global -> shared, completion counted on `bar` in bytes.
 // c0 (the innermost coordinate) must be a multiple of 16 bytes' worth of
 // elements; the callers pass multiples of 64 bf16 elements.

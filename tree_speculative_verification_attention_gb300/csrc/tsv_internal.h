@@ -47,6 +47,10 @@ struct AttnPlan {
   int32_t chunk_len[TSV_MAX_BATCH];
   int32_t cluster;
   int32_t keys_kernel;  // 1: keys-on-lanes kernel, 0: rows-on-lanes kernel
+  // Keys-on-lanes kernel: every unit runs in the first wave (n_units <= SMs),
+  // so each CTA pulls its first K/V blocks into L2 before waiting for the
+  // previous kernel; with later waves the prefetch would only add traffic.
+  int32_t prefetch_l2;
   // Rows-on-lanes kernel: 1 = two 128-row query tiles per CTA (units are
   // tile pairs), 0 = one tile per CTA (every request has mtiles <= 1).
   int32_t tc_tile_pairs;
