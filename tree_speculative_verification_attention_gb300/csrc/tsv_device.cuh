@@ -92,6 +92,13 @@ __device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
 }
 
+// Asks for `bytes` bytes at p (16-byte aligned, a multiple of 16) to be
+// brought into L2; like the tensor prefetch below it reads no value.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)), "r"(bytes)
+               : "memory");
+}
+
 // Asks for a 4-D tile to be brought into L2 (no shared memory, no completion
 // to wait for).  It reads no value, so it may run before the previous
 // kernel's writes are visible: L2 stays coherent with them.

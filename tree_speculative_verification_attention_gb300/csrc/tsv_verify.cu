@@ -31,6 +31,7 @@ namespace {
 
 constexpr int kArgmaxThreads = 256;
 constexpr int kArgmaxInFlight = 8;
+constexpr uint32_t kArgmaxPrefetchMax = 32768;  // largest slice pulled into L2 ahead of the wait
 constexpr int kMinSlice = 2048;  // vocab entries per CTA at least
 
 struct ArgMax {
@@ -248,6 +249,17 @@ __global__ void __launch_bounds__(kArgmaxThreads, 4)  // <= 64 registers: the lo
                          int32_t* __restrict__ counters, int32_t* __restrict__ path,
                          int32_t* __restrict__ accept_len, int32_t* __restrict__ bonus,
                          int32_t* __restrict__ status) {
+  // A small slice (short rows spread over many CTAs) is pulled into L2 while
+  // the previous kernel finishes: a prefetch reads no value, so it may run
+  // ahead of that kernel's writes.
+  if (threadIdx.x == 0 && (V & 3) == 0) {
+    const int64_t per = slice_len(V, splits);
+    const int64_t lo = min(V, (int64_t)blockIdx.x * per), hi = min(V, lo + per);
+    const float* src = logits + (size_t)blockIdx.y * (size_t)V + lo;
+    const uint32_t bytes = (uint32_t)((hi - lo) * 4);
+    if (bytes > 0 && bytes <= kArgmaxPrefetchMax && (reinterpret_cast<uintptr_t>(src) & 15) == 0)
+      bulk_prefetch_l2(src, bytes);
+  }
   pdl_wait();  // the previous kernel's results are visible from here on
   __shared__ int32_t offs[TSV_MAX_BATCH + 1];
   __shared__ WalkSmem w;
