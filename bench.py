@@ -62,6 +62,24 @@ def parse_args():
 # --------------------------------------------------------------------------- common
 
 
+def whole_job_ms(ms_total, world, device):
+    """Length of the timed region for the whole job: the largest over ranks
+    (the job ends when its slowest replica does).  Every rank calls it."""
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        t = torch.tensor([ms_total], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+    return ms_total
+
+
+def whole_job_value(ms_total, steps, nodes_per_step, world):
+    """Tree nodes verified per second by the whole job: each of the `world`
+    replicas verifies `nodes_per_step` nodes per step."""
+    return world * nodes_per_step / (ms_total / steps * 1e-3)
+
+
 def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -441,13 +459,9 @@ def run_ours(args, spec):
     t_wall1 = time.time()
     if world > 1:
         dist.barrier()
-    ms_total = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([ms_total], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = whole_job_ms(e0.elapsed_time(e1), world, dev)
     ms_step = ms_total / args.steps
-    value = world * N / (ms_step * 1e-3)
+    value = whole_job_value(ms_total, args.steps, N, world)
 
     # ---------------------------------------------------------------- attention kernel, per launch
     # Average launch duration of the attention call inside a graph of R
