@@ -366,6 +366,23 @@ tsv_status tsv_tree_verify_greedy_noalloc(tsv_handle h, const float* logits_d, i
                                           int32_t* path_d, int32_t* accept_len_d, int32_t* bonus_d,
                                           int32_t* status_d, void* stream);
 
+/*
+ * tsv_selftest_bounded_wait — checks on the caller's device that a device-side
+ * wait which never completes ends in TSV_ERR_TIMEOUT and a usable context,
+ * not a hang.  The pages have no counterpart; it exercises the bounded wait
+ * every kernel of this library uses for its mbarriers (about 1 s of wall
+ * clock, then an abort flag that every other waiting role of the CTA sees).
+ *   arrive          nonzero: the barriers are completed before the waits, so
+ *                   they return at once and status is TSV_OK; zero: nothing
+ *                   arrives, the waits run out and status is TSV_ERR_TIMEOUT
+ *   status_d (out)  int32 [1]
+ *   elapsed_ns_d (out)  int64 [1]: wall-clock nanoseconds from the start of
+ *                   the waits to the status write; may be NULL
+ * One CTA; allocates nothing; asynchronous on `stream`.
+ */
+tsv_status tsv_selftest_bounded_wait(tsv_handle h, int32_t arrive, int32_t* status_d,
+                                     int64_t* elapsed_ns_d, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

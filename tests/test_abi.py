@@ -70,6 +70,9 @@ def test_null_handle_and_bad_arguments_are_rejected_on_the_host(lib):
     assert lib.tsv_tree_verify_greedy_workspace_size(None, 1, 1, ctypes.c_int64(10), ctypes.byref(size)) == 1
     h = ctypes.c_void_p()
     assert lib.tsv_create(None, 0) == 1
+    lib.tsv_selftest_bounded_wait.argtypes = [ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p,
+                                              ctypes.c_void_p, ctypes.c_void_p]
+    assert lib.tsv_selftest_bounded_wait(None, 1, None, None, None) == 1
 
 
 def test_create_without_a_device_reports_cuda_error(lib):

@@ -37,7 +37,7 @@ EXPORTED = (
     "tsv_tree_verify_greedy_workspace_size", "tsv_tree_verify_greedy",
     "tsv_tree_verify_stochastic_workspace_size", "tsv_tree_verify_stochastic",
     "tsv_tree_verify_greedy_noalloc", "tsv_kv_commit", "tsv_tree_verify_stochastic_warped",
-    "tsv_tree_expand", "tsv_tree_merge",
+    "tsv_tree_expand", "tsv_tree_merge", "tsv_selftest_bounded_wait",
 )
 
 
@@ -78,6 +78,7 @@ def _load():
                            vp, vp]),
         "tsv_tree_expand": (ctypes.c_int, [vp, vp, i64, i32, i32, vp, vp]),
         "tsv_tree_merge": (ctypes.c_int, [vp, vp, vp, vp, vp, i32, vp, vp, vp, vp, vp, vp]),
+        "tsv_selftest_bounded_wait": (ctypes.c_int, [vp, i32, vp, vp, vp]),
         "tsv_kv_commit": (
             ctypes.c_int, [vp, ctypes.c_int, vp, vp, i64, i64, i64, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp]),
         "tsv_tree_verify_stochastic_workspace_size": (ctypes.c_int, [vp, i32, i32, i64, szp]),
@@ -225,6 +226,11 @@ def tsv_tree_merge(h, parent, tokens, tree_offsets, request_trees, B, out_parent
     _check(_lib.tsv_tree_merge(h, _ptr(parent), _ptr(tokens), _ptr(tree_offsets), _ptr(request_trees), int(B),
                                _ptr(out_parent), _ptr(out_tokens), _ptr(out_source), _ptr(out_count),
                                _ptr(status), _stream(stream)), "tsv_tree_merge")
+
+
+def tsv_selftest_bounded_wait(h, arrive, status, elapsed_ns=None, stream=None):
+    _check(_lib.tsv_selftest_bounded_wait(h, int(arrive), _ptr(status), _ptr(elapsed_ns), _stream(stream)),
+           "tsv_selftest_bounded_wait")
 
 
 def tsv_kv_commit(h, dtype_code, k_cache, v_cache, sb, sl, sh, B, Hkv, D, prefix_len, node_offsets, path,
@@ -391,3 +397,15 @@ def tree_merge(parent, tokens, tree_offsets, request_trees, stream=None):
     tsv_tree_merge(handle(dev.index), parent, tokens, tree_offsets, request_trees, B, o["parent"], o["tokens"],
                    o["source"], o["count"], o["status"], stream)
     return o
+
+
+def selftest_bounded_wait(arrive, device=None, stream=None):
+    """Runs the bounded-wait self-test on `device`; returns (status, elapsed
+    seconds) after synchronising: (TSV_OK, ~0) with `arrive`, (TSV_ERR_TIMEOUT,
+    about 1 s) without."""
+    dev = torch.device("cuda", torch.cuda.current_device() if device is None else int(device))
+    st = torch.full((1,), -1, dtype=torch.int32, device=dev)
+    ns = torch.zeros(1, dtype=torch.int64, device=dev)
+    tsv_selftest_bounded_wait(handle(dev.index), arrive, st, ns, stream)
+    torch.cuda.synchronize(dev)
+    return int(st.item()), ns.item() * 1e-9
