@@ -4,6 +4,7 @@ Paths, accept lengths and bonus tokens must be bit-exact; for stochastic
 verification a request may part from the oracle only after a decision the
 oracle marks as a near tie (margin below 1e-6), which is counted.
 """
+import dataclasses
 import json
 import os
 
@@ -171,6 +172,31 @@ def test_stochastic_temperature(tsv):
     ref = oracle.verify_stochastic(si.llm_logits, si.ssm_probs, si.tokens, trees.parent,
                                    trees.node_offsets, si.u_accept, si.u_sample, temperature=0.7)
     compare_stochastic(r, ref, trees)
+
+
+@pytest.mark.parametrize("V", [2000, 32000])
+def test_stochastic_vanishing_temperature_is_greedy(tsv, V):
+    """As T goes to zero the LLM distribution is one-hot at the argmax (every
+    other probability underflows to exactly zero at T = 2^-60), so stochastic
+    verification on the GPU must give greedy verification's result."""
+    spec = W.spec_variant(W.SPECS["batch8-ragged-merge64-mss"], V=V)
+    trees = W.make_trees(spec)
+    si = W.make_stochastic_inputs(spec, trees)
+    rng = np.random.default_rng(V)
+    tok = si.tokens.copy()
+    for b in range(spec.B):
+        off = int(trees.node_offsets[b])
+        for i in range(1, int(trees.node_offsets[b + 1]) - off):
+            if rng.random() < 0.5:
+                tok[off + i] = int(np.argmax(si.llm_logits[off + int(trees.parent[off + i])]))
+    top2 = np.sort(si.llm_logits, axis=1)[:, -2:]
+    assert (top2[:, 1] > top2[:, 0]).all()
+    r = _stochastic(tsv, trees, dataclasses.replace(si, tokens=tok), temperature=2.0 ** -60)
+    g = oracle.verify_greedy(si.llm_logits, tok, trees.parent, trees.node_offsets)
+    assert np.array_equal(r["path"].cpu().numpy(), g["path"])
+    assert np.array_equal(r["accept_len"].cpu().numpy(), g["accept_len"])
+    assert np.array_equal(r["bonus"].cpu().numpy(), g["bonus"])
+    assert (r["status"].cpu().numpy() == 0).all() and g["accept_len"].sum() > 0
 
 
 def _mss_golden():
