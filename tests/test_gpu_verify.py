@@ -199,6 +199,34 @@ def test_stochastic_vanishing_temperature_is_greedy(tsv, V):
     assert (r["status"].cpu().numpy() == 0).all() and g["accept_len"].sum() > 0
 
 
+@pytest.mark.parametrize("B,n,V,tree", [(1, 1, 1, "random"), (1, 1, 7, "random"), (3, 5, 1, "random"),
+                                        (2, 256, 64, "random"), (2, 256, 40, "chain"), (1, 256, 3, "star"),
+                                        (128, 2, 100, "random"), (5, 9, 4, "random")])
+def test_verify_edge_shapes(tsv, B, n, V, tree):
+    """Root-only trees, V = 1 (every decision forced), the largest tree
+    (256 nodes: deepest chain, widest star) and the largest batch (128)."""
+    spec = W.spec_variant(W.SPECS["tiny-f32-P128-n16"], wid=7000 + n + V, B=B, nodes=n, V=V, tree=tree)
+    trees = W.make_trees(spec)
+    gi = W.make_greedy_inputs(spec, trees)
+    si = W.make_stochastic_inputs(spec, trees)
+    if tree == "chain":
+        # Every node matches: both walks must run the whole 255-step chain.
+        for b in range(B):
+            off = int(trees.node_offsets[b])
+            for i in range(1, n):
+                u = off + int(trees.parent[off + i])
+                gi.tokens[off + i] = int(np.argmax(gi.logits[u]))
+                z = np.exp(si.llm_logits[u].astype(np.float64) - si.llm_logits[u].max())
+                si.ssm_probs[off + i] = (z / z.sum()).astype(np.float32)  # q = p: accepted unless u ~ 1
+    ref_g = oracle.verify_greedy(gi.logits, gi.tokens, trees.parent, trees.node_offsets)
+    _check_greedy(_greedy(tsv, trees, gi), ref_g)
+    ref = oracle.verify_stochastic(si.llm_logits, si.ssm_probs, si.tokens, trees.parent, trees.node_offsets,
+                                   si.u_accept, si.u_sample)
+    compare_stochastic(_stochastic(tsv, trees, si), ref, trees)
+    if tree == "chain":
+        assert (ref_g["accept_len"] == n - 1).all() and (ref["accept_len"] == n - 1).all()
+
+
 def _mss_golden():
     for case in json.load(open(os.path.join(GOLDEN, "mss_closed_forms.json")))["cases"]:
         for i, var in enumerate(case["variants"]):

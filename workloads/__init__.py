@@ -259,7 +259,8 @@ class GreedyInputs:
 
 def make_greedy_inputs(spec: Spec, trees: Trees) -> GreedyInputs:
     """Logits ~ N(0, sigma^2); a child's token equals its parent's argmax with
-    probability 1/2, else it is uniform over the other V-1 tokens."""
+    probability 1/2, else it is uniform over the other V-1 tokens (V = 1:
+    every token is 0)."""
     N = int(trees.node_offsets[-1])
     logits = normal_f32(spec.wid, S_GLOGITS, (N, spec.V), spec.greedy_sigma)
     rng = _rng(spec.wid, S_GTOK)
@@ -269,8 +270,8 @@ def make_greedy_inputs(spec: Spec, trees: Trees) -> GreedyInputs:
         n = int(trees.node_offsets[b + 1]) - off
         for i in range(n):
             p = int(trees.parent[off + i])
-            hit = rng.random() < 0.5
-            other = int(rng.integers(spec.V - 1))
+            hit = rng.random() < 0.5 or spec.V == 1  # with one token every child matches
+            other = int(rng.integers(spec.V - 1)) if spec.V > 1 else 0
             if p < 0:
                 tokens[off + i] = other
                 continue
