@@ -63,6 +63,28 @@ def test_greedy_fuzz(tsv, seed):
     _check_greedy(r, oracle.verify_greedy(gi.logits, gi.tokens, trees.parent, trees.node_offsets))
 
 
+@pytest.mark.parametrize("name", ["llama7b-layer-P1024-n20", "gqa64x8-P32768-n128", "batch32-P2048-n16"])
+def test_greedy_workspace_reused_across_calls(tsv, name):
+    """One workspace, zero-filled once, serves consecutive calls: each call
+    must leave its completion counters (per request and, when a row is split
+    into vocabulary slices, per row) at zero for the next one.  Outputs are
+    refilled with -7 before every call, so a walk that does not run shows."""
+    spec = W.SPECS[name]
+    trees = W.make_trees(spec)
+    gi = W.make_greedy_inputs(spec, trees)
+    ref = oracle.verify_greedy(gi.logits, gi.tokens, trees.parent, trees.node_offsets)
+    x = [d(gi.logits), d(gi.tokens), d(trees.parent), d(trees.node_offsets)]
+    N, B = len(gi.tokens), spec.B
+    h = tsv.handle()
+    ws = torch.zeros(tsv.tsv_tree_verify_greedy_workspace_size(h, B, N, spec.V), dtype=torch.uint8, device="cuda")
+    for _ in range(3):
+        out = {k: torch.full((n,), -7, dtype=torch.int32, device="cuda")
+               for k, n in (("path", N), ("accept_len", B), ("bonus", B), ("status", B))}
+        r = tsv.tree_verify_greedy(*x, workspace=ws, out=out)
+        torch.cuda.synchronize()
+        _check_greedy(r, ref)
+
+
 @pytest.mark.parametrize("case", json.load(open(os.path.join(GOLDEN, "greedy_walk.json")))["cases"],
                          ids=lambda c: c["name"])
 def test_greedy_golden(tsv, case):
