@@ -24,6 +24,7 @@ import hashlib
 import json
 import math
 import os
+import platform
 import subprocess
 import sys
 import threading
@@ -290,6 +291,42 @@ def oracle_step_time(spec, trees, att, gi, si, budget_s, heads_sample=None):
     return per_step, oracle.num_threads(), sample
 
 
+def host_cpu_model(cpuinfo="/proc/cpuinfo"):
+    """The host CPU as the OS describes it (x86: the model name; Arm: the
+    implementer and part codes), else the machine type."""
+    fields = {}
+    try:
+        with open(cpuinfo) as f:
+            for line in f:
+                key, sep, val = line.partition(":")
+                if sep and key.strip() not in fields:
+                    fields[key.strip()] = val.strip()
+    except OSError:
+        pass
+    if fields.get("model name"):
+        return fields["model name"]
+    if "CPU part" in fields:
+        return "%s (CPU implementer %s, part %s)" % (platform.machine(), fields.get("CPU implementer", "?"),
+                                                     fields["CPU part"])
+    return platform.machine() or None
+
+
+def oracle_baseline(spec, trees, att, gi, si, budget_s, heads, n_nodes):
+    """The cpu_baseline entry: the oracle on all host cores over a sample of
+    about budget_s seconds, then once more on one core (one repetition)."""
+    import oracle
+    per_step, cores, sample = oracle_step_time(spec, trees, att, gi, si, budget_s, heads)
+    oracle.set_num_threads(1)
+    try:
+        one_core, _, _ = oracle_step_time(spec, trees, att, gi, si, 0.0, heads)
+    finally:
+        oracle.set_num_threads(cores)
+    return {"value": n_nodes / per_step, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample,
+            "single_core": {"value": n_nodes / one_core, "unit": UNIT, "cores": 1,
+                            "sample": "one repetition of the same sample"},
+            "nproc": os.cpu_count(), "cpu_model": host_cpu_model()}
+
+
 def choose_heads_sample(spec, trees):
     """KV heads whose oracle attention takes about 0.5 s at ~1 GFLOP/s per core."""
     sizes = np.diff(trees.node_offsets)
@@ -315,12 +352,14 @@ def run_reference(args, spec):
         total += s
     ms = 1e3 * total / args.steps
     value = n_nodes / (total / args.steps)
+    base = oracle_baseline(spec, trees, att, gi, si, 0.0, heads, n_nodes)  # adds the one-core figure
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": config_of(spec, {"reference": "CPU fp64 oracle (the pages ship no code)"}),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
-                             "sample": "per step: " + sample},
+                             "sample": "per step: " + sample, "single_core": base["single_core"],
+                             "nproc": base["nproc"], "cpu_model": base["cpu_model"]},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -521,10 +560,8 @@ def run_ours(args, spec):
             "step_roofline_frac": step_bytes / (ms_step * 1e-3) / 1e9 / peak,
             "e2e": e2e, "gpu_launches": kernels_per_step * args.steps, "clocks": clocks}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        per_step, cores, sample = oracle_step_time(spec, trees, att, gi, si, args.cpu_seconds,
-                                                   choose_heads_sample(spec, trees))
-        line["cpu_baseline"] = {"value": N / per_step, "unit": UNIT, "cores": cores, "kind": "oracle",
-                                "sample": sample}
+        line["cpu_baseline"] = oracle_baseline(spec, trees, att, gi, si, args.cpu_seconds,
+                                               choose_heads_sample(spec, trees), N)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -60,6 +60,8 @@ def _bind(path):
         ctypes.c_int32, ctypes.c_double, ctypes.c_int32, ctypes.c_double,
         _i32p, _i32p, _i32p, _i32p, _i32p, _i32p, _i32p]
     lib.oracle_num_threads.argtypes = []
+    lib.oracle_set_num_threads.argtypes = [ctypes.c_int]
+    lib.oracle_set_num_threads.restype = None
     for f in (lib.oracle_tree_ancestors, lib.oracle_tree_attention,
               lib.oracle_verify_greedy, lib.oracle_verify_stochastic, lib.oracle_num_threads):
         f.restype = ctypes.c_int
@@ -76,6 +78,11 @@ def _lib():
 def num_threads() -> int:
     """Threads the oracle's OpenMP loops use."""
     return int(_lib().oracle_num_threads())
+
+
+def set_num_threads(n: int) -> None:
+    """Threads for the oracle's later calls from this thread (no effect on results)."""
+    _lib().oracle_set_num_threads(int(n))
 
 
 def _c(a, dtype):

@@ -472,10 +472,17 @@ int oracle_verify_stochastic(const float* llm_logits, const float* ssm_probs, in
   return rc;
 }
 
-/* Threads the OpenMP loops above use (1 when built without OpenMP). */
+/* Threads the OpenMP loops above use (1 when built without OpenMP), and a way
+ * to change that for later calls from the calling thread (the benchmark times
+ * the oracle on all host cores and on one).  Results do not depend on it: the
+ * loops only spread independent output units over threads. */
 #ifdef _OPENMP
 #include <omp.h>
 int oracle_num_threads(void) { return omp_get_max_threads(); }
+void oracle_set_num_threads(int n) {
+  if (n > 0) omp_set_num_threads(n);
+}
 #else
 int oracle_num_threads(void) { return 1; }
+void oracle_set_num_threads(int n) { (void)n; }
 #endif
