@@ -75,6 +75,35 @@ def test_null_handle_and_bad_arguments_are_rejected_on_the_host(lib):
     assert lib.tsv_selftest_bounded_wait(None, 1, None, None, None) == 1
 
 
+def test_every_entry_point_rejects_a_null_handle_on_the_host():
+    """No call touches a device, or any pointer, before checking its handle."""
+    import tree_speculative_verification_attention_gb300 as tsv
+    L = tsv._lib
+    size = ctypes.c_size_t()
+    calls = {
+        "tsv_tree_attention_workspace_size": (None, 1, 1, None, None, 1, 1, 64, 0, 0, ctypes.byref(size)),
+        "tsv_tree_attention": (None, 1, None, None, None, 0, 0, 0, None, None, None, None, None, None, None,
+                               1, 1, 1, 64, 0.0, None, 0, None, 0, None),
+        "tsv_tree_verify_greedy_workspace_size": (None, 1, 1, 10, ctypes.byref(size)),
+        "tsv_tree_verify_greedy": (None, None, 10, None, None, None, 1, 1, None, None, None, None, 0, None, None),
+        "tsv_tree_verify_greedy_noalloc": (None, None, 10, None, None, None, 1, 1, None, None, None, None, None),
+        "tsv_tree_verify_stochastic_workspace_size": (None, 1, 1, 10, ctypes.byref(size)),
+        "tsv_tree_verify_stochastic": (None, None, None, 10, None, None, None, None, None, 1.0, 1, 1, None, None,
+                                       None, None, None, 0, None, None),
+        "tsv_tree_verify_stochastic_warped": (None, None, None, 10, None, None, None, None, None, 1.0, 5, 0.9, 1,
+                                              1, None, None, None, None, None, 0, None, None),
+        "tsv_tree_expand": (None, None, 10, 1, 1, None, None),
+        "tsv_tree_merge": (None, None, None, None, None, 1, None, None, None, None, None, None),
+        "tsv_kv_commit": (None, 1, None, None, 0, 0, 0, 1, 1, 64, None, None, None, None, None, None, None),
+        "tsv_tree_prepare": (None, None, None, 1, None, None, None, None),
+        "tsv_selftest_bounded_wait": (None, 1, None, None, None),
+    }
+    for name, args in calls.items():
+        assert getattr(L, name)(*args) == tsv.TSV_ERR_INVALID_ARG, name
+    # The other exports make or free a handle (checked above) or take none.
+    assert set(calls) | {"tsv_create", "tsv_destroy", "tsv_status_string", "tsv_version"} == set(tsv.EXPORTED)
+
+
 def test_create_without_a_device_reports_cuda_error(lib):
     import torch
     if torch.cuda.is_available():
