@@ -111,3 +111,19 @@ def test_create_without_a_device_reports_cuda_error(lib):
     h = ctypes.c_void_p()
     assert lib.tsv_create(ctypes.byref(h), 0) == 4
     assert not h.value
+
+
+def test_plain_c_caller(lib, tmp_path):
+    """include/tsv.h compiles as strict C99 and the library links into a C
+    program that makes host-side calls (tests/c/abi_check.c)."""
+    libdir = os.path.dirname(_build_module().LIB)
+    exe = tmp_path / "abi_check"
+    cc = subprocess.run(["gcc", "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic",
+                         "-I" + os.path.join(ROOT, "include"), os.path.join(ROOT, "tests", "c", "abi_check.c"),
+                         "-L" + libdir, "-ltsv", "-Wl,-rpath," + libdir, "-o", str(exe)],
+                        capture_output=True, text=True)
+    assert cc.returncode == 0, cc.stderr
+    run = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert run.returncode == 0, run.stdout + run.stderr
+    assert run.stdout.startswith("bad tree")
+
