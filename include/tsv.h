@@ -354,8 +354,9 @@ tsv_status tsv_kv_commit(tsv_handle h, tsv_dtype dtype, void* k_cache_d, void* v
  *   returns TSV_ERR_SCRATCH_LIMIT (no shape within TSV_MAX_BATCH x
  *   TSV_MAX_NODES does).
  *   The first call on a device looks up the array's device address (a host-side
- *   set-up step, with that device current); make that first call before any
- *   stream capture.
+ *   set-up step, with that device current), and so does the first call after
+ *   the device's context was reset (cudaDeviceReset): make each such call
+ *   before any stream capture.
  *   All calls on a device share the array: each call clears the part that must
  *   start at zero on its stream, but calls that overlap on the GPU (streams not
  *   ordered with each other) race on it and give wrong results.

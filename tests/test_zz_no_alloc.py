@@ -62,11 +62,39 @@ def test_no_alloc_matches_workspace_entry_on_consecutive_calls(tsv):
             assert torch.equal(second[k], ref[k]), k
 
 
+def test_no_alloc_clears_counters_a_previous_call_left_nonzero(tsv):
+    """A call with few requests leaves argmax partials (nonzero floats) right
+    after its 256 bytes of counters; a later call with more requests has its
+    counters there.  Each call must clear its own counters first, or the
+    requests whose counters start nonzero never run their walk."""
+    h = tsv.handle()
+    small = W.SPECS["llama7b-layer-P1024-n20"]  # B = 1: counters in bytes 0..255, partials from 256
+    trees, x = _inputs(small)
+    first = _no_alloc(tsv, h, x, small.B, int(trees.node_offsets[-1]), small.V)
+    big = W.spec_variant(W.SPECS["batch32-P2048-n16"], name="noalloc-b128", B=128, prefix=64, V=4000,
+                         stochastic=False)  # B = 128: counters in bytes 0..511
+    btrees, bx = _inputs(big)
+    B, N, V = big.B, int(btrees.node_offsets[-1]), big.V
+    ref = _with_workspace(tsv, h, bx, B, N, V)
+    second = _no_alloc(tsv, h, bx, B, N, V)
+    torch.cuda.synchronize()
+    assert (first["status"].cpu() == 0).all() and (ref["status"].cpu() == 0).all()
+    for k in ref:
+        assert torch.equal(second[k], ref[k]), k
+
+
 def test_no_alloc_rejects_what_the_scratch_cannot_hold(tsv):
     h = tsv.handle()
-    x = dict(logits=None, tokens=None, parent=None, offs=None)
     o = _outputs(1, 1)
-    with pytest.raises(tsv.TSVError) as e:  # B beyond the library's maximum: rejected before launch
+    # A valid batch size whose node count needs more slice partials than the
+    # fixed scratch holds: rejected on the host, before anything is launched.
+    need = tsv.tsv_tree_verify_greedy_workspace_size(h, 1, 200000, 32000)
+    assert need > 1 << 20
+    with pytest.raises(tsv.TSVError) as e:
+        tsv.tsv_tree_verify_greedy_noalloc(h, None, 32000, None, None, None, 1, 200000, None, o["accept_len"],
+                                           o["bonus"], o["status"])
+    assert e.value.code == tsv.TSV_ERR_SCRATCH_LIMIT
+    with pytest.raises(tsv.TSVError) as e:  # B beyond the library's maximum
         tsv.tsv_tree_verify_greedy_noalloc(h, None, 10, None, None, None, 1000, 0, None, o["accept_len"],
                                            o["bonus"], o["status"])
-    assert e.value.code in (tsv.TSV_ERR_INVALID_ARG, tsv.TSV_ERR_SCRATCH_LIMIT)
+    assert e.value.code == tsv.TSV_ERR_INVALID_ARG

@@ -13,6 +13,7 @@
 // contents: the counters, which must start at zero, are cleared on the stream
 // at the start of every call.  Calls whose work overlaps on the GPU (different
 // streams, no ordering between them) race on the array and give wrong results.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -28,24 +29,63 @@ constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
 
-// Device address of g_noalloc_scratch, looked up once per device.  In host
-// code the symbol itself is only a host-side stand-in for the device array, so
-// the kernel must be given the address cudaGetSymbolAddress returns.
+// Device address of g_noalloc_scratch, looked up once per device and CUDA
+// context.  In host code the symbol itself is only a host-side stand-in for the
+// device array, so the kernel must be given the address cudaGetSymbolAddress
+// returns.  That address belongs to the context the module was loaded in: after
+// cudaDeviceReset (or a release and re-creation of the primary context) the
+// module loads again, possibly elsewhere, so the cache keeps the unique id of
+// the context it was filled in and looks the address up again when the current
+// context's id differs.
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
 std::mutex g_scratch_mutex;
 void* g_scratch_ptr[kMaxDevices] = {};
+unsigned long long g_scratch_ctx[kMaxDevices] = {};
+CtxGetCurrentFn g_ctx_get_current = nullptr;
+CtxGetIdFn g_ctx_get_id = nullptr;
 
+// Unique id of the calling thread's current context (the driver never reuses
+// one within a process).
+tsv_status current_context_id(unsigned long long* id) {
+  if (g_ctx_get_current == nullptr || g_ctx_get_id == nullptr) {
+    void* f1 = nullptr;
+    void* f2 = nullptr;
+    cudaDriverEntryPointQueryResult q1, q2;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f1, 12000, cudaEnableDefault, &q1) != cudaSuccess ||
+        q1 != cudaDriverEntryPointSuccess || f1 == nullptr ||
+        cudaGetDriverEntryPointByVersion("cuCtxGetId", &f2, 12000, cudaEnableDefault, &q2) != cudaSuccess ||
+        q2 != cudaDriverEntryPointSuccess || f2 == nullptr)
+      return TSV_ERR_CUDA;
+    g_ctx_get_current = reinterpret_cast<CtxGetCurrentFn>(f1);
+    g_ctx_get_id = reinterpret_cast<CtxGetIdFn>(f2);
+  }
+  CUcontext ctx = nullptr;
+  if (g_ctx_get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return TSV_ERR_CUDA;
+  return g_ctx_get_id(ctx, id) == CUDA_SUCCESS ? TSV_OK : TSV_ERR_CUDA;
+}
+
+// The device address of the scratch array on `device`, which the caller has
+// made current (cudaGetDevice), so cudaGetSymbolAddress runs with that device
+// current.  Looked up on the first call in each context, then cached.
 tsv_status scratch_address(int device, void** out) {
   if (device < 0 || device >= kMaxDevices) return TSV_ERR_UNSUPPORTED;
   std::lock_guard<std::mutex> lock(g_scratch_mutex);
-  if (g_scratch_ptr[device] == nullptr) {
-    int prev = -1;
-    if (cudaGetDevice(&prev) != cudaSuccess) return TSV_ERR_CUDA;
-    if (prev != device && cudaSetDevice(device) != cudaSuccess) return TSV_ERR_CUDA;
+  unsigned long long id = 0;
+  const bool have_ctx = current_context_id(&id) == TSV_OK;
+  if (!have_ctx || g_scratch_ptr[device] == nullptr || g_scratch_ctx[device] != id) {
+    // cudaGetSymbolAddress also sets up the device's context when no runtime
+    // call has yet; its id is read after it.
     void* p = nullptr;
-    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (prev != device) cudaSetDevice(prev);
-    if (e != cudaSuccess || p == nullptr) return TSV_ERR_CUDA;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
+      cudaGetLastError();
+      g_scratch_ptr[device] = nullptr;
+      return TSV_ERR_CUDA;
+    }
+    if (current_context_id(&id) != TSV_OK) return TSV_ERR_CUDA;
     g_scratch_ptr[device] = p;
+    g_scratch_ctx[device] = id;
   }
   *out = g_scratch_ptr[device];
   return TSV_OK;
