@@ -312,6 +312,23 @@ def make_stochastic_inputs(spec: Spec, trees: Trees) -> StochasticInputs:
     return StochasticInputs(llm, ssm, tokens, u[:N].copy(), u[N:].copy())
 
 
+def propose_near_llm(si: StochasticInputs, trees: Trees, mix: float = 0.7, seed: int = 0) -> StochasticInputs:
+    """Stochastic inputs whose proposals sit close to the LLM's law at each
+    node's parent (mix x softmax of the parent's LLM row + (1 - mix) x the
+    drawn proposal row), with each child's token redrawn from its new row, so
+    that accepted children are likely.  Returns a new StochasticInputs."""
+    offs = trees.node_offsets
+    prow = np.concatenate([np.maximum(trees.parent[offs[b]:offs[b + 1]], 0) + offs[b]
+                           for b in range(len(offs) - 1)])
+    q = (mix * proposal_rows(si.llm_logits[prow]).astype(np.float64)
+         + (1.0 - mix) * si.ssm_probs.astype(np.float64)).astype(np.float32)
+    rng = np.random.default_rng(seed)
+    cdf = np.cumsum(q.astype(np.float64), axis=1)
+    u = rng.random(len(cdf))[:, None] * cdf[:, -1:]
+    tokens = np.minimum((u >= cdf).sum(1), q.shape[1] - 1).astype(np.int32)
+    return StochasticInputs(si.llm_logits, q, tokens, si.u_accept, si.u_sample)
+
+
 def fuzz_spec(seed: int, dtype: str = "bf16", max_nodes: int = 40) -> Spec:
     """A small random shape for parity fuzzing: random n, V, D, GQA group, prefixes."""
     r = _rng(1000 + seed, 99)
