@@ -2,18 +2,26 @@
 """Throughput of token-tree verification on GB300: tree nodes verified per second.
 
 One step = one pass of the whole hot path over one batch of synthetic input:
-tree preparation (ancestor bitsets), one layer of tree attention, and the
-verification of the workload (greedy and/or multi-step speculative sampling).
-`value` = tree nodes verified / s over the whole job with inputs resident in
-HBM; `e2e` = the same metric when every step also copies its inputs from
-pinned host memory and reads its results back.
+one layer of tree attention (the kernel builds the topology-aware mask from
+parent[] itself) and the verification of the workload (greedy and/or
+multi-step speculative sampling).  Verification reads only the step's logits
+and proposals, not the attention output, so it runs on a second stream
+concurrently with the attention launch (--serial: after it).  `value` = tree
+nodes verified / s over the whole job with inputs resident in HBM; `e2e` = the
+same metric when every step also copies its inputs from pinned host memory and
+reads its results back.
 
-Timing: W untimed warm-up steps, then exactly K steps between CUDA events on
-the launching stream, bracketed by barrier + synchronize; each step replays a
-CUDA graph of the step on one of R input copies whose total size is at least
-4x the L2 cache, so every step reads its inputs from HBM.  Under torchrun each
-rank runs an independent replica (replicas only: no data exchange) and the
-maximum time over ranks is reported.
+Timing: W untimed warm-up steps (every CUDA graph has been replayed once before
+them), then exactly K steps between CUDA events on the launching stream,
+bracketed by barrier + synchronize; each step replays a CUDA graph of the step
+on one of R input copies whose total size is at least 4x the L2 cache (or one
+copy that alone is), so every step reads its inputs from HBM.  Clocks are
+sampled through NVML every few milliseconds during the timed region.  After
+it, outside the timed region: the median of per-step times, the same steps as
+plain launches (no graph), the serial composition, and each launch alone.  The
+default run also measures every other workload the same way (`per_workload`).
+Under torchrun each rank runs an independent replica (replicas only: no data
+exchange) and the maximum time over ranks is reported.
 
 `--impl reference` times the CPU oracle (the only reference implementation:
 the pages ship no code) on the host cores over a bounded sample of the same
@@ -37,17 +45,23 @@ sys.path.insert(0, ROOT)
 
 METRIC = "tree nodes verified/sec (attn+verify)"
 UNIT = "nodes/s"
-DEFAULT_WORKLOAD = "llama7b-layer-P1024-n20"
+DEFAULT_WORKLOAD = "batch32-P2048-n16"  # the largest configuration that fits one GPU
+# Every workload the bench line also reports in its per_workload record.
+PER_WORKLOAD = ["llama7b-layer-P1024-n20", "batch8-ragged-merge64-mss", "gqa64x8-P32768-n128",
+                "batch32-P2048-n16", "tiny-f32-P128-n16"]
 
 
 def parse_args():
     p = argparse.ArgumentParser(description=__doc__)
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=50000)
-    p.add_argument("--warmup", type=int, default=200)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default=DEFAULT_WORKLOAD)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-per-workload", action="store_true", help="skip the per_workload record")
+    p.add_argument("--serial", action="store_true",
+                   help="verification after attention on one stream (default: concurrent on a second stream)")
     p.add_argument("--no-e2e", action="store_true", help="profiling runs: skip e2e, baselines, JSON line")
     p.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU oracle sample budget")
     p.add_argument("--top-k", type=int, default=0, help="stochastic verification against the top-k warped LLM law")
@@ -105,7 +119,11 @@ def config_of(spec, extra=None):
            "prefix": list(spec.prefix) if isinstance(spec.prefix, tuple) else spec.prefix,
            "nodes_per_request": spec.nodes, "vocab": spec.V,
            "verify": "+".join(v for v, on in (("greedy", spec.greedy), ("stochastic", spec.stochastic)) if on),
-           "tree": spec.tree}
+           "tree": spec.tree,
+           # The same statement in both arms, so that their configs compare equal.
+           "l2": "inputs read from HBM every step: rotating input copies totalling >= 4x L2 "
+                 "(one copy when it alone is that large)",
+           "parallelism": "replicas"}
     if WARP:
         cfg["warp"] = dict(WARP)
     if extra:
@@ -136,15 +154,18 @@ def attention_flops(spec, trees):
     return 4.0 * spec.D * spec.Hq * keys_seen
 
 
-def verify_bytes(spec, trees, n_rejected_rows=0):
-    """Greedy: every logits row once.  Stochastic: every LLM row once plus the
-    full proposal row of each rejected child (count from the oracle)."""
+def verify_bytes(spec, trees, visited_rows=None, rejected_rows=0):
+    """Greedy: every logits row once (the one-pass verifier takes every row's
+    argmax in parallel instead of walking the rows one after another).
+    Stochastic: the LLM row of every node the walk visits, plus the full
+    proposal row of each rejected child (an accepted child needs one entry);
+    without a visit count, every LLM row."""
     N = int(trees.node_offsets[-1])
     b = 0
     if spec.greedy:
         b += N * spec.V * 4
     if spec.stochastic:
-        b += (N + n_rejected_rows) * spec.V * 4
+        b += ((N if visited_rows is None else visited_rows) + rejected_rows) * spec.V * 4
     return b
 
 
@@ -209,14 +230,158 @@ class ClockSampler:
                 "power_w_max": max((num(f[3]) or 0.0) for f in win)}
 
 
-def measured_peaks():
-    """(HBM GB/s, dense bf16 TFLOP/s for a kernel timed alone, which)."""
+def _peaks_file():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
         with open(path) as f:
-            j = json.load(f)
-        return float(j["hbm_gbs"]), float(j["bf16_tflops"]), "measured"
-    return 6800.0, 1900.0, "fallback"
+            return json.load(f)
+    return None
+
+
+def measured_peaks(sustained=False):
+    """(HBM GB/s, dense bf16 TFLOP/s, which): the burst tensor figure for a
+    kernel timed alone, the sustained one for a kernel inside a long run."""
+    j = _peaks_file()
+    if j is not None:
+        tf = j.get("bf16_tflops_sustained", j["bf16_tflops"]) if sustained else j["bf16_tflops"]
+        return float(j["hbm_gbs"]), float(tf), "measured"
+    return 6800.0, (1700.0 if sustained else 1900.0), "fallback"
+
+
+def measured_sm_max_mhz():
+    j = _peaks_file()
+    return float(j.get("sm_max_mhz", 2070.0)) if j is not None else 2070.0
+
+
+class NvmlClockSampler:
+    """SM clock, maximum SM clock, power and clock-event reasons of the bench's
+    GPU, read through NVML's C library every few milliseconds by a thread, so
+    that even a timed region of a few milliseconds has samples.  Queries only:
+    nothing here changes a setting of the GPU."""
+
+    REASON_BITS = {0x8: "hw_slowdown", 0x40: "hw_thermal_slowdown", 0x20: "sw_thermal_slowdown",
+                   0x4: "sw_power_cap"}
+
+    def __init__(self, ids, period_s=0.002):
+        import ctypes
+        self.samples = []
+        self.period = period_s
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.h = ctypes.c_void_p()
+        ok = False
+        for kind, key in ids:
+            if kind == "uuid":
+                ok = self.lib.nvmlDeviceGetHandleByUUID(key.encode(), ctypes.byref(self.h)) == 0
+            elif kind == "pci":
+                ok = self.lib.nvmlDeviceGetHandleByPciBusId_v2(key.encode(), ctypes.byref(self.h)) == 0
+            elif kind == "index":
+                ok = self.lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(int(key)), ctypes.byref(self.h)) == 0
+            if ok:
+                self.which = "%s %s" % (kind, key)
+                break
+        if not ok:
+            raise OSError("no NVML handle for the device")
+        self.reasons_fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(self.lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        self.stop_flag = False
+        self.thread = None
+
+    def mark(self):
+        """One sample taken now by the calling thread (kept with the others)."""
+        s = self.sample()
+        if s is not None:
+            self.samples.append(s)
+
+    def sample(self):
+        import ctypes
+        t = time.time()
+        sm, smax, mw, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        if self.lib.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(sm)) != 0:  # NVML_CLOCK_SM
+            return None
+        self.lib.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(smax))
+        power = float(mw.value) / 1e3 if self.lib.nvmlDeviceGetPowerUsage(self.h, ctypes.byref(mw)) == 0 else None
+        reasons = int(rs.value) if self.reasons_fn(self.h, ctypes.byref(rs)) == 0 else 0
+        return (t, float(sm.value), float(smax.value), power, reasons)
+
+    def _run(self):
+        while not self.stop_flag:
+            # (NVML's queries take milliseconds each on this part, so the
+            # period is a lower bound.)
+            s = self.sample()
+            if s is not None:
+                self.samples.append(s)
+            time.sleep(self.period)
+
+    def start(self):
+        self.thread = threading.Thread(target=self._run, daemon=True)
+        self.thread.start()
+
+    def stop(self):
+        self.stop_flag = True
+        if self.thread is not None:
+            self.thread.join(timeout=2)
+
+    def summary(self, t0, t1):
+        win = [s for s in self.samples if t0 <= s[0] <= t1]
+        note = None
+        if not win:  # nothing inside: the samples nearest to either end (within 50 ms)
+            win = [s for s in self.samples if t0 - 0.05 <= s[0] <= t1 + 0.05]
+            note = "nearest samples within 50 ms of the region (taken right at its edges when it is short)"
+        if not win:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no NVML samples"], "samples": 0,
+                    "source": "nvml"}
+        reasons = sorted({name for s in win for bit, name in self.REASON_BITS.items() if s[4] & bit})
+        out = {"sm_mhz": float(np.median([s[1] for s in win])), "sm_max_mhz": max(s[2] for s in win),
+               "sm_mhz_min": min(s[1] for s in win), "reasons": reasons, "samples": len(win),
+               "power_w_max": max((s[3] or 0.0) for s in win), "source": "nvml (%s), every %g ms"
+               % (self.which, self.period * 1e3)}
+        if note:
+            out["note"] = note
+        return out
+
+
+class ClockRecord:
+    """Clock samples during the bench: NVML (a few ms apart) when its library
+    loads, else nvidia-smi (200 ms apart)."""
+
+    def __init__(self, dev):
+        import torch
+        props = torch.cuda.get_device_properties(dev)
+        ids = []
+        uuid = getattr(props, "uuid", None)
+        if uuid is not None:
+            u = str(uuid)
+            ids += [("uuid", u if u.startswith("GPU-") else "GPU-" + u)]
+        if hasattr(props, "pci_bus_id") and hasattr(props, "pci_device_id"):
+            ids.append(("pci", "%08x:%02x:%02x.0" % (getattr(props, "pci_domain_id", 0), props.pci_bus_id,
+                                                     props.pci_device_id)))
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        parts = [x.strip() for x in vis.split(",") if x.strip()]
+        if parts and all(x.isdigit() for x in parts) and dev.index < len(parts):
+            ids.append(("index", parts[dev.index]))
+        elif not parts:
+            ids.append(("index", dev.index))
+        try:
+            self.impl = NvmlClockSampler(ids)
+        except (OSError, AttributeError):
+            self.impl = ClockSampler(int(ids[-1][1]) if ids and ids[-1][0] == "index" else dev.index)
+
+    def start(self):
+        self.impl.start()
+
+    def mark(self):
+        """A synchronous sample (NVML only): taken right before and right after
+        a timed region too short for the sampling thread to see."""
+        if hasattr(self.impl, "mark"):
+            self.impl.mark()
+
+    def stop(self):
+        self.impl.stop()
+
+    def summary(self, t0, t1):
+        return self.impl.summary(t0, t1)
 
 
 KERNEL_SOURCES = {
@@ -356,7 +521,7 @@ def run_reference(args, spec):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": config_of(spec, {"reference": "CPU fp64 oracle (the pages ship no code)"}),
+            "config": config_of(spec), "reference_impl": "CPU fp64 oracle (the pages ship no code)",
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                              "sample": "per step: " + sample, "single_core": base["single_core"],
                              "nproc": base["nproc"], "cpu_model": base["cpu_model"]},
@@ -365,6 +530,281 @@ def run_reference(args, spec):
 
 
 # --------------------------------------------------------------------------- GPU
+
+
+class DeviceWorkload:
+    """One workload on the device: R rotating copies of the step's inputs (their
+    total is at least 4x the L2 cache, or one copy is already larger, so each
+    step reads its inputs from HBM), each with its own outputs and workspaces,
+    and the calls of one step.
+
+    Within a step, verification reads only the given logits and proposals, so
+    it does not wait for the attention launch: with ``overlap`` the
+    verification launches go on a second stream forked from and joined back to
+    the main one, and the two run concurrently."""
+
+    def __init__(self, spec, tsv, dev, stream, overlap=True):
+        import torch
+        self.spec, self.tsv, self.dev, self.stream, self.overlap = spec, tsv, dev, stream, overlap
+        self.side = torch.cuda.Stream(dev)
+        trees, att, gi, si = workload_inputs(spec)
+        self.trees, self.att, self.gi, self.si = trees, att, gi, si
+        self.B, self.N = spec.B, int(trees.node_offsets[-1])
+
+        def to_dev(x):
+            t = x if isinstance(x, torch.Tensor) else torch.as_tensor(np.ascontiguousarray(x))
+            return t.to(dev)
+
+        base = {"q": to_dev(att.q), "k": to_dev(att.k_cache), "v": to_dev(att.v_cache),
+                "parent": to_dev(trees.parent), "offs": to_dev(trees.node_offsets),
+                "plen": to_dev(trees.prefix_len)}
+        if gi is not None:
+            base.update(logits=to_dev(gi.logits), gtok=to_dev(gi.tokens))
+        if si is not None:
+            base.update(llm=to_dev(si.llm_logits), ssm=to_dev(si.ssm_probs), stok=to_dev(si.tokens),
+                        ua=to_dev(si.u_accept), us=to_dev(si.u_sample))
+        self.per_copy = sum(t.numel() * t.element_size() for t in base.values())
+        l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+        self.R = int(min(64, max(1, math.ceil(4 * l2 / self.per_copy))))
+        self.copies = [base] + [{k: t.clone() for k, t in base.items()} for _ in range(self.R - 1)]
+        h = tsv.handle(dev.index)
+        B, N = self.B, self.N
+        code = tsv.TSV_BF16 if spec.dtype == "bf16" else tsv.TSV_F32
+        ws_attn = tsv.tsv_tree_attention_workspace_size(h, code, B, trees.prefix_len, trees.node_offsets, spec.Hq,
+                                                        spec.Hkv, spec.D, False)
+        ws_g = tsv.tsv_tree_verify_greedy_workspace_size(h, B, N, spec.V)
+        ws_s = tsv.tsv_tree_verify_stochastic_workspace_size(h, B, N, spec.V)
+        self.ws_sizes = (ws_attn, ws_g, ws_s)
+
+        def make_state(c):
+            st = {"status": torch.zeros(B, dtype=torch.int32, device=dev), "out": torch.empty_like(c["q"]),
+                  "ws_attn": torch.zeros(max(ws_attn, 1), dtype=torch.uint8, device=dev),
+                  "ws_g": torch.zeros(max(ws_g, 1), dtype=torch.uint8, device=dev),
+                  "ws_s": torch.zeros(max(ws_s, 1), dtype=torch.uint8, device=dev)}
+            mk = lambda: {k: torch.empty(n, dtype=torch.int32, device=dev) for k, n in
+                          (("path", N), ("accept_len", B), ("bonus", B), ("n_tried", B), ("status", B))}
+            st["g"], st["s"] = mk(), mk()
+            return st
+
+        self.states = [make_state(c) for c in self.copies]
+        # Kernels per step: one attention launch (masks built and splits merged
+        # inside; the fp32 CUDA-core path first prepares the ancestor bitsets in
+        # a launch of its own), one per verification kind.
+        self.kernels_per_step = (1 if spec.dtype == "bf16" else 2) + (gi is not None) + (si is not None)
+
+    # ------------------------------------------------------------------ calls
+    def attention(self, c, st):
+        # The kernel builds the ancestor masks from parent[] itself (and
+        # validates the tree), so tree preparation runs inside this launch.
+        t = self.trees
+        self.tsv.tree_attention(c["q"], c["k"], c["v"], t.prefix_len, t.node_offsets, c["plen"], c["offs"],
+                                parent=c["parent"], anc=None, out=st["out"], workspace=st["ws_attn"],
+                                status=st["status"])
+
+    def greedy(self, c, st):
+        self.tsv.tree_verify_greedy(c["logits"], c["gtok"], c["parent"], c["offs"], workspace=st["ws_g"],
+                                    out=st["g"])
+
+    def stochastic(self, c, st):
+        self.tsv.tree_verify_stochastic(c["llm"], c["ssm"], c["stok"], c["parent"], c["offs"], c["ua"], c["us"],
+                                        workspace=st["ws_s"], out=st["s"], **WARP)
+
+    def verify(self, c, st):
+        if self.gi is not None:
+            self.greedy(c, st)
+        if self.si is not None:
+            self.stochastic(c, st)
+
+    def step(self, c, st, overlap=None):
+        import torch
+        overlap = self.overlap if overlap is None else overlap
+        if not overlap:
+            self.attention(c, st)
+            self.verify(c, st)
+            return
+        self.side.wait_stream(self.stream)
+        with torch.cuda.stream(self.side):
+            self.verify(c, st)
+        self.attention(c, st)
+        self.stream.wait_stream(self.side)
+
+    # ------------------------------------------------------------------ graphs
+    def _graph(self, fn):
+        import torch
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=self.stream):
+            fn()
+        return g
+
+    def capture(self):
+        """CUDA graphs: all R copies' steps in one graph (so the host replays one
+        graph per R steps and stays ahead of the GPU), one graph per copy, and
+        graphs of the attention and verification launches alone."""
+        import torch
+        cs = list(zip(self.copies, self.states))
+        for c, st in cs:  # eager run once; checks the statuses
+            self.step(c, st)
+        torch.cuda.synchronize()
+        assert (self.states[0]["status"].cpu() == 0).all()
+        self.g_steps = self._graph(lambda: [self.step(c, st) for c, st in cs])
+        self.g_one = [self._graph(lambda c=c, st=st: self.step(c, st)) for c, st in cs]
+        self.g_serial = self._graph(lambda: [self.step(c, st, overlap=False) for c, st in cs])
+        self.g_attn = self._graph(lambda: [self.attention(c, st) for c, st in cs])
+        self.g_greedy = self._graph(lambda: [self.greedy(c, st) for c, st in cs]) if self.gi is not None else None
+        self.g_mss = self._graph(lambda: [self.stochastic(c, st) for c, st in cs]) if self.si is not None else None
+        # Every graph is replayed once here, so none launches for the first time
+        # inside a timed region.
+        for g in [self.g_steps, self.g_serial, self.g_attn, self.g_greedy, self.g_mss] + self.g_one:
+            if g is not None:
+                g.replay()
+        torch.cuda.synchronize()
+        counted = graph_kernel_count(self.g_one[0])
+        if counted is not None:
+            assert counted == self.kernels_per_step, (counted, self.kernels_per_step)
+
+    def run_steps(self, k):
+        for _ in range(k // self.R):
+            self.g_steps.replay()
+        for i in range(k % self.R):
+            self.g_one[i].replay()
+
+    # ------------------------------------------------------------------ timing forms
+    def _events(self, n):
+        import torch
+        return [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+
+    def graph_ms(self, g, launches_per_replay, reps):
+        """Mean device time per launch of a pre-replayed graph, replayed reps times."""
+        import torch
+        e0, e1 = self._events(2)
+        torch.cuda.synchronize()
+        e0.record(self.stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(self.stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / (reps * launches_per_replay)
+
+    def per_step_graph_ms(self, n):
+        """Device time of each of n steps replayed one graph per step (events between steps)."""
+        import torch
+        ev = self._events(n + 1)
+        torch.cuda.synchronize()
+        ev[0].record(self.stream)
+        for i in range(n):
+            self.g_one[i % self.R].replay()
+            ev[i + 1].record(self.stream)
+        torch.cuda.synchronize()
+        return [ev[i].elapsed_time(ev[i + 1]) for i in range(n)]
+
+    def per_step_plain_ms(self, n):
+        """Device time of each of n steps issued as plain launches from the host
+        (no graph; the calls go through the C ABI every step)."""
+        import torch
+        cs = list(zip(self.copies, self.states))
+        for c, st in cs[:3]:
+            self.step(c, st)
+        ev = self._events(n + 1)
+        torch.cuda.synchronize()
+        ev[0].record(self.stream)
+        for i in range(n):
+            c, st = cs[i % self.R]
+            self.step(c, st)
+            ev[i + 1].record(self.stream)
+        torch.cuda.synchronize()
+        return [ev[i].elapsed_time(ev[i + 1]) for i in range(n)]
+
+    def walk_rows(self):
+        """(visited, rejected) rows of copy 0's last stochastic walk, as the
+        kernel reports them: accept_len + 1 visited nodes per request, and every
+        child tried but not accepted (each needs its full proposal row)."""
+        if self.si is None:
+            return None, 0
+        s = self.states[0]["s"]
+        visited = int((s["accept_len"] + 1).sum().item())
+        return visited, int((s["n_tried"] - s["accept_len"]).sum().item())
+
+    def measure(self, n_steps):
+        """The step and each of its launches alone, outside any timed region of the bench line."""
+        reps = max(1, n_steps // self.R)
+        steps = self.per_step_graph_ms(n_steps)
+        out = {"graph_mean_ms": self.graph_ms(self.g_steps, self.R, reps),
+               "graph_median_ms": float(np.median(steps)),
+               "serial_graph_mean_ms": self.graph_ms(self.g_serial, self.R, reps),
+               "attention_ms": self.graph_ms(self.g_attn, self.R, reps)}
+        if self.g_greedy is not None:
+            out["greedy_ms"] = self.graph_ms(self.g_greedy, self.R, reps)
+        if self.g_mss is not None:
+            out["stochastic_ms"] = self.graph_ms(self.g_mss, self.R, reps)
+        plain = self.per_step_plain_ms(n_steps)
+        out["plain_median_ms"] = float(np.median(plain))
+        out["plain_mean_ms"] = float(np.mean(plain))
+        return out
+
+
+def attention_kernel_name(spec, trees):
+    G = spec.Hq // spec.Hkv
+    sizes = np.diff(trees.node_offsets)
+    keys_kernel = all(int(n) * G <= 64 for n in sizes) and 64 % G == 0
+    tile_pairs = any(int(n) * G > 128 for n in sizes)  # some request has 2+ row tiles
+    return ("tree_attn_simt_kernel" if spec.dtype != "bf16" else
+            "tree_attn_keys_kernel" if keys_kernel else
+            "tree_attn_tc_kernel" if tile_pairs else "tree_attn_tc1_kernel")
+
+
+def attention_exps(spec, trees):
+    """Exponentials of one tree-attention launch: one per query row per key it sees."""
+    return attention_flops(spec, trees) / (4.0 * spec.D)
+
+
+def sfu_exp_rate(num_sms):
+    """Exponentials per second: 16 ex2 per clock per SM at the maximum SM clock."""
+    return 16.0 * num_sms * measured_sm_max_mhz() * 1e6
+
+
+def rooflines(spec, trees, attn_ms, step_ms, walk_rows, num_sms):
+    """(attention-launch roofline, step roofline).  The attention launch is
+    timed alone (burst tensor peak); the step is a long run (sustained peak)."""
+    peak, peak_tf, peak_kind = measured_peaks()
+    peak_tf_sus = measured_peaks(sustained=True)[1]
+    abytes, aflops, aexps = attention_bytes(spec, trees), attention_flops(spec, trees), attention_exps(spec, trees)
+    kernel = attention_kernel_name(spec, trees)
+    gbs = abytes / (attn_ms * 1e-3) / 1e9
+    t_bytes, t_flops, t_exps = abytes / (peak * 1e9), aflops / (peak_tf * 1e12), aexps / sfu_exp_rate(num_sms)
+    if spec.dtype == "bf16" and t_flops > t_bytes:
+        tf = aflops / (attn_ms * 1e-3) / 1e12
+        att = {"bound": "tensor", "achieved": tf, "peak": peak_tf, "unit": "TFLOP/s", "frac": tf / peak_tf,
+               "peak_kind": peak_kind + " bf16_tflops (burst)"}
+    else:
+        att = {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
+               "peak_kind": peak_kind + " hbm_gbs"}
+    att.update({"traffic": recorded_traffic(spec.name, kernel), "kernel": kernel, "launch_ms": attn_ms,
+                "algorithmic_bytes": abytes, "algorithmic_flops": aflops, "exponentials": aexps,
+                "hbm_gbs": gbs, "hbm_frac": gbs / peak,
+                "combined_frac": max(t_bytes, t_flops if spec.dtype == "bf16" else 0.0, t_exps) / (attn_ms * 1e-3)})
+    vbytes = verify_bytes(spec, trees, *walk_rows)
+    sbytes = abytes + vbytes
+    sgbs = sbytes / (step_ms * 1e-3) / 1e9
+    s_flops = aflops / (peak_tf_sus * 1e12) if spec.dtype == "bf16" else 0.0
+    step = {"bound": "hbm", "achieved": sgbs, "peak": peak, "unit": "GB/s", "frac": sgbs / peak,
+            "peak_kind": peak_kind + " hbm_gbs",
+            "algorithmic_bytes": sbytes, "attention_bytes": abytes, "verify_bytes": vbytes,
+            "stochastic_rows": {"visited_llm": walk_rows[0], "rejected_proposals": walk_rows[1]},
+            "combined_frac": max(sbytes / (peak * 1e9), s_flops, t_exps) / (step_ms * 1e-3),
+            "what": "KV + Q + O of the attention launch, every greedy logits row, the visited LLM rows and "
+                    "rejected proposal rows of the stochastic walk; one step / step time"}
+    return att, step
+
+
+def workload_summary(spec, w, forms, step_ms, num_sms):
+    """A compact record of one workload measured in the same run."""
+    att, step = rooflines(spec, w.trees, forms["attention_ms"], step_ms, w.walk_rows(), num_sms)
+    out = {"nodes": w.N, "step_ms": step_ms, "nodes_per_s": w.N / (step_ms * 1e-3),
+           "attention": {k: att[k] for k in ("kernel", "launch_ms", "bound", "frac", "hbm_frac", "combined_frac")},
+           "step_roofline": {k: step[k] for k in ("frac", "combined_frac", "algorithmic_bytes")},
+           "rotating_copies": w.R}
+    out["timing"] = {k: v for k, v in forms.items() if k != "attention_ms"}
+    return out
 
 
 def run_ours(args, spec):
@@ -378,110 +818,16 @@ def run_ours(args, spec):
     dev = torch.device("cuda", local)
     import tree_speculative_verification_attention_gb300 as tsv
 
-    trees, att, gi, si = workload_inputs(spec)
-    B, N = spec.B, int(trees.node_offsets[-1])
     stream = torch.cuda.Stream(dev)
     torch.cuda.set_stream(stream)
+    num_sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    w = DeviceWorkload(spec, tsv, dev, stream, overlap=not args.serial)
+    w.capture()
+    N, R, kernels_per_step = w.N, w.R, w.kernels_per_step
 
-    def to_dev(x):
-        t = x if isinstance(x, torch.Tensor) else torch.as_tensor(np.ascontiguousarray(x))
-        return t.to(dev)
-
-    base = {"q": to_dev(att.q), "k": to_dev(att.k_cache), "v": to_dev(att.v_cache),
-            "parent": to_dev(trees.parent), "offs": to_dev(trees.node_offsets),
-            "plen": to_dev(trees.prefix_len)}
-    if gi is not None:
-        base.update(logits=to_dev(gi.logits), gtok=to_dev(gi.tokens))
-    if si is not None:
-        base.update(llm=to_dev(si.llm_logits), ssm=to_dev(si.ssm_probs), stok=to_dev(si.tokens),
-                    ua=to_dev(si.u_accept), us=to_dev(si.u_sample))
-    per_copy = sum(t.numel() * t.element_size() for t in base.values())
-    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    R = int(min(64, max(1, math.ceil(4 * l2 / per_copy))))
-    copies = [base] + [{k: t.clone() for k, t in base.items()} for _ in range(R - 1)]
-
-    h = tsv.handle(local)
-    ws_attn = tsv.tsv_tree_attention_workspace_size(h, tsv.TSV_BF16 if spec.dtype == "bf16" else tsv.TSV_F32,
-                                                    B, trees.prefix_len, trees.node_offsets, spec.Hq,
-                                                    spec.Hkv, spec.D, False)
-    ws_g = tsv.tsv_tree_verify_greedy_workspace_size(h, B, N, spec.V)
-    ws_s = tsv.tsv_tree_verify_stochastic_workspace_size(h, B, N, spec.V)
-    ws_bytes = max(ws_attn, 1) + max(ws_g, 1) + max(ws_s, 1) + 3 * 256
-
-    def make_state(c):
-        st = {"anc": torch.empty((N, tsv.TSV_ANC_WORDS), dtype=torch.int32, device=dev),
-              "depth": torch.empty(N, dtype=torch.int32, device=dev),
-              "status": torch.zeros(B, dtype=torch.int32, device=dev),
-              "out": torch.empty_like(c["q"]),
-              "ws": torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)}
-        st["ws_attn"] = st["ws"][:max(ws_attn, 1)]
-        off = (max(ws_attn, 1) + 255) // 256 * 256
-        st["ws_g"] = st["ws"][off:off + max(ws_g, 1)]
-        off += (max(ws_g, 1) + 255) // 256 * 256
-        st["ws_s"] = st["ws"][off:off + max(ws_s, 1)]
-        mk = lambda: {k: torch.empty(n, dtype=torch.int32, device=dev) for k, n in
-                      (("path", N), ("accept_len", B), ("bonus", B), ("n_tried", B), ("status", B))}
-        st["g"], st["s"] = mk(), mk()
-        return st
-
-    def attention(c, st):
-        # The kernel builds the ancestor masks from parent[] itself (and
-        # validates the tree), so tree preparation runs inside this launch.
-        tsv.tree_attention(c["q"], c["k"], c["v"], trees.prefix_len, trees.node_offsets, c["plen"],
-                           c["offs"], parent=c["parent"], anc=None, out=st["out"],
-                           workspace=st["ws_attn"], status=st["status"])
-
-    def step(c, st):
-        attention(c, st)
-        if gi is not None:
-            tsv.tree_verify_greedy(c["logits"], c["gtok"], c["parent"], c["offs"], workspace=st["ws_g"],
-                                   out=st["g"])
-        if si is not None:
-            tsv.tree_verify_stochastic(c["llm"], c["ssm"], c["stok"], c["parent"], c["offs"], c["ua"],
-                                       c["us"], workspace=st["ws_s"], out=st["s"], **WARP)
-
-    states = [make_state(c) for c in copies]
-    # Eager run once (also checks statuses), then capture one graph per input copy.
-    for c, st in zip(copies, states):
-        step(c, st)
-    torch.cuda.synchronize()
-    assert (states[0]["status"].cpu() == 0).all()
-    # One graph holds one step on every input copy (R steps), so the host
-    # replays one graph per R steps and stays ahead of the GPU.
-    g_steps = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g_steps, stream=stream):
-        for c, st in zip(copies, states):
-            step(c, st)
-    g_one = []
-    for c, st in zip(copies, states):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            step(c, st)
-        g_one.append(g)
-    g_attn = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g_attn, stream=stream):
-        for c, st in zip(copies, states):
-            attention(c, st)
-    torch.cuda.synchronize()
-    # Kernels per step: one attention launch (masks built inside, splits merged
-    # inside; the fp32 CUDA-core path first prepares the ancestor bitsets in a
-    # launch of its own), one for greedy verification, one for stochastic
-    # verification; checked against the captured graph when torch exposes it.
-    attn_kernels = 1 if spec.dtype == "bf16" else 2
-    kernels_per_step = attn_kernels + (1 if gi is not None else 0) + (1 if si is not None else 0)
-    counted = graph_kernel_count(g_one[0])
-    if counted is not None:
-        assert counted == kernels_per_step, (counted, kernels_per_step)
-
-    sampler = ClockSampler(local)
-    sampler.start()
-    def run_steps(k):
-        for _ in range(k // R):
-            g_steps.replay()
-        for i in range(k % R):
-            g_one[i].replay()
-
-    run_steps(args.warmup)
+    clocks = ClockRecord(dev)
+    clocks.start()
+    w.run_steps(max(3, args.warmup))
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
@@ -490,76 +836,69 @@ def run_ours(args, spec):
     if world > 1:
         dist.barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks.mark()
     t_wall0 = time.time()
     e0.record(stream)
-    run_steps(args.steps)
+    w.run_steps(args.steps)
     e1.record(stream)
     torch.cuda.synchronize()
     t_wall1 = time.time()
+    clocks.mark()
     if world > 1:
         dist.barrier()
     ms_total = whole_job_ms(e0.elapsed_time(e1), world, dev)
     ms_step = ms_total / args.steps
     value = whole_job_value(ms_total, args.steps, N, world)
+    timed_clocks = clocks.summary(t_wall0, t_wall1)
 
-    # ---------------------------------------------------------------- attention kernel, per launch
-    # Average launch duration of the attention call inside a graph of R
-    # back-to-back launches (one per input copy), events on the launching stream.
-    reps = max(1, min(2000, args.steps) // R)
-    g_attn.replay()
-    torch.cuda.synchronize()
-    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a0.record(stream)
-    for _ in range(reps):
-        g_attn.replay()
-    a1.record(stream)
-    torch.cuda.synchronize()
-    attn_ms = a0.elapsed_time(a1) / (reps * R)
-    sampler.stop()
-    clocks = sampler.summary(t_wall0, t_wall1)
+    # ---------------------------------------------------------------- the other timing forms
+    forms = w.measure(int(min(max(args.steps, 20), 200)))
+    attn_ms = forms["attention_ms"]
     if args.no_e2e:
-        print(json.dumps({"ms_per_step": ms_step, "attn_launch_ms": attn_ms}), flush=True)
+        clocks.stop()
+        print(json.dumps({"ms_per_step": ms_step, "attn_launch_ms": attn_ms, "timing": forms}), flush=True)
         return
 
-    # ---------------------------------------------------------------- end to end
-    e2e = measure_e2e(args, spec, trees, att, gi, si, h, tsv, dev, stream, ws_attn, ws_g, ws_s)
+    roofline, roofline_step = rooflines(spec, w.trees, attn_ms, ms_step, w.walk_rows(), num_sms)
+    e2e = measure_e2e(args, spec, w.trees, w.att, w.gi, w.si, tsv.handle(local), tsv, dev, stream, *w.ws_sizes)
 
-    # ---------------------------------------------------------------- roofline
-    peak, peak_tf, peak_kind = measured_peaks()
-    abytes = attention_bytes(spec, trees)
-    aflops = attention_flops(spec, trees)
-    achieved = abytes / (attn_ms * 1e-3) / 1e9
-    keys_kernel = all(int(n) * (spec.Hq // spec.Hkv) <= 64 for n in np.diff(trees.node_offsets)) and \
-        64 % (spec.Hq // spec.Hkv) == 0
-    G = spec.Hq // spec.Hkv
-    tile_pairs = any(int(n) * G > 128 for n in np.diff(trees.node_offsets))  # some request has 2+ row tiles
-    kernel_name = ("tree_attn_simt_kernel" if spec.dtype != "bf16" else
-                   "tree_attn_keys_kernel" if keys_kernel else
-                   "tree_attn_tc_kernel" if tile_pairs else "tree_attn_tc1_kernel")
-    traffic = recorded_traffic(spec.name, kernel_name)
-    # The bound is whichever of bytes / bandwidth and FLOPs / tensor peak takes longer.
-    tensor_bound = spec.dtype == "bf16" and aflops / (peak_tf * 1e12) > abytes / (peak * 1e9)
-    if tensor_bound:
-        tf = aflops / (attn_ms * 1e-3) / 1e12
-        roofline = {"bound": "tensor", "achieved": tf, "peak": peak_tf, "unit": "TFLOP/s",
-                    "frac": tf / peak_tf, "peak_kind": peak_kind + " bf16_tflops (burst)"}
-    else:
-        roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                    "frac": achieved / peak, "peak_kind": peak_kind + " hbm_gbs"}
-    roofline.update({"traffic": traffic, "kernel": kernel_name, "launch_ms": attn_ms,
-                     "algorithmic_bytes": abytes, "algorithmic_flops": aflops,
-                     "hbm_gbs": achieved, "hbm_frac": achieved / peak})
-    step_bytes = abytes + verify_bytes(spec, trees)
+    per_workload = None
+    if rank == 0 and world == 1 and not args.no_per_workload:
+        import workloads as W
+        per_workload = {spec.name: workload_summary(spec, w, forms, ms_step, num_sms)}
+        per_workload[spec.name]["clocks"] = timed_clocks
+        del w
+        torch.cuda.empty_cache()
+        for name in PER_WORKLOAD:
+            if name == spec.name:
+                continue
+            t0 = time.time()
+            ow = DeviceWorkload(W.SPECS[name], tsv, dev, stream, overlap=not args.serial)
+            ow.capture()
+            ow.run_steps(max(3, args.warmup))
+            of = ow.measure(200)
+            t1 = time.time()
+            per_workload[name] = workload_summary(W.SPECS[name], ow, of, of["graph_mean_ms"], num_sms)
+            per_workload[name]["clocks"] = clocks.summary(t0, t1)
+            del ow
+            torch.cuda.empty_cache()
+    clocks.stop()
+
+    how = ("mean over the K timed steps; CUDA graph replay (one graph per %d step(s), each step on the next of "
+           "%d rotating input copies); verification launches %s" %
+           (R, R, "after the attention launch on one stream" if args.serial else
+            "on a second stream, concurrent with the attention launch"))
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": spec.dtype, "data": "synthetic",
-            "config": config_of(spec, {"l2": "rotating %d input copies (%.0f MB > 4x L2)" % (R, R * per_copy / 1e6),
-                                       "graph": "one CUDA graph per step", "parallelism": "replicas"}),
-            "roofline": roofline,
-            "step_hbm_gbs": step_bytes / (ms_step * 1e-3) / 1e9,
-            "step_roofline_frac": step_bytes / (ms_step * 1e-3) / 1e9 / peak,
-            "e2e": e2e, "gpu_launches": kernels_per_step * args.steps, "clocks": clocks}
+            "config": config_of(spec),
+            "roofline": roofline, "roofline_step": roofline_step,
+            "timing": dict(forms, value=how, rotating_copies=R),
+            "e2e": e2e, "gpu_launches": kernels_per_step * args.steps, "clocks": timed_clocks}
+    if per_workload is not None:
+        line["per_workload"] = per_workload
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        trees, att, gi, si = workload_inputs(spec)
         line["cpu_baseline"] = oracle_baseline(spec, trees, att, gi, si, args.cpu_seconds,
                                                choose_heads_sample(spec, trees), N)
     if rank == 0:

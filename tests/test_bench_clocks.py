@@ -42,3 +42,33 @@ def test_unparsable_fields_are_skipped():
     s = _sampler([(1.0, _line("[N/A]", 2070, "[N/A]")), (1.1, _line(2000, "[N/A]", 250))])
     c = s.summary(1.0, 1.1)
     assert c["sm_mhz"] == 2000.0 and c["sm_max_mhz"] == 2070.0 and c["power_w_max"] == 250.0
+
+
+def _nvml(samples, period=0.002):
+    s = bench.NvmlClockSampler.__new__(bench.NvmlClockSampler)
+    s.samples, s.period, s.which = samples, period, "index 0"
+    return s
+
+
+def test_nvml_samples_inside_a_short_region():
+    # (time, SM MHz, max SM MHz, power W, clock-event reason bits)
+    s = _nvml([(0.990, 1500.0, 2070.0, 150.0, 0x1),           # idle, before the region: ignored
+               (1.000, 2070.0, 2070.0, 600.0, 0x0), (1.002, 2055.0, 2070.0, 620.0, 0x0),
+               (1.004, 2070.0, 2070.0, 640.0, 0x4),            # power cap (kept, reported)
+               (1.100, 900.0, 2070.0, 100.0, 0x0)])            # after: ignored
+    c = s.summary(1.0, 1.005)
+    assert c["samples"] == 3 and c["sm_mhz"] == 2070.0 and c["sm_mhz_min"] == 2055.0
+    assert c["sm_max_mhz"] == 2070.0 and c["power_w_max"] == 640.0 and c["reasons"] == ["sw_power_cap"]
+
+
+def test_nvml_throttle_bits_map_to_the_rejecting_reasons():
+    s = _nvml([(5.0, 1200.0, 2070.0, 1400.0, 0x8 | 0x20 | 0x40)])
+    assert s.summary(4.9, 5.1)["reasons"] == ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"]
+
+
+def test_nvml_region_shorter_than_the_sampling_period():
+    s = _nvml([(2.000, 2070.0, 2070.0, 500.0, 0), (2.040, 2040.0, 2070.0, 500.0, 0)])
+    c = s.summary(2.010, 2.012)  # no sample inside: the nearest ones, and a note saying so
+    assert c["samples"] == 2 and "nearest" in c["note"]
+    c = _nvml([]).summary(0.0, 1.0)
+    assert c["samples"] == 0 and c["sm_mhz"] is None

@@ -21,7 +21,13 @@ def test_reference_arm_prints_one_contract_line():
     assert d["impl"] == "reference"
     assert d["metric"] == "tree nodes verified/sec (attn+verify)" and d["unit"] == "nodes/s"
     assert d["higher_is_better"] is True and d["steps"] == 1 and d["warmup"] == 3
-    assert d["value"] > 0 and d["config"]["workload"] == "llama7b-layer-P1024-n20"
+    sys.path.insert(0, ROOT)
+    import bench
+    import workloads as W
+    # The default workload is the largest single-GPU one, and the config is the
+    # very dict the GPU arm prints for it (so the two arms compare equal).
+    assert bench.DEFAULT_WORKLOAD == "batch32-P2048-n16"
+    assert d["value"] > 0 and d["config"] == bench.config_of(W.SPECS[bench.DEFAULT_WORKLOAD])
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1 and cb["sample"]
     # ... and the same oracle on one core, with the host it ran on.

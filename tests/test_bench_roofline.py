@@ -65,3 +65,12 @@ def test_attention_flops_random_trees(name):
 def test_greedy_bytes():
     spec = W.SPECS["llama7b-layer-P1024-n20"]
     assert bench.verify_bytes(spec, W.make_trees(spec)) == 20 * 32000 * 4  # 2.56 MB
+
+
+def test_stochastic_bytes_count_the_visited_and_rejected_rows():
+    # Batch 32 x 16 nodes, V 32000, greedy + stochastic: every greedy row, then
+    # the LLM rows the walk visited and the proposal rows of rejected children.
+    spec = W.SPECS["batch32-P2048-n16"]
+    trees = W.make_trees(spec)
+    assert bench.verify_bytes(spec, trees, 40, 100) == 512 * 32000 * 4 + (40 + 100) * 32000 * 4
+    assert bench.verify_bytes(spec, trees) == 2 * 512 * 32000 * 4  # no visit count: every LLM row
