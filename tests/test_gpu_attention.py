@@ -95,6 +95,30 @@ def test_batch32_sampled(tsv):
     compare_attention(out, att, trees, "bf16", reqs=[0, 17, 31], kv_heads=[0, 31])
 
 
+# Batches with more (request, KV head) units than SMs and one key chunk per
+# unit run as a persistent launch: one CTA per SM walks a sequence of units,
+# its producer streaming the next unit's K/V while the previous one finishes.
+# Every output is checked, with NaN in the cache rows no request may read.
+PERSISTENT = {
+    "b16-h32-ragged": dict(B=16, Hq=32, Hkv=32, D=128, nodes=16, prefix=(0, 600), max_depth=6),
+    "b128-h4-d64-short": dict(B=128, Hq=4, Hkv=4, D=64, nodes=5, prefix=(0, 300), max_depth=3),
+    "b64-gqa4-n16": dict(B=64, Hq=16, Hkv=4, D=128, nodes=16, prefix=(100, 1500), max_depth=5),
+}
+
+
+@pytest.mark.parametrize("name", list(PERSISTENT))
+@pytest.mark.parametrize("use_prepare", [False, True])
+def test_persistent_keys_kernel_full(tsv, name, use_prepare):
+    kw = PERSISTENT[name]
+    spec = W.Spec(name, 3500 + list(PERSISTENT).index(name), "bf16", kw["B"], kw["Hq"], kw["Hkv"], kw["D"],
+                  10, kw["prefix"], kw["nodes"], "random", max_depth=kw["max_depth"], pad_value=float("nan"))
+    trees = W.make_trees(spec)
+    att = W.make_attention_inputs(spec, trees)
+    out, st = run_attention(tsv, trees, att, use_prepare=use_prepare)
+    assert (st.cpu() == 0).all()
+    compare_attention(out, att, trees, "bf16")
+
+
 # ------------------------------------------------------------------ fuzz and edges
 
 

@@ -198,6 +198,8 @@ void build_plan_keys(AttnPlan& p, int num_sms, int32_t B, const int32_t* prefix_
   p.unit_start[B] = (int32_t)units;
   p.n_units = (int32_t)units;
   p.prefetch_l2 = units <= num_sms ? 1 : 0;
+  p.persistent = (best_k == 1 && units > num_sms && units <= (int64_t)kKeysMaxUnitsPerCta * num_sms) ? 1 : 0;
+  p.grid = p.persistent ? num_sms : (int32_t)units;
 }
 
 // The keys-on-lanes kernel serves batches whose requests all have at most 64

@@ -51,6 +51,12 @@ struct AttnPlan {
   // so each CTA pulls its first K/V blocks into L2 before waiting for the
   // previous kernel; with later waves the prefetch would only add traffic.
   int32_t prefetch_l2;
+  // Keys-on-lanes kernel with one chunk per request and more units than SMs:
+  // a persistent launch of `grid` CTAs (one per SM), each taking a sequence of
+  // units, so that its producer streams the next unit's K/V while the key
+  // lanes finish the previous unit.
+  int32_t persistent;
+  int32_t grid;
   // Rows-on-lanes kernel: 1 = two 128-row query tiles per CTA (units are
   // tile pairs), 0 = one tile per CTA (every request has mtiles <= 1).
   int32_t tc_tile_pairs;
@@ -119,6 +125,7 @@ size_t attention_tc1_smem_bytes(int D);
 
 constexpr int kKeysBlockKeys = 128;  // keys per block of the keys-on-lanes kernel
 constexpr int kKeysTileRows = 64;    // query rows per CTA of the keys-on-lanes kernel
+constexpr int kKeysMaxUnitsPerCta = 48;  // units one CTA of a persistent keys launch may take
 cudaError_t launch_attention_keys(const CUtensorMap& tmap_q, const CUtensorMap& tmap_k,
                                   const CUtensorMap& tmap_v, const AttnPlan& plan,
                                   const int32_t* parent, const uint32_t* anc, void* out,
