@@ -69,6 +69,7 @@ constexpr float kKeysOverflow = 32.f;        // log2 units
 constexpr int kBarKeysSetup = 1;             // key lanes + MMA warp + epilogue warps
 constexpr int kBarKeys = 2;                  // key lanes
 constexpr int kKeysMaxUnits = kKeysMaxUnitsPerCta;
+constexpr int kKeysStages = 3;               // K/V ring depth
 
 // One unit of work: (request b, KV head g, key chunk c, M-tile mt) and the
 // key range it streams.  Each CTA writes the units it takes into a table in
@@ -138,11 +139,12 @@ __device__ __forceinline__ int keys_fill_units(const AttnPlan& plan, KeysUnit* t
 // units that have blocks (the Q buffer's phases follow it).
 struct KeysCursor {
   int k, j, jg, kq, nblk;
+  int st, ph;  // ring stage of block jg (jg % stages) and its use count parity ((jg / stages) & 1)
   bool valid;
 };
 
 __device__ __forceinline__ KeysCursor keys_cursor_first(const KeysUnit* table, int n_my) {
-  KeysCursor c{0, 0, 0, 0, 0, false};
+  KeysCursor c{0, 0, 0, 0, 0, 0, 0, false};
   for (; c.k < n_my; ++c.k) {
     c.nblk = table[c.k].nblk;
     if (c.nblk > 0) {
@@ -155,6 +157,10 @@ __device__ __forceinline__ KeysCursor keys_cursor_first(const KeysUnit* table, i
 
 __device__ __forceinline__ KeysCursor keys_cursor_next(const KeysUnit* table, int n_my, KeysCursor c) {
   ++c.jg;
+  if (++c.st == kKeysStages) {
+    c.st = 0;
+    c.ph ^= 1;
+  }
   if (++c.j < c.nblk) return c;
   c.j = 0;
   ++c.kq;
@@ -169,7 +175,7 @@ __device__ __forceinline__ KeysCursor keys_cursor_next(const KeysUnit* table, in
 template <int D>
 struct KeysCfg {
   static constexpr int kHalves = D / 64;
-  static constexpr int kStages = 3;
+  static constexpr int kStages = kKeysStages;
   static constexpr int kQBytes = kKeysRows * D * 2;
   static constexpr int kKTile = kKeysBlock * D * 2;
   static constexpr int kVTile = kKeysBlock * 128 * 2;  // always 128 d: upper half zero when D = 64
@@ -296,8 +302,8 @@ __global__ void __launch_bounds__(kKeysThreads, 1)
       for (KeysCursor x = keys_cursor_first(sUnits, n_my); x.valid; x = keys_cursor_next(sUnits, n_my, x)) {
         const KeysUnit& U = sUnits[x.k];
         const uint64_t pol = U.mtiles > 1 ? l2_policy_evict_last() : l2_policy_evict_first();
-        const int st = x.jg % S;
-        if (x.jg >= S && !mbar_wait(&kv_empty[st], ((x.jg / S) - 1) & 1, abort_v)) break;
+        const int st = x.st;
+        if (x.jg >= S && !mbar_wait(&kv_empty[st], x.ph ^ 1, abort_v)) break;
         mbar_arrive_expect_tx(&kv_full[st], 2 * C::kHalves * kKeysBlock * 128);
         const int key0 = U.k_begin + x.j * kKeysBlock;
         uint8_t* kt = sStage + st * C::kStageBytes;
@@ -336,33 +342,41 @@ __global__ void __launch_bounds__(kKeysThreads, 1)
       // tensor work of a full 64-row tile.
       auto n_of = [&](const KeysCursor& x) { return 16 * sUnits[x.k].ngrp; };
       const uint32_t qa = smem_u32(sQ), sa = smem_u32(sStage);
-      auto issue_s = [&](int jg, int nN) {
+      // Shared-memory descriptors are built once; a tile inside a stage, or a
+      // K slice inside a tile, is the base descriptor plus its offset / 16 in
+      // the start-address field (every address here is below 256 KB, so the
+      // field never carries into the next one).  The issuing thread's work
+      // per MMA is what bounds a block: one add per operand, no rebuild.
+      const uint64_t dK0 = sdesc_sw128(sa, 16, 1024);                             // K tile, K-major
+      const uint64_t dQ0 = sdesc_sw128(qa, 16, 1024);                             // Q tile, K-major
+      const uint64_t dV0 = sdesc_sw128(sa + C::kKTile, kKeysBlock * 128, 1024);   // V^T, M-major
+      const uint64_t dP0 = sdesc_sw128(sa, kKeysBlock * 128, 1024);               // P^T, N-major
+      constexpr uint32_t kStageDesc = C::kStageBytes >> 4;
+      auto issue_s = [&](const KeysCursor& x, int nN) {
         const uint32_t idS = idesc_bf16_f32_ab(kKeysBlock, nN, 0, 0);
-        const uint32_t ka = sa + (uint32_t)((jg % S) * C::kStageBytes);
-        const uint32_t dst = tmem + (uint32_t)((jg & 1) * kKeysRows);
+        const uint64_t dk = dK0 + (uint64_t)(x.st * kStageDesc);
+        const uint32_t dst = tmem + (uint32_t)((x.jg & 1) * kKeysRows);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t ao = (kk >> 2) * (kKeysBlock * 128) + (kk & 3) * 32;
-          const uint32_t bo = (kk >> 2) * (kKeysRows * 128) + (kk & 3) * 32;
-          umma_bf16(dst, sdesc_sw128(ka + ao, 16, 1024), sdesc_sw128(qa + bo, 16, 1024), idS,
-                    kk > 0 ? 1u : 0u);
+          constexpr uint32_t kA = kKeysBlock * 128 / 16, kB = kKeysRows * 128 / 16;
+          const uint32_t ao = (kk >> 2) * kA + (kk & 3) * 2;
+          const uint32_t bo = (kk >> 2) * kB + (kk & 3) * 2;
+          umma_bf16(dst, dk + ao, dQ0 + bo, idS, kk > 0 ? 1u : 0u);
         }
-        umma_commit(&s_full[jg & 1]);
+        umma_commit(&s_full[x.jg & 1]);
       };
       // O^T of unit kq: columns 128.. (buffer 0) or 192.. (buffer 1, persistent only).
-      auto issue_pv = [&](int jg, bool first, int kq, int nN) {
+      auto issue_pv = [&](const KeysCursor& x, int nN) {
         const uint32_t idO = idesc_bf16_f32_ab(128, nN, 1, 1);
-        const uint32_t tO = tmem + (uint32_t)((2 + (plan.persistent ? kq & 1 : 0)) * kKeysRows);
-        const uint32_t pb = sa + (uint32_t)((jg % S) * C::kStageBytes);  // P^T over K(jg)
-        const uint32_t va = pb + (uint32_t)C::kKTile;
+        const uint32_t tO = tmem + (uint32_t)((2 + (plan.persistent ? x.kq & 1 : 0)) * kKeysRows);
+        const uint64_t dv = dV0 + (uint64_t)(x.st * kStageDesc);
+        const uint64_t dp = dP0 + (uint64_t)(x.st * kStageDesc);  // P^T over K(jg)
+        const uint32_t acc0 = x.j > 0 ? 1u : 0u;
 #pragma unroll
-        for (int kk = 0; kk < kKeysBlock / 16; ++kk) {
-          const uint64_t bdesc = sdesc_sw128(pb + kk * 2048, kKeysBlock * 128, 1024);
-          const uint32_t acc = (!first || kk > 0) ? 1u : 0u;
-          umma_bf16(tO, sdesc_sw128(va + kk * 2048, kKeysBlock * 128, 1024), bdesc, idO, acc);
-        }
-        umma_commit(&pv_done[jg & 1]);
-        umma_commit(&kv_empty[jg % S]);
+        for (int kk = 0; kk < kKeysBlock / 16; ++kk)
+          umma_bf16(tO, dv + kk * (2048 / 16), dp + kk * (2048 / 16), idO, kk > 0 ? 1u : acc0);
+        umma_commit(&pv_done[x.jg & 1]);
+        umma_commit(&kv_empty[x.st]);
       };
       // Two independent streams of work, issued in whichever order their
       // inputs arrive: S^T of block xs (its unit's Q, first block only, and its
@@ -383,9 +397,9 @@ __global__ void __launch_bounds__(kKeysThreads, 1)
       while (xp.valid) {
         bool did = false;
         if (xs.valid && xs.jg <= xp.jg + 1 && (xs.j != 0 || mbar_test_wait(q_full, xs.kq & 1)) &&
-            mbar_test_wait(&kv_full[xs.jg % S], (xs.jg / S) & 1)) {
+            mbar_test_wait(&kv_full[xs.st], xs.ph)) {
           tc_fence_after();
-          issue_s(xs.jg, n_of(xs));
+          issue_s(xs, n_of(xs));
           if (xs.j == xs.nblk - 1) umma_commit(q_empty);
           xs = keys_cursor_next(sUnits, n_my, xs);
           did = true;
@@ -394,7 +408,7 @@ __global__ void __launch_bounds__(kKeysThreads, 1)
             (xp.j != 0 || !plan.persistent || xp.kq < 2 ||
              mbar_test_wait(&o_free[xp.kq & 1], ((xp.kq >> 1) - 1) & 1))) {
           tc_fence_after();
-          issue_pv(xp.jg, xp.j == 0, xp.kq, n_of(xp));
+          issue_pv(xp, n_of(xp));
           if (plan.persistent && xp.j == xp.nblk - 1) umma_commit(&o_full[xp.kq & 1]);
           xp = keys_cursor_next(sUnits, n_my, xp);
           did = true;
@@ -462,6 +476,7 @@ __global__ void __launch_bounds__(kKeysThreads, 1)
     // so every named barrier below is reached by all key-lane threads.
     bool ok = true;
     int jg = 0, kq = 0;
+    int lst = 0;  // ring stage of block jg
     for (int k = 0; ok && k < n_my; ++k) {
       const KeysUnit U = sUnits[k];
       const int my_par = nx_par;
@@ -602,7 +617,7 @@ __global__ void __launch_bounds__(kKeysThreads, 1)
           }
         }
         // P^T goes over the K tile of this block: S^T(j) has finished reading it.
-        uint8_t* prow = sStage + (jg % S) * C::kStageBytes + kl * 128;
+        uint8_t* prow = sStage + lst * C::kStageBytes + kl * 128;
 #pragma unroll
         for (int g16 = 0; g16 < 4; ++g16) {
           if (g16 >= ngrp) break;
@@ -628,7 +643,7 @@ __global__ void __launch_bounds__(kKeysThreads, 1)
         }
         // A V row past the request's keys may hold anything (even NaN): zero it.
         if (key >= k_end && h < C::kHalves) {
-          uint4* vrow = reinterpret_cast<uint4*>(sStage + (jg % S) * C::kStageBytes + C::kKTile +
+          uint4* vrow = reinterpret_cast<uint4*>(sStage + lst * C::kStageBytes + C::kKTile +
                                                  h * (kKeysBlock * 128) + kl * 128);
 #pragma unroll
           for (int i = 0; i < 8; ++i) vrow[i] = make_uint4(0u, 0u, 0u, 0u);
@@ -636,6 +651,7 @@ __global__ void __launch_bounds__(kKeysThreads, 1)
         fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(&p_full[jg & 1]);
+        lst = lst + 1 == S ? 0 : lst + 1;
       }
       const bool last_unit = k + 1 >= n_my;
       if (last_unit) pdl_trigger();  // the main loop is done: let the next kernel be scheduled
