@@ -622,10 +622,12 @@ class DeviceWorkload:
             self.attention(c, st)
             self.verify(c, st)
             return
+        # Attention is launched first, so its CTAs are placed first and the
+        # verification CTAs fill the SMs it leaves idle.
         self.side.wait_stream(self.stream)
+        self.attention(c, st)
         with torch.cuda.stream(self.side):
             self.verify(c, st)
-        self.attention(c, st)
         self.stream.wait_stream(self.side)
 
     # ------------------------------------------------------------------ graphs
