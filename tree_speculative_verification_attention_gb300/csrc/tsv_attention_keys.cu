@@ -536,23 +536,36 @@ __global__ void __launch_bounds__(kKeysThreads, 1)
         if (!full_vis && key < k_end)
           vis = (uint64_t)sDesc[2 * (key - P)] | ((uint64_t)sDesc[2 * (key - P) + 1] << 32);
         const uint32_t s_col = tmem + lane_base + (uint32_t)((jg & 1) * kKeysRows);
-        // The first block always moves the maxima (they start at -inf): skip the test.
+        // P of this block against the current reference maxima, kept packed
+        // in registers: if no visible score exceeds its row's reference by
+        // more than 2^32 (the common case) these are the block's P; else the
+        // maxima move and P is computed again.  The first block always moves
+        // the maxima (they start at -inf): it skips the optimistic pass.
+        uint32_t pk[4][4];
         float over = j == 0 ? INFINITY : -INFINITY;
-#pragma unroll 1
-        for (int g16 = 0; j > 0 && g16 < ngrp; ++g16) {
-          const int c0 = g16 * 16 + h * 8;
-          float sv[8];
-          tmem_ld8(s_col + c0, sv);
-          const float4 ma = *reinterpret_cast<const float4*>(sMref + c0);
-          const float4 mb = *reinterpret_cast<const float4*>(sMref + c0 + 4);
-          const float m[8] = {ma.x, ma.y, ma.z, ma.w, mb.x, mb.y, mb.z, mb.w};
-          const uint32_t vm = full_vis ? 0xFFu : (uint32_t)(vis >> c0) & 0xFFu;
+        auto p_pass = [&](bool track) {
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const float x = fmaf(sv[e], sl2, -m[e]);
-            over = fmaxf(over, ((vm >> e) & 1u) ? x : -INFINITY);
+          for (int g16 = 0; g16 < 4; ++g16) {
+            if (g16 >= ngrp) break;
+            const int c0 = g16 * 16 + h * 8;
+            float sv[8];
+            tmem_ld8(s_col + c0, sv);
+            const float4 ma = *reinterpret_cast<const float4*>(sMref + c0);
+            const float4 mb = *reinterpret_cast<const float4*>(sMref + c0 + 4);
+            const float m[8] = {ma.x, ma.y, ma.z, ma.w, mb.x, mb.y, mb.z, mb.w};
+            const uint32_t vm = full_vis ? 0xFFu : (uint32_t)(vis >> c0) & 0xFFu;
+            float p[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const float x = ((vm >> e) & 1u) ? fmaf(sv[e], sl2, -m[e]) : -INFINITY;
+              if (track) over = fmaxf(over, x);
+              p[e] = fast_exp2(x);
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) pk[g16][i] = pack_bf16x2(p[2 * i], p[2 * i + 1]);
           }
-        }
+        };
+        if (j > 0) p_pass(true);
         if (!okj) *fail_flag = 1;
         const bool any_over = named_bar_or(kBarKeys, kKeysLaneThreads, over > kKeysOverflow || !okj);
         if (*fail_flag) {
@@ -615,31 +628,21 @@ __global__ void __launch_bounds__(kKeysThreads, 1)
               tmem_st8(tO + c0, o);
             }
           }
+          p_pass(false);  // against the moved maxima
         }
         // P^T goes over the K tile of this block: S^T(j) has finished reading it.
         uint8_t* prow = sStage + lst * C::kStageBytes + kl * 128;
 #pragma unroll
         for (int g16 = 0; g16 < 4; ++g16) {
           if (g16 >= ngrp) break;
-          const int c0 = g16 * 16 + h * 8;
-          float sv[8];
-          tmem_ld8(s_col + c0, sv);
-          const float4 ma = *reinterpret_cast<const float4*>(sMref + c0);
-          const float4 mb = *reinterpret_cast<const float4*>(sMref + c0 + 4);
-          const float m[8] = {ma.x, ma.y, ma.z, ma.w, mb.x, mb.y, mb.z, mb.w};
-          const uint32_t vm = full_vis ? 0xFFu : (uint32_t)(vis >> c0) & 0xFFu;
-          float p[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) p[e] = fast_exp2(((vm >> e) & 1u) ? fmaf(sv[e], sl2, -m[e]) : -INFINITY);
-          uint32_t pk[4];
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            pk[i] = pack_bf16x2(p[2 * i], p[2 * i + 1]);
-            lsum[g16][2 * i] += __uint_as_float(pk[i] << 16);
-            lsum[g16][2 * i + 1] += __uint_as_float(pk[i] & 0xFFFF0000u);
+            lsum[g16][2 * i] += __uint_as_float(pk[g16][i] << 16);
+            lsum[g16][2 * i + 1] += __uint_as_float(pk[g16][i] & 0xFFFF0000u);
           }
           const int chunk = 2 * g16 + h;
-          *reinterpret_cast<uint4*>(prow + ((chunk ^ (kl & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          *reinterpret_cast<uint4*>(prow + ((chunk ^ (kl & 7)) << 4)) =
+              make_uint4(pk[g16][0], pk[g16][1], pk[g16][2], pk[g16][3]);
         }
         // A V row past the request's keys may hold anything (even NaN): zero it.
         if (key >= k_end && h < C::kHalves) {
