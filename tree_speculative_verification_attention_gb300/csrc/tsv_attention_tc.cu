@@ -338,9 +338,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         break;
       }
       tc_fence_after();
+      // The row's 128 scores: four loads in flight, one wait.
       float s[kBN];
+      {
+        uint32_t sr[kBN / 32][32];
 #pragma unroll
-      for (int q4 = 0; q4 < kBN / 32; ++q4) tmem_ld32(sbuf + 32 * q4, *reinterpret_cast<float(*)[32]>(&s[32 * q4]));
+        for (int q4 = 0; q4 < kBN / 32; ++q4) tmem_ld32_nowait(sbuf + 32 * q4, sr[q4]);
+        tmem_wait_ld_tie32(sr[0]);
+        reg_tie32(sr[1]);
+        reg_tie32(sr[2]);
+        reg_tie32(sr[3]);
+#pragma unroll
+        for (int e = 0; e < kBN; ++e) s[e] = __uint_as_float(sr[e >> 5][e & 31]);
+      }
       const int key0 = k_begin + j * kBN;  // this block's first key
       if (key0 + kBN > P) {  // uniform: the block reaches the tree keys (or the end)
         // Keys key0 + e are visible iff e < k_end - key0 and they are prefix
@@ -359,9 +369,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
         for (int e = 0; e < kBN; ++e) s[e] = -INFINITY;
       }
+      // Four independent chains of three-input maxima (two keys per step).
       float mx[4] = {s[0], s[1], s[2], s[3]};
 #pragma unroll
-      for (int e = 4; e < kBN; ++e) mx[e & 3] = fmaxf(mx[e & 3], s[e]);
+      for (int e = 4; e < kBN; e += 2) mx[(e >> 1) & 3] = fmax3(mx[(e >> 1) & 3], s[e], s[e + 1]);
       // Raw maximum times the (positive) scale = maximum of the scaled scores.
       const float hmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl2;
       // Move the reference only when a score exceeds it by more than the
@@ -390,20 +401,26 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
       }
       const float neg_ref = m_ref == -INFINITY ? 0.f : -m_ref;
-      float ps[4] = {0.f, 0.f, 0.f, 0.f};
+      // Two keys per step: the exponent arguments by one paired FMA, the row
+      // sums in four paired accumulators.
+      const uint64_t sl2x2 = f2_pack(sl2, sl2), refx2 = f2_pack(neg_ref, neg_ref);
+      uint64_t ps2[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
       for (int hh = 0; hh < 4; ++hh) {  // 32 keys -> 16 P columns at a time
         uint32_t h[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          const float p0 = fast_exp2(fmaf(s[32 * hh + e], sl2, neg_ref));
-          const float p1 = fast_exp2(fmaf(s[32 * hh + e + 1], sl2, neg_ref));
-          ps[(e >> 1) & 3] += p0 + p1;
+          const uint64_t x2 = ffma2(f2_pack(s[32 * hh + e], s[32 * hh + e + 1]), sl2x2, refx2);
+          const float p0 = fast_exp2(f2_lo(x2));
+          const float p1 = fast_exp2(f2_hi(x2));
+          ps2[(e >> 1) & 3] = fadd2(ps2[(e >> 1) & 3], f2_pack(p0, p1));
           h[e >> 1] = pack_bf16x2(p0, p1);
         }
-        tmem_st16u(sbuf + 16 * hh, h);
+        tmem_st16u_nowait(sbuf + 16 * hh, h);
       }
-      l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
+      tmem_wait_st();  // P is in TMEM before the arrival below
+      const uint64_t pq = fadd2(fadd2(ps2[0], ps2[1]), fadd2(ps2[2], ps2[3]));
+      l += f2_lo(pq) + f2_hi(pq);
       // V rows of the last block past the request's keys may hold anything
       // (even NaN): once the block has landed, tile 0 zeroes them before
       // either tile's PV reads the block (PV_1 follows PV_0), so that
