@@ -760,8 +760,9 @@ def attention_exps(spec, trees):
 
 
 def sfu_exp_rate(num_sms):
-    """Exponentials per second: 16 ex2 per clock per SM at the maximum SM clock."""
-    return 16.0 * num_sms * measured_sm_max_mhz() * 1e6
+    """Exponentials per second: 32 ex2 per clock per SM (measured on this GPU by a
+    throughput loop of ex2.approx.f32) at the maximum SM clock."""
+    return 32.0 * num_sms * measured_sm_max_mhz() * 1e6
 
 
 def rooflines(spec, trees, attn_ms, step_ms, walk_rows, num_sms):
