@@ -112,6 +112,7 @@ def workload_inputs(spec):
 
 
 WARP = {}  # top_k / top_p of the stochastic verification, when warped
+MIN_GRAPH_LAUNCHES = 4  # steps (or launches of one kind) per captured timing graph, at least
 
 
 def config_of(spec, extra=None):
@@ -567,6 +568,19 @@ class DeviceWorkload:
         l2 = torch.cuda.get_device_properties(dev).L2_cache_size
         self.R = int(min(64, max(1, math.ceil(4 * l2 / self.per_copy))))
         self.copies = [base] + [{k: t.clone() for k, t in base.items()} for _ in range(self.R - 1)]
+        # Steps (and attention launches) per captured graph: at least
+        # MIN_GRAPH_LAUNCHES, cycling over the R copies, so a graph replay's own
+        # launch gap is not charged to every step.  One copy streams at least
+        # 4 x L2 when R is 1, so consecutive steps on it still start cold.
+        self.L = max(self.R, MIN_GRAPH_LAUNCHES)
+        # Verification alone reads only the logits and proposals: its graphs
+        # cycle over Rv copies of those inputs, together at least 4 x L2 (the
+        # full copies first, then clones of the verification inputs).
+        vkeys = [k for k in ("logits", "gtok", "llm", "ssm", "stok", "ua", "us", "parent", "offs") if k in base]
+        vbytes = sum(base[k].numel() * base[k].element_size() for k in vkeys)
+        self.Rv = int(min(64, max(self.R, math.ceil(4 * l2 / vbytes))))
+        self.vcopies = self.copies + [{k: base[k].clone() for k in vkeys} for _ in range(self.Rv - self.R)]
+        self.Lv = max(self.Rv, MIN_GRAPH_LAUNCHES)
         h = tsv.handle(dev.index)
         B, N = self.B, self.N
         code = tsv.TSV_BF16 if spec.dtype == "bf16" else tsv.TSV_F32
@@ -587,6 +601,16 @@ class DeviceWorkload:
             return st
 
         self.states = [make_state(c) for c in self.copies]
+
+        def make_vstate():  # verification workspaces and outputs of a verification-only copy
+            st = {"ws_g": torch.zeros(max(ws_g, 1), dtype=torch.uint8, device=dev),
+                  "ws_s": torch.zeros(max(ws_s, 1), dtype=torch.uint8, device=dev)}
+            mk = lambda: {k: torch.empty(n, dtype=torch.int32, device=dev) for k, n in
+                          (("path", N), ("accept_len", B), ("bonus", B), ("n_tried", B), ("status", B))}
+            st["g"], st["s"] = mk(), mk()
+            return st
+
+        self.vstates = self.states + [make_vstate() for _ in range(self.Rv - self.R)]
         # Kernels per step: one attention launch (masks built and splits merged
         # inside; the fp32 CUDA-core path first prepares the ancestor bitsets in
         # a launch of its own), one per verification kind.
@@ -639,21 +663,27 @@ class DeviceWorkload:
         return g
 
     def capture(self):
-        """CUDA graphs: all R copies' steps in one graph (so the host replays one
-        graph per R steps and stays ahead of the GPU), one graph per copy, and
-        graphs of the attention and verification launches alone."""
+        """CUDA graphs: L steps cycling over the R copies in one graph (so the
+        host replays one graph per L steps and stays ahead of the GPU), one
+        graph per copy, and graphs of L attention launches and of Lv launches
+        of each verification alone (cycling over the Rv verification copies)."""
         import torch
         cs = list(zip(self.copies, self.states))
+        vs = list(zip(self.vcopies, self.vstates))
         for c, st in cs:  # eager run once; checks the statuses
             self.step(c, st)
+        for c, st in vs[self.R:]:
+            self.verify(c, st)
         torch.cuda.synchronize()
         assert (self.states[0]["status"].cpu() == 0).all()
-        self.g_steps = self._graph(lambda: [self.step(c, st) for c, st in cs])
+        cyc = [cs[i % self.R] for i in range(self.L)]
+        vcyc = [vs[i % self.Rv] for i in range(self.Lv)]
+        self.g_steps = self._graph(lambda: [self.step(c, st) for c, st in cyc])
         self.g_one = [self._graph(lambda c=c, st=st: self.step(c, st)) for c, st in cs]
-        self.g_serial = self._graph(lambda: [self.step(c, st, overlap=False) for c, st in cs])
-        self.g_attn = self._graph(lambda: [self.attention(c, st) for c, st in cs])
-        self.g_greedy = self._graph(lambda: [self.greedy(c, st) for c, st in cs]) if self.gi is not None else None
-        self.g_mss = self._graph(lambda: [self.stochastic(c, st) for c, st in cs]) if self.si is not None else None
+        self.g_serial = self._graph(lambda: [self.step(c, st, overlap=False) for c, st in cyc])
+        self.g_attn = self._graph(lambda: [self.attention(c, st) for c, st in cyc])
+        self.g_greedy = self._graph(lambda: [self.greedy(c, st) for c, st in vcyc]) if self.gi is not None else None
+        self.g_mss = self._graph(lambda: [self.stochastic(c, st) for c, st in vcyc]) if self.si is not None else None
         # Every graph is replayed once here, so none launches for the first time
         # inside a timed region.
         for g in [self.g_steps, self.g_serial, self.g_attn, self.g_greedy, self.g_mss] + self.g_one:
@@ -665,10 +695,10 @@ class DeviceWorkload:
             assert counted == self.kernels_per_step, (counted, self.kernels_per_step)
 
     def run_steps(self, k):
-        for _ in range(k // self.R):
+        for _ in range(k // self.L):
             self.g_steps.replay()
-        for i in range(k % self.R):
-            self.g_one[i].replay()
+        for i in range(k % self.L):
+            self.g_one[i % self.R].replay()
 
     # ------------------------------------------------------------------ timing forms
     def _events(self, n):
@@ -728,16 +758,17 @@ class DeviceWorkload:
 
     def measure(self, n_steps):
         """The step and each of its launches alone, outside any timed region of the bench line."""
-        reps = max(1, n_steps // self.R)
+        reps = max(1, n_steps // self.L)
+        vreps = max(1, n_steps // self.Lv)
         steps = self.per_step_graph_ms(n_steps)
-        out = {"graph_mean_ms": self.graph_ms(self.g_steps, self.R, reps),
+        out = {"graph_mean_ms": self.graph_ms(self.g_steps, self.L, reps),
                "graph_median_ms": float(np.median(steps)),
-               "serial_graph_mean_ms": self.graph_ms(self.g_serial, self.R, reps),
-               "attention_ms": self.graph_ms(self.g_attn, self.R, reps)}
+               "serial_graph_mean_ms": self.graph_ms(self.g_serial, self.L, reps),
+               "attention_ms": self.graph_ms(self.g_attn, self.L, reps)}
         if self.g_greedy is not None:
-            out["greedy_ms"] = self.graph_ms(self.g_greedy, self.R, reps)
+            out["greedy_ms"] = self.graph_ms(self.g_greedy, self.Lv, vreps)
         if self.g_mss is not None:
-            out["stochastic_ms"] = self.graph_ms(self.g_mss, self.R, reps)
+            out["stochastic_ms"] = self.graph_ms(self.g_mss, self.Lv, vreps)
         plain = self.per_step_plain_ms(n_steps)
         out["plain_median_ms"] = float(np.median(plain))
         out["plain_mean_ms"] = float(np.mean(plain))
@@ -805,7 +836,7 @@ def workload_summary(spec, w, forms, step_ms, num_sms):
     out = {"nodes": w.N, "step_ms": step_ms, "nodes_per_s": w.N / (step_ms * 1e-3),
            "attention": {k: att[k] for k in ("kernel", "launch_ms", "bound", "frac", "hbm_frac", "combined_frac")},
            "step_roofline": {k: step[k] for k in ("frac", "combined_frac", "algorithmic_bytes")},
-           "rotating_copies": w.R}
+           "rotating_copies": w.R, "steps_per_graph": w.L, "verification_copies": w.Rv}
     out["timing"] = {k: v for k, v in forms.items() if k != "attention_ms"}
     return out
 
@@ -826,7 +857,7 @@ def run_ours(args, spec):
     num_sms = torch.cuda.get_device_properties(dev).multi_processor_count
     w = DeviceWorkload(spec, tsv, dev, stream, overlap=not args.serial)
     w.capture()
-    N, R, kernels_per_step = w.N, w.R, w.kernels_per_step
+    N, R, L, kernels_per_step = w.N, w.R, w.L, w.kernels_per_step
 
     clocks = ClockRecord(dev)
     clocks.start()
@@ -887,16 +918,17 @@ def run_ours(args, spec):
             torch.cuda.empty_cache()
     clocks.stop()
 
-    how = ("mean over the K timed steps; CUDA graph replay (one graph per %d step(s), each step on the next of "
+    how = ("mean over the K timed steps; CUDA graph replay (one graph per %d steps, each step on the next of "
            "%d rotating input copies); verification launches %s" %
-           (R, R, "after the attention launch on one stream" if args.serial else
+           (L, R, "after the attention launch on one stream" if args.serial else
             "on a second stream, concurrent with the attention launch"))
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": spec.dtype, "data": "synthetic",
             "config": config_of(spec),
             "roofline": roofline, "roofline_step": roofline_step,
-            "timing": dict(forms, value=how, rotating_copies=R),
+            "timing": dict(forms, value=how, rotating_copies=R, steps_per_graph=L,
+                           verification_copies=w.Rv, verification_launches_per_graph=w.Lv),
             "e2e": e2e, "gpu_launches": kernels_per_step * args.steps, "clocks": timed_clocks}
     if per_workload is not None:
         line["per_workload"] = per_workload

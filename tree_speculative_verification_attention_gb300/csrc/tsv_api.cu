@@ -27,6 +27,7 @@ struct tsv_handle_s {
   bool keys_attr_set[2];  // keys-on-lanes kernel, D = 64, 128
   bool mss_attr_set;      // MSS kernel's shared-memory limit
   size_t mss_staged_limit;
+  int mss_max_clusters[kMssClusterSizes];  // resident MSS clusters of each size
 };
 
 namespace {
@@ -520,13 +521,14 @@ static tsv_status verify_stochastic(tsv_handle h, const float* llm_logits_d, con
   if (!workspace_d || workspace_bytes < need) return TSV_ERR_INVALID_ARG;
   float* resid = static_cast<float*>(workspace_d);
   if (!h->mss_attr_set) {
-    if (mss_set_attributes(h->device, &h->mss_staged_limit) != cudaSuccess) return TSV_ERR_CUDA;
+    if (mss_set_attributes(h->device, &h->mss_staged_limit, h->mss_max_clusters) != cudaSuccess)
+      return TSV_ERR_CUDA;
     h->mss_attr_set = true;
   }
   return cuda_status(launch_mss_verify(llm_logits_d, ssm_probs_d, V, tree_tokens_d, parent_d,
                                        node_offsets_d, u_accept_d, u_sample_d, 1.0f / temperature,
                                        top_k, top_p, B, resid, path_d, accept_len_d, bonus_d,
-                                       n_tried_d, status_d, h->mss_staged_limit,
+                                       n_tried_d, status_d, h->mss_staged_limit, h->mss_max_clusters,
                                        static_cast<cudaStream_t>(stream)));
 }
 

@@ -106,6 +106,11 @@ __device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
 }
 
+// Asks for the line holding p to be brought into L2 (reads no value).
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(p)) : "memory");
+}
+
 // Asks for `bytes` bytes at p (16-byte aligned, a multiple of 16) to be
 // brought into L2; like the tensor prefetch below it reads no value.
 __device__ __forceinline__ void bulk_prefetch_l2(const void* p, uint32_t bytes) {
@@ -416,6 +421,11 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) 
 
 // ----------------------------------------------------------------- barriers, clusters
 
+// Named barrier `id` over `count` threads (a multiple of 32).
+__device__ __forceinline__ void named_bar_sync(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // Named barrier over `count` threads that also ORs a predicate across them.
 __device__ __forceinline__ bool named_bar_or(int id, int count, bool pred) {
   uint32_t r;
@@ -441,6 +451,16 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
                    : "memory");
+}
+
+// The same barrier in two halves, so that work runs between them: every
+// thread arrives (releasing its earlier writes) and later waits (acquiring
+// the others'); an arrive is always followed by its wait before the next one.
+__device__ __forceinline__ void cluster_arrive_release() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait_acquire() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 // Atomic add at GPU scope with acquire-release ordering: the caller's earlier

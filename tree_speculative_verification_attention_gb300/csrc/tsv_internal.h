@@ -157,19 +157,23 @@ cudaError_t launch_greedy_walk(const float* part_val, const int32_t* part_idx, i
 // verification workspace (the layout tsv_tree_verify_greedy uses).
 inline size_t greedy_counter_bytes(int32_t B) { return ((size_t)B * 4 + 255) & ~(size_t)255; }
 
-// Stochastic verification: one cluster of mss_cluster_size(V) CTAs per
-// request, each owning a slice of the vocabulary.
-int mss_cluster_size(int64_t V);
+// Stochastic verification: one cluster of mss_cluster_size(V, B, ...) CTAs
+// per request, each owning a slice of the vocabulary.
+constexpr int kMssClusterSizes = 9;  // entries of the resident-cluster table (sizes 0..8)
+int mss_cluster_size(int64_t V, int32_t B, const int* max_clusters);
 cudaError_t launch_mss_verify(const float* llm_logits, const float* ssm_probs, int64_t V,
                               const int32_t* tokens, const int32_t* parent,
                               const int32_t* node_offsets, const float* u_acc, const float* u_smp,
                               float inv_t, int32_t top_k, float top_p, int32_t B, float* resid,
                               int32_t* path, int32_t* accept_len, int32_t* bonus, int32_t* n_tried,
-                              int32_t* status, size_t staged_limit, cudaStream_t st);
-// Sets the MSS kernel's dynamic shared-memory limit on `device` to all that is
-// left beside its static shared memory, and returns that limit (the largest
-// staged slice set a launch may use).
-cudaError_t mss_set_attributes(int device, size_t* staged_limit);
+                              int32_t* status, size_t staged_limit, const int* max_clusters,
+                              cudaStream_t st);
+// Sets the MSS kernels' dynamic shared-memory limit on `device` to all that is
+// left beside their static shared memory, returns the staged kernel's limit
+// (the largest staged slice set a launch may use) and fills
+// max_clusters[0..kMssClusterSizes-1] with the clusters of each size the
+// device holds at once.
+cudaError_t mss_set_attributes(int device, size_t* staged_limit, int* max_clusters);
 constexpr int kMssMaxTopK = 1024;  // largest top_k of the warped stochastic verification
 
 // Token-tree construction: expansion (top-k children per frontier row) and

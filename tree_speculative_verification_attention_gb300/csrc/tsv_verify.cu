@@ -332,8 +332,10 @@ cudaError_t launch_greedy_walk(const float* part_val, const int32_t* part_idx, i
 
 namespace {
 
-constexpr int kMssThreads = 256;
+constexpr int kMssThreads = 512;  // stochastic verification CTAs: 16 warps, one CTA per SM
 constexpr int kMssWarps = kMssThreads / 32;
+constexpr int kSelThreads = 256;  // tree-expansion CTAs
+constexpr int kSelWarps = kSelThreads / 32;
 constexpr int kMssMaxCluster = 8;
 constexpr int64_t kMssMinSlice = 4096;  // vocab entries per CTA at least
 constexpr int kMssGroups = 4;           // 4-float groups in flight per thread
@@ -400,6 +402,7 @@ __device__ __forceinline__ F2 warp_sum_f2(F2 a) {
   return a;
 }
 
+template <int kWarps>
 __device__ float block_max(float v, float* red) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 #pragma unroll
@@ -408,7 +411,27 @@ __device__ float block_max(float v, float* red) {
   if (lane == 0) red[warp] = v;
   __syncthreads();
   v = -INFINITY;
-  for (int w = 0; w < kMssWarps; ++w) v = fmaxf(v, red[w]);
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) v = fmaxf(v, red[w]);
+  return v;
+}
+
+__device__ __forceinline__ F2 shfl_f2(F2 v, int src) {
+  return {__shfl_sync(0xffffffffu, v.hi, src), __shfl_sync(0xffffffffu, v.lo, src)};
+}
+
+__device__ __forceinline__ F2 shfl_up_f2(F2 v, int o) {
+  return {__shfl_up_sync(0xffffffffu, v.hi, o), __shfl_up_sync(0xffffffffu, v.lo, o)};
+}
+
+// Inclusive prefix sum over the warp's lanes (lane l: lanes 0..l).
+__device__ __forceinline__ F2 warp_scan_f2(F2 v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const F2 t = shfl_up_f2(v, o);
+    if (lane >= o) v = f2_add(t, v);
+  }
   return v;
 }
 
@@ -473,11 +496,10 @@ __device__ __forceinline__ bool kept(float l, int64_t y, float tau, int ycut) {
   return l > tau || (l == tau && y <= ycut);
 }
 
-// Shared scratch of the warped support.
-static_assert(kMssThreads == 256, "one histogram bin per thread");
+// Shared scratch of the warped support (CTAs of up to kMssThreads threads).
 struct SelSmem {
   int hist[2][256];  // per-CTA digit histograms, alternating with the exchanges
-  int wsum[kMssThreads / 32];
+  int wsum[kMssWarps];
   int ints[8];
   float cand_v[kMaxTopK];
   int cand_i[kMaxTopK];
@@ -486,6 +508,7 @@ struct SelSmem {
   F2 tsum[kMssWarps];
   F2 s_cut;
 };
+static_assert(kSelThreads >= 256 && kMssThreads >= 256, "one histogram bin per thread of the first 256");
 
 struct Support {
   float tau;
@@ -500,7 +523,8 @@ struct Support {
 // then, for equal logits at the boundary, the cut by token index; the kept
 // tokens (at most kMaxTopK) are gathered into every CTA and sorted there, the
 // same way in every CTA, for the top-p cut and the mass.  Every CTA of the
-// cluster runs it in lockstep; `xk` counts the exchanges.
+// cluster runs it in lockstep; `xk` counts the exchanges.  kT threads per CTA.
+template <int kT>
 __device__ __noinline__ Support warped_support(const Slice lrow, int64_t V, int64_t lo,
                                                int64_t hi, float inv_t, float M, int top_k, float top_p,
                                                int ncl, int rank, int& xk, float (*pub)[4], SelSmem& w) {
@@ -514,16 +538,17 @@ __device__ __noinline__ Support warped_support(const Slice lrow, int64_t V, int6
     for (int pass = 0; pass < 4; ++pass) {
       const int shift = 24 - 8 * pass;
       int* h = w.hist[xk & 1];
-      h[tid] = 0;  // kMssThreads == 256 bins
+      if (tid < 256) h[tid] = 0;
       __syncthreads();
-      for (int64_t y = lo + tid; y < hi; y += kMssThreads) {
+      for (int64_t y = lo + tid; y < hi; y += kT) {
         const uint32_t k = order_key(lrow[y]);
         if (pass == 0 || (k >> (shift + 8)) == prefix) atomicAdd(&h[(k >> shift) & 255], 1);
       }
       __syncthreads();
       cluster_sync_all();
-      int cnt = 0;
-      for (int rr = 0; rr < ncl; ++rr) cnt += ld_dsmem_s32(mapa_shared(smem_u32(&h[tid]), (uint32_t)rr));
+      int cnt = 0;  // bin tid's count over the cluster (threads past the 256 bins: none)
+      if (tid < 256)
+        for (int rr = 0; rr < ncl; ++rr) cnt += ld_dsmem_s32(mapa_shared(smem_u32(&h[tid]), (uint32_t)rr));
       ++xk;
       // Suffix sums over the digits (larger digit = larger logit).
       int sfx = cnt;
@@ -534,7 +559,7 @@ __device__ __noinline__ Support warped_support(const Slice lrow, int64_t V, int6
       }
       if (lane == 0) w.wsum[warp] = sfx;
       __syncthreads();
-      for (int ww = warp + 1; ww < kMssWarps; ++ww) sfx += w.wsum[ww];
+      for (int ww = warp + 1; ww < kT / 32; ++ww) sfx += w.wsum[ww];
       if (sfx >= r && sfx - cnt < r) {
         w.ints[0] = tid;
         w.ints[1] = sfx - cnt;
@@ -552,7 +577,7 @@ __device__ __noinline__ Support warped_support(const Slice lrow, int64_t V, int6
       if (tid == 0) w.ints[3] = 0;
       __syncthreads();
       int c = 0;
-      for (int64_t y = lo + tid; y < hi; y += kMssThreads) c += order_key(lrow[y]) == prefix;
+      for (int64_t y = lo + tid; y < hi; y += kT) c += order_key(lrow[y]) == prefix;
       atomicAdd(&w.ints[3], c);
       __syncthreads();
       if (tid == 0) pub[xk & 1][0] = __int_as_float(w.ints[3]);
@@ -593,7 +618,7 @@ __device__ __noinline__ Support warped_support(const Slice lrow, int64_t V, int6
   // equal logits by lower index) identically in every CTA.
   if (tid == 0) w.ints[4] = 0;
   __syncthreads();
-  for (int64_t y = lo + tid; y < hi; y += kMssThreads) {
+  for (int64_t y = lo + tid; y < hi; y += kT) {
     const float l = lrow[y];
     if (kept(l, y, tau, ycut)) {
       const int j = atomicAdd(&w.ints[4], 1);
@@ -614,7 +639,7 @@ __device__ __noinline__ Support warped_support(const Slice lrow, int64_t V, int6
   ++xk;
   int P2 = 1;
   while (P2 < K) P2 <<= 1;
-  for (int j = tid; j < P2; j += kMssThreads) {
+  for (int j = tid; j < P2; j += kT) {
     float v = -INFINITY;
     int id = INT32_MAX;
     if (j < K) {
@@ -629,7 +654,7 @@ __device__ __noinline__ Support warped_support(const Slice lrow, int64_t V, int6
   __syncthreads();
   for (int k = 2; k <= P2; k <<= 1) {
     for (int j = k >> 1; j > 0; j >>= 1) {
-      for (int i = tid; i < P2; i += kMssThreads) {
+      for (int i = tid; i < P2; i += kT) {
         const int ixj = i ^ j;
         if (ixj > i) {
           const float a = w.srt_v[i], bv = w.srt_v[ixj];
@@ -647,7 +672,7 @@ __device__ __noinline__ Support warped_support(const Slice lrow, int64_t V, int6
     }
   }
   // Cumulative mass in ranking order: thread t owns a run of consecutive entries.
-  const int per = (K + kMssThreads - 1) / kMssThreads;
+  const int per = (K + kT - 1) / kT;
   const int j0 = min(K, tid * per), j1 = min(K, j0 + per);
   F2 run{0.f, 0.f};
   for (int j = j0; j < j1; ++j) run = f2_add(run, F2{exp_diff(w.srt_v[j] * inv_t, M), 0.f});
@@ -661,7 +686,7 @@ __device__ __noinline__ Support warped_support(const Slice lrow, int64_t V, int6
   if (tid == 0) w.ints[5] = INT32_MAX;
   __syncthreads();
   F2 base{0.f, 0.f}, total{0.f, 0.f};
-  for (int ww = 0; ww < kMssWarps; ++ww) {
+  for (int ww = 0; ww < kT / 32; ++ww) {
     if (ww < warp) base = f2_add(base, w.tsum[ww]);
     total = f2_add(total, w.tsum[ww]);
   }
@@ -708,66 +733,116 @@ __device__ __noinline__ Support warped_support(const Slice lrow, int64_t V, int6
 // uniforms, proposal probabilities q_c(x_c) and parent logits l(x_c) (read
 // once, in parallel, at the start), the row statistics and residual sums
 // (combined in a fixed order from partials every CTA pushes into every
-// other's shared memory), and p at the next child's token, which the residual
-// pass of the CTA owning that token publishes with the sums.  A CTA reads only
-// its own slice of the logits, proposals and residual rows.
+// other's shared memory), and p at the next child's token, which the thread
+// owning that token publishes with the sums.  A CTA reads only its own slice
+// of the logits, proposals and residual rows.
 //
-// Exchanges: each CTA (or each warp of each CTA) stores its 16-byte partial
-// into a slot of every CTA of the cluster with st.async, which completes the
-// receiver's mbarrier transaction count; a CTA waits on its own mbarrier and
-// reads the slots locally.  Two slot sets alternate: a CTA pushes exchange
-// k + 2 only after exchange k + 1 completed, that is after every CTA pushed
-// k + 1, which each does only after its threads have read exchange k.
+// Within a CTA, warp 0 (the leader) runs the walk: it waits for exchanges,
+// combines them, takes the accept decisions, keeps the buffer bookkeeping and
+// issues the copies.  It hands each vocabulary-wide step to the other warps
+// through a descriptor in shared memory and one barrier: the row statistics
+// and residual passes to the 15 worker warps, the statistics of a warped row
+// and the bonus draw to all 16.  While the workers run a pass, the leader
+// prepares the next decision (the next child, its sibling, the owner of the
+// sibling's token, the proposal copies), so only the exchange, its combine
+// and the accept test lie between two passes.
 //
-// Staged (`staged`, when the slices fit): each CTA holds three slice buffers
+// Exchanges: each CTA (or each worker warp of each CTA) stores its 16-byte
+// partial into a slot of every CTA of the cluster with st.async, which
+// completes the receiver's mbarrier transaction count; the receiver's leader
+// waits on its own mbarrier and reads the slots locally.  Two slot sets
+// alternate: a CTA pushes exchange k + 2 only after exchange k + 1 completed,
+// that is after every CTA pushed k + 1, which each does only after its
+// leader has read exchange k (a step barrier lies between).  The last
+// exchange (the bonus token's position) goes to rank 0 alone.
+//
+// Staged (kStaged, when the slices fit): each CTA holds three slice buffers
 // in shared memory.  One holds the row the current distribution comes from
 // (the logits of the node being expanded, or the last residual); the others
 // hold the proposals of the child being tested and of its next sibling,
 // fetched ahead.  A rejection writes the residual max(0, p - q) over the
 // tested child's proposals, which are not needed again, and that buffer
 // becomes the distribution's row; the old row's buffer is free.  Slices move
-// by bulk asynchronous copies counted on one mbarrier per buffer.  Otherwise
-// the slices are read from global memory and the residual rows live in the
+// by bulk asynchronous copies counted on one mbarrier per buffer, issued and
+// waited for by the leader before the step that reads them; the logits rows
+// of a node's first two children are pulled into L2 meanwhile.  Otherwise the
+// slices are read from global memory and the residual rows live in the
 // workspace.
-__global__ void __launch_bounds__(kMssThreads, 2)
+struct MssStep {
+  int kind;        // kStepRow, kStepPass or kStepBonus
+  int u;           // the node being expanded
+  int src;         // staged: buffer of the distribution's row; else -1 (logits of u) or a residual row
+  int qj;          // residual pass, staged: buffer of the proposals, overwritten by the residual
+  int c;           // residual pass: the rejected child
+  int nxt;         // residual pass, unstaged: the residual row written
+  int xs;          // slot set of the step's exchange
+  int xn;          // residual pass: the next child's token (-1: none)
+  int ycut, len;
+  float pscale;    // p(y) = source(y) * pscale (staged or residual rows)
+  float m_u, inv_s, tau;  // unstaged logits rows: p(y) from the logit
+  float bscale, us;       // bonus: weight scale, sampling uniform
+};
+constexpr int kStepNone = 0, kStepRow = 1, kStepPass = 2, kStepBonus = 3;
+constexpr int kMssWorkerWarps = kMssWarps - 1;     // warps 1..15
+constexpr int kMssWorkers = kMssWorkerWarps * 32;  // threads of the row statistics and residual passes
+constexpr int kMssSlots = kMssMaxCluster * kMssWorkerWarps;
+
+template <bool kStaged>
+__global__ void __launch_bounds__(kMssThreads, 1)
     mss_verify_kernel(const float* __restrict__ llm_logits, const float* __restrict__ ssm_probs,
                       int64_t V, const int32_t* __restrict__ tokens,
                       const int32_t* __restrict__ parent, const int32_t* __restrict__ node_offsets,
                       const float* __restrict__ u_acc, const float* __restrict__ u_smp, float inv_t,
-                      int top_k, float top_p, int ncl, int vec, int staged,
+                      int top_k, float top_p, int ncl, int vec_in,
                       float* __restrict__ resid_all, int32_t* __restrict__ path,
                       int32_t* __restrict__ accept_len, int32_t* __restrict__ bonus,
                       int32_t* __restrict__ n_tried, int32_t* __restrict__ status) {
+  // The request's offsets are pulled into L2 while the previous kernel
+  // finishes (a prefetch reads no value, so it may run ahead of its writes).
+  if (threadIdx.x == 0) prefetch_l2(node_offsets + blockIdx.x / ncl);
   pdl_wait();  // the previous kernel's results are visible from here on
+  // The next kernel may be scheduled now: it waits for this one's completion
+  // itself, and it is launched only once every CTA of this grid has started,
+  // so its CTAs never hold SMs this grid still needs.
+  pdl_trigger();
   __shared__ int32_t tok_s[TSV_MAX_NODES], par_s[TSV_MAX_NODES];
-  __shared__ float ua_s[TSV_MAX_NODES], qx_s[TSV_MAX_NODES], lx_s[TSV_MAX_NODES];
-  __shared__ float red[128];
-  __shared__ F2 scan_s[kMssWarps];
-  __shared__ __align__(16) float pub[2][4];  // exchange slots, alternating
-  __shared__ int bad, bad_tok;
-  __shared__ int pick_s, last_s;
+  __shared__ float ua_s[TSV_MAX_NODES], us_s[TSV_MAX_NODES], qx_s[TSV_MAX_NODES], lx_s[TSV_MAX_NODES];
+  __shared__ float red[kMssWarps];
+  __shared__ F2 scan_s[kMssWarps], wpre_s[kMssWarps], target_s;
+  __shared__ float mx_s;
+  __shared__ __align__(16) float pub[2][4];  // exchange slots of the warped support, alternating
+  __shared__ int bad, bad_tok, tmo_s, pick_s, last_s;
   __shared__ __align__(8) uint64_t cbar[3];  // staged copies: one barrier per slice buffer
   __shared__ __align__(8) uint64_t xbar[2];  // exchanges, alternating
-  __shared__ __align__(16) float4 xslot[2][kMssMaxCluster * kMssWarps];
+  __shared__ __align__(16) float4 xslot[2][kMssSlots];
+  __shared__ MssStep dsc[2];                 // step descriptors, alternating
   __shared__ SelSmem sel;
   extern __shared__ __align__(128) float mss_dyn[];
+  constexpr int T = kMssThreads;
+  constexpr int TW = kMssWorkers;
+  constexpr int G = kStaged ? 3 : kMssGroups;  // 4-float groups in flight per worker (shared memory: 3)
+  const bool vec = kStaged || vec_in != 0;     // staged slices are always 16-byte aligned
   const bool warped = top_k > 0 || top_p < 1.0f;
   const int b = blockIdx.x / ncl;
   const int rank = blockIdx.x - b * ncl;  // == %cluster_ctarank for 1-D clusters of ncl
   const int tid = threadIdx.x;
-  const int T = blockDim.x;
-  const int lane = tid & 31;
+  const int lane = tid & 31, warp = tid >> 5;
+  const bool leader = warp == 0;
+  const int wid = tid - 32;  // worker index (warps 1..15)
+  const int off = node_offsets[b];
+  const int n = node_offsets[b + 1] - off;
   if (tid == 0) {
     pick_s = INT32_MAX;
     last_s = -1;
-    if (staged)
+    tmo_s = 0;
+    bad = (n < 1) ? TSV_ERR_BAD_TREE : (n > TSV_MAX_NODES ? TSV_ERR_UNSUPPORTED : 0);
+    bad_tok = 0;
+    if (kStaged)
       for (int i = 0; i < 3; ++i) mbar_init(&cbar[i], 1);
     mbar_init(&xbar[0], 1);
     mbar_init(&xbar[1], 1);
     mbar_fence_init();
   }
-  const int off = node_offsets[b];
-  const int n = node_offsets[b + 1] - off;
 
   // This CTA's slice (a multiple of 4 long, so 16-byte aligned rows stay aligned).
   const int64_t per = (((V + ncl - 1) / ncl) + 3) & ~int64_t(3);
@@ -775,116 +850,106 @@ __global__ void __launch_bounds__(kMssThreads, 2)
   const int64_t n4 = (hi - lo) >> 2;  // full groups
   const int64_t per_al = (per + 31) & ~int64_t(31);
   const uint32_t slice_bytes = (uint32_t)((hi - lo) * 4);  // a multiple of 16 when staged
-  // Staged buffers (bookkeeping identical in every thread): buffer pb holds
-  // the distribution's row; node_of[j] is the child whose proposals buffer j
-  // holds or receives (-1: none); pend[j]: a copy into j not yet waited for;
-  // par[j]: parity of the next phase of j's barrier.
   auto buf = [&](int j) { return mss_dyn + (size_t)j * (size_t)per_al; };
+  // Staged bookkeeping, the leader's (identical in its lanes, held in
+  // registers): buffer pb holds the distribution's row; 10-bit field j of
+  // `nodes` is one more than the child whose proposals buffer j holds or
+  // receives (0: none); bit j of `pend`: a copy into j not yet waited for;
+  // bit j of `par`: parity of the next phase of j's barrier.  Only lane 0 of
+  // the leader waits on these barriers, and the step barrier orders every
+  // other thread's reads after its wait.
   int pb = 0;
-  int node_of[3] = {-1, -1, -1};
-  bool pend[3] = {false, false, false};
-  uint32_t par_bar[3] = {0u, 0u, 0u};
-  bool tmo = false;
-  auto ready = [&](int j) {  // the copy into buffer j (if any) has landed
-    if (pend[j]) {
-      if (!mbar_wait(&cbar[j], par_bar[j], nullptr)) tmo = true;
-      par_bar[j] ^= 1u;
-      pend[j] = false;
+  uint32_t nodes = 0u, pend = 0u, par = 0u;
+  auto node_of = [&](int j) { return (int)((nodes >> (10 * j)) & 1023u) - 1; };
+  auto set_node = [&](int j, int c) {
+    nodes = (nodes & ~(1023u << (10 * j))) | ((uint32_t)(c + 1) << (10 * j));
+  };
+  auto land = [&](int j) {  // the copy into buffer j (if any) has landed
+    if ((pend >> j) & 1u) {
+      if (lane == 0 && !mbar_wait(&cbar[j], (par >> j) & 1u, nullptr)) tmo_s = 1;
+      par ^= 1u << j;
+      pend &= ~(1u << j);
     }
   };
-  // Thread 0 copies this CTA's slice of a global row into buffer j.  Every
-  // thread is done reading j (a barrier since) and has fenced its writes.
+  // This CTA's slice of a global row into buffer j, which no thread reads any
+  // more (an exchange or a barrier since its last use); a copy into j that
+  // nobody waited for lands first.
   auto issue_copy = [&](int j, const float* row) {
-    if (pend[j]) {  // a copy still in flight into j lands first ...
-      ready(j);
-      // ... and every thread has seen that phase complete before the next
-      // one can (a waiter that slept through both would wait for a third).
-      __syncthreads();
-    }
-    if (tid == 0) {
-      fence_proxy_async_smem();
+    land(j);
+    if (lane == 0) {
       mbar_arrive_expect_tx(&cbar[j], slice_bytes);
       for (uint32_t o = 0; o < slice_bytes; o += kBulkChunk)
         bulk_copy_g2s(buf(j) + o / 4, row + lo + o / 4, min(kBulkChunk, slice_bytes - o), &cbar[j]);
     }
-    pend[j] = true;
+    pend |= 1u << j;
   };
   auto q_buffer_of = [&](int c) {
-    for (int j = 0; j < 3; ++j)
-      if (j != pb && node_of[j] == c) return j;
-    return -1;
+    int r = -1;
+#pragma unroll
+    for (int j = 2; j >= 0; --j)
+      if (j != pb && node_of(j) == c) r = j;
+    return r;
   };
-  // A buffer other than pb and `not_j`, preferring one with no copy in flight.
-  auto free_buffer = [&](int not_j) {
+  // A buffer other than pb, preferring one with no copy in flight.
+  auto free_buffer = [&]() {
     int pick = -1;
+#pragma unroll
     for (int j = 0; j < 3; ++j)
-      if (j != pb && j != not_j && (pick < 0 || (pend[pick] && !pend[j]))) pick = j;
+      if (j != pb && (pick < 0 || (((pend >> pick) & 1u) && !((pend >> j) & 1u)))) pick = j;
     return pick;
   };
   auto q_issue = [&](int j, int c) {
     issue_copy(j, ssm_probs + (size_t)(off + c) * (size_t)V);
-    node_of[j] = c;
+    set_node(j, c);
   };
   // Row of node u into buffer pb, and the proposals of its first child c.
   auto stage_row = [&](int u, int c) {
     issue_copy(pb, llm_logits + (size_t)(off + u) * (size_t)V);
-    node_of[pb] = -1;
-    if (c >= 0 && q_buffer_of(c) < 0) q_issue(free_buffer(-1), c);
+    set_node(pb, -1);
+    if (c >= 0 && q_buffer_of(c) < 0) q_issue(free_buffer(), c);
   };
-  auto drain = [&]() {  // no copy may be in flight when the CTA leaves
-    if (!staged) return;
-    for (int j = 0; j < 3; ++j) ready(j);
+  auto drain = [&]() {  // leader: no copy may be in flight when the CTA leaves
+    if (kStaged)
+      for (int j = 0; j < 3; ++j) land(j);
   };
   __syncthreads();  // barriers initialised ...
-  cluster_sync_all();  // ... in every CTA of the cluster, before anyone pushes
+  cluster_arrive_release();  // ... and every CTA waits for the others' before its first push
   // Node 0 is the root and node 1 (if any) its first child in every valid
   // tree: their slices travel while the tree is read and checked.
-  if (staged && n >= 1) stage_row(0, n >= 2 ? 1 : -1);
+  if (kStaged && leader && n >= 1) stage_row(0, n >= 2 ? 1 : -1);
 
-  // One parallel step reads every node's parent, token and accept uniform,
-  // and checks them: a single root at node 0, every other parent earlier in
-  // the order (else TSV_ERR_BAD_TREE), tokens in [0, V) (else
-  // TSV_ERR_INVALID_ARG; tree errors take precedence).
-  if (tid == 0) {
-    bad = (n < 1) ? TSV_ERR_BAD_TREE : (n > TSV_MAX_NODES ? TSV_ERR_UNSUPPORTED : 0);
-    bad_tok = 0;
-  }
-  __syncthreads();
-  if (bad == 0) {
-    for (int i = tid; i < n; i += T) {
-      const int p = parent[off + i];
-      const int x = i > 0 ? tokens[off + i] : 0;
-      const float ua = i > 0 ? u_acc[off + i] : 0.f;
-      par_s[i] = p;
-      if (!((i == 0) ? (p == -1) : (p >= 0 && p < i))) atomicMax(&bad, TSV_ERR_BAD_TREE);
-      if (i > 0) {
-        tok_s[i] = x;
-        ua_s[i] = ua;
-        if (x < 0 || (int64_t)x >= V) bad_tok = TSV_ERR_INVALID_ARG;
-      }
+  // One parallel step reads every node's parent, token and uniforms, and
+  // checks them: a single root at node 0, every other parent earlier in the
+  // order (else TSV_ERR_BAD_TREE), tokens in [0, V) (else TSV_ERR_INVALID_ARG;
+  // tree errors take precedence).
+  static_assert(kMssThreads >= TSV_MAX_NODES, "one node per thread");
+  if (bad == 0 && tid < n) {
+    const int i = tid;
+    const int p = parent[off + i];
+    const int x = i > 0 ? tokens[off + i] : 0;
+    const float ua = i > 0 ? u_acc[off + i] : 0.f;
+    const float us = u_smp[off + i];
+    par_s[i] = p;
+    us_s[i] = us;
+    if (!((i == 0) ? (p == -1) : (p >= 0 && p < i))) atomicMax(&bad, TSV_ERR_BAD_TREE);
+    if (i > 0) {
+      tok_s[i] = x;
+      ua_s[i] = ua;
+      if (x < 0 || (int64_t)x >= V) bad_tok = TSV_ERR_INVALID_ARG;
     }
   }
   __syncthreads();
   const int code = bad ? bad : bad_tok;
-  if (code) {
-    drain();
+  cluster_wait_acquire();
+  if (code) {  // uniform over the cluster: every CTA sees the same tree
+    if (leader) drain();
     if (rank == 0)
       fail_request(path + off, n, accept_len + b, bonus + b, n_tried ? n_tried + b : nullptr,
                    status + b, code);
-    return;  // uniform over the cluster: every CTA sees the same tree
-  }
-  // Per child c: q_c(x_c) and the parent row's logit at x_c, loaded now and
-  // stored once the root's row statistics are done (the loads travel
-  // meanwhile; the first accept test is the first use).
-  static_assert(kMssThreads >= TSV_MAX_NODES, "one child per thread");
-  float my_qx = 0.f, my_lx = 0.f;
-  if (tid >= 1 && tid < n) {
-    my_qx = __ldg(ssm_probs + (size_t)(off + tid) * (size_t)V + tok_s[tid]);
-    my_lx = __ldg(llm_logits + (size_t)(off + par_s[tid]) * (size_t)V + tok_s[tid]);
+    return;
   }
   // The lowest-index child of p after node `from` (children follow their
-  // parent in the order), or -1: a ballot scan by the calling warp; every
-  // warp finds the same node.
+  // parent in the order), or -1: a ballot scan by the calling warp.
   auto next_child = [&](int p, int from) {
     for (int base = from + 1; base < n; base += 32) {
       const int c = base + lane;
@@ -893,384 +958,574 @@ __global__ void __launch_bounds__(kMssThreads, 2)
     }
     return -1;
   };
+  // The logits rows of u's first two children (the next row the walk reads
+  // if one of them is accepted) into L2; called by one warp.
+  auto prefetch_children = [&](int u) {
+    if (!kStaged || slice_bytes == 0) return;
+    const int c1 = next_child(u, u);
+    const int c2 = c1 >= 0 ? next_child(u, c1) : -1;
+    const int c = lane == 0 ? c1 : c2;
+    if (lane < 2 && c >= 0)
+      for (uint32_t o = 0; o < slice_bytes; o += kBulkChunk)
+        bulk_prefetch_l2(llm_logits + (size_t)(off + c) * (size_t)V + lo + o / 4, min(kBulkChunk, slice_bytes - o));
+  };
 
-  float* resid[2] = {resid_all + (size_t)b * 2 * (size_t)V, resid_all + ((size_t)b * 2 + 1) * (size_t)V};
-  int xk = 0;  // exchanges of the warped support so far (the same count in every CTA)
-  int xp = 0;  // pushed exchanges so far (the same count in every CTA)
-  uint32_t xpar = 0u;  // bit s: parity of the next phase of xbar[s]
-  // Pushed exchange: `per_warp` false, one float4 per CTA (slot = rank);
-  // true, one per warp of every CTA (slot = rank * kMssWarps + warp).
-  // Returns the slots once all have landed.
-  auto push = [&](float4 v, bool per_warp) -> const float4* {
+  float* const resid0 = resid_all + (size_t)b * 2 * (size_t)V;  // unstaged residual rows 0 and 1
+  auto resid_row = [&](int r) { return resid0 + (size_t)r * (size_t)V; };
+  int xk = 0;  // exchanges of the warped support so far (the same count in every thread)
+  int xp = 0;  // leader: pushed exchanges so far (the same count in every CTA)
+  uint32_t xpar = 0u;  // leader: bit s, parity of the next phase of xbar[s]
+  // Exchange of one float4 per CTA into slot set xs (slot = rank, sent by
+  // threads 0..ncl-1, every thread of the leader calling).
+  auto push_cta = [&](float4 v, int xs) {
+    if (tid == 0) mbar_arrive_expect_tx(&xbar[xs], (uint32_t)ncl * 16u);
+    if (tid < ncl)
+      st_async_v4(mapa_shared(smem_u32(&xslot[xs][rank]), (uint32_t)tid), v,
+                  mapa_shared(smem_u32(&xbar[xs]), (uint32_t)tid));
+  };
+  // Exchange of one float4 per worker warp (slot = rank * 15 + warp - 1, sent
+  // by lanes 0..ncl-1; v uniform over the warp).  The leader expects the
+  // bytes when it releases the step.
+  auto push_warp = [&](float4 v, int xs) {
+    if (lane < ncl)
+      st_async_v4(mapa_shared(smem_u32(&xslot[xs][rank * kMssWorkerWarps + warp - 1]), (uint32_t)lane), v,
+                  mapa_shared(smem_u32(&xbar[xs]), (uint32_t)lane));
+  };
+  // Leader: waits for the exchange in flight and returns its slots.
+  auto push_wait = [&]() -> const float4* {
     const int s = xp & 1;
-    const int slots = per_warp ? ncl * kMssWarps : ncl;
-    if (tid == 0) mbar_arrive_expect_tx(&xbar[s], (uint32_t)slots * 16u);
-    const int w = tid >> 5;
-    if (per_warp ? lane < ncl : tid < ncl) {
-      const int dst = per_warp ? lane : tid;
-      const int slot = per_warp ? rank * kMssWarps + w : rank;
-      st_async_v4(mapa_shared(smem_u32(&xslot[s][slot]), (uint32_t)dst), v,
-                  mapa_shared(smem_u32(&xbar[s]), (uint32_t)dst));
-    }
-    if (!mbar_wait(&xbar[s], (xpar >> s) & 1u, nullptr)) tmo = true;
+    if (!mbar_wait(&xbar[s], (xpar >> s) & 1u, nullptr)) tmo_s = 1;
     xpar ^= 1u << s;
     ++xp;
     return xslot[s];
   };
-  // Node u's logits, this CTA's slice.
-  auto logits_of = [&](int u) {
-    return staged ? Slice{buf(pb), lo} : Slice{llm_logits + (size_t)(off + u) * (size_t)V, 0};
-  };
 
-  // Row statistics of node u's logits: m = max(l / T), s = sum exp(l / T - m)
-  // over the kept tokens (all tokens unless warped), and the boundary
-  // (tau, ycut) of the kept set.  Staged, the row's slice is left holding
-  // weights w(y) with p(y) = w(y) * wscale: exp(l / T - m_local) (0 for tokens
-  // the warp drops), so later passes multiply instead of exponentiating.
-  float m_u = 0.f, inv_s = 0.f, tau = -INFINITY, wscale = 0.f;
-  int ycut = INT32_MAX;
-  auto row_stats = [&](int u) {
-    if (staged) ready(pb);
-    const Slice lrow = logits_of(u);
-    float m = -INFINITY;
-    for (int64_t g0 = tid; g0 < n4; g0 += (int64_t)T * kMssGroups) {
-      float4 v[kMssGroups];
-#pragma unroll
-      for (int k = 0; k < kMssGroups; ++k) {
-        const int64_t g = g0 + (int64_t)k * T;
-        if (g < n4) v[k] = lrow.ld4(lo + 4 * g, vec);
-      }
-#pragma unroll
-      for (int k = 0; k < kMssGroups; ++k)
-        if (g0 + (int64_t)k * T < n4)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) m = fmaxf(m, at(v[k], e) * inv_t);
-    }
-    for (int64_t y = lo + 4 * n4 + tid; y < hi; y += T) m = fmaxf(m, lrow[y] * inv_t);
-    m = block_max(m, red);
-    if (warped) {
-      const float4* e = push(make_float4(m, 0.f, 0.f, 0.f), false);
-      float M = -INFINITY;
-      for (int r = 0; r < ncl; ++r) M = fmaxf(M, e[r].x);
-      const Support sp = warped_support(lrow, V, lo, hi, inv_t, M, top_k, top_p, ncl, rank, xk, pub, sel);
-      m_u = M;
-      inv_s = f2_inv(sp.S);
-      tau = sp.tau;
-      ycut = sp.ycut;
-      if (staged) {  // weights relative to the row maximum M
-        float* w = buf(pb);
-        for (int64_t y = lo + tid; y < hi; y += T) {
-          const float l = w[y - lo];
-          w[y - lo] = kept(l, y, tau, ycut) ? exp_diff(l * inv_t, M) : 0.f;
-        }
-        wscale = inv_s;
-        fence_proxy_async_smem();  // the slice may be overwritten by a later copy
-        __syncthreads();
-      }
-      return;
-    }
-    CompSum acc;
-    for (int64_t g0 = tid; g0 < n4; g0 += (int64_t)T * kMssGroups) {
-      float4 v[kMssGroups];
-#pragma unroll
-      for (int k = 0; k < kMssGroups; ++k) {
-        const int64_t g = g0 + (int64_t)k * T;
-        if (g < n4) v[k] = lrow.ld4(lo + 4 * g, vec);
-      }
-#pragma unroll
-      for (int k = 0; k < kMssGroups; ++k) {
-        const int64_t g = g0 + (int64_t)k * T;
-        if (g < n4) {
-          float4 w;
-          w.x = exp_diff(v[k].x * inv_t, m);
-          w.y = exp_diff(v[k].y * inv_t, m);
-          w.z = exp_diff(v[k].z * inv_t, m);
-          w.w = exp_diff(v[k].w * inv_t, m);
-          acc.add(w.x);
-          acc.add(w.y);
-          acc.add(w.z);
-          acc.add(w.w);
-          if (staged) *reinterpret_cast<float4*>(buf(pb) + 4 * g) = w;
-        }
-      }
-    }
-    for (int64_t y = lo + 4 * n4 + tid; y < hi; y += T) {
-      const float w = exp_diff(lrow[y] * inv_t, m);
-      acc.add(w);
-      if (staged) buf(pb)[y - lo] = w;
-    }
-    if (staged) fence_proxy_async_smem();  // the slice may be overwritten by a later copy
-    F2 s = warp_sum_f2(comp_value(acc));
-    // Combine the warp partials (identical in every CTA):
-    // M = max m_i, S = sum s_i e^(m_i - M).
-    const float4* e = push(make_float4(m, s.hi, s.lo, 0.f), true);
-    const int cnt = ncl * kMssWarps;
-    const float4 e0 = lane < cnt ? e[lane] : make_float4(-INFINITY, 0.f, 0.f, 0.f);
-    const float4 e1 = lane + 32 < cnt ? e[lane + 32] : make_float4(-INFINITY, 0.f, 0.f, 0.f);
-    float M = fmaxf(e0.x, e1.x);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    F2 S{0.f, 0.f};
-    if (e0.x != -INFINITY) S = f2_scale(F2{e0.y, e0.z}, exp_diff(e0.x, M));
-    if (e1.x != -INFINITY) S = f2_add(S, f2_scale(F2{e1.y, e1.z}, exp_diff(e1.x, M)));
-    S = warp_sum_f2(S);
-    const float own = m != -INFINITY ? exp_diff(m, M) : 0.f;  // e^(m - M) of this CTA
-    m_u = M;
-    inv_s = f2_inv(S);
-    wscale = own * inv_s;
-    tau = -INFINITY;
-    ycut = INT32_MAX;
-  };
-
-  int u = 0, len = 1, cur = 0, tried = 0;
+  // The walk's state (the leader's; the statistics of a warped row are
+  // computed by every thread).
+  int u = 0, len = 1, cur = 0, tried = 0, qj = -1, last = kStepNone;
+  int tc = -1, tn = -1, txn = -1, t_oslot = -1;  // next child to test, its next sibling, the sibling's token, owner slot
+  int o_slot = -1;          // owner slot of the running residual pass (-1: none)
+  bool last_loads = true;   // the children's q_c(x_c) and l(x_c) are still to be read
   bool from_resid = false;  // false: p = softmax(row u); true: p = residual / Z
-  bool px_known = false;    // p at the current child's token came with the last exchange
+  bool px_known = false;    // p at the child to test came with the last exchange
   float px_next = 0.f;
   F2 Z{0.f, 0.f};
-  if (rank == 0 && tid == 0) path[off] = 0;
-  row_stats(0);
-  if (tid >= 1 && tid < n) {
-    qx_s[tid] = my_qx;
-    lx_s[tid] = my_lx;
-  }
-  __syncthreads();
-  while (true) {
-    int accepted = -1;
-    int c = next_child(u, u);
-    while (c >= 0) {
-      // p(x) of the current distribution (fp32, ~2 ulp); the test is exact.
-      const float px = px_known ? px_next
-                                : (kept(lx_s[c], tok_s[c], tau, ycut) ? exp_diff(lx_s[c] * inv_t, m_u) * inv_s : 0.f);
-      ++tried;
-      if (accept_test(ua_s[c], qx_s[c], px)) {
-        accepted = c;
-        break;
-      }
-      // Rejected: residual pass over the slice, r = max(0, p - q).  The owner
-      // of the next child's token records r and p there for the exchange.
-      const int cn = next_child(u, c);
-      const int64_t xn = cn >= 0 ? (int64_t)tok_s[cn] : -1;
-      const int nxt = cur ^ 1;
-      // p(y) = source(y) * pscale, except on a logits row read from global
-      // memory, where it is exponentiated here.
-      const float pscale = from_resid ? f2_inv(Z) : wscale;
-      Slice src, q;
-      float* rout;
-      int64_t rout_off;
-      int qj = -1;  // staged: the buffer of c's proposals, then of the residual
-      if (staged) {
-        qj = q_buffer_of(c);
-        if (qj < 0) {  // not fetched ahead
-          qj = free_buffer(-1);
-          q_issue(qj, c);
-        }
-        if (cn >= 0 && q_buffer_of(cn) < 0) q_issue(free_buffer(qj), cn);  // the next sibling's, ahead
-        ready(qj);
-        src = Slice{buf(pb), lo};
-        q = Slice{buf(qj), lo};
-        rout = buf(qj);  // over q: every element is read, then written, by one thread
-        rout_off = lo;
-      } else {
-        src = from_resid ? Slice{resid[cur], 0} : logits_of(u);
-        q = Slice{ssm_probs + (size_t)(off + c) * (size_t)V, 0};
-        rout = resid[nxt];
-        rout_off = 0;
-      }
-      CompSum acc;
-      float r_x = 0.f, p_x = 0.f;
-      for (int64_t g0 = tid; g0 < n4; g0 += (int64_t)T * kMssGroups) {
-        float4 a[kMssGroups], qq[kMssGroups];
-#pragma unroll
-        for (int k = 0; k < kMssGroups; ++k) {
-          const int64_t g = g0 + (int64_t)k * T;
-          if (g < n4) {
-            a[k] = src.ld4(lo + 4 * g, vec);
-            qq[k] = q.ld4(lo + 4 * g, vec);
-          }
-        }
-#pragma unroll
-        for (int k = 0; k < kMssGroups; ++k) {
-          const int64_t g = g0 + (int64_t)k * T;
-          if (g < n4) {
-            const int64_t y = lo + 4 * g;
-            float r[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float py = staged || from_resid
-                                   ? at(a[k], e) * pscale
-                                   : (kept(at(a[k], e), y + e, tau, ycut)
-                                          ? exp_diff(at(a[k], e) * inv_t, m_u) * inv_s : 0.f);
-              r[e] = fmaxf(py - at(qq[k], e), 0.0f);
-              acc.add(r[e]);
-              if (y + e == xn) {
-                r_x = r[e];
-                p_x = py;
-              }
-            }
-            float* o = rout + (y - rout_off);
-            if (vec) {
-              *reinterpret_cast<float4*>(o) = make_float4(r[0], r[1], r[2], r[3]);
-            } else {
-#pragma unroll
-              for (int e = 0; e < 4; ++e) o[e] = r[e];
-            }
-          }
-        }
-      }
-      for (int64_t y = lo + 4 * n4 + tid; y < hi; y += T) {
-        const float a = src[y];
-        const float py = staged || from_resid
-                             ? a * pscale
-                             : (kept(a, y, tau, ycut) ? exp_diff(a * inv_t, m_u) * inv_s : 0.f);
-        const float r = fmaxf(py - q[y], 0.0f);
-        rout[y - rout_off] = r;
-        acc.add(r);
-        if (y == xn) {
-          r_x = r;
-          p_x = py;
-        }
-      }
-      if (staged) fence_proxy_async_smem();  // the residual may be overwritten by a later copy
-      // Warp partials, then every warp of every CTA combines them in the
-      // same order (r and p at xn: one owner, the rest add zeros).
-      const F2 zs = warp_sum_f2(comp_value(acc));
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        r_x += __shfl_xor_sync(0xffffffffu, r_x, o);
-        p_x += __shfl_xor_sync(0xffffffffu, p_x, o);
-      }
-      const float4* e = push(make_float4(zs.hi, zs.lo, r_x, p_x), true);
-      const int cnt = ncl * kMssWarps;
-      const float4 e0 = lane < cnt ? e[lane] : make_float4(0.f, 0.f, 0.f, 0.f);
-      const float4 e1 = lane + 32 < cnt ? e[lane + 32] : make_float4(0.f, 0.f, 0.f, 0.f);
-      F2 Znew = warp_sum_f2(f2_add(F2{e0.x, e0.y}, F2{e1.x, e1.y}));
-      float rxn = e0.z + e1.z, pxn = e0.w + e1.w;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        rxn += __shfl_xor_sync(0xffffffffu, rxn, o);
-        pxn += __shfl_xor_sync(0xffffffffu, pxn, o);
-      }
-      if (staged) node_of[qj] = -1;  // c's proposals are spent
-      if (Znew.hi > 0.f) {  // else p = q up to rounding: keep p
-        cur = nxt;
-        if (staged) pb = qj;  // the residual is the distribution's row now
-        Z = Znew;
-        from_resid = true;
-        px_next = rxn * f2_inv(Znew);
-      } else {
-        px_next = pxn;
-      }
-      px_known = true;
-      c = cn;
-    }
-    if (accepted < 0) break;
-    u = accepted;
-    if (rank == 0 && tid == 0) path[off + len] = u;
-    ++len;
-    from_resid = false;
-    px_known = false;
-    if (staged) stage_row(u, next_child(u, u));
-    row_stats(u);
-  }
+  // Row statistics of the node being expanded: m_u = max(l / T), inv_s =
+  // 1 / sum exp(l / T - m_u) over the kept tokens (all unless warped), the
+  // boundary (tau, ycut) of the kept set, and wscale: p(y) = w(y) * wscale
+  // for the staged weights w(y) = exp(l / T - m_cta) (m_cta: this CTA's
+  // maximum; with warping, M itself).
+  float m_u = 0.f, inv_s = 0.f, tau = -INFINITY, wscale = 0.f;
+  int ycut = INT32_MAX;
 
-  pdl_trigger();  // the walk is done: let the next kernel be scheduled
-  // Bonus token: smallest y with cumsum(w)[y] > u_smp[u] * sum(w), w = the
-  // unnormalised current distribution.  Each thread owns a contiguous run of
-  // its CTA's slice; runs and slices are in vocabulary order.
-  {
-    const Slice wsrc = staged ? Slice{buf(pb), lo} : (from_resid ? Slice{resid[cur], 0} : logits_of(u));
-    const int64_t per_t = ((((hi - lo) + T - 1) / T) + 3) & ~int64_t(3);
-    const int64_t tlo = min(hi, lo + (int64_t)tid * per_t), thi = min(hi, tlo + per_t);
-    const float bscale = from_resid ? 1.f : wscale;  // staged weights to one common scale
-    auto weight = [&](float a, int64_t y) {
-      if (staged) return a * bscale;
-      return from_resid ? a : (kept(a, y, tau, ycut) ? exp_diff(a * inv_t, m_u) : 0.f);
+  // Leader, while the step `d` runs: the child to test after it, that
+  // child's next sibling and the owner of the sibling's token (its slot in a
+  // residual exchange), and the proposal copies of both when a buffer is free
+  // (not the distribution's row, not the one the step writes, not one
+  // holding either child's proposals).
+  auto leader_prep = [&](const MssStep& d) {
+    if (last_loads) {  // first step: q_c(x_c) and the parent row's logit at x_c of every child c
+      for (int i = 1 + lane; i < n; i += 32) {
+        qx_s[i] = __ldg(ssm_probs + (size_t)(off + i) * (size_t)V + tok_s[i]);
+        lx_s[i] = __ldg(llm_logits + (size_t)(off + par_s[i]) * (size_t)V + tok_s[i]);
+      }
+      __syncwarp();
+      last_loads = false;
+    }
+    tc = d.kind == kStepRow ? next_child(u, u) : tn;
+    tn = tc >= 0 ? next_child(u, tc) : -1;
+    txn = tn >= 0 ? tok_s[tn] : -1;
+    t_oslot = -1;
+    if (txn >= 0) {  // rank xn / per; there, group (xn - lo') / 4 goes to worker group % TW,
+      const int p32 = (int)per, v32 = (int)V;  // a tail element to worker (index past the groups) % TW
+      const int orank = txn / p32;
+      const int olo = orank * p32, ohi = min(v32, olo + p32), on4 = (ohi - olo) >> 2;
+      const int rel = txn - olo;
+      const int own = rel < 4 * on4 ? (rel >> 2) % TW : (rel - 4 * on4) % TW;
+      t_oslot = orank * kMssWorkerWarps + (own >> 5);
+    }
+    if (kStaged) {
+      const int busy = d.kind == kStepPass ? d.qj : pb;
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int x = k == 0 ? tc : tn;
+        if (x < 0 || q_buffer_of(x) >= 0) continue;
+        int j = -1;
+#pragma unroll
+        for (int jj = 0; jj < 3; ++jj) {
+          const int nd = node_of(jj);
+          if (jj == pb || jj == busy || (nd >= 0 && (nd == tc || nd == tn))) continue;
+          if (j < 0 || (((pend >> j) & 1u) && !((pend >> jj) & 1u))) j = jj;
+        }
+        if (j < 0) break;  // no room now: issued when the child is tested
+        q_issue(j, x);
+      }
+    }
+  };
+
+  // Leader: the exchange of the step `d` (unwarped row statistics or a
+  // residual pass), combined.
+  auto leader_consume = [&](const MssStep& d) {
+    const float4* e = push_wait();
+    const int cnt = ncl * kMssWorkerWarps;
+    if (d.kind == kStepRow) {
+      // M = max m_r, S = sum_r e^(m_r - M) sum_w s_rw: every warp partial of
+      // rank r shares its m_r.  Lanes 4r..4r+3 take rank r's slots (warps
+      // 4k + lane % 4), sum them, scale once and sum over the ranks.
+      static_assert(kMssMaxCluster * 4 == 32 && kMssWorkerWarps <= 16, "four lanes per rank");
+      const int r = lane >> 2;
+      float mr = -INFINITY;
+      F2 S{0.f, 0.f};
+      if (r < ncl) {
+        mr = e[r * kMssWorkerWarps].x;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int w = (lane & 3) + 4 * k;
+          if (w < kMssWorkerWarps) {
+            const float4 ev = e[r * kMssWorkerWarps + w];
+            S = f2_add(S, F2{ev.y, ev.z});
+          }
+        }
+      }
+      S = f2_add(S, shfl_xor_f2(S, 1));
+      S = f2_add(S, shfl_xor_f2(S, 2));
+      float M = mr;
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+      S = mr != -INFINITY ? f2_scale(S, exp_diff(mr, M)) : F2{0.f, 0.f};
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) S = f2_add(S, shfl_xor_f2(S, o));
+      const float m_cta = e[rank * kMssWorkerWarps].x;
+      const float own = m_cta != -INFINITY ? exp_diff(m_cta, M) : 0.f;  // e^(m - M) of this CTA
+      m_u = M;
+      inv_s = f2_inv(S);
+      wscale = own * inv_s;
+      tau = -INFINITY;
+      ycut = INT32_MAX;
+      return;
+    }
+    // Z = sum of the residual partials (the same order in every CTA); r and
+    // p at the next child's token from its owner's slot.
+    F2 Zp{0.f, 0.f};
+#pragma unroll
+    for (int k = 0; k < kMssSlots / 32 + 1; ++k)
+      if (lane + 32 * k < cnt) Zp = f2_add(Zp, F2{e[lane + 32 * k].x, e[lane + 32 * k].y});
+    const F2 Znew = warp_sum_f2(Zp);
+    float rxn = 0.f, pxn = 0.f;
+    if (o_slot >= 0) {
+      const float4 eo = e[o_slot];
+      rxn = eo.z;
+      pxn = eo.w;
+    }
+    if (kStaged) set_node(qj, -1);  // the rejected child's proposals are spent
+    if (Znew.hi > 0.f) {  // else p = q up to rounding: keep p
+      cur ^= 1;
+      if (kStaged) pb = qj;  // the residual is the distribution's row now
+      Z = Znew;
+      from_resid = true;
+      px_next = rxn * f2_inv(Znew);
+    } else {
+      px_next = pxn;
+    }
+    px_known = true;
+  };
+
+  // Leader: the accept test of child tc (if any) and the next step.
+  auto leader_decide = [&](MssStep& d) {
+    int kind = kStepRow;  // first: the root's statistics
+    if (last != kStepNone) {
+      if (tc < 0) {
+        kind = kStepBonus;
+      } else {
+        // p(x) of the current distribution (fp32, ~2 ulp); the test is exact.
+        const float px = px_known ? px_next
+                                  : (kept(lx_s[tc], tok_s[tc], tau, ycut) ? exp_diff(lx_s[tc] * inv_t, m_u) * inv_s
+                                                                           : 0.f);
+        ++tried;
+        if (accept_test(ua_s[tc], qx_s[tc], px)) {
+          u = tc;
+          if (rank == 0 && lane == 0) path[off + len] = u;
+          ++len;
+          from_resid = false;
+          px_known = false;
+          if (kStaged) stage_row(u, next_child(u, u));
+          kind = kStepRow;
+        } else {
+          kind = kStepPass;
+        }
+      }
+    }
+    d.kind = kind;
+    d.u = u;
+    d.xs = xp & 1;
+    d.m_u = m_u;
+    d.inv_s = inv_s;
+    d.tau = tau;
+    d.ycut = ycut;
+    d.len = len;
+    if (kind == kStepRow) {
+      if (kStaged) land(pb);
+      d.src = pb;
+    } else if (kind == kStepPass) {
+      // Rejected: residual pass r = max(0, p - q) over the slice.  p(y) =
+      // source(y) * pscale, except on a logits row read from global memory,
+      // where it is exponentiated in the pass.
+      d.pscale = from_resid ? f2_inv(Z) : wscale;
+      d.c = tc;
+      d.xn = txn;
+      o_slot = t_oslot;
+      if (kStaged) {
+        qj = q_buffer_of(tc);
+        if (qj < 0) {  // not fetched ahead
+          qj = free_buffer();
+          q_issue(qj, tc);
+        }
+        land(qj);
+        d.src = pb;
+        d.qj = qj;
+      } else {
+        d.src = from_resid ? cur : -1;
+        d.nxt = cur ^ 1;
+      }
+    } else {
+      d.src = kStaged ? pb : (from_resid ? cur : -1);
+      d.bscale = from_resid ? 1.f : wscale;  // staged weights to one common scale
+      d.us = us_s[u];
+    }
+    last = kind;
+  };
+
+  // Row statistics of an unwarped row (workers): the maximum, the weights
+  // exp(l / T - m) (staged: stored over the logits) and their warp partial
+  // sums, pushed for the leaders.  When the slice is at most G groups per
+  // worker, its values stay in registers between the two.
+  auto row_step = [&](const MssStep& d) {
+    const Slice lrow = kStaged ? Slice{buf(d.src), lo} : Slice{llm_logits + (size_t)(off + d.u) * (size_t)V, 0};
+    const bool one = n4 <= (int64_t)TW * G;
+    float4 v[G];
+    float m = -INFINITY;
+    for (int64_t g0 = wid; g0 < n4; g0 += (int64_t)TW * G) {
+#pragma unroll
+      for (int k = 0; k < G; ++k) {
+        const int64_t g = g0 + (int64_t)k * TW;
+        if (g < n4) v[k] = lrow.ld4(lo + 4 * g, vec);
+      }
+#pragma unroll
+      for (int k = 0; k < G; ++k)
+        if (g0 + (int64_t)k * TW < n4)
+          m = fmaxf(m, fmaxf(fmaxf(v[k].x * inv_t, v[k].y * inv_t), fmaxf(v[k].z * inv_t, v[k].w * inv_t)));
+    }
+    for (int64_t y = lo + 4 * n4 + wid; y < hi; y += TW) m = fmaxf(m, lrow[y] * inv_t);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (lane == 0) red[warp] = m;
+    named_bar_sync(1, TW);
+#pragma unroll
+    for (int w = 1; w < kMssWarps; ++w) m = fmaxf(m, red[w]);
+    CompSum acc;
+    auto weigh = [&](float4 x, int64_t g) {  // exp(l / T - m) of group g, summed (and staged: stored)
+      float4 w;
+      w.x = exp_diff(x.x * inv_t, m);
+      w.y = exp_diff(x.y * inv_t, m);
+      w.z = exp_diff(x.z * inv_t, m);
+      w.w = exp_diff(x.w * inv_t, m);
+      acc.add(w.x);
+      acc.add(w.y);
+      acc.add(w.z);
+      acc.add(w.w);
+      if (kStaged) *reinterpret_cast<float4*>(buf(d.src) + 4 * g) = w;
+    };
+    if (one) {
+#pragma unroll
+      for (int k = 0; k < G; ++k) {
+        const int64_t g = wid + (int64_t)k * TW;
+        if (g < n4) weigh(v[k], g);
+      }
+    } else {
+      for (int64_t g0 = wid; g0 < n4; g0 += (int64_t)TW * G) {
+#pragma unroll
+        for (int k = 0; k < G; ++k) {
+          const int64_t g = g0 + (int64_t)k * TW;
+          if (g < n4) v[k] = lrow.ld4(lo + 4 * g, vec);
+        }
+#pragma unroll
+        for (int k = 0; k < G; ++k) {
+          const int64_t g = g0 + (int64_t)k * TW;
+          if (g < n4) weigh(v[k], g);
+        }
+      }
+    }
+    for (int64_t y = lo + 4 * n4 + wid; y < hi; y += TW) {
+      const float w = exp_diff(lrow[y] * inv_t, m);
+      acc.add(w);
+      if (kStaged) buf(d.src)[y - lo] = w;
+    }
+    if (kStaged) fence_proxy_async_smem();  // the slice may be overwritten by a later copy
+    const F2 s = warp_sum_f2(comp_value(acc));
+    push_warp(make_float4(m, s.hi, s.lo, 0.f), d.xs);
+    if (warp == kMssWarps - 1) prefetch_children(d.u);
+  };
+
+  // Row statistics of a warped row (every thread): the maximum exchanged,
+  // then the warped support found by the cluster; staged, the slice is left
+  // holding the weights exp(l / T - M) of the kept tokens.
+  auto row_step_warped = [&](const MssStep& d) {
+    const Slice lrow = kStaged ? Slice{buf(d.src), lo} : Slice{llm_logits + (size_t)(off + d.u) * (size_t)V, 0};
+    float m = -INFINITY;
+    for (int64_t y = lo + tid; y < hi; y += T) m = fmaxf(m, lrow[y] * inv_t);
+    m = block_max<kMssWarps>(m, red);
+    push_cta(make_float4(m, 0.f, 0.f, 0.f), d.xs);
+    if (warp == kMssWarps - 1) prefetch_children(d.u);
+    if (leader) {
+      const float4* e = push_wait();
+      float M = -INFINITY;
+      for (int r = 0; r < ncl; ++r) M = fmaxf(M, e[r].x);
+      if (lane == 0) mx_s = M;
+    }
+    __syncthreads();
+    const float M = mx_s;
+    const Support sp = warped_support<kMssThreads>(lrow, V, lo, hi, inv_t, M, top_k, top_p, ncl, rank, xk,
+                                                   pub, sel);
+    m_u = M;
+    inv_s = f2_inv(sp.S);
+    tau = sp.tau;
+    ycut = sp.ycut;
+    if (kStaged) {  // weights relative to the row maximum M
+      float* w = buf(d.src);
+      for (int64_t y = lo + tid; y < hi; y += T) {
+        const float l = w[y - lo];
+        w[y - lo] = kept(l, y, tau, ycut) ? exp_diff(l * inv_t, M) : 0.f;
+      }
+      wscale = inv_s;
+      fence_proxy_async_smem();  // the slice may be overwritten by a later copy
+      __syncthreads();
+    }
+  };
+
+  // Residual pass (workers): r = max(0, p - q) over the slice, its warp
+  // partial sums pushed for the leaders with r and p at the next child's
+  // token, which its owner reads back from its own writes.
+  auto pass_step = [&](const MssStep& d) {
+    const bool direct = kStaged || d.src >= 0;  // p = source * pscale
+    const Slice src = kStaged ? Slice{buf(d.src), lo}
+                              : (d.src >= 0 ? Slice{resid_row(d.src), 0}
+                                            : Slice{llm_logits + (size_t)(off + d.u) * (size_t)V, 0});
+    const Slice q = kStaged ? Slice{buf(d.qj), lo} : Slice{ssm_probs + (size_t)(off + d.c) * (size_t)V, 0};
+    float* const rout = kStaged ? buf(d.qj) : resid_row(d.nxt);  // staged: over q, element by element
+    const int64_t rout_off = kStaged ? lo : 0;
+    const float pscale = d.pscale;
+    auto p_of = [&](float a, int64_t y) {
+      return direct ? a * pscale : (kept(a, y, d.tau, d.ycut) ? exp_diff(a * inv_t, d.m_u) * d.inv_s : 0.f);
     };
     CompSum acc;
-    int64_t last_pos = -1;
-    {
-      int64_t y = tlo;
-      for (; y + 4 <= thi; y += 4) {
-        const float4 a = wsrc.ld4(y, vec);
+    for (int64_t g0 = wid; g0 < n4; g0 += (int64_t)TW * G) {
+      float4 a[G], qq[G];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float w = weight(at(a, e), y + e);
-          acc.add(w);
-          if (w > 0.0f) last_pos = y + e;
+      for (int k = 0; k < G; ++k) {
+        const int64_t g = g0 + (int64_t)k * TW;
+        if (g < n4) {
+          a[k] = src.ld4(lo + 4 * g, vec);
+          qq[k] = q.ld4(lo + 4 * g, vec);
         }
       }
-      for (; y < thi; ++y) {
-        const float w = weight(wsrc[y], y);
-        acc.add(w);
-        if (w > 0.0f) last_pos = y;
-      }
-    }
-    const F2 mine = comp_value(acc);
-    // Exclusive prefix over the CTA's threads: warp scan, then across warps.
-    const int warp = tid >> 5;
-    F2 incl = mine;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const F2 t{__shfl_up_sync(0xffffffffu, incl.hi, o), __shfl_up_sync(0xffffffffu, incl.lo, o)};
-      if (lane >= o) incl = f2_add(t, incl);
-    }
-    F2 wexcl{__shfl_up_sync(0xffffffffu, incl.hi, 1), __shfl_up_sync(0xffffffffu, incl.lo, 1)};
-    if (lane == 0) wexcl = F2{0.f, 0.f};
-    if (lane == 31) scan_s[warp] = incl;
-    if (last_pos >= 0) atomicMax(&last_s, (int)last_pos);
-    __syncthreads();
-    F2 wbase{0.f, 0.f}, cta_total{0.f, 0.f};
-    for (int w = 0; w < kMssWarps; ++w) {
-      if (w < warp) wbase = f2_add(wbase, scan_s[w]);
-      cta_total = f2_add(cta_total, scan_s[w]);
-    }
-    const float4* e = push(make_float4(cta_total.hi, cta_total.lo, __int_as_float(last_s), 0.f), false);
-    F2 base{0.f, 0.f}, total{0.f, 0.f};
-    int last_all = -1;
-    for (int r = 0; r < ncl; ++r) {  // in rank order, identical in every CTA
-      const F2 t{e[r].x, e[r].y};
-      if (r < rank) base = f2_add(base, t);
-      total = f2_add(total, t);
-      last_all = max(last_all, __float_as_int(e[r].z));
-    }
-    const F2 excl = f2_add(f2_add(base, wbase), wexcl);
-    const F2 target = f2_scale(total, __ldg(u_smp + off + u));
-    if (mine.hi > 0.f && !f2_lt(target, excl) && f2_lt(target, f2_add(excl, mine))) {
-      // This run holds the crossing; walk it in order.
-      int64_t pick = -1;
-      CompSum run;
-      for (int64_t y = tlo; y < thi; ++y) {
-        const float w = weight(wsrc[y], y);
-        run.add(w);
-        if (f2_lt(target, f2_add(excl, comp_value(run)))) {
-          pick = y;
-          break;
+      for (int k = 0; k < G; ++k) {
+        const int64_t g = g0 + (int64_t)k * TW;
+        if (g < n4) {
+          const int64_t y = lo + 4 * g;
+          float4 r;
+          r.x = fmaxf(p_of(a[k].x, y) - qq[k].x, 0.0f);
+          r.y = fmaxf(p_of(a[k].y, y + 1) - qq[k].y, 0.0f);
+          r.z = fmaxf(p_of(a[k].z, y + 2) - qq[k].z, 0.0f);
+          r.w = fmaxf(p_of(a[k].w, y + 3) - qq[k].w, 0.0f);
+          acc.add(r.x);
+          acc.add(r.y);
+          acc.add(r.z);
+          acc.add(r.w);
+          float* o = rout + (y - rout_off);
+          if (vec) {
+            *reinterpret_cast<float4*>(o) = r;
+          } else {
+            o[0] = r.x;
+            o[1] = r.y;
+            o[2] = r.z;
+            o[3] = r.w;
+          }
         }
       }
-      if (pick < 0) pick = last_pos;  // rounding inside the run
-      atomicMin(&pick_s, (int)pick);
     }
-    drain();
-    __syncthreads();
-    const float4* e2 = push(make_float4(__int_as_float(pick_s), tmo ? 1.f : 0.f, 0.f, 0.f), false);
-    if (rank == 0 && tid == 0) {
-      int pick = INT32_MAX;
-      bool timed_out = tmo;
-      for (int r = 0; r < ncl; ++r) {
-        pick = min(pick, __float_as_int(e2[r].x));
-        timed_out = timed_out || e2[r].y != 0.f;
+    for (int64_t y = lo + 4 * n4 + wid; y < hi; y += TW) {
+      const float r = fmaxf(p_of(src[y], y) - q[y], 0.0f);
+      rout[y - rout_off] = r;
+      acc.add(r);
+    }
+    if (kStaged) fence_proxy_async_smem();  // the residual may be overwritten by a later copy
+    // The owner of xn in this CTA: group (xn - lo) / 4 goes to worker
+    // group % TW, a tail element to worker (index past the groups) % TW.
+    int own = -1;
+    if (d.xn >= lo && d.xn < hi) {
+      const int64_t rel = d.xn - lo;
+      own = (int)(rel < 4 * n4 ? (rel >> 2) % TW : (rel - 4 * n4) % TW);
+    }
+    float r_x = 0.f, p_x = 0.f;
+    if (own == wid) {  // its own writes, read back
+      p_x = p_of(src[d.xn], d.xn);
+      r_x = rout[d.xn - rout_off];
+    }
+    const F2 zs = warp_sum_f2(comp_value(acc));
+    if (own >= 0 && (own >> 5) == warp - 1) {  // uniform over the warp for the push
+      r_x = __shfl_sync(0xffffffffu, r_x, own & 31);
+      p_x = __shfl_sync(0xffffffffu, p_x, own & 31);
+    }
+    push_warp(make_float4(zs.hi, zs.lo, r_x, p_x), d.xs);
+  };
+
+  if (rank == 0 && tid == 0) path[off] = 0;
+  MssStep d;
+  for (int st = 0;; ++st) {
+    if (leader) {
+      leader_decide(d);
+      if (lane == 0) {
+        dsc[st & 1] = d;
+        if (d.kind == kStepPass || (d.kind == kStepRow && !warped))  // the workers' partials
+          mbar_arrive_expect_tx(&xbar[d.xs], (uint32_t)(ncl * kMssWorkerWarps) * 16u);
       }
-      // No crossing (rounding left the target at the total): last positive entry.
-      bonus[b] = pick != INT32_MAX ? pick : last_all;
-      accept_len[b] = len - 1;
-      if (n_tried) n_tried[b] = tried;
-      status[b] = timed_out ? TSV_ERR_TIMEOUT : TSV_OK;
     }
-    // Every push into this CTA has landed (the last wait counted them all) and
-    // it reads no other CTA's memory from here on: it may leave.
+    __syncthreads();  // the step is described and its input has landed
+    d = dsc[st & 1];
+    if (d.kind == kStepBonus) break;
+    if (d.kind == kStepRow && warped) {
+      row_step_warped(d);
+      if (leader) leader_prep(d);
+    } else if (leader) {
+      leader_prep(d);
+      leader_consume(d);
+    } else if (d.kind == kStepRow) {
+      row_step(d);
+    } else {
+      pass_step(d);
+    }
   }
+
   if (rank == 0)
-    for (int i = len + tid; i < n; i += T) path[off + i] = -1;
+    for (int i = d.len + tid; i < n; i += T) path[off + i] = -1;
+  if (leader) drain();  // no copy may be in flight when the CTA leaves
+  // Bonus token: smallest y with cumsum(w)[y] > u_smp[u] * sum(w), w = the
+  // unnormalised current distribution.  Each thread owns a contiguous run of
+  // its CTA's slice; runs and slices are in vocabulary order.  The CTA totals
+  // are exchanged; from their prefix sums every CTA finds the same rank whose
+  // interval holds the target, and only that CTA searches its runs and
+  // writes the token.
+  const Slice wsrc = kStaged ? Slice{buf(d.src), lo}
+                             : (d.src >= 0 ? Slice{resid_row(d.src), 0}
+                                           : Slice{llm_logits + (size_t)(off + d.u) * (size_t)V, 0});
+  const int64_t per_t = ((((hi - lo) + T - 1) / T) + 3) & ~int64_t(3);
+  const int64_t tlo = min(hi, lo + (int64_t)tid * per_t), thi = min(hi, tlo + per_t);
+  auto weight = [&](float a, int64_t y) {
+    if (kStaged) return a * d.bscale;
+    return d.src >= 0 ? a : (kept(a, y, d.tau, d.ycut) ? exp_diff(a * inv_t, d.m_u) : 0.f);
+  };
+  CompSum acc;
+  int64_t last_pos = -1;
+  {
+    int64_t y = tlo;
+    for (; y + 4 <= thi; y += 4) {
+      const float4 a = wsrc.ld4(y, vec);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float w = weight(at(a, e), y + e);
+        acc.add(w);
+        if (w > 0.0f) last_pos = y + e;
+      }
+    }
+    for (; y < thi; ++y) {
+      const float w = weight(wsrc[y], y);
+      acc.add(w);
+      if (w > 0.0f) last_pos = y;
+    }
+  }
+  const F2 mine = comp_value(acc);
+  // Exclusive prefix over the CTA's threads: a warp scan here; the leader
+  // scans the warp totals and the CTA totals.
+  const F2 incl = warp_scan_f2(mine);
+  F2 wexcl = shfl_up_f2(incl, 1);
+  if (lane == 0) wexcl = F2{0.f, 0.f};
+  if (lane == 31) scan_s[warp] = incl;
+  if (last_pos >= 0) atomicMax(&last_s, (int)last_pos);
+  __syncthreads();
+  if (leader) {
+    F2 wt = lane < kMssWarps ? scan_s[lane] : F2{0.f, 0.f};
+#pragma unroll
+    for (int o = 1; o < kMssWarps; o <<= 1) {
+      const F2 t = shfl_up_f2(wt, o);
+      if (lane >= o) wt = f2_add(t, wt);
+    }
+    const F2 cta_total = shfl_f2(wt, kMssWarps - 1);
+    F2 wex = shfl_up_f2(wt, 1);
+    if (lane == 0) wex = F2{0.f, 0.f};
+    push_cta(make_float4(cta_total.hi, cta_total.lo, __int_as_float(last_s), tmo_s ? 1.f : 0.f), xp & 1);
+    const float4* e = push_wait();
+    // The CTA totals in rank order, scanned by lanes 0..ncl-1 (identical in
+    // every CTA); the crossing rank is the first whose inclusive prefix
+    // exceeds the target.
+    F2 ct = lane < ncl ? F2{e[lane].x, e[lane].y} : F2{0.f, 0.f};
+    int last_all = lane < ncl ? __float_as_int(e[lane].z) : -1;
+    const bool timed_out = __ballot_sync(0xffffffffu, lane < ncl && e[lane].w != 0.f) != 0u;
+#pragma unroll
+    for (int o = 1; o < kMssMaxCluster; o <<= 1) {
+      const F2 t = shfl_up_f2(ct, o);
+      if (lane >= o) ct = f2_add(t, ct);
+      last_all = max(last_all, __shfl_xor_sync(0xffffffffu, last_all, o));
+    }
+    const F2 total = shfl_f2(ct, ncl - 1);
+    F2 base = shfl_f2(ct, rank > 0 ? rank - 1 : 0);
+    if (rank == 0) base = F2{0.f, 0.f};
+    const F2 target = f2_scale(total, d.us);
+    const uint32_t over = __ballot_sync(0xffffffffu, lane < ncl && f2_lt(target, ct));
+    const int rc = over ? __ffs(over) - 1 : -1;
+    if (lane < kMssWarps) wpre_s[lane] = f2_add(base, wex);
+    if (lane == 0) {
+      target_s = target;
+      pick_s = rc;
+      if (rank == 0) {
+        // No crossing (rounding left the target at the total): last positive entry.
+        if (rc < 0) bonus[b] = last_all;
+        accept_len[b] = d.len - 1;
+        if (n_tried) n_tried[b] = tried;
+        status[b] = timed_out ? TSV_ERR_TIMEOUT : TSV_OK;
+      }
+    }
+  }
+  __syncthreads();
+  if (pick_s != rank) return;  // uniform over the CTA
+  __syncthreads();  // every thread has read pick_s
+  if (tid == 0) pick_s = INT32_MAX;
+  __syncthreads();
+  const F2 excl = f2_add(wpre_s[warp], wexcl);
+  const F2 target = target_s;
+  // The run holding the crossing is walked by its whole warp, 32 entries at
+  // a time (an inclusive scan per chunk).
+  const bool cross = mine.hi > 0.f && !f2_lt(target, excl) && f2_lt(target, f2_add(excl, mine));
+  const uint32_t cb = __ballot_sync(0xffffffffu, cross);
+  if (cb) {
+    const int sl = __ffs(cb) - 1;
+    const int64_t rlo = __shfl_sync(0xffffffffu, tlo, sl), rhi = __shfl_sync(0xffffffffu, thi, sl);
+    F2 run = shfl_f2(excl, sl);
+    int64_t pick = -1;
+    for (int64_t base_y = rlo; base_y < rhi && pick < 0; base_y += 32) {
+      const int64_t y = base_y + lane;
+      const float w = y < rhi ? weight(wsrc[y], y) : 0.f;
+      const F2 inc = warp_scan_f2(F2{w, 0.f});
+      const uint32_t hit = __ballot_sync(0xffffffffu, w > 0.f && f2_lt(target, f2_add(run, inc)));
+      if (hit) pick = base_y + __ffs(hit) - 1;
+      run = f2_add(run, shfl_f2(inc, 31));
+    }
+    if (pick < 0) pick = __shfl_sync(0xffffffffu, last_pos, sl);  // rounding inside the run
+    if (lane == 0) atomicMin(&pick_s, (int)pick);
+  }
+  __syncthreads();
+  // No run holds it (rounding at the slice's end): the slice's last positive entry.
+  if (tid == 0) bonus[b] = pick_s != INT32_MAX ? pick_s : last_s;
 }
 
 // ------------------------------------------------------------------ tree construction
@@ -1328,14 +1583,14 @@ __device__ void expand_small(const float* __restrict__ row, int64_t lo, int64_t 
   const bool vec = ((lo & 3) == 0) && ((reinterpret_cast<uintptr_t>(row) & 15) == 0);
   const int64_t n4 = vec ? (hi - lo) / 4 : 0;
   const float4* r4 = reinterpret_cast<const float4*>(row + lo);
-  for (int64_t g0 = tid; g0 < n4; g0 += kInFlight * kMssThreads) {
+  for (int64_t g0 = tid; g0 < n4; g0 += kInFlight * kSelThreads) {
     float4 a[kInFlight];
 #pragma unroll
     for (int u = 0; u < kInFlight; ++u)
-      if (g0 + u * kMssThreads < n4) a[u] = __ldg(r4 + g0 + u * kMssThreads);
+      if (g0 + u * kSelThreads < n4) a[u] = __ldg(r4 + g0 + u * kSelThreads);
 #pragma unroll
     for (int u = 0; u < kInFlight; ++u) {
-      const int64_t g = g0 + u * kMssThreads;
+      const int64_t g = g0 + u * kSelThreads;
       if (g < n4) {
         const int y = (int)(lo + 4 * g);
         offer(a[u].x, y);
@@ -1345,7 +1600,7 @@ __device__ void expand_small(const float* __restrict__ row, int64_t lo, int64_t 
       }
     }
   }
-  for (int64_t y = lo + 4 * n4 + tid; y < hi; y += kMssThreads) offer(__ldg(row + y), (int)y);
+  for (int64_t y = lo + 4 * n4 + tid; y < hi; y += kSelThreads) offer(__ldg(row + y), (int)y);
 #pragma unroll
   for (int i = 0; i < KP; ++i) {
     lv[tid * KP + i] = bv[i];
@@ -1372,7 +1627,7 @@ __device__ void expand_small(const float* __restrict__ row, int64_t lo, int64_t 
     __syncthreads();
     float bvv = rv[0];
     int bid = ri[0];
-    for (int ww = 1; ww < kMssWarps; ++ww)
+    for (int ww = 1; ww < kSelWarps; ++ww)
       if (ranks_before(rv[ww], ri[ww], bvv, bid)) {
         bvv = rv[ww];
         bid = ri[ww];
@@ -1390,7 +1645,7 @@ __device__ void expand_small(const float* __restrict__ row, int64_t lo, int64_t 
 // taking vocabulary slice r.  k <= 8: every CTA finds its slice's top-k, rank
 // 0 merges the ncl lists through distributed shared memory.  Wider: the
 // cluster runs the warped support's selection (maximum first, exchanged).
-__global__ void __launch_bounds__(kMssThreads)
+__global__ void __launch_bounds__(kSelThreads)
     tree_expand_kernel(const float* __restrict__ logits, int64_t V, int k, int ncl,
                        int32_t* __restrict__ tokens) {
   pdl_trigger();
@@ -1398,10 +1653,10 @@ __global__ void __launch_bounds__(kMssThreads)
   __shared__ __align__(16) float pub[2][4];
   __shared__ SelSmem sel;
   __shared__ float red[128];
-  __shared__ float lv[kMssThreads * kExpandSmallK];
-  __shared__ int li[kMssThreads * kExpandSmallK];
-  __shared__ float rv[kMssWarps];
-  __shared__ int ri[kMssWarps];
+  __shared__ float lv[kSelThreads * kExpandSmallK];
+  __shared__ int li[kSelThreads * kExpandSmallK];
+  __shared__ float rv[kSelWarps];
+  __shared__ int ri[kSelWarps];
   __shared__ float top_v[kExpandSmallK];
   __shared__ int32_t top_i[kExpandSmallK];
   const int f = blockIdx.x / ncl;
@@ -1462,8 +1717,8 @@ __global__ void __launch_bounds__(kMssThreads)
     return;
   }
   float m = -INFINITY;
-  for (int64_t y = lo + threadIdx.x; y < hi; y += kMssThreads) m = fmaxf(m, __ldg(row + y));
-  m = block_max(m, red);
+  for (int64_t y = lo + threadIdx.x; y < hi; y += kSelThreads) m = fmaxf(m, __ldg(row + y));
+  m = block_max<kSelWarps>(m, red);
   int xk = 0;
   if (ncl > 1) {  // the row maximum over the cluster
     if (threadIdx.x == 0) pub[0][0] = m;
@@ -1471,9 +1726,9 @@ __global__ void __launch_bounds__(kMssThreads)
     for (int r = 0; r < ncl; ++r) m = fmaxf(m, ld_dsmem_f32(mapa_shared(smem_u32(&pub[0][0]), (uint32_t)r)));
     ++xk;
   }
-  warped_support(Slice{row, 0}, V, lo, hi, 1.0f, m, k, 1.0f, ncl, rank, xk, pub, sel);
+  warped_support<kSelThreads>(Slice{row, 0}, V, lo, hi, 1.0f, m, k, 1.0f, ncl, rank, xk, pub, sel);
   if (rank == 0)
-    for (int j = threadIdx.x; j < k; j += kMssThreads) out[j] = sel.srt_i[j];
+    for (int j = threadIdx.x; j < k; j += kSelThreads) out[j] = sel.srt_i[j];
   if (ncl > 1) cluster_sync_all();  // peers' candidate lists were read in the selection
 }
 
@@ -1592,7 +1847,7 @@ cudaError_t launch_tree_expand(const float* logits, int64_t V, int32_t F, int32_
                                int num_sms, cudaStream_t st) {
   if (F == 0) return cudaSuccess;
   const int ncl = expand_cluster_size(V, F, num_sms);
-  return launch_pdl(tree_expand_kernel, dim3((unsigned)(F * ncl)), dim3(kMssThreads), 0, st,
+  return launch_pdl(tree_expand_kernel, dim3((unsigned)(F * ncl)), dim3(kSelThreads), 0, st,
                     ncl > 1 ? (unsigned)ncl : 0u, logits, V, k, ncl, tokens);
 }
 
@@ -1604,27 +1859,60 @@ cudaError_t launch_tree_merge(const int32_t* parent, const int32_t* tokens, cons
                     out_parent, out_tokens, out_source, out_count, status);
 }
 
-int mss_cluster_size(int64_t V) {
-  const int64_t c = (V + kMssMinSlice - 1) / kMssMinSlice;
-  return (int)(c < 1 ? 1 : (c > kMssMaxCluster ? kMssMaxCluster : c));
+// CTAs per request: slices of at least kMssMinSlice entries, at most 8 (one
+// portable cluster), and no more than lets every request's cluster be
+// resident at once (max_clusters[c]: clusters of c CTAs the device holds at
+// once; the kernel runs one CTA per SM).
+int mss_cluster_size(int64_t V, int32_t B, const int* max_clusters) {
+  int64_t c = (V + kMssMinSlice - 1) / kMssMinSlice;
+  c = c < 1 ? 1 : (c > kMssMaxCluster ? kMssMaxCluster : c);
+  if (max_clusters != nullptr)
+    while (c > 1 && max_clusters[c] < B) --c;
+  return (int)c;
 }
 
-cudaError_t mss_set_attributes(int device, size_t* staged_limit) {
-  cudaFuncAttributes fa;
-  cudaError_t e = cudaFuncGetAttributes(&fa, mss_verify_kernel);
-  if (e != cudaSuccess) return e;
+cudaError_t mss_set_attributes(int device, size_t* staged_limit, int* max_clusters) {
   int optin = 0;
-  e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
+  cudaError_t e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
   if (e != cudaSuccess) return e;
-  const size_t limit = (size_t)optin > fa.sharedSizeBytes ? (size_t)optin - fa.sharedSizeBytes : 0;
-  e = cudaFuncSetAttribute(mss_verify_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)limit);
-  if (e != cudaSuccess) return e;
+  size_t limit = (size_t)optin;
+  void (*kernels[2])(const float*, const float*, int64_t, const int32_t*, const int32_t*, const int32_t*,
+                     const float*, const float*, float, int, float, int, int, float*, int32_t*, int32_t*,
+                     int32_t*, int32_t*, int32_t*) = {mss_verify_kernel<true>, mss_verify_kernel<false>};
+  for (auto* k : kernels) {
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, k);
+    if (e != cudaSuccess) return e;
+    const size_t l = (size_t)optin > fa.sharedSizeBytes ? (size_t)optin - fa.sharedSizeBytes : 0;
+    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)l);
+    if (e != cudaSuccess) return e;
+    if (k == kernels[0]) limit = l;
+  }
   *staged_limit = limit;
+  // Resident clusters per size, for the staged kernel at its largest slice
+  // set (one CTA per SM either way: its threads and registers fill an SM).
+  max_clusters[0] = 0;
+  for (int c = 1; c <= kMssMaxCluster; ++c) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)c);
+    cfg.blockDim = dim3(kMssThreads);
+    cfg.dynamicSmemBytes = limit;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = (unsigned)c;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int nc = 0;
+    e = cudaOccupancyMaxActiveClusters(&nc, mss_verify_kernel<true>, &cfg);
+    if (e != cudaSuccess) return e;
+    max_clusters[c] = nc;
+  }
   return cudaSuccess;
 }
 
-size_t mss_staged_bytes(int64_t V) {
-  const int ncl = mss_cluster_size(V);
+size_t mss_staged_bytes(int64_t V, int ncl) {
   const int64_t per = (((V + ncl - 1) / ncl) + 3) & ~int64_t(3);
   const int64_t per_al = (per + 31) & ~int64_t(31);
   return (size_t)(3 * per_al * 4);
@@ -1635,18 +1923,22 @@ cudaError_t launch_mss_verify(const float* llm_logits, const float* ssm_probs, i
                               const int32_t* node_offsets, const float* u_acc, const float* u_smp,
                               float inv_t, int32_t top_k, float top_p, int32_t B, float* resid,
                               int32_t* path, int32_t* accept_len, int32_t* bonus, int32_t* n_tried,
-                              int32_t* status, size_t staged_limit, cudaStream_t st) {
-  const int ncl = mss_cluster_size(V);
+                              int32_t* status, size_t staged_limit, const int* max_clusters,
+                              cudaStream_t st) {
+  const int ncl = mss_cluster_size(V, B, max_clusters);
   const int vec = (V % 4 == 0) && ((reinterpret_cast<uintptr_t>(llm_logits) |
                                     reinterpret_cast<uintptr_t>(ssm_probs) |
                                     reinterpret_cast<uintptr_t>(resid)) & 15) == 0;
   // Slices staged in shared memory when three of them fit (bulk copies want
   // the 16-byte alignment `vec` stands for).
-  const size_t dyn = mss_staged_bytes(V);
-  const int staged = vec && dyn <= staged_limit;
-  return launch_pdl(mss_verify_kernel, dim3((unsigned)(B * ncl)), dim3(kMssThreads), staged ? dyn : 0, st,
+  const size_t dyn = mss_staged_bytes(V, ncl);
+  if (vec && dyn <= staged_limit)
+    return launch_pdl(mss_verify_kernel<true>, dim3((unsigned)(B * ncl)), dim3(kMssThreads), dyn, st,
+                      (unsigned)ncl, llm_logits, ssm_probs, V, tokens, parent, node_offsets, u_acc, u_smp,
+                      inv_t, top_k, top_p, ncl, vec, resid, path, accept_len, bonus, n_tried, status);
+  return launch_pdl(mss_verify_kernel<false>, dim3((unsigned)(B * ncl)), dim3(kMssThreads), 0, st,
                     (unsigned)ncl, llm_logits, ssm_probs, V, tokens, parent, node_offsets, u_acc, u_smp, inv_t,
-                    top_k, top_p, ncl, vec, staged, resid, path, accept_len, bonus, n_tried, status);
+                    top_k, top_p, ncl, vec, resid, path, accept_len, bonus, n_tried, status);
 }
 
 }  // namespace tsv
