@@ -63,10 +63,11 @@ def test_no_alloc_matches_workspace_entry_on_consecutive_calls(tsv):
 
 
 def test_no_alloc_clears_counters_a_previous_call_left_nonzero(tsv):
-    """A call with few requests leaves argmax partials (nonzero floats) right
-    after its 256 bytes of counters; a later call with more requests has its
-    counters there.  Each call must clear its own counters first, or the
-    requests whose counters start nonzero never run their walk."""
+    """Calls of different shapes in a row share the scratch: a call with one
+    request has its row argmax words right after its 256 bytes of counters,
+    where a later call with 128 requests has counters.  Every call leaves its
+    words and counters at zero and the entry point clears them before each
+    launch; a nonzero counter would keep that request's walk from running."""
     h = tsv.handle()
     small = W.SPECS["llama7b-layer-P1024-n20"]  # B = 1: counters in bytes 0..255, partials from 256
     trees, x = _inputs(small)
@@ -86,7 +87,7 @@ def test_no_alloc_clears_counters_a_previous_call_left_nonzero(tsv):
 def test_no_alloc_rejects_what_the_scratch_cannot_hold(tsv):
     h = tsv.handle()
     o = _outputs(1, 1)
-    # A valid batch size whose node count needs more slice partials than the
+    # A valid batch size whose node count needs more row argmax words than the
     # fixed scratch holds: rejected on the host, before anything is launched.
     need = tsv.tsv_tree_verify_greedy_workspace_size(h, 1, 200000, 32000)
     assert need > 1 << 20

@@ -459,8 +459,7 @@ tsv_status tsv_tree_verify_greedy_workspace_size(tsv_handle h, int32_t B, int32_
                                                  size_t* bytes) {
   if (!h || !bytes || B < 1 || B > TSV_MAX_BATCH || N < 0 || V < 1 || V > INT32_MAX)
     return TSV_ERR_INVALID_ARG;
-  const int splits = greedy_splits(V, N, h->num_sms);
-  *bytes = round256((size_t)B * 4) + 2 * round256((size_t)N * splits * 4);
+  *bytes = greedy_workspace_bytes(B, N);
   return TSV_OK;
 }
 
@@ -476,18 +475,16 @@ tsv_status tsv_tree_verify_greedy(tsv_handle h, const float* logits_d, int64_t V
   if (B < 1 || B > TSV_MAX_BATCH || N < 0 || V < 1 || V > INT32_MAX) return TSV_ERR_INVALID_ARG;
   if (N > 0 && (!logits_d || !path_d)) return TSV_ERR_INVALID_ARG;
   const int splits = greedy_splits(V, N, h->num_sms);
-  const size_t ctr = round256((size_t)B * 4), part = round256((size_t)N * splits * 4);
-  if (!workspace_d || workspace_bytes < ctr + 2 * part) return TSV_ERR_INVALID_ARG;
+  if (!workspace_d || workspace_bytes < greedy_workspace_bytes(B, N)) return TSV_ERR_INVALID_ARG;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   char* ws = static_cast<char*>(workspace_d);
   int32_t* counters = reinterpret_cast<int32_t*>(ws);
-  float* pv = reinterpret_cast<float*>(ws + ctr);
-  int32_t* pi = reinterpret_cast<int32_t*>(ws + ctr + part);
+  unsigned long long* rowbest = reinterpret_cast<unsigned long long*>(ws + greedy_counter_bytes(B));
   if (N == 0)
-    return cuda_status(launch_greedy_walk(pv, pi, splits, tree_tokens_d, parent_d, node_offsets_d, B,
-                                          path_d, accept_len_d, bonus_d, status_d, cs));
+    return cuda_status(launch_greedy_walk(rowbest, tree_tokens_d, parent_d, node_offsets_d, B, path_d,
+                                          accept_len_d, bonus_d, status_d, cs));
   return cuda_status(launch_greedy_verify(logits_d, V, N, splits, tree_tokens_d, parent_d,
-                                          node_offsets_d, B, pv, pi, counters, path_d, accept_len_d,
+                                          node_offsets_d, B, rowbest, counters, path_d, accept_len_d,
                                           bonus_d, status_d, cs));
 }
 

@@ -139,23 +139,27 @@ cudaError_t launch_attention_simt(bool bf16, const void* q, const void* k, const
                                   const uint32_t* anc, int32_t B, int32_t N, int32_t Hq,
                                   int32_t Hkv, int32_t D, float scale, cudaStream_t st);
 
-// Greedy verification: argmax over vocab slices, the last CTA of a request walks.
+// Greedy verification: argmax over vocab slices folded into one 64-bit word
+// per row, the last CTA of a request walks.
 int greedy_splits(int64_t V, int32_t N, int num_sms);
 cudaError_t launch_greedy_verify(const float* logits, int64_t V, int32_t N, int splits,
                                  const int32_t* tokens, const int32_t* parent,
-                                 const int32_t* node_offsets, int32_t B, float* part_val,
-                                 int32_t* part_idx, int32_t* counters, int32_t* path,
-                                 int32_t* accept_len, int32_t* bonus, int32_t* status,
-                                 cudaStream_t st);
-cudaError_t launch_greedy_walk(const float* part_val, const int32_t* part_idx, int splits,
-                               const int32_t* tokens, const int32_t* parent,
+                                 const int32_t* node_offsets, int32_t B, unsigned long long* rowbest,
+                                 int32_t* counters, int32_t* path, int32_t* accept_len, int32_t* bonus,
+                                 int32_t* status, cudaStream_t st);
+cudaError_t launch_greedy_walk(unsigned long long* rowbest, const int32_t* tokens, const int32_t* parent,
                                const int32_t* node_offsets, int32_t B, int32_t* path,
                                int32_t* accept_len, int32_t* bonus, int32_t* status,
                                cudaStream_t st);
 
-// Bytes of the per-request completion counters at the start of a greedy
-// verification workspace (the layout tsv_tree_verify_greedy uses).
+// Layout of a greedy verification workspace (the one tsv_tree_verify_greedy
+// uses): B int32 completion counters, then N 64-bit row argmax words; both
+// start at zero and every call leaves them at zero.
 inline size_t greedy_counter_bytes(int32_t B) { return ((size_t)B * 4 + 255) & ~(size_t)255; }
+inline size_t greedy_row_word_bytes(int32_t N) { return ((size_t)N * 8 + 255) & ~(size_t)255; }
+inline size_t greedy_workspace_bytes(int32_t B, int32_t N) {
+  return greedy_counter_bytes(B) + greedy_row_word_bytes(N);
+}
 
 // Stochastic verification: one cluster of mss_cluster_size(V, B, ...) CTAs
 // per request, each owning a slice of the vocabulary.

@@ -4,14 +4,14 @@
 // allocation is not allowed or not possible (inside an engine or plugin whose
 // allocator owns all device memory, a real-time loop that must never enter the
 // CUDA allocator, a host language binding without device-memory management).
-// tsv_tree_verify_greedy_noalloc serves them: its scratch (per-slice argmax
-// partials and per-request completion counters) lives in one file-scope
+// tsv_tree_verify_greedy_noalloc serves them: its scratch (per-request
+// completion counters and per-row argmax words) lives in one file-scope
 // __device__ array of fixed size, which every GPU that loads the library keeps
 // until the process exits.  The caller still passes every input and output.
 //
 // The array is shared by all calls on a device and keeps the last call's
-// contents: the counters, which must start at zero, are cleared on the stream
-// at the start of every call.  Calls whose work overlaps on the GPU (different
+// contents: the counters and row words, which must start at zero (every call
+// leaves them so), are also cleared on the stream at the start of every call.  Calls whose work overlaps on the GPU (different
 // streams, no ordering between them) race on the array and give wrong results.
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -23,7 +23,7 @@
 namespace {
 
 // Fixed scratch: enough for TSV_MAX_BATCH requests of TSV_MAX_NODES rows at any
-// vocabulary size (the slice partials need at most (N + 2 * SM count) entries).
+// vocabulary size (4 bytes per request and 8 per row).
 constexpr size_t kNoallocScratchBytes = size_t(1) << 20;
 constexpr int kMaxDevices = 64;
 
@@ -107,10 +107,12 @@ extern "C" tsv_status tsv_tree_verify_greedy_noalloc(
   void* scratch = nullptr;
   st = scratch_address(device, &scratch);
   if (st != TSV_OK) return st;
-  // The workspace of greedy verification starts with B int32 completion
-  // counters (tsv_tree_verify_greedy's layout); they must be zero.
-  const size_t counter_bytes = tsv::greedy_counter_bytes(B);
-  if (cudaMemsetAsync(scratch, 0, counter_bytes, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+  // The workspace of greedy verification holds B int32 completion counters
+  // and N 64-bit row argmax words (tsv_tree_verify_greedy's layout); they
+  // must be zero.  Every call leaves them at zero; clearing them here also
+  // covers a call that never completed.
+  const size_t zeroed_bytes = tsv::greedy_workspace_bytes(B, N);
+  if (cudaMemsetAsync(scratch, 0, zeroed_bytes, static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return TSV_ERR_CUDA;
   return tsv_tree_verify_greedy(h, logits_d, V, tree_tokens_d, parent_d, node_offsets_d, B, N, path_d,
                                 accept_len_d, bonus_d, scratch, kNoallocScratchBytes, status_d,

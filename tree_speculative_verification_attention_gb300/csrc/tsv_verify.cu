@@ -60,10 +60,30 @@ __device__ __forceinline__ int64_t slice_len(int64_t V, int splits) {
   return (per + 3) & ~int64_t(3);
 }
 
+// Order-preserving 32-bit key of a float (-0 counts as +0): larger logit,
+// larger key.
+__device__ __forceinline__ uint32_t order_key(float l) {
+  const uint32_t u = __float_as_uint(l + 0.0f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// (value, index) as one word whose unsigned order is the argmax order:
+// larger value first, equal values by lower index.
+__device__ __forceinline__ unsigned long long argmax_word(ArgMax a) {
+  return ((unsigned long long)order_key(a.v) << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)a.i);
+}
+
+__device__ __forceinline__ int32_t argmax_word_index(unsigned long long w) {
+  return (int32_t)(0xFFFFFFFFu - (uint32_t)w);
+}
+
 }  // namespace
 
 // Argmax (lowest index on ties) of vocab slice s of logits row `row`, reduced
-// over the CTA; the result is valid in thread 0.  `red` holds one entry per warp.
+// over the CTA; the result is valid in thread 0.  Every thread issues all of
+// its loads (up to kArgmaxInFlight 16-byte loads) before using any, so a
+// slice of up to kArgmaxInFlight * 4 * kArgmaxThreads entries costs one
+// memory round trip.  `red` holds one entry per warp.
 __device__ __forceinline__ ArgMax slice_argmax(const float* __restrict__ logits, int64_t V, int splits,
                                                int row, int s, ArgMax* red) {
   const int64_t per = slice_len(V, splits);
@@ -74,28 +94,21 @@ __device__ __forceinline__ ArgMax slice_argmax(const float* __restrict__ logits,
   if ((V & 3) == 0 && (reinterpret_cast<uintptr_t>(x) & 15) == 0) {
     const float4* x4 = reinterpret_cast<const float4*>(x);
     const int64_t lo4 = lo >> 2, hi4 = hi >> 2;
-    int64_t k = lo4 + threadIdx.x;
-    // Eight independent 16-byte loads in flight per thread (32 KB per CTA).
-    for (; k + (kArgmaxInFlight - 1) * kArgmaxThreads < hi4; k += kArgmaxInFlight * kArgmaxThreads) {
+    for (int64_t k = lo4 + threadIdx.x; k < hi4; k += kArgmaxInFlight * kArgmaxThreads) {
       float4 a[kArgmaxInFlight];
 #pragma unroll
-      for (int u = 0; u < kArgmaxInFlight; ++u) a[u] = __ldcs(x4 + k + u * kArgmaxThreads);
+      for (int u = 0; u < kArgmaxInFlight; ++u)
+        if (k + u * kArgmaxThreads < hi4) a[u] = __ldcs(x4 + k + u * kArgmaxThreads);
 #pragma unroll
       for (int u = 0; u < kArgmaxInFlight; ++u) {
-        const int32_t base = (int32_t)((k + u * kArgmaxThreads) << 2);
-        best = better(best, ArgMax{a[u].x, base});
-        best = better(best, ArgMax{a[u].y, base + 1});
-        best = better(best, ArgMax{a[u].z, base + 2});
-        best = better(best, ArgMax{a[u].w, base + 3});
+        if (k + u * kArgmaxThreads < hi4) {
+          const int32_t base = (int32_t)((k + u * kArgmaxThreads) << 2);
+          best = better(best, ArgMax{a[u].x, base});
+          best = better(best, ArgMax{a[u].y, base + 1});
+          best = better(best, ArgMax{a[u].z, base + 2});
+          best = better(best, ArgMax{a[u].w, base + 3});
+        }
       }
-    }
-    for (; k < hi4; k += kArgmaxThreads) {
-      const float4 a = __ldcs(x4 + k);
-      const int32_t base = (int32_t)(k << 2);
-      best = better(best, ArgMax{a.x, base});
-      best = better(best, ArgMax{a.y, base + 1});
-      best = better(best, ArgMax{a.z, base + 2});
-      best = better(best, ArgMax{a.w, base + 3});
     }
   } else {
     for (int64_t k = lo + threadIdx.x; k < hi; k += kArgmaxThreads)
@@ -124,76 +137,44 @@ __device__ void fail_request(int32_t* path, int n, int32_t* accept_len, int32_t*
 }
 
 // Shared scratch of one greedy walk: the request's parents, tokens and
-// per-node results, and its (row, slice) argmax partials when they fit.
-constexpr int kWalkPartials = 1024;
+// per-node results.
 struct WalkSmem {
   int32_t par[TSV_MAX_NODES];
   int32_t tok[TSV_MAX_NODES];
   int32_t am[TSV_MAX_NODES];
   int32_t nxt[TSV_MAX_NODES];
-  ArgMax part[kWalkPartials];
 };
 
-// The greedy walk of request b from its per-slice argmax partials: every
-// child c whose token equals argmax(parent(c)) proposes itself to its parent
-// with atomicMin (lowest index wins), then the chain is followed from the
-// root.  Run by one whole CTA of kArgmaxThreads threads: one load step
-// (parents, tokens, partials), then three barriers — partials staged; every
-// node's argmax known and the tree checked; proposals made — and warp 0
-// follows the chain and writes the path.
-__device__ void greedy_walk_request(int b, int off, int n, const float* part_val,
-                                    const int32_t* part_idx, int splits, const int32_t* tokens,
-                                    const int32_t* parent, int32_t* path, int32_t* accept_len,
-                                    int32_t* bonus, int32_t* status, WalkSmem& w) {
+// The greedy walk of request b from its rows' argmax words: every child c
+// whose token equals argmax(parent(c)) proposes itself to its parent with
+// atomicMin (lowest index wins), then the chain is followed from the root.
+// Run by one whole CTA of kArgmaxThreads threads; thread i holds node i's
+// parent pv and token tv (read before, while the argmax words were
+// completing).  The words are read and reset to zero (the workspace is left
+// as it was found), then three barriers: every node's argmax known and the
+// tree checked; proposals made; warp 0 follows the chain and writes the path.
+__device__ void greedy_walk_request(int b, int off, int n, unsigned long long* rowbest, int pv, int tv,
+                                    int32_t* path, int32_t* accept_len, int32_t* bonus, int32_t* status,
+                                    WalkSmem& w) {
   const int T = blockDim.x;
   const int i = threadIdx.x;
-  static_assert(kWalkPartials <= 4 * kArgmaxThreads && TSV_MAX_NODES <= kArgmaxThreads, "one pass");
+  static_assert(TSV_MAX_NODES <= kArgmaxThreads, "one node per thread");
+  for (int r = i; r < n; r += T) {
+    const unsigned long long word = __ldcg(rowbest + off + r);
+    rowbest[off + r] = 0ull;
+    if (r < TSV_MAX_NODES) w.am[r] = argmax_word_index(word);
+  }
   const int size_code = (n < 1) ? TSV_ERR_BAD_TREE : (n > TSV_MAX_NODES ? TSV_ERR_UNSUPPORTED : 0);
   if (size_code) {  // uniform: n is the same for every thread
     fail_request(path + off, n, accept_len + b, bonus + b, nullptr, status + b, size_code);
     return;
   }
-  const int items = n * splits;  // rows of a request are consecutive, so its partials are too
-  const bool staged = items <= kWalkPartials;
-  // Every load is issued before the first shared-memory store, so they all
-  // travel together.
-  int pv = 0, tv = 0;
-  if (i < n) {
-    pv = parent[off + i];
-    tv = tokens[off + i];
-  }
-  float pval[4];
-  int32_t pidx[4];
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const int e = i + k * T;
-    if (staged && e < items) {
-      pval[k] = __ldcg(part_val + (size_t)off * splits + e);
-      pidx[k] = __ldcg(part_idx + (size_t)off * splits + e);
-    }
-  }
+  bool bad = false;
   if (i < n) {
     w.par[i] = pv;
     w.tok[i] = tv;
     w.nxt[i] = INT32_MAX;
-  }
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const int e = i + k * T;
-    if (staged && e < items) w.part[e] = ArgMax{pval[k], pidx[k]};
-  }
-  __syncthreads();
-  // Node i: its parent is checked (a single root at 0, every other parent
-  // earlier) and its row's slices merged into its argmax.
-  bool bad = false;
-  if (i < n) {
     bad = !((i == 0) ? (pv == -1) : (pv >= 0 && pv < i));
-    ArgMax best{-INFINITY, INT32_MAX};
-    for (int sl = 0; sl < splits; ++sl) {
-      const size_t k = (size_t)(off + i) * splits + sl;
-      best = better(best, staged ? w.part[i * splits + sl] : ArgMax{__ldcg(part_val + k), __ldcg(part_idx + k)});
-    }
-    w.am[i] = best.i;
   }
   if (__syncthreads_or(bad)) {
     fail_request(path + off, n, accept_len + b, bonus + b, nullptr, status + b, TSV_ERR_BAD_TREE);
@@ -219,10 +200,10 @@ __device__ void greedy_walk_request(int b, int off, int n, const float* part_val
   }
 }
 
-// Walk-only kernel: one CTA per request (used when N == 0, where no argmax CTA exists).
-__global__ void __launch_bounds__(TSV_MAX_NODES)
-    greedy_walk_kernel(const float* __restrict__ part_val, const int32_t* __restrict__ part_idx,
-                       int splits, const int32_t* __restrict__ tokens,
+// Walk-only kernel: one CTA per request (used when N == 0, where no argmax
+// CTA exists; every request then has no node and is reported as a bad tree).
+__global__ void __launch_bounds__(kArgmaxThreads)
+    greedy_walk_kernel(unsigned long long* __restrict__ rowbest, const int32_t* __restrict__ tokens,
                        const int32_t* __restrict__ parent, const int32_t* __restrict__ node_offsets,
                        int32_t* __restrict__ path, int32_t* __restrict__ accept_len,
                        int32_t* __restrict__ bonus, int32_t* __restrict__ status) {
@@ -230,25 +211,25 @@ __global__ void __launch_bounds__(TSV_MAX_NODES)
   pdl_wait();  // the previous kernel's results are visible from here on
   __shared__ WalkSmem w;
   const int b = blockIdx.x;
-  const int off = node_offsets[b];
-  greedy_walk_request(b, off, node_offsets[b + 1] - off, part_val, part_idx, splits, tokens, parent,
-                      path, accept_len, bonus, status, w);
+  const int off = node_offsets[b], n = node_offsets[b + 1] - off;
+  const int i = threadIdx.x;
+  const int pv = i < n ? parent[off + i] : 0, tv = i < n ? tokens[off + i] : 0;
+  greedy_walk_request(b, off, n, rowbest, pv, tv, path, accept_len, bonus, status, w);
 }
 
 // Fused greedy verification: grid (splits, N).  Each CTA reduces one vocab
-// slice of one row; the last CTA to finish among a request's rows x slices
-// (atomic counter, no waiting) walks that request's tree.  CTA (0, 0) also
-// reports requests that own no rows.  Counters start at zero and are reset.
-// Thread 0 writes the CTA's partial and counts it with one acquire-release
-// atomic, so the last CTA sees every partial without a separate fence.
+// slice of one row and folds its (maximum, lowest index) into the row's
+// argmax word with one 64-bit atomicMax; the last CTA to finish among a
+// request's rows x slices (an acquire-release counter, no waiting) walks that
+// request's tree.  CTA (0, 0) also reports requests that own no rows.  Words
+// and counters start at zero and are left at zero.
 __global__ void __launch_bounds__(kArgmaxThreads, 4)  // <= 64 registers: the loads stay in flight
     greedy_verify_kernel(const float* __restrict__ logits, int64_t V, int splits,
                          const int32_t* __restrict__ tokens, const int32_t* __restrict__ parent,
                          const int32_t* __restrict__ node_offsets, int B,
-                         float* __restrict__ part_val, int32_t* __restrict__ part_idx,
-                         int32_t* __restrict__ counters, int32_t* __restrict__ path,
-                         int32_t* __restrict__ accept_len, int32_t* __restrict__ bonus,
-                         int32_t* __restrict__ status) {
+                         unsigned long long* __restrict__ rowbest, int32_t* __restrict__ counters,
+                         int32_t* __restrict__ path, int32_t* __restrict__ accept_len,
+                         int32_t* __restrict__ bonus, int32_t* __restrict__ status) {
   // A small slice (short rows spread over many CTAs) is pulled into L2 while
   // the previous kernel finishes: a prefetch reads no value, so it may run
   // ahead of that kernel's writes.
@@ -289,15 +270,17 @@ __global__ void __launch_bounds__(kArgmaxThreads, 4)  // <= 64 registers: the lo
         status[e] = TSV_ERR_BAD_TREE;
       }
   }
+  // The request's tree, read by every CTA while its atomics complete: the
+  // one that finishes last walks it without another memory round trip.
+  const int i = threadIdx.x;
+  const int pv = i < n ? __ldg(parent + off + i) : 0, tv = i < n ? __ldg(tokens + off + i) : 0;
   if (threadIdx.x == 0) {
-    part_val[(size_t)row * splits + s] = best.v;
-    part_idx[(size_t)row * splits + s] = best.i;
+    atomicMax(rowbest + row, argmax_word(best));
     last = atom_add_acq_rel_gpu(counters + b, 1) == n * splits - 1;
   }
   __syncthreads();
   if (!last) return;
-  greedy_walk_request(b, off, n, part_val, part_idx, splits, tokens, parent, path, accept_len, bonus,
-                      status, w);
+  greedy_walk_request(b, off, n, rowbest, pv, tv, path, accept_len, bonus, status, w);
   if (threadIdx.x == 0) counters[b] = 0;
 }
 
@@ -310,22 +293,20 @@ int greedy_splits(int64_t V, int32_t N, int num_sms) {
 
 cudaError_t launch_greedy_verify(const float* logits, int64_t V, int32_t N, int splits,
                                  const int32_t* tokens, const int32_t* parent,
-                                 const int32_t* node_offsets, int32_t B, float* part_val,
-                                 int32_t* part_idx, int32_t* counters, int32_t* path,
-                                 int32_t* accept_len, int32_t* bonus, int32_t* status,
-                                 cudaStream_t st) {
+                                 const int32_t* node_offsets, int32_t B, unsigned long long* rowbest,
+                                 int32_t* counters, int32_t* path, int32_t* accept_len, int32_t* bonus,
+                                 int32_t* status, cudaStream_t st) {
   dim3 grid(splits, N);
   return launch_pdl(greedy_verify_kernel, grid, dim3(kArgmaxThreads), 0, st, 0u, logits, V, splits, tokens, parent,
-                    node_offsets, B, part_val, part_idx, counters, path, accept_len, bonus, status);
+                    node_offsets, B, rowbest, counters, path, accept_len, bonus, status);
 }
 
-cudaError_t launch_greedy_walk(const float* part_val, const int32_t* part_idx, int splits,
-                               const int32_t* tokens, const int32_t* parent,
+cudaError_t launch_greedy_walk(unsigned long long* rowbest, const int32_t* tokens, const int32_t* parent,
                                const int32_t* node_offsets, int32_t B, int32_t* path,
                                int32_t* accept_len, int32_t* bonus, int32_t* status,
                                cudaStream_t st) {
-  return launch_pdl(greedy_walk_kernel, dim3(B), dim3(TSV_MAX_NODES), 0, st, 0u, part_val, part_idx, splits, tokens,
-                    parent, node_offsets, path, accept_len, bonus, status);
+  return launch_pdl(greedy_walk_kernel, dim3(B), dim3(kArgmaxThreads), 0, st, 0u, rowbest, tokens, parent,
+                    node_offsets, path, accept_len, bonus, status);
 }
 
 // ------------------------------------------------------------------ stochastic
@@ -470,13 +451,6 @@ __device__ __forceinline__ bool accept_test(float u, float q, float p) {
   const float p0 = __fmul_rn(u, q);
   const float e = fmaf(u, q, -p0);
   return p0 < p || (p0 == p && e < 0.f);
-}
-
-// Order-preserving 32-bit key of a float (-0 counts as +0): larger logit,
-// larger key.
-__device__ __forceinline__ uint32_t order_key(float l) {
-  const uint32_t u = __float_as_uint(l + 0.0f);
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
 __device__ __forceinline__ float key_value(uint32_t k) {
