@@ -541,13 +541,15 @@ class DeviceWorkload:
 
     Within a step, verification reads only the given logits and proposals, so
     it does not wait for the attention launch: with ``overlap`` the
-    verification launches go on a second stream forked from and joined back to
-    the main one, and the two run concurrently."""
+    verification launches follow attention on the same stream, greedy
+    verification in the library's overlap mode (tsv_set_verify_overlap): its
+    compact CTAs are launched once every attention CTA is resident, run in the
+    SM room attention leaves, and complete after it.  Stochastic verification
+    then runs after attention, at full size."""
 
     def __init__(self, spec, tsv, dev, stream, overlap=True):
         import torch
         self.spec, self.tsv, self.dev, self.stream, self.overlap = spec, tsv, dev, stream, overlap
-        self.side = torch.cuda.Stream(dev)
         trees, att, gi, si = workload_inputs(spec)
         self.trees, self.att, self.gi, self.si = trees, att, gi, si
         self.B, self.N = spec.B, int(trees.node_offsets[-1])
@@ -640,19 +642,13 @@ class DeviceWorkload:
             self.stochastic(c, st)
 
     def step(self, c, st, overlap=None):
-        import torch
         overlap = self.overlap if overlap is None else overlap
+        self.attention(c, st)
         if not overlap:
-            self.attention(c, st)
             self.verify(c, st)
             return
-        # Attention is launched first, so its CTAs are placed first and the
-        # verification CTAs fill the SMs it leaves idle.
-        self.side.wait_stream(self.stream)
-        self.attention(c, st)
-        with torch.cuda.stream(self.side):
+        with self.tsv.verify_overlap(self.tsv.TSV_OVERLAP_GREEDY, device=self.dev.index):
             self.verify(c, st)
-        self.stream.wait_stream(self.side)
 
     # ------------------------------------------------------------------ graphs
     def _graph(self, fn):
@@ -921,7 +917,8 @@ def run_ours(args, spec):
     how = ("mean over the K timed steps; CUDA graph replay (one graph per %d steps, each step on the next of "
            "%d rotating input copies); verification launches %s" %
            (L, R, "after the attention launch on one stream" if args.serial else
-            "on a second stream, concurrent with the attention launch"))
+            "after the attention launch on the same stream; greedy in the overlap mode (compact CTAs run "
+            "beside the attention CTAs and complete after them)"))
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": spec.dtype, "data": "synthetic",
@@ -1011,14 +1008,19 @@ def measure_e2e(args, spec, trees, att, gi, si, h, tsv, dev, stream, ws_attn, ws
             stream.wait_stream(s2)
         tsv.tree_attention(d["q"], d["k"], d["v"], trees.prefix_len, trees.node_offsets, d["plen"], d["offs"],
                            parent=d["parent"], anc=None, out=out, workspace=wsa, status=status)
+        # The verification calls follow attention directly (in overlap mode
+        # they run beside it); the results are read back after all launches.
+        with tsv.verify_overlap(0 if args.serial else tsv.TSV_OVERLAP_GREEDY, device=dev.index):
+            if gi is not None:
+                tsv.tree_verify_greedy(d["logits"], d["gtok"], d["parent"], d["offs"], workspace=wsg, out=res)
+            if si is not None:
+                tsv.tree_verify_stochastic(d["llm"], d["ssm"], d["stok"], d["parent"], d["offs"], d["ua"],
+                                           d["us"], workspace=wss, out=res2, **WARP)
         out_h.copy_(out, non_blocking=True)
         if gi is not None:
-            tsv.tree_verify_greedy(d["logits"], d["gtok"], d["parent"], d["offs"], workspace=wsg, out=res)
             for k in ("path", "accept_len", "bonus"):
                 res_h[k].copy_(res[k], non_blocking=True)
         if si is not None:
-            tsv.tree_verify_stochastic(d["llm"], d["ssm"], d["stok"], d["parent"], d["offs"], d["ua"], d["us"],
-                                       workspace=wss, out=res2, **WARP)
             for k in ("path", "accept_len", "bonus"):
                 res_h[k].copy_(res2[k], non_blocking=True)
 

@@ -102,6 +102,30 @@ tsv_status tsv_create(tsv_handle* out, int device);
 tsv_status tsv_destroy(tsv_handle h);
 
 /*
+ * tsv_set_verify_overlap — how this handle's verification calls are ordered
+ * against the kernel launched before them on the same stream.  `kinds` is a
+ * set of flags; a call of a kind not in it (the default: none) waits for that
+ * kernel's results before it reads.  A call of a kind in it starts while that
+ * kernel still runs, in small CTAs that fit on an SM beside a running
+ * keys-on-lanes tree-attention CTA (the attention kernels' trigger lets it
+ * launch once every attention CTA is resident), and completes only after that
+ * kernel completes, so every later launch on the stream still sees both
+ * finished.  The caller guarantees the call's inputs were complete before that
+ * kernel began: the verification of one batch then runs in the shadow of the
+ * attention launch of another.  Results are identical either way.
+ *   TSV_OVERLAP_GREEDY       tsv_tree_verify_greedy (and _noalloc)
+ *   TSV_OVERLAP_STOCHASTIC   tsv_tree_verify_stochastic (unwarped; in two-warp
+ *                            CTAs reading their slices from global memory, so
+ *                            a walk is several times slower than alone: worth
+ *                            it only when the kernel before it runs longer)
+ *   Takes effect for calls made (or captured into a CUDA graph) after it;
+ *   TSV_ERR_INVALID_ARG for other bits.
+ */
+#define TSV_OVERLAP_GREEDY 1u
+#define TSV_OVERLAP_STOCHASTIC 2u
+tsv_status tsv_set_verify_overlap(tsv_handle h, uint32_t kinds);
+
+/*
  * tsv_tree_prepare — ancestor bitsets of every tree node (the topology-aware
  * causal mask of SpecInfer §4, Tree-Based Parallel Decoding, stored as one bit
  * per (node, tree key)).

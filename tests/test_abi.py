@@ -97,6 +97,7 @@ def test_every_entry_point_rejects_a_null_handle_on_the_host():
         "tsv_kv_commit": (None, 1, None, None, 0, 0, 0, 1, 1, 64, None, None, None, None, None, None, None),
         "tsv_tree_prepare": (None, None, None, 1, None, None, None, None),
         "tsv_selftest_bounded_wait": (None, 1, None, None, None),
+        "tsv_set_verify_overlap": (None, 1),
     }
     for name, args in calls.items():
         assert getattr(L, name)(*args) == tsv.TSV_ERR_INVALID_ARG, name

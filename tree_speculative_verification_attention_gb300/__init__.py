@@ -16,6 +16,7 @@ Two layers:
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 
@@ -37,7 +38,7 @@ EXPORTED = (
     "tsv_tree_verify_greedy_workspace_size", "tsv_tree_verify_greedy",
     "tsv_tree_verify_stochastic_workspace_size", "tsv_tree_verify_stochastic",
     "tsv_tree_verify_greedy_noalloc", "tsv_kv_commit", "tsv_tree_verify_stochastic_warped",
-    "tsv_tree_expand", "tsv_tree_merge", "tsv_selftest_bounded_wait",
+    "tsv_tree_expand", "tsv_tree_merge", "tsv_selftest_bounded_wait", "tsv_set_verify_overlap",
 )
 
 
@@ -79,6 +80,7 @@ def _load():
         "tsv_tree_expand": (ctypes.c_int, [vp, vp, i64, i32, i32, vp, vp]),
         "tsv_tree_merge": (ctypes.c_int, [vp, vp, vp, vp, vp, i32, vp, vp, vp, vp, vp, vp]),
         "tsv_selftest_bounded_wait": (ctypes.c_int, [vp, i32, vp, vp, vp]),
+        "tsv_set_verify_overlap": (ctypes.c_int, [vp, u32]),
         "tsv_kv_commit": (
             ctypes.c_int, [vp, ctypes.c_int, vp, vp, i64, i64, i64, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp]),
         "tsv_tree_verify_stochastic_workspace_size": (ctypes.c_int, [vp, i32, i32, i64, szp]),
@@ -228,6 +230,13 @@ def tsv_tree_merge(h, parent, tokens, tree_offsets, request_trees, B, out_parent
                                _ptr(status), _stream(stream)), "tsv_tree_merge")
 
 
+TSV_OVERLAP_GREEDY, TSV_OVERLAP_STOCHASTIC = 1, 2
+
+
+def tsv_set_verify_overlap(h, kinds):
+    _check(_lib.tsv_set_verify_overlap(h, int(kinds)), "tsv_set_verify_overlap")
+
+
 def tsv_selftest_bounded_wait(h, arrive, status, elapsed_ns=None, stream=None):
     _check(_lib.tsv_selftest_bounded_wait(h, int(arrive), _ptr(status), _ptr(elapsed_ns), _stream(stream)),
            "tsv_selftest_bounded_wait")
@@ -269,6 +278,19 @@ def handle(device=None):
     if dev not in _HANDLES:
         _HANDLES[dev] = tsv_create(dev)
     return _HANDLES[dev]
+
+
+@contextlib.contextmanager
+def verify_overlap(kinds=TSV_OVERLAP_GREEDY | TSV_OVERLAP_STOCHASTIC, device=None):
+    """Verification calls of the given kinds made inside the block run beside
+    the kernel launched before them on their stream (tsv_set_verify_overlap):
+    their inputs must be complete before that kernel began."""
+    h = handle(device)
+    tsv_set_verify_overlap(h, int(kinds))
+    try:
+        yield
+    finally:
+        tsv_set_verify_overlap(h, 0)
 
 
 def _workspace(nbytes, device):

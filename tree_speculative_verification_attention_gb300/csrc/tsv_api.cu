@@ -28,6 +28,7 @@ struct tsv_handle_s {
   bool mss_attr_set;      // MSS kernel's shared-memory limit
   size_t mss_staged_limit;
   int mss_max_clusters[kMssClusterSizes];  // resident MSS clusters of each size
+  uint32_t verify_overlap;  // tsv_set_verify_overlap: TSV_OVERLAP_* flags
 };
 
 namespace {
@@ -320,7 +321,14 @@ tsv_status tsv_create(tsv_handle* out, int device) {
   h->keys_attr_set[0] = h->keys_attr_set[1] = false;
   h->mss_attr_set = false;
   h->mss_staged_limit = 0;
+  h->verify_overlap = 0u;
   *out = h;
+  return TSV_OK;
+}
+
+tsv_status tsv_set_verify_overlap(tsv_handle h, uint32_t kinds) {
+  if (!h || (kinds & ~(TSV_OVERLAP_GREEDY | TSV_OVERLAP_STOCHASTIC)) != 0u) return TSV_ERR_INVALID_ARG;
+  h->verify_overlap = kinds;
   return TSV_OK;
 }
 
@@ -485,7 +493,8 @@ tsv_status tsv_tree_verify_greedy(tsv_handle h, const float* logits_d, int64_t V
                                           accept_len_d, bonus_d, status_d, cs));
   return cuda_status(launch_greedy_verify(logits_d, V, N, splits, tree_tokens_d, parent_d,
                                           node_offsets_d, B, rowbest, counters, path_d, accept_len_d,
-                                          bonus_d, status_d, cs));
+                                          bonus_d, status_d, (h->verify_overlap & TSV_OVERLAP_GREEDY) ? 1 : 0,
+                                          cs));
 }
 
 tsv_status tsv_tree_verify_stochastic_workspace_size(tsv_handle h, int32_t B, int32_t N, int64_t V,
@@ -526,6 +535,7 @@ static tsv_status verify_stochastic(tsv_handle h, const float* llm_logits_d, con
                                        node_offsets_d, u_accept_d, u_sample_d, 1.0f / temperature,
                                        top_k, top_p, B, resid, path_d, accept_len_d, bonus_d,
                                        n_tried_d, status_d, h->mss_staged_limit, h->mss_max_clusters,
+                                       (h->verify_overlap & TSV_OVERLAP_STOCHASTIC) ? 1 : 0,
                                        static_cast<cudaStream_t>(stream)));
 }
 

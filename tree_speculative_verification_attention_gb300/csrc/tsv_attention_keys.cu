@@ -288,6 +288,11 @@ __global__ void __launch_bounds__(kKeysThreads, 1)
       }
   }
   pdl_wait();  // the previous kernel's results are visible from here on
+  // The next kernel may be scheduled now: it waits for this one's completion
+  // itself, and it is launched only once every CTA of this grid has started,
+  // so it only takes SM room this grid leaves free (verification launched to
+  // run beside this attention fills that room).
+  pdl_trigger();
 
   if (warp == kKeysProducerWarp) {
     // ------------------------------------------------------------ producer
@@ -656,8 +661,6 @@ __global__ void __launch_bounds__(kKeysThreads, 1)
         mbar_arrive(&p_full[jg & 1]);
         lst = lst + 1 == S ? 0 : lst + 1;
       }
-      const bool last_unit = k + 1 >= n_my;
-      if (last_unit) pdl_trigger();  // the main loop is done: let the next kernel be scheduled
       // Row sums over the 128 key lanes: a transposed warp reduction (as for the
       // maxima) leaves lane l of each warp with row c0 + ((l >> 2) & 7) summed
       // over the warp's 32 keys; then the four lane-group warps' sums are added.

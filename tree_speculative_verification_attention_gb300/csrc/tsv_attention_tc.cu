@@ -167,6 +167,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
   __syncthreads();
   pdl_wait();  // the previous kernel's results are visible from here on
+  // The next kernel may be scheduled now: it waits for this one's completion
+  // itself, and it is launched only once every CTA of this grid has started,
+  // so it only takes SM room this grid leaves free (verification launched to
+  // run beside this attention fills that room).
+  pdl_trigger();
 
   if (warp == kTcProducerWarp) {
     // ------------------------------------------------------------ producer
@@ -444,7 +449,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tc_fence_before();
       mbar_arrive(&p_full[t]);
     }
-    pdl_trigger();  // the main loop is done: let the next kernel be scheduled
     // The tile's last PV must be complete before the epilogue reads O_t.
     if (active && ok && nblk > 0)
       ok = __all_sync(0xffffffffu, mbar_wait(&pv_done[t], (nblk - 1) & 1, abort_v));

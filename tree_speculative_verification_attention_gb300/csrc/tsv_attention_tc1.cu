@@ -163,6 +163,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
   __syncthreads();
   pdl_wait();  // the previous kernel's results are visible from here on
+  // The next kernel may be scheduled now: it waits for this one's completion
+  // itself, and it is launched only once every CTA of this grid has started,
+  // so it only takes SM room this grid leaves free (verification launched to
+  // run beside this attention fills that room).
+  pdl_trigger();
 
   if (warp == kTcProducerWarp) {
     // ------------------------------------------------------------ producer
@@ -412,7 +417,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tc_fence_before();
       mbar_arrive(&p_mine[j & 1]);
     }
-    pdl_trigger();  // the main loop is done: let the next kernel be scheduled
     // Both halves' last PV must be complete before the epilogue reads O0 and O1.
     if (ok && nblk > 0) {
       const int jl = nblk - 1;

@@ -146,7 +146,7 @@ cudaError_t launch_greedy_verify(const float* logits, int64_t V, int32_t N, int 
                                  const int32_t* tokens, const int32_t* parent,
                                  const int32_t* node_offsets, int32_t B, unsigned long long* rowbest,
                                  int32_t* counters, int32_t* path, int32_t* accept_len, int32_t* bonus,
-                                 int32_t* status, cudaStream_t st);
+                                 int32_t* status, int beside, cudaStream_t st);
 cudaError_t launch_greedy_walk(unsigned long long* rowbest, const int32_t* tokens, const int32_t* parent,
                                const int32_t* node_offsets, int32_t B, int32_t* path,
                                int32_t* accept_len, int32_t* bonus, int32_t* status,
@@ -171,7 +171,7 @@ cudaError_t launch_mss_verify(const float* llm_logits, const float* ssm_probs, i
                               float inv_t, int32_t top_k, float top_p, int32_t B, float* resid,
                               int32_t* path, int32_t* accept_len, int32_t* bonus, int32_t* n_tried,
                               int32_t* status, size_t staged_limit, const int* max_clusters,
-                              cudaStream_t st);
+                              int beside, cudaStream_t st);
 // Sets the MSS kernels' dynamic shared-memory limit on `device` to all that is
 // left beside their static shared memory, returns the staged kernel's limit
 // (the largest staged slice set a launch may use) and fills

@@ -22,6 +22,8 @@
 #include <float.h>
 #include <math.h>
 
+#include <type_traits>
+
 #include "tsv_device.cuh"
 #include "tsv_internal.h"
 
@@ -30,7 +32,7 @@ namespace tsv {
 namespace {
 
 constexpr int kArgmaxThreads = 256;
-constexpr int kArgmaxInFlight = 8;
+constexpr int kArgmaxInFlight = 4;
 constexpr uint32_t kArgmaxPrefetchMax = 32768;  // largest slice pulled into L2 ahead of the wait
 constexpr int kMinSlice = 2048;  // vocab entries per CTA at least
 
@@ -222,14 +224,20 @@ __global__ void __launch_bounds__(kArgmaxThreads)
 // argmax word with one 64-bit atomicMax; the last CTA to finish among a
 // request's rows x slices (an acquire-release counter, no waiting) walks that
 // request's tree.  CTA (0, 0) also reports requests that own no rows.  Words
-// and counters start at zero and are left at zero.
-__global__ void __launch_bounds__(kArgmaxThreads, 4)  // <= 64 registers: the loads stay in flight
+// and counters start at zero and are left at zero.  `beside`: the inputs were
+// complete before the preceding kernel on the stream began, so the CTAs start
+// while it runs; each walker waits for it before leaving, so this grid still
+// completes after it.
+// At most 32 registers a thread (8192 a CTA) and under 5 KB of shared memory:
+// a CTA fits on an SM beside a running keys-on-lanes attention CTA, so
+// verification launched on another stream reads its logits during attention.
+__global__ void __launch_bounds__(kArgmaxThreads, 8)
     greedy_verify_kernel(const float* __restrict__ logits, int64_t V, int splits,
                          const int32_t* __restrict__ tokens, const int32_t* __restrict__ parent,
                          const int32_t* __restrict__ node_offsets, int B,
                          unsigned long long* __restrict__ rowbest, int32_t* __restrict__ counters,
                          int32_t* __restrict__ path, int32_t* __restrict__ accept_len,
-                         int32_t* __restrict__ bonus, int32_t* __restrict__ status) {
+                         int32_t* __restrict__ bonus, int32_t* __restrict__ status, int beside) {
   // A small slice (short rows spread over many CTAs) is pulled into L2 while
   // the previous kernel finishes: a prefetch reads no value, so it may run
   // ahead of that kernel's writes.
@@ -241,7 +249,8 @@ __global__ void __launch_bounds__(kArgmaxThreads, 4)  // <= 64 registers: the lo
     if (bytes > 0 && bytes <= kArgmaxPrefetchMax && (reinterpret_cast<uintptr_t>(src) & 15) == 0)
       bulk_prefetch_l2(src, bytes);
   }
-  pdl_wait();  // the previous kernel's results are visible from here on
+  if (beside) pdl_trigger();  // the next kernel may start beside this one too
+  else pdl_wait();            // the previous kernel's results are visible from here on
   __shared__ int32_t offs[TSV_MAX_BATCH + 1];
   __shared__ WalkSmem w;
   __shared__ ArgMax red[kArgmaxThreads / 32];
@@ -251,7 +260,7 @@ __global__ void __launch_bounds__(kArgmaxThreads, 4)  // <= 64 registers: the lo
   static_assert(TSV_MAX_BATCH < kArgmaxThreads, "one offset per thread");
   const int my_off = threadIdx.x <= B ? node_offsets[threadIdx.x] : 0;
   const ArgMax best = slice_argmax(logits, V, splits, row, s, red);
-  pdl_trigger();  // this CTA's share of the logits is read: let the next kernel be scheduled
+  if (!beside) pdl_trigger();  // this CTA's share of the logits is read: let the next kernel be scheduled
   if (threadIdx.x <= B) offs[threadIdx.x] = my_off;
   __syncthreads();
   int lo = 0, hi = B;
@@ -282,10 +291,17 @@ __global__ void __launch_bounds__(kArgmaxThreads, 4)  // <= 64 registers: the lo
   if (!last) return;
   greedy_walk_request(b, off, n, rowbest, pv, tv, path, accept_len, bonus, status, w);
   if (threadIdx.x == 0) counters[b] = 0;
+  if (beside && threadIdx.x == 0) pdl_wait();
 }
 
+// Slices per row: at least one CTA per SM (a short row is then read in one
+// round trip, and few CTAs share a request's counter) and slices of at most
+// kMaxSlice entries (long rows: more CTAs, more loads in flight), of at
+// least kMinSlice.
+constexpr int64_t kMaxSlice = 16384;
 int greedy_splits(int64_t V, int32_t N, int num_sms) {
-  int64_t s = (2LL * num_sms + N - 1) / (N > 0 ? N : 1);
+  int64_t s = ((int64_t)num_sms + N - 1) / (N > 0 ? N : 1);
+  s = s > (V + kMaxSlice - 1) / kMaxSlice ? s : (V + kMaxSlice - 1) / kMaxSlice;
   const int64_t cap = (V + kMinSlice - 1) / kMinSlice;
   s = s < cap ? s : cap;
   return (int)(s < 1 ? 1 : s);
@@ -295,10 +311,10 @@ cudaError_t launch_greedy_verify(const float* logits, int64_t V, int32_t N, int 
                                  const int32_t* tokens, const int32_t* parent,
                                  const int32_t* node_offsets, int32_t B, unsigned long long* rowbest,
                                  int32_t* counters, int32_t* path, int32_t* accept_len, int32_t* bonus,
-                                 int32_t* status, cudaStream_t st) {
+                                 int32_t* status, int beside, cudaStream_t st) {
   dim3 grid(splits, N);
   return launch_pdl(greedy_verify_kernel, grid, dim3(kArgmaxThreads), 0, st, 0u, logits, V, splits, tokens, parent,
-                    node_offsets, B, rowbest, counters, path, accept_len, bonus, status);
+                    node_offsets, B, rowbest, counters, path, accept_len, bonus, status, beside);
 }
 
 cudaError_t launch_greedy_walk(unsigned long long* rowbest, const int32_t* tokens, const int32_t* parent,
@@ -314,6 +330,7 @@ cudaError_t launch_greedy_walk(unsigned long long* rowbest, const int32_t* token
 namespace {
 
 constexpr int kMssThreads = 512;  // stochastic verification CTAs: 16 warps, one CTA per SM
+constexpr int kMssCompactWarps = 2;  // compact CTAs (leader and one worker) that run beside attention
 constexpr int kMssWarps = kMssThreads / 32;
 constexpr int kSelThreads = 256;  // tree-expansion CTAs
 constexpr int kSelWarps = kSelThreads / 32;
@@ -761,39 +778,47 @@ constexpr int kMssWorkerWarps = kMssWarps - 1;     // warps 1..15
 constexpr int kMssWorkers = kMssWorkerWarps * 32;  // threads of the row statistics and residual passes
 constexpr int kMssSlots = kMssMaxCluster * kMssWorkerWarps;
 
-template <bool kStaged>
-__global__ void __launch_bounds__(kMssThreads, 1)
+template <bool kStaged, int kWarps>
+__global__ void __launch_bounds__(kWarps * 32, kWarps == kMssWarps ? 1 : 65536 / (kWarps * 32 * 128))
     mss_verify_kernel(const float* __restrict__ llm_logits, const float* __restrict__ ssm_probs,
                       int64_t V, const int32_t* __restrict__ tokens,
                       const int32_t* __restrict__ parent, const int32_t* __restrict__ node_offsets,
                       const float* __restrict__ u_acc, const float* __restrict__ u_smp, float inv_t,
-                      int top_k, float top_p, int ncl, int vec_in,
+                      int top_k, float top_p, int ncl, int vec_in, int beside,
                       float* __restrict__ resid_all, int32_t* __restrict__ path,
                       int32_t* __restrict__ accept_len, int32_t* __restrict__ bonus,
                       int32_t* __restrict__ n_tried, int32_t* __restrict__ status) {
   // The request's offsets are pulled into L2 while the previous kernel
   // finishes (a prefetch reads no value, so it may run ahead of its writes).
   if (threadIdx.x == 0) prefetch_l2(node_offsets + blockIdx.x / ncl);
-  pdl_wait();  // the previous kernel's results are visible from here on
+  // `beside`: the inputs were complete before the preceding kernel on the
+  // stream began, so the walk runs alongside that kernel; every CTA's thread
+  // 0 waits for it before leaving instead, so this grid still completes
+  // after it (the stream order every later kernel relies on).
+  if (!beside) pdl_wait();  // the previous kernel's results are visible from here on
   // The next kernel may be scheduled now: it waits for this one's completion
   // itself, and it is launched only once every CTA of this grid has started,
   // so its CTAs never hold SMs this grid still needs.
   pdl_trigger();
   __shared__ int32_t tok_s[TSV_MAX_NODES], par_s[TSV_MAX_NODES];
   __shared__ float ua_s[TSV_MAX_NODES], us_s[TSV_MAX_NODES], qx_s[TSV_MAX_NODES], lx_s[TSV_MAX_NODES];
-  __shared__ float red[kMssWarps];
-  __shared__ F2 scan_s[kMssWarps], wpre_s[kMssWarps], target_s;
+  constexpr int T = kWarps * 32;
+  constexpr int kWorkerWarps = kWarps - 1;     // warps 1..kWarps-1
+  constexpr int TW = kWorkerWarps * 32;        // threads of the row statistics and residual passes
+  constexpr int kSlots = kMssMaxCluster * kWorkerWarps;
+  constexpr bool kWarpedOK = kWarps == kMssWarps;  // the warped support runs on full CTAs only
+  static_assert(kWorkerWarps >= 1 && kSlots >= kMssMaxCluster, "a leader and at least one worker");
+  __shared__ float red[kWarps];
+  __shared__ F2 scan_s[kWarps], wpre_s[kWarps], target_s;
   __shared__ float mx_s;
   __shared__ __align__(16) float pub[2][4];  // exchange slots of the warped support, alternating
   __shared__ int bad, bad_tok, tmo_s, pick_s, last_s;
   __shared__ __align__(8) uint64_t cbar[3];  // staged copies: one barrier per slice buffer
   __shared__ __align__(8) uint64_t xbar[2];  // exchanges, alternating
-  __shared__ __align__(16) float4 xslot[2][kMssSlots];
+  __shared__ __align__(16) float4 xslot[2][kSlots];
   __shared__ MssStep dsc[2];                 // step descriptors, alternating
-  __shared__ SelSmem sel;
+  __shared__ typename std::conditional<kWarpedOK, SelSmem, int>::type sel;
   extern __shared__ __align__(128) float mss_dyn[];
-  constexpr int T = kMssThreads;
-  constexpr int TW = kMssWorkers;
   constexpr int G = kStaged ? 3 : kMssGroups;  // 4-float groups in flight per worker (shared memory: 3)
   const bool vec = kStaged || vec_in != 0;     // staged slices are always 16-byte aligned
   const bool warped = top_k > 0 || top_p < 1.0f;
@@ -896,9 +921,7 @@ __global__ void __launch_bounds__(kMssThreads, 1)
   // checks them: a single root at node 0, every other parent earlier in the
   // order (else TSV_ERR_BAD_TREE), tokens in [0, V) (else TSV_ERR_INVALID_ARG;
   // tree errors take precedence).
-  static_assert(kMssThreads >= TSV_MAX_NODES, "one node per thread");
-  if (bad == 0 && tid < n) {
-    const int i = tid;
+  for (int i = tid; bad == 0 && i < n; i += T) {
     const int p = parent[off + i];
     const int x = i > 0 ? tokens[off + i] : 0;
     const float ua = i > 0 ? u_acc[off + i] : 0.f;
@@ -920,6 +943,7 @@ __global__ void __launch_bounds__(kMssThreads, 1)
     if (rank == 0)
       fail_request(path + off, n, accept_len + b, bonus + b, n_tried ? n_tried + b : nullptr,
                    status + b, code);
+    if (beside && tid == 0) pdl_wait();
     return;
   }
   // The lowest-index child of p after node `from` (children follow their
@@ -962,7 +986,7 @@ __global__ void __launch_bounds__(kMssThreads, 1)
   // bytes when it releases the step.
   auto push_warp = [&](float4 v, int xs) {
     if (lane < ncl)
-      st_async_v4(mapa_shared(smem_u32(&xslot[xs][rank * kMssWorkerWarps + warp - 1]), (uint32_t)lane), v,
+      st_async_v4(mapa_shared(smem_u32(&xslot[xs][rank * kWorkerWarps + warp - 1]), (uint32_t)lane), v,
                   mapa_shared(smem_u32(&xbar[xs]), (uint32_t)lane));
   };
   // Leader: waits for the exchange in flight and returns its slots.
@@ -1016,7 +1040,7 @@ __global__ void __launch_bounds__(kMssThreads, 1)
       const int olo = orank * p32, ohi = min(v32, olo + p32), on4 = (ohi - olo) >> 2;
       const int rel = txn - olo;
       const int own = rel < 4 * on4 ? (rel >> 2) % TW : (rel - 4 * on4) % TW;
-      t_oslot = orank * kMssWorkerWarps + (own >> 5);
+      t_oslot = orank * kWorkerWarps + (own >> 5);
     }
     if (kStaged) {
       const int busy = d.kind == kStepPass ? d.qj : pb;
@@ -1041,22 +1065,22 @@ __global__ void __launch_bounds__(kMssThreads, 1)
   // residual pass), combined.
   auto leader_consume = [&](const MssStep& d) {
     const float4* e = push_wait();
-    const int cnt = ncl * kMssWorkerWarps;
+    const int cnt = ncl * kWorkerWarps;
     if (d.kind == kStepRow) {
       // M = max m_r, S = sum_r e^(m_r - M) sum_w s_rw: every warp partial of
       // rank r shares its m_r.  Lanes 4r..4r+3 take rank r's slots (warps
       // 4k + lane % 4), sum them, scale once and sum over the ranks.
-      static_assert(kMssMaxCluster * 4 == 32 && kMssWorkerWarps <= 16, "four lanes per rank");
+      static_assert(kMssMaxCluster * 4 == 32 && kWorkerWarps <= 16, "four lanes per rank");
       const int r = lane >> 2;
       float mr = -INFINITY;
       F2 S{0.f, 0.f};
       if (r < ncl) {
-        mr = e[r * kMssWorkerWarps].x;
+        mr = e[r * kWorkerWarps].x;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const int w = (lane & 3) + 4 * k;
-          if (w < kMssWorkerWarps) {
-            const float4 ev = e[r * kMssWorkerWarps + w];
+          if (w < kWorkerWarps) {
+            const float4 ev = e[r * kWorkerWarps + w];
             S = f2_add(S, F2{ev.y, ev.z});
           }
         }
@@ -1069,7 +1093,7 @@ __global__ void __launch_bounds__(kMssThreads, 1)
       S = mr != -INFINITY ? f2_scale(S, exp_diff(mr, M)) : F2{0.f, 0.f};
 #pragma unroll
       for (int o = 4; o < 32; o <<= 1) S = f2_add(S, shfl_xor_f2(S, o));
-      const float m_cta = e[rank * kMssWorkerWarps].x;
+      const float m_cta = e[rank * kWorkerWarps].x;
       const float own = m_cta != -INFINITY ? exp_diff(m_cta, M) : 0.f;  // e^(m - M) of this CTA
       m_u = M;
       inv_s = f2_inv(S);
@@ -1082,7 +1106,7 @@ __global__ void __launch_bounds__(kMssThreads, 1)
     // p at the next child's token from its owner's slot.
     F2 Zp{0.f, 0.f};
 #pragma unroll
-    for (int k = 0; k < kMssSlots / 32 + 1; ++k)
+    for (int k = 0; k < kSlots / 32 + 1; ++k)
       if (lane + 32 * k < cnt) Zp = f2_add(Zp, F2{e[lane + 32 * k].x, e[lane + 32 * k].y});
     const F2 Znew = warp_sum_f2(Zp);
     float rxn = 0.f, pxn = 0.f;
@@ -1195,7 +1219,7 @@ __global__ void __launch_bounds__(kMssThreads, 1)
     if (lane == 0) red[warp] = m;
     named_bar_sync(1, TW);
 #pragma unroll
-    for (int w = 1; w < kMssWarps; ++w) m = fmaxf(m, red[w]);
+    for (int w = 1; w < kWarps; ++w) m = fmaxf(m, red[w]);
     CompSum acc;
     auto weigh = [&](float4 x, int64_t g) {  // exp(l / T - m) of group g, summed (and staged: stored)
       float4 w;
@@ -1237,42 +1261,44 @@ __global__ void __launch_bounds__(kMssThreads, 1)
     if (kStaged) fence_proxy_async_smem();  // the slice may be overwritten by a later copy
     const F2 s = warp_sum_f2(comp_value(acc));
     push_warp(make_float4(m, s.hi, s.lo, 0.f), d.xs);
-    if (warp == kMssWarps - 1) prefetch_children(d.u);
+    if (warp == kWarps - 1) prefetch_children(d.u);
   };
 
   // Row statistics of a warped row (every thread): the maximum exchanged,
   // then the warped support found by the cluster; staged, the slice is left
   // holding the weights exp(l / T - M) of the kept tokens.
   auto row_step_warped = [&](const MssStep& d) {
-    const Slice lrow = kStaged ? Slice{buf(d.src), lo} : Slice{llm_logits + (size_t)(off + d.u) * (size_t)V, 0};
-    float m = -INFINITY;
-    for (int64_t y = lo + tid; y < hi; y += T) m = fmaxf(m, lrow[y] * inv_t);
-    m = block_max<kMssWarps>(m, red);
-    push_cta(make_float4(m, 0.f, 0.f, 0.f), d.xs);
-    if (warp == kMssWarps - 1) prefetch_children(d.u);
-    if (leader) {
-      const float4* e = push_wait();
-      float M = -INFINITY;
-      for (int r = 0; r < ncl; ++r) M = fmaxf(M, e[r].x);
-      if (lane == 0) mx_s = M;
-    }
-    __syncthreads();
-    const float M = mx_s;
-    const Support sp = warped_support<kMssThreads>(lrow, V, lo, hi, inv_t, M, top_k, top_p, ncl, rank, xk,
-                                                   pub, sel);
-    m_u = M;
-    inv_s = f2_inv(sp.S);
-    tau = sp.tau;
-    ycut = sp.ycut;
-    if (kStaged) {  // weights relative to the row maximum M
-      float* w = buf(d.src);
-      for (int64_t y = lo + tid; y < hi; y += T) {
-        const float l = w[y - lo];
-        w[y - lo] = kept(l, y, tau, ycut) ? exp_diff(l * inv_t, M) : 0.f;
+    if constexpr (kWarpedOK) {
+      const Slice lrow = kStaged ? Slice{buf(d.src), lo} : Slice{llm_logits + (size_t)(off + d.u) * (size_t)V, 0};
+      float m = -INFINITY;
+      for (int64_t y = lo + tid; y < hi; y += T) m = fmaxf(m, lrow[y] * inv_t);
+      m = block_max<kWarps>(m, red);
+      push_cta(make_float4(m, 0.f, 0.f, 0.f), d.xs);
+      if (warp == kWarps - 1) prefetch_children(d.u);
+      if (leader) {
+        const float4* e = push_wait();
+        float M = -INFINITY;
+        for (int r = 0; r < ncl; ++r) M = fmaxf(M, e[r].x);
+        if (lane == 0) mx_s = M;
       }
-      wscale = inv_s;
-      fence_proxy_async_smem();  // the slice may be overwritten by a later copy
       __syncthreads();
+      const float M = mx_s;
+      const Support sp = warped_support<T>(lrow, V, lo, hi, inv_t, M, top_k, top_p, ncl, rank, xk,
+                                                     pub, sel);
+      m_u = M;
+      inv_s = f2_inv(sp.S);
+      tau = sp.tau;
+      ycut = sp.ycut;
+      if (kStaged) {  // weights relative to the row maximum M
+        float* w = buf(d.src);
+        for (int64_t y = lo + tid; y < hi; y += T) {
+          const float l = w[y - lo];
+          w[y - lo] = kept(l, y, tau, ycut) ? exp_diff(l * inv_t, M) : 0.f;
+        }
+        wscale = inv_s;
+        fence_proxy_async_smem();  // the slice may be overwritten by a later copy
+        __syncthreads();
+      }
     }
   };
 
@@ -1362,7 +1388,7 @@ __global__ void __launch_bounds__(kMssThreads, 1)
       if (lane == 0) {
         dsc[st & 1] = d;
         if (d.kind == kStepPass || (d.kind == kStepRow && !warped))  // the workers' partials
-          mbar_arrive_expect_tx(&xbar[d.xs], (uint32_t)(ncl * kMssWorkerWarps) * 16u);
+          mbar_arrive_expect_tx(&xbar[d.xs], (uint32_t)(ncl * kWorkerWarps) * 16u);
       }
     }
     __syncthreads();  // the step is described and its input has landed
@@ -1428,13 +1454,13 @@ __global__ void __launch_bounds__(kMssThreads, 1)
   if (last_pos >= 0) atomicMax(&last_s, (int)last_pos);
   __syncthreads();
   if (leader) {
-    F2 wt = lane < kMssWarps ? scan_s[lane] : F2{0.f, 0.f};
+    F2 wt = lane < kWarps ? scan_s[lane] : F2{0.f, 0.f};
 #pragma unroll
-    for (int o = 1; o < kMssWarps; o <<= 1) {
+    for (int o = 1; o < kWarps; o <<= 1) {
       const F2 t = shfl_up_f2(wt, o);
       if (lane >= o) wt = f2_add(t, wt);
     }
-    const F2 cta_total = shfl_f2(wt, kMssWarps - 1);
+    const F2 cta_total = shfl_f2(wt, kWarps - 1);
     F2 wex = shfl_up_f2(wt, 1);
     if (lane == 0) wex = F2{0.f, 0.f};
     push_cta(make_float4(cta_total.hi, cta_total.lo, __int_as_float(last_s), tmo_s ? 1.f : 0.f), xp & 1);
@@ -1457,7 +1483,7 @@ __global__ void __launch_bounds__(kMssThreads, 1)
     const F2 target = f2_scale(total, d.us);
     const uint32_t over = __ballot_sync(0xffffffffu, lane < ncl && f2_lt(target, ct));
     const int rc = over ? __ffs(over) - 1 : -1;
-    if (lane < kMssWarps) wpre_s[lane] = f2_add(base, wex);
+    if (lane < kWarps) wpre_s[lane] = f2_add(base, wex);
     if (lane == 0) {
       target_s = target;
       pick_s = rc;
@@ -1471,7 +1497,10 @@ __global__ void __launch_bounds__(kMssThreads, 1)
     }
   }
   __syncthreads();
-  if (pick_s != rank) return;  // uniform over the CTA
+  if (pick_s != rank) {  // uniform over the CTA
+    if (beside && tid == 0) pdl_wait();
+    return;
+  }
   __syncthreads();  // every thread has read pick_s
   if (tid == 0) pick_s = INT32_MAX;
   __syncthreads();
@@ -1500,6 +1529,7 @@ __global__ void __launch_bounds__(kMssThreads, 1)
   __syncthreads();
   // No run holds it (rounding at the slice's end): the slice's last positive entry.
   if (tid == 0) bonus[b] = pick_s != INT32_MAX ? pick_s : last_s;
+  if (beside && tid == 0) pdl_wait();
 }
 
 // ------------------------------------------------------------------ tree construction
@@ -1851,8 +1881,9 @@ cudaError_t mss_set_attributes(int device, size_t* staged_limit, int* max_cluste
   if (e != cudaSuccess) return e;
   size_t limit = (size_t)optin;
   void (*kernels[2])(const float*, const float*, int64_t, const int32_t*, const int32_t*, const int32_t*,
-                     const float*, const float*, float, int, float, int, int, float*, int32_t*, int32_t*,
-                     int32_t*, int32_t*, int32_t*) = {mss_verify_kernel<true>, mss_verify_kernel<false>};
+                     const float*, const float*, float, int, float, int, int, int, float*, int32_t*, int32_t*,
+                     int32_t*, int32_t*, int32_t*) = {mss_verify_kernel<true, kMssWarps>,
+                                                     mss_verify_kernel<false, kMssWarps>};
   for (auto* k : kernels) {
     cudaFuncAttributes fa;
     e = cudaFuncGetAttributes(&fa, k);
@@ -1879,7 +1910,7 @@ cudaError_t mss_set_attributes(int device, size_t* staged_limit, int* max_cluste
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     int nc = 0;
-    e = cudaOccupancyMaxActiveClusters(&nc, mss_verify_kernel<true>, &cfg);
+    e = cudaOccupancyMaxActiveClusters(&nc, mss_verify_kernel<true, kMssWarps>, &cfg);
     if (e != cudaSuccess) return e;
     max_clusters[c] = nc;
   }
@@ -1898,7 +1929,7 @@ cudaError_t launch_mss_verify(const float* llm_logits, const float* ssm_probs, i
                               float inv_t, int32_t top_k, float top_p, int32_t B, float* resid,
                               int32_t* path, int32_t* accept_len, int32_t* bonus, int32_t* n_tried,
                               int32_t* status, size_t staged_limit, const int* max_clusters,
-                              cudaStream_t st) {
+                              int beside, cudaStream_t st) {
   const int ncl = mss_cluster_size(V, B, max_clusters);
   const int vec = (V % 4 == 0) && ((reinterpret_cast<uintptr_t>(llm_logits) |
                                     reinterpret_cast<uintptr_t>(ssm_probs) |
@@ -1906,13 +1937,19 @@ cudaError_t launch_mss_verify(const float* llm_logits, const float* ssm_probs, i
   // Slices staged in shared memory when three of them fit (bulk copies want
   // the 16-byte alignment `vec` stands for).
   const size_t dyn = mss_staged_bytes(V, ncl);
+  const bool warped = top_k > 0 || top_p < 1.0f;
+  if (beside && !warped)  // two warps, slices read from global memory: fits beside an attention CTA
+    return launch_pdl(mss_verify_kernel<false, kMssCompactWarps>, dim3((unsigned)(B * ncl)),
+                      dim3(kMssCompactWarps * 32), 0, st, (unsigned)ncl, llm_logits, ssm_probs, V, tokens, parent,
+                      node_offsets, u_acc, u_smp, inv_t, top_k, top_p, ncl, vec, 1, resid, path, accept_len, bonus,
+                      n_tried, status);
   if (vec && dyn <= staged_limit)
-    return launch_pdl(mss_verify_kernel<true>, dim3((unsigned)(B * ncl)), dim3(kMssThreads), dyn, st,
+    return launch_pdl(mss_verify_kernel<true, kMssWarps>, dim3((unsigned)(B * ncl)), dim3(kMssThreads), dyn, st,
                       (unsigned)ncl, llm_logits, ssm_probs, V, tokens, parent, node_offsets, u_acc, u_smp,
-                      inv_t, top_k, top_p, ncl, vec, resid, path, accept_len, bonus, n_tried, status);
-  return launch_pdl(mss_verify_kernel<false>, dim3((unsigned)(B * ncl)), dim3(kMssThreads), 0, st,
+                      inv_t, top_k, top_p, ncl, vec, 0, resid, path, accept_len, bonus, n_tried, status);
+  return launch_pdl(mss_verify_kernel<false, kMssWarps>, dim3((unsigned)(B * ncl)), dim3(kMssThreads), 0, st,
                     (unsigned)ncl, llm_logits, ssm_probs, V, tokens, parent, node_offsets, u_acc, u_smp, inv_t,
-                    top_k, top_p, ncl, vec, resid, path, accept_len, bonus, n_tried, status);
+                    top_k, top_p, ncl, vec, 0, resid, path, accept_len, bonus, n_tried, status);
 }
 
 }  // namespace tsv
