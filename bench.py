@@ -853,7 +853,7 @@ def run_ours(args, spec):
     num_sms = torch.cuda.get_device_properties(dev).multi_processor_count
     w = DeviceWorkload(spec, tsv, dev, stream, overlap=not args.serial)
     w.capture()
-    N, R, L, kernels_per_step = w.N, w.R, w.L, w.kernels_per_step
+    N, R, L, Rv, Lv, kernels_per_step = w.N, w.R, w.L, w.Rv, w.Lv, w.kernels_per_step
 
     clocks = ClockRecord(dev)
     clocks.start()
@@ -925,7 +925,7 @@ def run_ours(args, spec):
             "config": config_of(spec),
             "roofline": roofline, "roofline_step": roofline_step,
             "timing": dict(forms, value=how, rotating_copies=R, steps_per_graph=L,
-                           verification_copies=w.Rv, verification_launches_per_graph=w.Lv),
+                           verification_copies=Rv, verification_launches_per_graph=Lv),
             "e2e": e2e, "gpu_launches": kernels_per_step * args.steps, "clocks": timed_clocks}
     if per_workload is not None:
         line["per_workload"] = per_workload
