@@ -552,6 +552,7 @@ class DeviceWorkload:
         self.spec, self.tsv, self.dev, self.stream, self.overlap = spec, tsv, dev, stream, overlap
         trees, att, gi, si = workload_inputs(spec)
         self.trees, self.att, self.gi, self.si = trees, att, gi, si
+        self.greedy_after_walk = attention_hbm_bound(spec, trees)
         self.B, self.N = spec.B, int(trees.node_offsets[-1])
 
         def to_dev(x):
@@ -647,8 +648,19 @@ class DeviceWorkload:
         if not overlap:
             self.verify(c, st)
             return
-        with self.tsv.verify_overlap(self.tsv.TSV_OVERLAP_GREEDY, device=self.dev.index):
-            self.verify(c, st)
+        # Greedy (bandwidth-bound) runs beside the launch before it: after
+        # an HBM-bound attention launch, beside the stochastic walk (which is
+        # latency-bound and leaves HBM idle) when there is one; after a
+        # tensor-bound one, beside attention itself.
+        beside_walk = self.si is not None and self.greedy_after_walk
+        with self.tsv.verify_overlap(self.tsv.TSV_OVERLAP_GREEDY if self.gi is not None else 0,
+                                     device=self.dev.index):
+            if beside_walk:
+                self.stochastic(c, st)  # leaves room beside its CTAs for greedy's
+            if self.gi is not None:
+                self.greedy(c, st)
+        if self.si is not None and not beside_walk:
+            self.stochastic(c, st)
 
     # ------------------------------------------------------------------ graphs
     def _graph(self, fn):
@@ -779,6 +791,16 @@ def attention_kernel_name(spec, trees):
     return ("tree_attn_simt_kernel" if spec.dtype != "bf16" else
             "tree_attn_keys_kernel" if keys_kernel else
             "tree_attn_tc_kernel" if tile_pairs else "tree_attn_tc1_kernel")
+
+
+def attention_hbm_bound(spec, trees):
+    """Whether the attention launch's bytes take longer at the measured HBM
+    bandwidth than its flops at the measured bf16 peak (the bound its roofline
+    reports)."""
+    peak, peak_tf, _ = measured_peaks()
+    t_bytes = attention_bytes(spec, trees) / (peak * 1e9)
+    t_flops = attention_flops(spec, trees) / (peak_tf * 1e12)
+    return not (spec.dtype == "bf16" and t_flops > t_bytes)
 
 
 def attention_exps(spec, trees):
@@ -1008,14 +1030,19 @@ def measure_e2e(args, spec, trees, att, gi, si, h, tsv, dev, stream, ws_attn, ws
             stream.wait_stream(s2)
         tsv.tree_attention(d["q"], d["k"], d["v"], trees.prefix_len, trees.node_offsets, d["plen"], d["offs"],
                            parent=d["parent"], anc=None, out=out, workspace=wsa, status=status)
-        # The verification calls follow attention directly (in overlap mode
-        # they run beside it); the results are read back after all launches.
-        with tsv.verify_overlap(0 if args.serial else tsv.TSV_OVERLAP_GREEDY, device=dev.index):
+        # The verification calls follow attention directly (greedy in overlap
+        # mode beside the launch before it); the results are read back after
+        # all launches.
+        walk_first = si is not None and attention_hbm_bound(spec, trees)  # as DeviceWorkload.step
+        stochastic = lambda: tsv.tree_verify_stochastic(d["llm"], d["ssm"], d["stok"], d["parent"], d["offs"],
+                                                        d["ua"], d["us"], workspace=wss, out=res2, **WARP)
+        with tsv.verify_overlap(0 if args.serial or gi is None else tsv.TSV_OVERLAP_GREEDY, device=dev.index):
+            if walk_first:
+                stochastic()
             if gi is not None:
                 tsv.tree_verify_greedy(d["logits"], d["gtok"], d["parent"], d["offs"], workspace=wsg, out=res)
-            if si is not None:
-                tsv.tree_verify_stochastic(d["llm"], d["ssm"], d["stok"], d["parent"], d["offs"], d["ua"],
-                                           d["us"], workspace=wss, out=res2, **WARP)
+        if si is not None and not walk_first:
+            stochastic()
         out_h.copy_(out, non_blocking=True)
         if gi is not None:
             for k in ("path", "accept_len", "bonus"):

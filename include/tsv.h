@@ -113,7 +113,11 @@ tsv_status tsv_destroy(tsv_handle h);
  * finished.  The caller guarantees the call's inputs were complete before that
  * kernel began: the verification of one batch then runs in the shadow of the
  * attention launch of another.  Results are identical either way.
- *   TSV_OVERLAP_GREEDY       tsv_tree_verify_greedy (and _noalloc)
+ *   TSV_OVERLAP_GREEDY       tsv_tree_verify_greedy (and _noalloc); while it is
+ *                            set, a stochastic call of a kind not in the set
+ *                            also leaves room for a greedy CTA beside each of
+ *                            its CTAs, so greedy launched after it runs during
+ *                            its walk
  *   TSV_OVERLAP_STOCHASTIC   tsv_tree_verify_stochastic (unwarped; in two-warp
  *                            CTAs reading their slices from global memory, so
  *                            a walk is several times slower than alone: worth

@@ -536,6 +536,7 @@ static tsv_status verify_stochastic(tsv_handle h, const float* llm_logits_d, con
                                        top_k, top_p, B, resid, path_d, accept_len_d, bonus_d,
                                        n_tried_d, status_d, h->mss_staged_limit, h->mss_max_clusters,
                                        (h->verify_overlap & TSV_OVERLAP_STOCHASTIC) ? 1 : 0,
+                                       (h->verify_overlap & TSV_OVERLAP_GREEDY) ? 1 : 0,
                                        static_cast<cudaStream_t>(stream)));
 }
 

@@ -171,7 +171,7 @@ cudaError_t launch_mss_verify(const float* llm_logits, const float* ssm_probs, i
                               float inv_t, int32_t top_k, float top_p, int32_t B, float* resid,
                               int32_t* path, int32_t* accept_len, int32_t* bonus, int32_t* n_tried,
                               int32_t* status, size_t staged_limit, const int* max_clusters,
-                              int beside, cudaStream_t st);
+                              int beside, int room, cudaStream_t st);
 // Sets the MSS kernels' dynamic shared-memory limit on `device` to all that is
 // left beside their static shared memory, returns the staged kernel's limit
 // (the largest staged slice set a launch may use) and fills

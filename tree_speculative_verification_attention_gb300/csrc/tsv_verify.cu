@@ -331,6 +331,9 @@ namespace {
 
 constexpr int kMssThreads = 512;  // stochastic verification CTAs: 16 warps, one CTA per SM
 constexpr int kMssCompactWarps = 2;  // compact CTAs (leader and one worker) that run beside attention
+// Registers a thread: 128 fill an SM's 65536 with 512 threads; the form that
+// leaves room for greedy verification beside it takes 112 (8192 left).
+constexpr int kMssRegs = 128, kMssRoomRegs = 112;
 constexpr int kMssWarps = kMssThreads / 32;
 constexpr int kSelThreads = 256;  // tree-expansion CTAs
 constexpr int kSelWarps = kSelThreads / 32;
@@ -778,8 +781,8 @@ constexpr int kMssWorkerWarps = kMssWarps - 1;     // warps 1..15
 constexpr int kMssWorkers = kMssWorkerWarps * 32;  // threads of the row statistics and residual passes
 constexpr int kMssSlots = kMssMaxCluster * kMssWorkerWarps;
 
-template <bool kStaged, int kWarps>
-__global__ void __launch_bounds__(kWarps * 32, kWarps == kMssWarps ? 1 : 65536 / (kWarps * 32 * 128))
+template <bool kStaged, int kWarps, int kRegs>
+__global__ void __maxnreg__(kRegs)
     mss_verify_kernel(const float* __restrict__ llm_logits, const float* __restrict__ ssm_probs,
                       int64_t V, const int32_t* __restrict__ tokens,
                       const int32_t* __restrict__ parent, const int32_t* __restrict__ node_offsets,
@@ -819,7 +822,9 @@ __global__ void __launch_bounds__(kWarps * 32, kWarps == kMssWarps ? 1 : 65536 /
   __shared__ MssStep dsc[2];                 // step descriptors, alternating
   __shared__ typename std::conditional<kWarpedOK, SelSmem, int>::type sel;
   extern __shared__ __align__(128) float mss_dyn[];
-  constexpr int G = kStaged ? 3 : kMssGroups;  // 4-float groups in flight per worker (shared memory: 3)
+  // 4-float groups in flight per worker: shared memory 3 (2 in the form with
+  // fewer registers, which would spill at 3), global memory kMssGroups.
+  constexpr int G = kStaged ? (kRegs >= kMssRegs ? 3 : 2) : kMssGroups;
   const bool vec = kStaged || vec_in != 0;     // staged slices are always 16-byte aligned
   const bool warped = top_k > 0 || top_p < 1.0f;
   const int b = blockIdx.x / ncl;
@@ -1880,10 +1885,11 @@ cudaError_t mss_set_attributes(int device, size_t* staged_limit, int* max_cluste
   cudaError_t e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
   if (e != cudaSuccess) return e;
   size_t limit = (size_t)optin;
-  void (*kernels[2])(const float*, const float*, int64_t, const int32_t*, const int32_t*, const int32_t*,
+  void (*kernels[3])(const float*, const float*, int64_t, const int32_t*, const int32_t*, const int32_t*,
                      const float*, const float*, float, int, float, int, int, int, float*, int32_t*, int32_t*,
-                     int32_t*, int32_t*, int32_t*) = {mss_verify_kernel<true, kMssWarps>,
-                                                     mss_verify_kernel<false, kMssWarps>};
+                     int32_t*, int32_t*, int32_t*) = {mss_verify_kernel<true, kMssWarps, kMssRegs>,
+                                                     mss_verify_kernel<true, kMssWarps, kMssRoomRegs>,
+                                                     mss_verify_kernel<false, kMssWarps, kMssRegs>};
   for (auto* k : kernels) {
     cudaFuncAttributes fa;
     e = cudaFuncGetAttributes(&fa, k);
@@ -1910,7 +1916,7 @@ cudaError_t mss_set_attributes(int device, size_t* staged_limit, int* max_cluste
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     int nc = 0;
-    e = cudaOccupancyMaxActiveClusters(&nc, mss_verify_kernel<true, kMssWarps>, &cfg);
+    e = cudaOccupancyMaxActiveClusters(&nc, mss_verify_kernel<true, kMssWarps, kMssRegs>, &cfg);
     if (e != cudaSuccess) return e;
     max_clusters[c] = nc;
   }
@@ -1929,7 +1935,7 @@ cudaError_t launch_mss_verify(const float* llm_logits, const float* ssm_probs, i
                               float inv_t, int32_t top_k, float top_p, int32_t B, float* resid,
                               int32_t* path, int32_t* accept_len, int32_t* bonus, int32_t* n_tried,
                               int32_t* status, size_t staged_limit, const int* max_clusters,
-                              int beside, cudaStream_t st) {
+                              int beside, int room, cudaStream_t st) {
   const int ncl = mss_cluster_size(V, B, max_clusters);
   const int vec = (V % 4 == 0) && ((reinterpret_cast<uintptr_t>(llm_logits) |
                                     reinterpret_cast<uintptr_t>(ssm_probs) |
@@ -1939,15 +1945,17 @@ cudaError_t launch_mss_verify(const float* llm_logits, const float* ssm_probs, i
   const size_t dyn = mss_staged_bytes(V, ncl);
   const bool warped = top_k > 0 || top_p < 1.0f;
   if (beside && !warped)  // two warps, slices read from global memory: fits beside an attention CTA
-    return launch_pdl(mss_verify_kernel<false, kMssCompactWarps>, dim3((unsigned)(B * ncl)),
+    return launch_pdl(mss_verify_kernel<false, kMssCompactWarps, kMssRegs>, dim3((unsigned)(B * ncl)),
                       dim3(kMssCompactWarps * 32), 0, st, (unsigned)ncl, llm_logits, ssm_probs, V, tokens, parent,
                       node_offsets, u_acc, u_smp, inv_t, top_k, top_p, ncl, vec, 1, resid, path, accept_len, bonus,
                       n_tried, status);
-  if (vec && dyn <= staged_limit)
-    return launch_pdl(mss_verify_kernel<true, kMssWarps>, dim3((unsigned)(B * ncl)), dim3(kMssThreads), dyn, st,
+  if (vec && dyn <= staged_limit)  // `room`: leave registers for a greedy CTA beside each CTA
+    return launch_pdl(room ? mss_verify_kernel<true, kMssWarps, kMssRoomRegs>
+                           : mss_verify_kernel<true, kMssWarps, kMssRegs>,
+                      dim3((unsigned)(B * ncl)), dim3(kMssThreads), dyn, st,
                       (unsigned)ncl, llm_logits, ssm_probs, V, tokens, parent, node_offsets, u_acc, u_smp,
                       inv_t, top_k, top_p, ncl, vec, 0, resid, path, accept_len, bonus, n_tried, status);
-  return launch_pdl(mss_verify_kernel<false, kMssWarps>, dim3((unsigned)(B * ncl)), dim3(kMssThreads), 0, st,
+  return launch_pdl(mss_verify_kernel<false, kMssWarps, kMssRegs>, dim3((unsigned)(B * ncl)), dim3(kMssThreads), 0, st,
                     (unsigned)ncl, llm_logits, ssm_probs, V, tokens, parent, node_offsets, u_acc, u_smp, inv_t,
                     top_k, top_p, ncl, vec, 0, resid, path, accept_len, bonus, n_tried, status);
 }
