@@ -274,12 +274,15 @@ __global__ void __launch_bounds__(kKeysThreads, 1)
   const int n_my = keys_fill_units(plan, sUnits);  // the same count in every thread
   __syncthreads();
   // The unit comes from the plan alone, so when all units run in the first
-  // wave the first ring's worth of K/V is pulled into L2 while the previous
-  // kernel finishes.
+  // wave its Q tile and the first ring's worth of K/V are pulled into L2
+  // while the previous kernel finishes.
   if (plan.prefetch_l2 && warp == kKeysProducerWarp && lane == 0) {
     const KeysUnit& U = sUnits[0];
+    tma_prefetch_desc(&tmap_q);
     tma_prefetch_desc(&tmap_k);
     tma_prefetch_desc(&tmap_v);
+#pragma unroll
+    for (int hf = 0; hf < C::kHalves; ++hf) tma_prefetch_3d(&tmap_q, hf * 64, U.g * G, U.off + U.row0 / G);
     for (int j = 0; j < U.nblk && j < C::kStages; ++j)
 #pragma unroll
       for (int hf = 0; hf < C::kHalves; ++hf) {

@@ -128,6 +128,14 @@ __device__ __forceinline__ void tma_prefetch_4d(const void* tmap, int c0, int c1
                : "memory");
 }
 
+// The same for a 3-D tile.
+__device__ __forceinline__ void tma_prefetch_3d(const void* tmap, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                   reinterpret_cast<uint64_t>(tmap)),
+               "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
+}
+
 // 4-D tiled tensor load global -> shared, completion counted on `bar` in bytes.
 // c0 (the innermost coordinate) must be a multiple of 16 bytes' worth of
 // elements; the callers pass multiples of 64 bf16 elements.
