@@ -50,6 +50,11 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units: P stays below 2^8 betw
 constexpr int kBarTcSetup = 1;             // softmax warps + MMA warp
 constexpr int kBarTcSoftmax = 2;           // softmax warps
 
+template <bool B>
+struct BoolTag {
+  static constexpr bool value = B;
+};
+
 template <int D>
 struct TcCfg {
   static constexpr int kHalves = D / 64;      // 128-byte column groups per row
@@ -337,11 +342,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // warps' waits end quickly too); the CTA agrees after the loop.
     bool ok = true;
     const bool active = t < ntiles;
-    for (int j = 0; active && j < nblk; ++j) {
-      if (!__all_sync(0xffffffffu, mbar_wait(&s_full[t], j & 1, abort_v))) {
-        ok = false;
-        break;
-      }
+    // One block: false when a wait timed out (the CTA's abort flag is set).
+    auto block_step = [&](int j, auto masked) -> bool {
+      if (!__all_sync(0xffffffffu, mbar_wait(&s_full[t], j & 1, abort_v))) return false;
       tc_fence_after();
       // The row's 128 scores: four loads in flight, one wait.
       float s[kBN];
@@ -357,7 +360,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int e = 0; e < kBN; ++e) s[e] = __uint_as_float(sr[e >> 5][e & 31]);
       }
       const int key0 = k_begin + j * kBN;  // this block's first key
-      if (key0 + kBN > P) {  // uniform: the block reaches the tree keys (or the end)
+      if constexpr (decltype(masked)::value) {  // the block reaches the tree keys (or the end)
         // Keys key0 + e are visible iff e < k_end - key0 and they are prefix
         // keys or the row's node and its ancestors.
         const int lim = k_end - key0;  // 1 .. 128
@@ -370,9 +373,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           s[e] = ((v0 >> e) & 1ull) ? s[e] : -INFINITY;
           s[64 + e] = ((v1 >> e) & 1ull) ? s[64 + e] : -INFINITY;
         }
-      } else if (!valid) {
-#pragma unroll
-        for (int e = 0; e < kBN; ++e) s[e] = -INFINITY;
       }
       // Four independent chains of three-input maxima (two keys per step).
       float mx[4] = {s[0], s[1], s[2], s[3]};
@@ -392,17 +392,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // O_t must hold PV_t(j-1) before it is rescaled (lanes with alpha = 1
         // rewrite their row unchanged: TMEM loads and stores are warp-wide).
         if (!__all_sync(0xffffffffu, mbar_wait(&pv_done[t], (j - 1) & 1, abort_v))) {
-          ok = false;
-          break;
+          return false;
         }
         tc_fence_after();
+        // 16 columns at a time, so the scores can stay in registers meanwhile;
+        // the wait for the P stores below also covers these stores.
 #pragma unroll 1
-        for (int cc = 0; cc < D; cc += 32) {
-          float o[32];
-          tmem_ld32(o_mine + cc, o);
+        for (int cc = 0; cc < D; cc += 16) {
+          float o[16];
+          tmem_ld16(o_mine + cc, o);
+          uint32_t u[16];
 #pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] *= alpha;
-          tmem_st32(o_mine + cc, o);
+          for (int e = 0; e < 16; ++e) u[e] = __float_as_uint(o[e] * alpha);
+          tmem_st16u_nowait(o_mine + cc, u);
         }
       }
       const float neg_ref = m_ref == -INFINITY ? 0.f : -m_ref;
@@ -433,8 +435,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int vrows = k_end - key0;
       if (t == 0 && vrows < kBN) {
         if (!__all_sync(0xffffffffu, mbar_wait(&v_full[j % SV], (j / SV) & 1, abort_v))) {
-          ok = false;
-          break;
+          return false;
         }
         uint8_t* vt = sV + (j % SV) * C::kTileBytes;
         const int pieces = (kBN - vrows) * C::kHalves * 8;
@@ -448,7 +449,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       tc_fence_before();
       mbar_arrive(&p_full[t]);
-    }
+      return true;
+    };
+    // Blocks wholly inside the prefix take no mask: every row sees all their
+    // keys (rows past the request compute on finite inputs in their own TMEM
+    // lanes and are never stored).  The blocks from the first that reaches
+    // the tree keys (or the end of the chunk) on apply it.
+    const int jm = active ? min(nblk, max(0, (P - k_begin) / kBN)) : 0;
+    for (int j = 0; ok && active && j < jm; ++j) ok = block_step(j, BoolTag<false>{});
+    for (int j = jm; ok && active && j < nblk; ++j) ok = block_step(j, BoolTag<true>{});
     // The tile's last PV must be complete before the epilogue reads O_t.
     if (active && ok && nblk > 0)
       ok = __all_sync(0xffffffffu, mbar_wait(&pv_done[t], (nblk - 1) & 1, abort_v));
