@@ -541,18 +541,21 @@ class DeviceWorkload:
 
     Within a step, verification reads only the given logits and proposals, so
     it does not wait for the attention launch: with ``overlap`` the
-    verification launches follow attention on the same stream, greedy
-    verification in the library's overlap mode (tsv_set_verify_overlap): its
-    compact CTAs are launched once every attention CTA is resident, run in the
-    SM room attention leaves, and complete after it.  Stochastic verification
-    then runs after attention, at full size."""
+    verification launches follow attention on the same stream in the
+    library's overlap mode (tsv_set_verify_overlap): they are launched once
+    every CTA of the launch before them is resident, run in the SM room it
+    leaves, and complete after it.  After an HBM-bound attention launch (every
+    SM busy), the stochastic walk runs after it at full size and greedy
+    verification, bandwidth-bound, beside the walk; after a tensor-bound launch
+    (fewer units than SMs), the walk starts beside attention at full size on
+    the idle SMs, and greedy beside both."""
 
     def __init__(self, spec, tsv, dev, stream, overlap=True):
         import torch
         self.spec, self.tsv, self.dev, self.stream, self.overlap = spec, tsv, dev, stream, overlap
         trees, att, gi, si = workload_inputs(spec)
         self.trees, self.att, self.gi, self.si = trees, att, gi, si
-        self.greedy_after_walk = attention_hbm_bound(spec, trees)
+        self.hbm_bound = attention_hbm_bound(spec, trees)
         self.B, self.N = spec.B, int(trees.node_offsets[-1])
 
         def to_dev(x):
@@ -648,19 +651,12 @@ class DeviceWorkload:
         if not overlap:
             self.verify(c, st)
             return
-        # Greedy (bandwidth-bound) runs beside the launch before it: after
-        # an HBM-bound attention launch, beside the stochastic walk (which is
-        # latency-bound and leaves HBM idle) when there is one; after a
-        # tensor-bound one, beside attention itself.
-        beside_walk = self.si is not None and self.greedy_after_walk
-        with self.tsv.verify_overlap(self.tsv.TSV_OVERLAP_GREEDY if self.gi is not None else 0,
+        with self.tsv.verify_overlap(overlap_kinds(self.tsv, self.hbm_bound, self.gi is not None),
                                      device=self.dev.index):
-            if beside_walk:
+            if self.si is not None:
                 self.stochastic(c, st)  # leaves room beside its CTAs for greedy's
             if self.gi is not None:
                 self.greedy(c, st)
-        if self.si is not None and not beside_walk:
-            self.stochastic(c, st)
 
     # ------------------------------------------------------------------ graphs
     def _graph(self, fn):
@@ -801,6 +797,16 @@ def attention_hbm_bound(spec, trees):
     t_bytes = attention_bytes(spec, trees) / (peak * 1e9)
     t_flops = attention_flops(spec, trees) / (peak_tf * 1e12)
     return not (spec.dtype == "bf16" and t_flops > t_bytes)
+
+
+def overlap_kinds(tsv, hbm_bound, greedy):
+    """Overlap flags of a step's verification calls (stochastic first, then
+    greedy): greedy beside the launch before it; the stochastic walk beside a
+    tensor-bound attention launch, whose units leave SMs idle, at full size."""
+    kinds = tsv.TSV_OVERLAP_GREEDY if greedy else 0
+    if not hbm_bound:
+        kinds |= tsv.TSV_OVERLAP_STOCHASTIC_FULL
+    return kinds
 
 
 def attention_exps(spec, trees):
@@ -1030,19 +1036,15 @@ def measure_e2e(args, spec, trees, att, gi, si, h, tsv, dev, stream, ws_attn, ws
             stream.wait_stream(s2)
         tsv.tree_attention(d["q"], d["k"], d["v"], trees.prefix_len, trees.node_offsets, d["plen"], d["offs"],
                            parent=d["parent"], anc=None, out=out, workspace=wsa, status=status)
-        # The verification calls follow attention directly (greedy in overlap
-        # mode beside the launch before it); the results are read back after
-        # all launches.
-        walk_first = si is not None and attention_hbm_bound(spec, trees)  # as DeviceWorkload.step
-        stochastic = lambda: tsv.tree_verify_stochastic(d["llm"], d["ssm"], d["stok"], d["parent"], d["offs"],
-                                                        d["ua"], d["us"], workspace=wss, out=res2, **WARP)
-        with tsv.verify_overlap(0 if args.serial or gi is None else tsv.TSV_OVERLAP_GREEDY, device=dev.index):
-            if walk_first:
-                stochastic()
+        # The verification calls follow attention directly, in overlap mode as
+        # in DeviceWorkload.step; the results are read back after all launches.
+        kinds = 0 if args.serial else overlap_kinds(tsv, attention_hbm_bound(spec, trees), gi is not None)
+        with tsv.verify_overlap(kinds, device=dev.index):
+            if si is not None:
+                tsv.tree_verify_stochastic(d["llm"], d["ssm"], d["stok"], d["parent"], d["offs"], d["ua"], d["us"],
+                                           workspace=wss, out=res2, **WARP)
             if gi is not None:
                 tsv.tree_verify_greedy(d["logits"], d["gtok"], d["parent"], d["offs"], workspace=wsg, out=res)
-        if si is not None and not walk_first:
-            stochastic()
         out_h.copy_(out, non_blocking=True)
         if gi is not None:
             for k in ("path", "accept_len", "bonus"):

@@ -122,11 +122,21 @@ tsv_status tsv_destroy(tsv_handle h);
  *                            CTAs reading their slices from global memory, so
  *                            a walk is several times slower than alone: worth
  *                            it only when the kernel before it runs longer)
+ *   TSV_OVERLAP_STOCHASTIC_FULL
+ *                            tsv_tree_verify_stochastic (warped or not) in its
+ *                            usual full-size CTAs, which need whole SMs, in
+ *                            clusters of at most 4 so that they find room: for
+ *                            a kernel before it that leaves SMs idle (the
+ *                            rows-on-lanes tree attention on fewer units than
+ *                            SMs); where none are free the walk starts as that
+ *                            kernel's CTAs leave.  Takes precedence over
+ *                            TSV_OVERLAP_STOCHASTIC.
  *   Takes effect for calls made (or captured into a CUDA graph) after it;
  *   TSV_ERR_INVALID_ARG for other bits.
  */
 #define TSV_OVERLAP_GREEDY 1u
 #define TSV_OVERLAP_STOCHASTIC 2u
+#define TSV_OVERLAP_STOCHASTIC_FULL 4u
 tsv_status tsv_set_verify_overlap(tsv_handle h, uint32_t kinds);
 
 /*

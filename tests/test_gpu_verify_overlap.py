@@ -1,8 +1,9 @@
-"""Verification in overlap mode (tsv_set_verify_overlap, both kinds): the
-calls start while the kernel before them on the stream still runs, in compact
-CTAs, and complete after it.  The results must be bit-identical to the default mode
-(itself checked against the oracle), whether or not an attention launch
-precedes them, and every output must be complete when the stream is.
+"""Verification in overlap mode (tsv_set_verify_overlap): the calls start
+while the kernel before them on the stream still runs (in compact CTAs, or the
+stochastic walk at full size) and complete after it.  The results must be
+bit-identical to the default mode (itself checked against the oracle), whether
+or not an attention launch precedes them, and every output must be complete
+when the stream is.
 """
 import numpy as np
 import pytest
@@ -48,10 +49,20 @@ def _same(a, b):
                 assert torch.equal(a[kind][k], b[kind][k]), (kind, k)
 
 
-@pytest.mark.parametrize("name,warp", [("batch32-P2048-n16", {}), ("batch8-ragged-merge64-mss", {}),
-                                       ("gqa64x8-P32768-n128", {}), ("llama7b-layer-P1024-n20", {}),
-                                       ("batch8-ragged-merge64-mss", {"top_k": 50, "top_p": 0.9})])
-def test_overlap_mode_matches_default_mode(tsv, name, warp):
+COMPACT, FULL = "compact", "full"
+
+
+def _kinds(tsv, form):
+    return tsv.TSV_OVERLAP_GREEDY | (tsv.TSV_OVERLAP_STOCHASTIC if form == COMPACT else
+                                     tsv.TSV_OVERLAP_STOCHASTIC_FULL)
+
+
+@pytest.mark.parametrize("name,warp,form", [("batch32-P2048-n16", {}, COMPACT), ("batch8-ragged-merge64-mss", {}, COMPACT),
+                                            ("gqa64x8-P32768-n128", {}, COMPACT), ("llama7b-layer-P1024-n20", {}, COMPACT),
+                                            ("batch8-ragged-merge64-mss", {"top_k": 50, "top_p": 0.9}, COMPACT),
+                                            ("gqa64x8-P32768-n128", {}, FULL), ("batch32-P2048-n16", {}, FULL),
+                                            ("batch8-ragged-merge64-mss", {"top_k": 50, "top_p": 0.9}, FULL)])
+def test_overlap_mode_matches_default_mode(tsv, name, warp, form):
     spec = W.SPECS[name]
     trees, att, gi, si = _inputs(spec)
     ref = _verify(tsv, trees, gi, si, warp)
@@ -63,22 +74,23 @@ def test_overlap_mode_matches_default_mode(tsv, name, warp):
     for precede in (True, False):
         if precede:
             _attention(tsv, spec, trees, att)
-        with tsv.verify_overlap():
+        with tsv.verify_overlap(_kinds(tsv, form)):
             got = _verify(tsv, trees, gi, si, warp)
         torch.cuda.synchronize()
         _same(ref, got)
 
 
-def test_overlap_mode_results_are_complete_when_a_later_kernel_runs(tsv):
+@pytest.mark.parametrize("form", [COMPACT, FULL])
+def test_overlap_mode_results_are_complete_when_a_later_kernel_runs(tsv, form):
     """A kernel launched after an overlap-mode call (in stream order) must see
-    its finished outputs: the next launch here reads them through the
-    stochastic call's own inputs (its path is fed back as a token row)."""
+    its finished outputs: the next launch here copies the stochastic call's
+    path."""
     spec = W.SPECS["batch8-ragged-merge64-mss"]
     trees, att, gi, si = _inputs(spec)
     ref = _verify(tsv, trees, gi, si, {})["s"]
     torch.cuda.synchronize()
     _attention(tsv, spec, trees, att)
-    with tsv.verify_overlap():
+    with tsv.verify_overlap(_kinds(tsv, form)):
         got = _verify(tsv, trees, gi, si, {})["s"]
     later = got["path"].clone()  # an ordinary copy kernel, after the call on the stream
     torch.cuda.synchronize()
@@ -89,6 +101,7 @@ def test_overlap_mode_results_are_complete_when_a_later_kernel_runs(tsv):
 def test_overlap_option_rejects_other_values(tsv):
     h = tsv.handle()
     with pytest.raises(tsv.TSVError):
-        tsv.tsv_set_verify_overlap(h, 4)
-    tsv.tsv_set_verify_overlap(h, tsv.TSV_OVERLAP_GREEDY | tsv.TSV_OVERLAP_STOCHASTIC)
+        tsv.tsv_set_verify_overlap(h, 8)
+    tsv.tsv_set_verify_overlap(h, tsv.TSV_OVERLAP_GREEDY | tsv.TSV_OVERLAP_STOCHASTIC |
+                               tsv.TSV_OVERLAP_STOCHASTIC_FULL)
     tsv.tsv_set_verify_overlap(h, 0)

@@ -230,7 +230,7 @@ def tsv_tree_merge(h, parent, tokens, tree_offsets, request_trees, B, out_parent
                                _ptr(status), _stream(stream)), "tsv_tree_merge")
 
 
-TSV_OVERLAP_GREEDY, TSV_OVERLAP_STOCHASTIC = 1, 2
+TSV_OVERLAP_GREEDY, TSV_OVERLAP_STOCHASTIC, TSV_OVERLAP_STOCHASTIC_FULL = 1, 2, 4
 
 
 def tsv_set_verify_overlap(h, kinds):

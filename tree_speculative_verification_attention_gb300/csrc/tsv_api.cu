@@ -327,7 +327,8 @@ tsv_status tsv_create(tsv_handle* out, int device) {
 }
 
 tsv_status tsv_set_verify_overlap(tsv_handle h, uint32_t kinds) {
-  if (!h || (kinds & ~(TSV_OVERLAP_GREEDY | TSV_OVERLAP_STOCHASTIC)) != 0u) return TSV_ERR_INVALID_ARG;
+  if (!h || (kinds & ~(TSV_OVERLAP_GREEDY | TSV_OVERLAP_STOCHASTIC | TSV_OVERLAP_STOCHASTIC_FULL)) != 0u)
+    return TSV_ERR_INVALID_ARG;
   h->verify_overlap = kinds;
   return TSV_OK;
 }
@@ -535,7 +536,9 @@ static tsv_status verify_stochastic(tsv_handle h, const float* llm_logits_d, con
                                        node_offsets_d, u_accept_d, u_sample_d, 1.0f / temperature,
                                        top_k, top_p, B, resid, path_d, accept_len_d, bonus_d,
                                        n_tried_d, status_d, h->mss_staged_limit, h->mss_max_clusters,
-                                       (h->verify_overlap & TSV_OVERLAP_STOCHASTIC) ? 1 : 0,
+                                       (h->verify_overlap & TSV_OVERLAP_STOCHASTIC_FULL) ? kMssBesideFull
+                                       : (h->verify_overlap & TSV_OVERLAP_STOCHASTIC)    ? kMssBesideCompact
+                                                                                         : 0,
                                        (h->verify_overlap & TSV_OVERLAP_GREEDY) ? 1 : 0,
                                        static_cast<cudaStream_t>(stream)));
 }

@@ -162,9 +162,19 @@ inline size_t greedy_workspace_bytes(int32_t B, int32_t N) {
 }
 
 // Stochastic verification: one cluster of mss_cluster_size(V, B, ...) CTAs
-// per request, each owning a slice of the vocabulary.
+// per request, each owning a slice of the vocabulary.  `beside`: 0 waits for
+// the previous kernel on the stream before reading; kMssBesideCompact and
+// kMssBesideFull start beside it (two-warp CTAs that fit next to an attention
+// CTA, or the full-size CTAs on SMs it leaves free) and complete after it.
+// `room`: the full-size CTAs leave registers for a greedy CTA beside each.
 constexpr int kMssClusterSizes = 9;  // entries of the resident-cluster table (sizes 0..8)
-int mss_cluster_size(int64_t V, int32_t B, const int* max_clusters);
+constexpr int kMssBesideCompact = 1, kMssBesideFull = 2;
+// Largest cluster of the full-size CTAs beside a running kernel: a cluster
+// needs that many idle SMs in one GPC, which a running grid seldom leaves
+// (measured beside the GQA rows-on-lanes launch: clusters of 8 started only as
+// it ended, clusters of 4 or 2 ran beside it).
+constexpr int kMssBesideMaxCluster = 4;
+int mss_cluster_size(int64_t V, int32_t B, const int* max_clusters, int cap);
 cudaError_t launch_mss_verify(const float* llm_logits, const float* ssm_probs, int64_t V,
                               const int32_t* tokens, const int32_t* parent,
                               const int32_t* node_offsets, const float* u_acc, const float* u_smp,

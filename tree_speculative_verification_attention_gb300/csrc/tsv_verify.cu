@@ -1872,9 +1872,9 @@ cudaError_t launch_tree_merge(const int32_t* parent, const int32_t* tokens, cons
 // portable cluster), and no more than lets every request's cluster be
 // resident at once (max_clusters[c]: clusters of c CTAs the device holds at
 // once; the kernel runs one CTA per SM).
-int mss_cluster_size(int64_t V, int32_t B, const int* max_clusters) {
+int mss_cluster_size(int64_t V, int32_t B, const int* max_clusters, int cap) {
   int64_t c = (V + kMssMinSlice - 1) / kMssMinSlice;
-  c = c < 1 ? 1 : (c > kMssMaxCluster ? kMssMaxCluster : c);
+  c = c < 1 ? 1 : (c > cap ? cap : c);
   if (max_clusters != nullptr)
     while (c > 1 && max_clusters[c] < B) --c;
   return (int)c;
@@ -1936,7 +1936,7 @@ cudaError_t launch_mss_verify(const float* llm_logits, const float* ssm_probs, i
                               int32_t* path, int32_t* accept_len, int32_t* bonus, int32_t* n_tried,
                               int32_t* status, size_t staged_limit, const int* max_clusters,
                               int beside, int room, cudaStream_t st) {
-  const int ncl = mss_cluster_size(V, B, max_clusters);
+  const int ncl = mss_cluster_size(V, B, max_clusters, beside == kMssBesideFull ? kMssBesideMaxCluster : kMssMaxCluster);
   const int vec = (V % 4 == 0) && ((reinterpret_cast<uintptr_t>(llm_logits) |
                                     reinterpret_cast<uintptr_t>(ssm_probs) |
                                     reinterpret_cast<uintptr_t>(resid)) & 15) == 0;
@@ -1944,7 +1944,11 @@ cudaError_t launch_mss_verify(const float* llm_logits, const float* ssm_probs, i
   // the 16-byte alignment `vec` stands for).
   const size_t dyn = mss_staged_bytes(V, ncl);
   const bool warped = top_k > 0 || top_p < 1.0f;
-  if (beside && !warped)  // two warps, slices read from global memory: fits beside an attention CTA
+  // The full-size forms start beside the previous kernel only in the full
+  // overlap mode; a warped call in the compact mode takes them and waits (the
+  // warped support needs every warp).
+  const int full = beside == kMssBesideFull ? 1 : 0;
+  if (beside == kMssBesideCompact && !warped)  // two warps, slices from global memory: fits beside an attention CTA
     return launch_pdl(mss_verify_kernel<false, kMssCompactWarps, kMssRegs>, dim3((unsigned)(B * ncl)),
                       dim3(kMssCompactWarps * 32), 0, st, (unsigned)ncl, llm_logits, ssm_probs, V, tokens, parent,
                       node_offsets, u_acc, u_smp, inv_t, top_k, top_p, ncl, vec, 1, resid, path, accept_len, bonus,
@@ -1954,10 +1958,10 @@ cudaError_t launch_mss_verify(const float* llm_logits, const float* ssm_probs, i
                            : mss_verify_kernel<true, kMssWarps, kMssRegs>,
                       dim3((unsigned)(B * ncl)), dim3(kMssThreads), dyn, st,
                       (unsigned)ncl, llm_logits, ssm_probs, V, tokens, parent, node_offsets, u_acc, u_smp,
-                      inv_t, top_k, top_p, ncl, vec, 0, resid, path, accept_len, bonus, n_tried, status);
+                      inv_t, top_k, top_p, ncl, vec, full, resid, path, accept_len, bonus, n_tried, status);
   return launch_pdl(mss_verify_kernel<false, kMssWarps, kMssRegs>, dim3((unsigned)(B * ncl)), dim3(kMssThreads), 0, st,
                     (unsigned)ncl, llm_logits, ssm_probs, V, tokens, parent, node_offsets, u_acc, u_smp, inv_t,
-                    top_k, top_p, ncl, vec, 0, resid, path, accept_len, bonus, n_tried, status);
+                    top_k, top_p, ncl, vec, full, resid, path, accept_len, bonus, n_tried, status);
 }
 
 }  // namespace tsv
