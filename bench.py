@@ -544,18 +544,16 @@ class DeviceWorkload:
     verification launches follow attention on the same stream in the
     library's overlap mode (tsv_set_verify_overlap): they are launched once
     every CTA of the launch before them is resident, run in the SM room it
-    leaves, and complete after it.  After an HBM-bound attention launch (every
-    SM busy), the stochastic walk runs after it at full size and greedy
-    verification, bandwidth-bound, beside the walk; after a tensor-bound launch
-    (fewer units than SMs), the walk starts beside attention at full size on
-    the idle SMs, and greedy beside both."""
+    leaves, and complete after it.  The stochastic walk starts beside
+    attention at full size on the SMs attention leaves idle (a tensor-bound
+    launch's spare SMs, a persistent launch's SMs as its tail frees them), and
+    greedy verification beside both."""
 
     def __init__(self, spec, tsv, dev, stream, overlap=True):
         import torch
         self.spec, self.tsv, self.dev, self.stream, self.overlap = spec, tsv, dev, stream, overlap
         trees, att, gi, si = workload_inputs(spec)
         self.trees, self.att, self.gi, self.si = trees, att, gi, si
-        self.hbm_bound = attention_hbm_bound(spec, trees)
         self.B, self.N = spec.B, int(trees.node_offsets[-1])
 
         def to_dev(x):
@@ -651,7 +649,7 @@ class DeviceWorkload:
         if not overlap:
             self.verify(c, st)
             return
-        with self.tsv.verify_overlap(overlap_kinds(self.tsv, self.hbm_bound, self.gi is not None),
+        with self.tsv.verify_overlap(overlap_kinds(self.tsv, self.gi is not None),
                                      device=self.dev.index):
             if self.si is not None:
                 self.stochastic(c, st)  # leaves room beside its CTAs for greedy's
@@ -789,24 +787,12 @@ def attention_kernel_name(spec, trees):
             "tree_attn_tc_kernel" if tile_pairs else "tree_attn_tc1_kernel")
 
 
-def attention_hbm_bound(spec, trees):
-    """Whether the attention launch's bytes take longer at the measured HBM
-    bandwidth than its flops at the measured bf16 peak (the bound its roofline
-    reports)."""
-    peak, peak_tf, _ = measured_peaks()
-    t_bytes = attention_bytes(spec, trees) / (peak * 1e9)
-    t_flops = attention_flops(spec, trees) / (peak_tf * 1e12)
-    return not (spec.dtype == "bf16" and t_flops > t_bytes)
-
-
-def overlap_kinds(tsv, hbm_bound, greedy):
+def overlap_kinds(tsv, greedy):
     """Overlap flags of a step's verification calls (stochastic first, then
-    greedy): greedy beside the launch before it; the stochastic walk beside a
-    tensor-bound attention launch, whose units leave SMs idle, at full size."""
-    kinds = tsv.TSV_OVERLAP_GREEDY if greedy else 0
-    if not hbm_bound:
-        kinds |= tsv.TSV_OVERLAP_STOCHASTIC_FULL
-    return kinds
+    greedy): the stochastic walk beside attention at full size, on the SMs the
+    launch leaves idle (a tensor-bound launch's spare SMs, a persistent
+    launch's SMs as its tail frees them), and greedy beside the walk."""
+    return (tsv.TSV_OVERLAP_GREEDY if greedy else 0) | tsv.TSV_OVERLAP_STOCHASTIC_FULL
 
 
 def attention_exps(spec, trees):
@@ -1038,7 +1024,7 @@ def measure_e2e(args, spec, trees, att, gi, si, h, tsv, dev, stream, ws_attn, ws
                            parent=d["parent"], anc=None, out=out, workspace=wsa, status=status)
         # The verification calls follow attention directly, in overlap mode as
         # in DeviceWorkload.step; the results are read back after all launches.
-        kinds = 0 if args.serial else overlap_kinds(tsv, attention_hbm_bound(spec, trees), gi is not None)
+        kinds = 0 if args.serial else overlap_kinds(tsv, gi is not None)
         with tsv.verify_overlap(kinds, device=dev.index):
             if si is not None:
                 tsv.tree_verify_stochastic(d["llm"], d["ssm"], d["stok"], d["parent"], d["offs"], d["ua"], d["us"],

@@ -128,9 +128,10 @@ tsv_status tsv_destroy(tsv_handle h);
  *                            clusters of at most 4 so that they find room: for
  *                            a kernel before it that leaves SMs idle (the
  *                            rows-on-lanes tree attention on fewer units than
- *                            SMs); where none are free the walk starts as that
- *                            kernel's CTAs leave.  Takes precedence over
- *                            TSV_OVERLAP_STOCHASTIC.
+ *                            SMs) or frees them one by one as it ends (the
+ *                            persistent tree attention's tail); the walk's
+ *                            clusters start wherever SMs are free.  Takes
+ *                            precedence over TSV_OVERLAP_STOCHASTIC.
  *   Takes effect for calls made (or captured into a CUDA graph) after it;
  *   TSV_ERR_INVALID_ARG for other bits.
  */

@@ -158,6 +158,10 @@ EDGE = {
     # three tiles (a full pair and a pair with one tile)
     "one-row-tile-mha": dict(B=2, Hq=4, Hkv=4, nodes=100, prefix=(300, 900), tree="random", max_depth=9),
     "three-row-tiles": dict(B=2, Hq=4, Hkv=2, nodes=150, prefix=(200, 700), tree="random", max_depth=9),
+    # tile pairs with prefixes of whole 128-key blocks: a block ends exactly
+    # where the tree keys begin, and the next one starts with them
+    "row-tiles-prefix-of-whole-blocks": dict(B=2, Hq=16, Hkv=2, nodes=100, prefix=1024, tree="random",
+                                             max_depth=9),
 }
 
 
