@@ -105,3 +105,33 @@ def test_overlap_option_rejects_other_values(tsv):
     tsv.tsv_set_verify_overlap(h, tsv.TSV_OVERLAP_GREEDY | tsv.TSV_OVERLAP_STOCHASTIC |
                                tsv.TSV_OVERLAP_STOCHASTIC_FULL)
     tsv.tsv_set_verify_overlap(h, 0)
+
+
+@pytest.mark.parametrize("form", [COMPACT, FULL])
+def test_overlap_mode_reports_bad_requests_like_the_default_mode(tsv, form):
+    """A malformed tree in one request and a token outside the vocabulary in
+    another make those requests' CTAs leave early; in overlap mode they still
+    wait for the kernel before them, and every output, the statuses included,
+    equals the default mode's."""
+    spec = W.SPECS["batch8-ragged-merge64-mss"]
+    trees, att, gi, si = _inputs(spec)
+    offs = trees.node_offsets
+    parent = trees.parent.copy()
+    parent[offs[2] + 3] = 5  # points forward (parents are local indices below the node)
+    tokens = si.tokens.copy()
+    tokens[offs[5] + 1] = spec.V + 7
+
+    def run():
+        return tsv.tree_verify_stochastic(d(si.llm_logits), d(si.ssm_probs), d(tokens), d(parent), d(offs),
+                                          d(si.u_accept), d(si.u_sample))
+
+    ref = run()
+    torch.cuda.synchronize()
+    want = [0] * spec.B
+    want[2], want[5] = tsv.TSV_ERR_BAD_TREE, tsv.TSV_ERR_INVALID_ARG
+    assert ref["status"].cpu().tolist() == want
+    _attention(tsv, spec, trees, att)
+    with tsv.verify_overlap(_kinds(tsv, form)):
+        got = run()
+    torch.cuda.synchronize()
+    _same({"s": ref}, {"s": got})
