@@ -33,8 +33,11 @@ namespace {
 
 constexpr int kArgmaxThreads = 256;
 constexpr int kArgmaxInFlight = 4;
-constexpr uint32_t kArgmaxPrefetchMax = 32768;  // largest slice pulled into L2 ahead of the wait
 constexpr int kMinSlice = 2048;  // vocab entries per CTA at least
+constexpr int64_t kMaxSlice = 16384;  // vocab entries per CTA at most
+// Largest slice pulled into L2 at the start (every slice: a 64 KB slice is
+// four rounds of the threads' loads, which the bulk prefetch overlaps).
+constexpr uint32_t kArgmaxPrefetchMax = (uint32_t)kMaxSlice * 4;
 
 struct ArgMax {
   float v;
@@ -238,9 +241,9 @@ __global__ void __launch_bounds__(kArgmaxThreads, 8)
                          unsigned long long* __restrict__ rowbest, int32_t* __restrict__ counters,
                          int32_t* __restrict__ path, int32_t* __restrict__ accept_len,
                          int32_t* __restrict__ bonus, int32_t* __restrict__ status, int beside) {
-  // A small slice (short rows spread over many CTAs) is pulled into L2 while
-  // the previous kernel finishes: a prefetch reads no value, so it may run
-  // ahead of that kernel's writes.
+  // The slice is pulled into L2 while the previous kernel finishes (or, beside
+  // it, while the threads' first loads are in flight): a prefetch reads no
+  // value, so it may run ahead of that kernel's writes.
   if (threadIdx.x == 0 && (V & 3) == 0) {
     const int64_t per = slice_len(V, splits);
     const int64_t lo = min(V, (int64_t)blockIdx.x * per), hi = min(V, lo + per);
@@ -298,7 +301,6 @@ __global__ void __launch_bounds__(kArgmaxThreads, 8)
 // round trip, and few CTAs share a request's counter) and slices of at most
 // kMaxSlice entries (long rows: more CTAs, more loads in flight), of at
 // least kMinSlice.
-constexpr int64_t kMaxSlice = 16384;
 int greedy_splits(int64_t V, int32_t N, int num_sms) {
   int64_t s = ((int64_t)num_sms + N - 1) / (N > 0 ? N : 1);
   s = s > (V + kMaxSlice - 1) / kMaxSlice ? s : (V + kMaxSlice - 1) / kMaxSlice;
@@ -777,9 +779,6 @@ struct MssStep {
   float bscale, us;       // bonus: weight scale, sampling uniform
 };
 constexpr int kStepNone = 0, kStepRow = 1, kStepPass = 2, kStepBonus = 3;
-constexpr int kMssWorkerWarps = kMssWarps - 1;     // warps 1..15
-constexpr int kMssWorkers = kMssWorkerWarps * 32;  // threads of the row statistics and residual passes
-constexpr int kMssSlots = kMssMaxCluster * kMssWorkerWarps;
 
 template <bool kStaged, int kWarps, int kRegs>
 __global__ void __maxnreg__(kRegs)
