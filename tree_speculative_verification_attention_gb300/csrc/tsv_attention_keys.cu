@@ -61,7 +61,7 @@ namespace tsv {
 constexpr int kKeysLaneThreads = 256;
 constexpr int kKeysEpiThreads = 128;  // epilogue warps of a persistent launch
 constexpr int kKeysThreads = kKeysLaneThreads + 64 + kKeysEpiThreads;
-constexpr int kKeysProducerWarp = 8, kKeysMmaWarp = 9, kKeysEpiWarp0 = 10;
+constexpr int kKeysProducerWarp = 8, kKeysMmaWarp = 9;  // then the epilogue warps
 constexpr int kKeysBlock = kKeysBlockKeys;   // keys per block (MMA M)
 constexpr int kKeysRows = kKeysTileRows;     // query rows per CTA (MMA N)
 constexpr int kKeysMaxTree = kKeysTileRows;  // n * G <= 64 implies n <= 64

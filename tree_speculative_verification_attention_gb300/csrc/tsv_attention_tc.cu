@@ -343,6 +343,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     bool ok = true;
     const bool active = t < ntiles;
     // One block: false when a wait timed out (the CTA's abort flag is set).
+    // `masked` (BoolTag<true>) for a block that reaches the tree keys or the
+    // chunk's end: the ancestor mask and the key count apply.
     auto block_step = [&](int j, auto masked) -> bool {
       if (!__all_sync(0xffffffffu, mbar_wait(&s_full[t], j & 1, abort_v))) return false;
       tc_fence_after();
