@@ -55,6 +55,25 @@ def test_binding_mirrors_the_header(lib):
             assert callable(getattr(tsv, name))
 
 
+def header_constants():
+    """Every numeric #define and enum value of the header (name -> value)."""
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    found = {m.group(1): int(m.group(2)) for m in re.finditer(r"^#define\s+(TSV_[A-Z0-9_]+)\s+(\d+)u?\s*$", text, re.M)}
+    for body in re.findall(r"typedef\s+enum\s*\{(.*?)\}", text, re.S):
+        found.update({m.group(1): int(m.group(2)) for m in re.finditer(r"(TSV_[A-Z0-9_]+)\s*=\s*(\d+)", body)})
+    return found
+
+
+def test_binding_constants_match_the_header(lib):
+    import tree_speculative_verification_attention_gb300 as tsv
+    consts = header_constants()
+    for name in ("TSV_OK", "TSV_ERR_TIMEOUT", "TSV_BF16", "TSV_MAX_NODES", "TSV_ANC_WORDS", "TSV_ATTN_SIMT",
+                 "TSV_OVERLAP_GREEDY", "TSV_OVERLAP_STOCHASTIC", "TSV_OVERLAP_STOCHASTIC_FULL"):
+        assert name in consts, name
+    for name, value in consts.items():
+        assert getattr(tsv, name) == value, name
+
+
 def test_status_strings(lib):
     lib.tsv_status_string.restype = ctypes.c_char_p
     assert lib.tsv_status_string(0) == b"ok"
