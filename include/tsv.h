@@ -106,18 +106,19 @@ tsv_status tsv_destroy(tsv_handle h);
  * against the kernel launched before them on the same stream.  `kinds` is a
  * set of flags; a call of a kind not in it (the default: none) waits for that
  * kernel's results before it reads.  A call of a kind in it starts while that
- * kernel still runs, in small CTAs that fit on an SM beside a running
- * keys-on-lanes tree-attention CTA (the attention kernels' trigger lets it
- * launch once every attention CTA is resident), and completes only after that
- * kernel completes, so every later launch on the stream still sees both
- * finished.  The caller guarantees the call's inputs were complete before that
- * kernel began: the verification of one batch then runs in the shadow of the
- * attention launch of another.  Results are identical either way.
- *   TSV_OVERLAP_GREEDY       tsv_tree_verify_greedy (and _noalloc); while it is
- *                            set, a stochastic call of a kind not in the set
- *                            also leaves room for a greedy CTA beside each of
- *                            its CTAs, so greedy launched after it runs during
- *                            its walk
+ * kernel still runs, in the CTAs its flag names below (the attention kernels'
+ * trigger lets it launch once every attention CTA is resident), and completes
+ * only after that kernel completes, so every later launch on the stream still
+ * sees both finished.  The caller guarantees the call's inputs were complete
+ * before that kernel began: the verification of one batch then runs in the
+ * shadow of the attention launch of another.  Results are identical either
+ * way.
+ *   TSV_OVERLAP_GREEDY       tsv_tree_verify_greedy (and _noalloc), in small
+ *                            CTAs that fit on an SM beside a running
+ *                            keys-on-lanes tree-attention CTA; while it is set,
+ *                            a stochastic call in full-size CTAs also leaves
+ *                            room for a greedy CTA beside each of them, so
+ *                            greedy launched after it runs during its walk
  *   TSV_OVERLAP_STOCHASTIC   tsv_tree_verify_stochastic (unwarped; in two-warp
  *                            CTAs reading their slices from global memory, so
  *                            a walk is several times slower than alone: worth
