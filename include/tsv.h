@@ -112,7 +112,9 @@ tsv_status tsv_destroy(tsv_handle h);
  * sees both finished.  The caller guarantees the call's inputs were complete
  * before that kernel began: the verification of one batch then runs in the
  * shadow of the attention launch of another.  Results are identical either
- * way.
+ * way, except that the full-size walk of TSV_OVERLAP_STOCHASTIC_FULL may run
+ * in smaller clusters, whose sums go in another order: a decision within
+ * rounding of a tie (what the oracle reports as a near tie) can then differ.
  *   TSV_OVERLAP_GREEDY       tsv_tree_verify_greedy (and _noalloc), in small
  *                            CTAs that fit on an SM beside a running
  *                            keys-on-lanes tree-attention CTA; while it is set,
