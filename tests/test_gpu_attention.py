@@ -162,6 +162,11 @@ EDGE = {
     # where the tree keys begin, and the next one starts with them
     "row-tiles-prefix-of-whole-blocks": dict(B=2, Hq=16, Hkv=2, nodes=100, prefix=1024, tree="random",
                                              max_depth=9),
+    # head dim 64 on the one-tile rows kernel (120 rows per KV head) and on a
+    # persistent keys-on-lanes launch (48 x 4 units of 40 rows, more than SMs)
+    "one-row-tile-head-dim-64": dict(B=2, Hq=8, Hkv=2, D=64, nodes=30, prefix=(300, 900), tree="random",
+                                     max_depth=7),
+    "persistent-keys-head-dim-64": dict(B=48, Hq=8, Hkv=4, D=64, nodes=20, prefix=(100, 600), tree="random"),
 }
 
 
